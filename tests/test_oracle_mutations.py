@@ -1,0 +1,54 @@
+"""The oracle pins must catch plausible mistakes.
+
+Each case edits one line of a copy of the oracle source (a dropped term, a
+wrong sign or index, a swapped operand), compiles it to a temporary library on
+the CPU, and runs the pin checks against it: at least one must fail.  The
+unmodified source must pass the same checks.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from tests import test_oracle_pins as pins
+
+MUTATIONS = {
+    "causal_diagonal_dropped": ("const int pos = nb - w + t;", "const int pos = nb - w + t - 1;"),
+    "ratio_without_one_minus_p": ("const double ratio = p / one_minus_p;", "const double ratio = p;"),
+    "residual_sign": ("const double diff = a[c] - load_elem", "const double diff = a[c] + load_elem"),
+    "gqa_sum_not_mean": ("raw[j] = s_sum[j] / (double)g;", "raw[j] = s_sum[j];"),
+    "gqa_interleaved_heads": ("const int hq = h * g + hl;", "const int hq = hl * s->Hkv + h;"),
+    "scale_1_over_d": ("1.0 / sqrt((double)d)", "1.0 / (double)d"),
+    "unnormalised_output": ("a[c] += p * load_elem", "a[c] += e[j] * load_elem"),
+    "pool_window_short": ("int lo = j - half, hi = j + half;", "int lo = j - half, hi = j + half - 1;"),
+    "protect_one_short": ("for (int j = nb - job->protect; j < nb; ++j)",
+                          "for (int j = nb - job->protect + 1; j < nb; ++j)"),
+    "tie_break_reversed": ("return (a->idx > b->idx) - (a->idx < b->idx);",
+                           "return (a->idx < b->idx) - (a->idx > b->idx);"),
+    "square_not_taken": ("s_head[j] += ratio * ratio * dist;", "s_head[j] += ratio * dist;"),
+}
+
+
+def _run_pins():
+    pins.test_raw_score_equals_actual_deletion_tiny(42)
+    pins.test_raw_score_gqa_group7()
+    pins.test_raw_score_equals_actual_deletion_ragged_mha()
+    pins.test_window_attention_vs_sdpa(42)
+    pins.test_pool_vs_max_pool1d_and_protection(3)
+    pins.test_select_vs_stable_sort_with_ties(0)
+
+
+def test_unmodified_source_passes(tmp_path):
+    lib = oracle.compile_variant(oracle.source(), str(tmp_path / "lib_ok.so"))
+    with oracle.use_library(lib):
+        _run_pins()
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_planted_mistake_is_caught(name, tmp_path):
+    old, new = MUTATIONS[name]
+    src = oracle.source()
+    assert src.count(old) == 1, name
+    lib = oracle.compile_variant(src.replace(old, new), str(tmp_path / ("lib_%s.so" % name)))
+    with oracle.use_library(lib):
+        with pytest.raises((AssertionError, oracle.OracleError)):
+            _run_pins()

@@ -1,0 +1,361 @@
+"""Pins of the CPU oracle to the pages and to the mathematics (no GPU).
+
+Each check compares the oracle with something that is not the oracle: actual
+deletion of a key followed by a fresh softmax, torch's fp64 attention and
+pooling routines, torch's stable sort, numpy fancy indexing, a crafted singular
+input, and the approximation bound of Theorem 1 checked by exhaustive search.
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle
+from kv_cache_eviction_dropkv_gb300 import synth
+
+GOLDEN = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "pages_values.json")))
+SEEDS = GOLDEN["synthetic_case_seeds"]["value"]
+
+
+def _softmax_out(keys, vals, q, d):
+    x = keys @ q / math.sqrt(d)
+    e = np.exp(x - x.max())
+    return (e / e.sum()) @ vals
+
+
+def brute_force_raw(q, k, v, lengths):
+    """Window score by actual deletion: for each visible row and each key j,
+    delete j, recompute the softmax output from scratch, and add the squared
+    change; average over the query heads of the group."""
+    B, Hq, w, d = q.shape
+    Hkv, n = k.shape[1], k.shape[2]
+    g = Hq // Hkv
+    raw = np.full((B, Hkv, n), np.nan)
+    for b in range(B):
+        nb = int(lengths[b])
+        for h in range(Hkv):
+            acc = np.zeros(nb)
+            for hl in range(g):
+                for t in range(w):
+                    pos = nb - w + t
+                    qq = q[b, h * g + hl, t]
+                    keys, vals = k[b, h, :pos + 1], v[b, h, :pos + 1]
+                    a = _softmax_out(keys, vals, qq, d)
+                    for j in range(nb):
+                        keep = np.array([i for i in range(pos + 1) if i != j])
+                        aj = _softmax_out(keys[keep], vals[keep], qq, d)
+                        acc[j] += float(((aj - a) ** 2).sum())
+            raw[b, h, :nb] = acc / g
+    return raw
+
+
+def _gauss(shape_q, shape_kv, seed):
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal(shape_q)
+    k = rng.standard_normal(shape_kv)
+    v = rng.standard_normal(shape_kv)
+    return q, k, v
+
+
+def _check_raw(raw_o, raw_bf, lengths):
+    # The brute force subtracts two nearly equal softmax outputs, so its
+    # squared difference carries an absolute error of order eps*|a|*|Delta|;
+    # the tolerance is that error bound plus a 1e-11 relative term.
+    eps = np.finfo(np.float64).eps
+    for b in range(raw_o.shape[0]):
+        nb = int(lengths[b])
+        ro, rb = raw_o[b, :, :nb], raw_bf[b, :, :nb]
+        tol = 1e-11 * np.abs(rb) + 256 * eps * np.sqrt(np.abs(rb)) * 8.0 + 1e-300
+        assert np.all(np.abs(ro - rb) <= tol), np.max(np.abs(ro - rb) / (np.abs(rb) + 1e-300))
+        assert np.all(np.isnan(raw_o[b, :, nb:]))
+
+
+@pytest.mark.parametrize("seed", SEEDS)
+def test_raw_score_equals_actual_deletion_tiny(seed):
+    """S1-S4 against actual deletion on the tiny workload (fp32 draws)."""
+    wl = synth.make_workload("tiny_d16_n128", seed=seed)
+    q, k, v = (x.astype(np.float64) for x in (wl.q32, wl.k32, wl.v32))
+    lengths = wl.lengths.numpy()
+    res = oracle.score(q, k, v, lengths, pool_kernel=1, protect=0)
+    _check_raw(res["raw"], brute_force_raw(q, k, v, lengths), lengths)
+
+
+@pytest.mark.parametrize("seed", SEEDS)
+def test_raw_score_equals_actual_deletion_page_case(seed):
+    """The README's own synthetic shape: 4 query heads, 2 KV heads, 19 slots,
+    3 queries; 'width 8' read as the head dimension."""
+    sh = GOLDEN["synthetic_case_shape"]["value"]
+    q, k, v = _gauss((1, sh["Hq"], sh["w"], sh["width"]), (1, sh["Hkv"], sh["n"], sh["width"]), seed)
+    lengths = np.array([sh["n"]], dtype=np.int32)
+    res = oracle.score(q, k, v, lengths, pool_kernel=1, protect=0)
+    _check_raw(res["raw"], brute_force_raw(q, k, v, lengths), lengths)
+
+
+def test_raw_score_equals_actual_deletion_ragged_mha():
+    """Ragged lengths (padding must be ignored) and g=1 (no averaging)."""
+    q, k, v = _gauss((2, 3, 3, 8), (2, 3, 40, 8), 7)
+    lengths = np.array([40, 23], dtype=np.int32)
+    k[1, :, 23:] = np.nan          # padding is never read
+    v[1, :, 23:] = np.nan
+    res = oracle.score(q, k, v, lengths, pool_kernel=1, protect=0)
+    _check_raw(res["raw"], brute_force_raw(q, k, v, lengths), lengths)
+
+
+def test_raw_score_gqa_group7():
+    q, k, v = _gauss((1, 7, 2, 8), (1, 1, 30, 8), 11)
+    lengths = np.array([30], dtype=np.int32)
+    res = oracle.score(q, k, v, lengths, pool_kernel=1, protect=0)
+    _check_raw(res["raw"], brute_force_raw(q, k, v, lengths), lengths)
+
+
+def test_deletion_agreement_vs_page_receipt():
+    """The README reports agreement with actual deletion to 5.55e-16 on its
+    data; in fp64 the oracle agrees with deletion to a comparable absolute
+    level on the tiny workload (scores of order 1e-2)."""
+    wl = synth.make_workload("tiny_d16_n128", seed=42)
+    q, k, v = (x.astype(np.float64) for x in (wl.q32, wl.k32, wl.v32))
+    lengths = wl.lengths.numpy()
+    res = oracle.score(q, k, v, lengths, pool_kernel=1, protect=0)
+    bf = brute_force_raw(q, k, v, lengths)
+    worst = float(np.nanmax(np.abs(res["raw"] - bf)))
+    assert worst < 100 * GOLDEN["deletion_vs_closed_form_max_abs"]["value"], worst
+
+
+def _sdpa_reference(q, k, v, lengths):
+    B, Hq, w, d = q.shape
+    Hkv, n = k.shape[1], k.shape[2]
+    g = Hq // Hkv
+    qt, kt, vt = (torch.from_numpy(np.ascontiguousarray(x)) for x in (q, k, v))
+    kt = kt.repeat_interleave(g, dim=1)
+    vt = vt.repeat_interleave(g, dim=1)
+    outs, lses = [], []
+    for b in range(B):
+        nb = int(lengths[b])
+        mask = torch.zeros(w, nb, dtype=torch.bool)
+        for t in range(w):
+            mask[t, :nb - w + t + 1] = True
+        kb, vb = kt[b:b + 1, :, :nb], vt[b:b + 1, :, :nb]
+        outs.append(F.scaled_dot_product_attention(qt[b:b + 1], kb, vb, attn_mask=mask))
+        logits = (qt[b:b + 1] @ kb.transpose(-1, -2)) / math.sqrt(d)
+        lses.append(torch.logsumexp(logits.masked_fill(~mask, float("-inf")), dim=-1))
+    return torch.cat(outs).numpy(), torch.cat(lses).numpy()
+
+
+@pytest.mark.parametrize("seed", SEEDS)
+def test_window_attention_vs_sdpa(seed):
+    """m, l and a against torch fp64 scaled_dot_product_attention with an
+    explicit tail-aligned causal mask, and logsumexp for m + log l."""
+    wl = synth.make_workload("tiny_d16_n128", seed=seed)
+    q, k, v = (x.astype(np.float64) for x in (wl.q32, wl.k32, wl.v32))
+    res = oracle.score(q, k, v, wl.lengths.numpy(), 3, 4)
+    a_ref, lse_ref = _sdpa_reference(q, k, v, wl.lengths.numpy())
+    np.testing.assert_allclose(res["a"], a_ref, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(res["m"] + np.log(res["l"]), lse_ref, rtol=1e-13, atol=1e-13)
+    assert np.all(res["l"] >= 1.0)    # the max term contributes exactly 1
+
+
+def test_window_attention_vs_sdpa_outlier_workload():
+    wl = synth.make_workload("phi3mini_mha_d96_n4k", n_max=512)
+    q, k, v = (x.double().numpy() for x in (wl.q, wl.k, wl.v))
+    res = oracle.score(wl.q, wl.k, wl.v, wl.lengths.numpy(), 5, 8)
+    a_ref, lse_ref = _sdpa_reference(q, k, v, wl.lengths.numpy())
+    np.testing.assert_allclose(res["a"], a_ref, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(res["m"] + np.log(res["l"]), lse_ref, rtol=1e-12)
+
+
+@pytest.mark.parametrize("kappa", [1, 3, 5, 7])
+def test_pool_vs_max_pool1d_and_protection(kappa):
+    wl = synth.make_workload("tiny_d16_n128", seed=43)
+    q, k, v = (x.astype(np.float64) for x in (wl.q32, wl.k32, wl.v32))
+    lengths = wl.lengths.numpy()
+    base = oracle.score(q, k, v, lengths, pool_kernel=kappa, protect=0)
+    pooled = F.max_pool1d(torch.from_numpy(base["raw"]), kappa, stride=1, padding=kappa // 2).numpy()
+    assert np.array_equal(base["final"], pooled)
+    if kappa == 1:
+        assert np.array_equal(base["final"], base["raw"])
+    prot = oracle.score(q, k, v, lengths, pool_kernel=kappa, protect=4)
+    assert np.all(np.isposinf(prot["final"][..., -4:]))
+    assert np.array_equal(prot["final"][..., :-4], pooled[..., :-4])
+    assert np.all(np.isfinite(prot["final"][..., :-4]))
+
+
+def test_pool_respects_ragged_end():
+    q, k, v = _gauss((2, 2, 3, 8), (2, 1, 40, 8), 5)
+    lengths = np.array([40, 17], dtype=np.int32)
+    res = oracle.score(q, k, v, lengths, pool_kernel=5, protect=0)
+    raw = res["raw"][1, 0, :17]
+    ref = F.max_pool1d(torch.from_numpy(raw)[None, None], 5, stride=1, padding=2).numpy()[0, 0]
+    assert np.array_equal(res["final"][1, 0, :17], ref)
+    assert np.all(np.isnan(res["final"][1, 0, 17:]))
+
+
+def test_window_tokens_seen_by_fewer_queries():
+    """A key that only the last t queries see gets exactly the contributions of
+    those rows: with w rows the key at n-1 is seen by one row only."""
+    q, k, v = _gauss((1, 1, 4, 8), (1, 1, 24, 8), 3)
+    lengths = np.array([24], dtype=np.int32)
+    full = oracle.score(q, k, v, lengths)["raw"][0, 0]
+    last_row = oracle.score(q[:, :, 3:4], k, v, lengths)["raw"][0, 0]   # w=1 with the last query
+    assert full[23] == pytest.approx(last_row[23], rel=1e-14)
+
+
+def test_singular_input_rejected():
+    """One logit more than 2000 nats above all others: p_j is exactly 1 in fp64
+    and the oracle rejects the input instead of patching it."""
+    q, k, v = _gauss((1, 1, 2, 16), (1, 1, 32, 16), 9)
+    q[..., 0] = 100.0
+    k[0, 0, 5, 0] = 100.0
+    k[0, 0, np.arange(32) != 5, 0] = 0.0
+    with pytest.raises(oracle.SingularInput):
+        oracle.score(q, k, v, np.array([32], dtype=np.int32))
+    k[0, 0, 5, 0] = 0.5          # moderate peak: finite scores, no rejection
+    res = oracle.score(q, k, v, np.array([32], dtype=np.int32))
+    assert np.all(np.isfinite(res["raw"]))
+
+
+def test_invalid_arguments_rejected():
+    q, k, v = _gauss((1, 2, 3, 8), (1, 2, 20, 8), 1)
+    with pytest.raises(oracle.OracleError):
+        oracle.score(q, k, v, np.array([2], dtype=np.int32))      # n_b < w
+    with pytest.raises(oracle.OracleError):
+        oracle.score(q, k, v, np.array([20], dtype=np.int32), pool_kernel=4)
+    fin = np.zeros((1, 2, 20))
+    with pytest.raises(oracle.OracleError):
+        oracle.select(fin, np.array([20]), np.array([18]), protect=3)
+
+
+def _sort_reference(fin, nb, kb):
+    order = torch.sort(torch.from_numpy(fin[:nb]), stable=True).indices.numpy()
+    return np.sort(order[kb:])
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2, 3])
+def test_select_vs_stable_sort_with_ties(seed):
+    rng = np.random.default_rng(seed)
+    B, H, n = 2, 3, 300
+    fin = rng.integers(0, 6, size=(B, H, n)).astype(np.float64)   # many ties
+    fin[..., -5:] = np.inf
+    lengths = np.array([300, 211], dtype=np.int32)
+    fin[1, :, 211:] = np.nan
+    fin[1, :, 206:211] = np.inf
+    ks = np.array([120, 206], dtype=np.int32)
+    kept, kl = oracle.select(fin, lengths, ks, protect=5)
+    assert list(kl) == [180, 5]
+    for b in range(B):
+        for h in range(H):
+            ref = _sort_reference(fin[b, h], int(lengths[b]), int(ks[b]))
+            assert np.array_equal(kept[b, h, :kl[b]], ref)
+
+
+def test_select_brute_force_n128():
+    rng = np.random.default_rng(5)
+    n = 128
+    fin = np.round(rng.standard_normal((1, 1, n)) ** 2, 2)
+    for kb in [0, 1, 12, 64, 127, 128]:
+        kept, kl = oracle.select(fin, np.array([n]), np.array([kb]), protect=0)
+        order = sorted(range(n), key=lambda j: (fin[0, 0, j], j))
+        assert np.array_equal(kept[0, 0, :kl[0]], np.array(sorted(order[kb:]), dtype=np.int32))
+
+
+def test_compact_byte_exact():
+    rng = np.random.default_rng(3)
+    B, H, n, d = 2, 3, 50, 24
+    k = rng.integers(0, 2 ** 16, size=(B, H, n, d), dtype=np.uint16)
+    v = rng.integers(0, 2 ** 16, size=(B, H, n, d), dtype=np.uint16)
+    kl = np.array([17, 9], dtype=np.int32)
+    kept = np.full((B, H, n), -1, dtype=np.int32)
+    for b in range(B):
+        for h in range(H):
+            kept[b, h, :kl[b]] = np.sort(rng.choice(n, kl[b], replace=False))
+    k_out, v_out = oracle.compact(k, v, kept, kl, out_rows=20)
+    for b in range(B):
+        for h in range(H):
+            assert np.array_equal(k_out[b, h, :kl[b]], k[b, h, kept[b, h, :kl[b]]])
+            assert np.array_equal(v_out[b, h, :kl[b]], v[b, h, kept[b, h, :kl[b]]])
+
+
+def test_thread_count_does_not_change_results():
+    wl = synth.make_workload("phi3mini_mha_d96_n4k", n_max=256)
+    r1 = oracle.score(wl.q, wl.k, wl.v, wl.lengths, 5, 8, nthreads=1)
+    r8 = oracle.score(wl.q, wl.k, wl.v, wl.lengths, 5, 8, nthreads=8)
+    assert np.array_equal(r1["final"], r8["final"], equal_nan=True)
+
+
+def _min_norm_direction(rhat):
+    """Certified lower bound on the cone constant c* = max_u min_i <u, rhat_i>:
+    take u along the (numerically) minimum-norm point of conv{rhat_i} and
+    evaluate min_i <u, rhat_i> exactly; any unit u gives a lower bound."""
+    from scipy.optimize import minimize
+    N = rhat.shape[0]
+    G = rhat @ rhat.T
+    res = minimize(lambda lam: lam @ G @ lam, np.full(N, 1.0 / N), jac=lambda lam: 2 * G @ lam,
+                   bounds=[(0, None)] * N, constraints=[{"type": "eq", "fun": lambda lam: lam.sum() - 1}],
+                   method="SLSQP", options={"ftol": 1e-15, "maxiter": 500})
+    u = res.x @ rhat
+    nu = np.linalg.norm(u)
+    if nu < 1e-9:
+        return -1.0
+    return float(np.min(rhat @ (u / nu)))
+
+
+def test_theorem1_bound_exhaustive():
+    """Theorem 1 on the tiny workload: within a pool L of the 20 lowest-weight
+    tokens, evicting the k tokens with the smallest single-query oracle scores
+    has objective F(J) = |a_{-J} - a| within 1/[c (1 - eps)(1 - k eps)] of the
+    best k-subset found by exhaustive search, wherever the cone holds."""
+    nL = GOLDEN["brute_force_candidate_pool"]["value"]
+    k_ev = GOLDEN["brute_force_k"]["value"]
+    combos = np.array(list(itertools.combinations(range(nL), k_ev)))
+    M = np.zeros((len(combos), nL))
+    np.put_along_axis(M, combos, 1.0, axis=1)
+    ratios, applied, total = [], 0, 0
+    for seed in SEEDS:
+        wl = synth.make_workload("tiny_d16_n128", seed=seed)
+        q, k, v = (x.astype(np.float64) for x in (wl.q32, wl.k32, wl.v32))
+        s = wl.spec
+        n, w, g, d = s.n_max, s.w, s.g, s.d
+        for h in range(s.Hkv):
+            for hl in range(g):
+                for t in range(w):
+                    total += 1
+                    pos = n - w + t
+                    qq = q[0, h * g + hl, t]
+                    keys, vals = k[0, h, :pos + 1], v[0, h, :pos + 1]
+                    # single-query oracle scores |Delta_j|^2 over this query's visible keys
+                    sub = oracle.score(qq[None, None, None, :], keys[None, None], vals[None, None],
+                                       np.array([pos + 1], dtype=np.int32))
+                    score = sub["raw"][0, 0]
+                    x = keys @ qq / math.sqrt(d)
+                    e = np.exp(x - x.max())
+                    l = e.sum()
+                    p = e / l
+                    a = p @ vals
+                    np.testing.assert_allclose(sub["a"][0, 0, 0], a, rtol=1e-12)
+                    cand = np.arange(0, min(pos + 1, n - s.protect))
+                    L = cand[np.argsort(p[cand], kind="stable")[:nL]]
+                    eps = float(p[L].max())
+                    r = a[None, :] - vals[L]
+                    c = _min_norm_direction(r / np.linalg.norm(r, axis=1, keepdims=True))
+                    # exhaustive objective over all k-subsets of L (recomputed softmax output)
+                    num = (e[:, None] * vals).sum(0)[None, :] - M @ (e[L, None] * vals[L])
+                    den = l - M @ e[L]
+                    Fall = np.linalg.norm(num / den[:, None] - a[None, :], axis=1)
+                    best = float(Fall.min())
+                    pick = set(L[np.argsort(score[L], kind="stable")[:k_ev]].tolist())
+                    row = np.array([set(L[cmb].tolist()) == pick for cmb in combos])
+                    assert row.sum() == 1
+                    Fhat = float(Fall[row][0])
+                    ratios.append(Fhat / best)
+                    assert Fhat >= best * (1 - 1e-12)
+                    if c > 0 and 1 - k_ev * eps > 0:
+                        applied += 1
+                        bound = 1.0 / (c * (1 - eps) * (1 - k_ev * eps))
+                        assert Fhat <= best * bound * (1 + 1e-9), (Fhat / best, bound)
+    assert applied >= total // 2
+    print("proxy ratio median %.4f p95 %.4f max %.4f; bound applied on %d/%d triples" % (
+        np.median(ratios), np.percentile(ratios, 95), np.max(ratios), applied, total))
