@@ -1,0 +1,363 @@
+#!/usr/bin/env python
+"""Benchmark of the DropKV score -> select -> compact path on one GB300 per rank.
+
+One step = the whole path (window attention, scoring, pool + protect, bottom-k
+selection, compaction) over one layer of the named workload, inputs already
+resident in HBM.  Prints ONE JSON line on rank 0.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+
+--impl reference times the fp64 CPU oracle on the host cores (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from kv_cache_eviction_dropkv_gb300 import synth  # noqa: E402
+
+METRIC = "DropKV scored tokens/s and ms per layer at n=128K; achieved HBM GB/s vs peak"
+UNIT = "tokens/s"
+KERNELS_PER_STEP = 7      # window attention, score, pool+protect, 3 selection kernels, compaction
+L2_FLUSH_BYTES = 256 << 20
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--workload", default=synth.HEADLINE, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def config_of(spec, lengths):
+    return {"workload": spec.name, "B": spec.B, "Hq": spec.Hq, "Hkv": spec.Hkv, "d": spec.d, "n_max": spec.n_max,
+            "n_tokens": int(sum(lengths)), "w": spec.w, "pool_kernel": spec.pool_kernel, "protect": spec.protect,
+            "budget_pct_kept": spec.budget_pct, "inputs": "bf16",
+            "l2": "inputs larger than L2 (K+V %.0f MB); 256 MB write flushes L2 between steps" % (
+                2 * spec.B * spec.Hkv * spec.n_max * spec.d * 2 / 1e6)}
+
+
+def workload_bytes(spec, lengths, kept):
+    """Algorithmic bytes of the two-pass structure (byte model)."""
+    U_tok = spec.Hkv * int(sum(lengths))                  # head-tokens
+    kv = 4 * spec.d                                       # K + V bytes per head-token
+    p1 = U_tok * kv
+    p2 = U_tok * (kv + 4)                                 # + raw score write
+    pool = U_tok * 8
+    sel = U_tok * 4 * 3 + spec.Hkv * int(sum(kept)) * 4   # hist, candidates, write passes + kept idx
+    comp = spec.Hkv * int(sum(kept)) * (4 + 2 * 2 * spec.d * 2)
+    return {"window_attention": p1, "score": p2, "pool_protect": pool, "select": sel, "compact": comp,
+            "path": p1 + p2 + pool + sel + comp}
+
+
+def source_hash():
+    h = hashlib.sha256()
+    for f in ("dropkv_attn.cu", "sm103_ptx.cuh", "dropkv_internal.cuh"):
+        with open(os.path.join(ROOT, "kv_cache_eviction_dropkv_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel, workload):
+    """DRAM bytes per launch from a committed ncu summary, if taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    e = d.get(workload, {}).get(kernel)
+    if not e or e.get("source_hash") != source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = None
+
+    def start(self):
+        try:
+            self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.out, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.flush()
+        self.out.seek(0)
+        rows = [ln.strip().split(",") for ln in self.out.read().splitlines() if ln.strip()]
+        os.unlink(self.out.name)
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+                power.append(float(r[3]))
+            except (ValueError, IndexError):
+                continue
+            for nm, val in zip(names, r[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+def run_reference(args, spec, wl):
+    """Reference arm: the fp64 CPU oracle on the host cores, same workload and metric."""
+    import oracle
+    lengths = wl.lengths.numpy()
+    units = int(sum(lengths))
+    cores = min(spec.B * spec.Hkv, os.cpu_count() or 1)
+
+    def step():
+        oracle.run_path(wl.q, wl.k, wl.v, wl.lengths, wl.evict_k, spec.pool_kernel, spec.protect, nthreads=cores)
+
+    for _ in range(args.warmup):
+        step()
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        step()
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = units * len(times) / total
+    sample = "the full layer (%d KV heads x %d tokens) per step, fp64, %d threads over KV heads" % (
+        spec.B * spec.Hkv, units, cores)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded generator; stands in for RULER/LongBench layers)",
+            "config": config_of(spec, lengths),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def cpu_baseline(spec, wl):
+    import oracle
+    cores = min(spec.B * spec.Hkv, os.cpu_count() or 1)
+    units = int(wl.lengths.sum())
+    t0 = time.perf_counter()
+    oracle.run_path(wl.q, wl.k, wl.v, wl.lengths, wl.evict_k, spec.pool_kernel, spec.protect, nthreads=cores)
+    dt = time.perf_counter() - t0
+    return {"value": units / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": "one full layer (%d KV heads, %d tokens), fp64, %.1f s on %d threads" % (
+                spec.B * spec.Hkv, units, dt, cores)}
+
+
+def main():
+    args = parse_args()
+    rank, world, local = dist_env()
+    spec = synth.WORKLOADS[args.workload]
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        wl = synth.make_workload(args.workload)
+        run_reference(args, spec, wl)
+        return
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+
+    from kv_cache_eviction_dropkv_gb300 import DropKV, _binding as B, _build
+    _build.build_library()
+
+    # each rank scores its own layer (weak scaling, no data-path collective)
+    wl = synth.make_workload(args.workload, seed=spec.seed + rank)
+    lengths_np = wl.lengths.numpy()
+    kept_np = wl.kept_len()
+    units = int(sum(lengths_np))
+    op = DropKV(spec.B, spec.Hq, spec.Hkv, spec.d, spec.n_max, spec.w, spec.pool_kernel, spec.protect,
+                out_rows=int(kept_np.max()), device=dev)
+    q, k, v = wl.q.to(dev), wl.k.to(dev), wl.v.to(dev)
+    lengths, ev = wl.lengths.to(dev), wl.evict_k.to(dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(events=None):
+        if events is None:
+            op.run(q, k, v, lengths, ev, stream=stream, keep_raw=False)
+        else:
+            B.dropkv_score_timed(op.shape, q, k, v, lengths, op.pool_kernel, op.protect, op.scores, None,
+                                 op.workspace, op.status, events[1:5], stream)
+            op.select(lengths, ev, stream)
+            events[5].record(stream)
+            op.compact(k, v, stream)
+
+    for _ in range(max(3, args.warmup)):
+        flush.fill_(1.0)
+        step()
+    op.check(stream)
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(K)]
+    sampler = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local])
+                           if os.environ.get("CUDA_VISIBLE_DEVICES") else local)
+    sampler.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(K):
+        flush.fill_(float(i))
+        e = evs[i]
+        e[0].record(stream)
+        step(e)
+        e[6].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop()
+    op.check(stream)
+
+    def ms(a, b):
+        return [evs[i][a].elapsed_time(evs[i][b]) for i in range(K)]
+
+    t_step = ms(0, 6)
+    phases = {"window_attention": ms(1, 2), "score": ms(2, 3), "pool_protect": ms(3, 4),
+              "select": ms(4, 5), "compact": ms(5, 6)}
+    step_ms = sum(t_step) / K
+    if world > 1:
+        t = torch.tensor([step_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        step_ms = float(t.item())
+    value = units * world / (step_ms / 1e3)
+
+    nbytes = workload_bytes(spec, lengths_np, kept_np)
+    peak, peak_kind = measured_peaks()
+    phase_ms = {kname: sum(v_) / K for kname, v_ in phases.items()}
+    dom = max(("window_attention", "score"), key=lambda kk: phase_ms[kk])
+    achieved = nbytes[dom] / (phase_ms[dom] / 1e3) / 1e9
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "peak_source": peak_kind,
+                "traffic": recorded_traffic(dom, spec.name),
+                "algorithmic_bytes_per_launch": nbytes[dom]}
+    path_gbs = nbytes["path"] / (step_ms / 1e3) / 1e9
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+            "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic (seeded generator; stands in for RULER/LongBench layers)",
+            "config": dict(config_of(spec, lengths_np), parallelism="one independent layer per GPU"),
+            "roofline": roofline,
+            "path_roofline": {"achieved": path_gbs, "peak": peak, "unit": "GB/s", "frac": path_gbs / peak,
+                              "algorithmic_bytes_per_step": nbytes["path"]},
+            "phases_ms": phase_ms, "wall_s_timed": wall, "gpu_launches": KERNELS_PER_STEP * K,
+            "clocks": clocks}
+
+    if not args.no_e2e:
+        line["e2e"] = e2e_leg(op, wl, dev, stream, args, world)
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(spec, wl)
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def e2e_leg(op, wl, dev, stream, args, world):
+    """Same metric through the public API with host buffers: every step copies
+    its inputs from pinned host memory and reads the kept set and the compacted
+    K/V back."""
+    hq, hk, hv = wl.q.pin_memory(), wl.k.pin_memory(), wl.v.pin_memory()
+    hl, he = wl.lengths.pin_memory(), wl.evict_k.pin_memory()
+    dq, dk, dv = torch.empty_like(hq, device=dev), torch.empty_like(hk, device=dev), torch.empty_like(hv, device=dev)
+    dl, de = torch.empty_like(hl, device=dev), torch.empty_like(he, device=dev)
+    outs = [op.kept_len, op.kept_idx, op.k_out, op.v_out]
+    houts = [torch.empty_like(t, device="cpu").pin_memory() for t in outs]
+    bi = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hl, he))
+    bo = sum(t.numel() * t.element_size() for t in houts)
+
+    def one():
+        for src, dst in ((hq, dq), (hk, dk), (hv, dv), (hl, dl), (he, de)):
+            dst.copy_(src, non_blocking=True)
+        op.run(dq, dk, dv, dl, de, stream=stream, keep_raw=False)
+        for src, dst in zip(outs, houts):
+            dst.copy_(src, non_blocking=True)
+
+    for _ in range(2):
+        one()
+    torch.cuda.synchronize()
+    K = max(1, min(args.steps, 20))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(K):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / K
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    units = int(wl.lengths.sum())
+    return {"value": units * world / (ms / 1e3), "unit": UNIT, "ms_per_step": ms, "steps": K,
+            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
+
+
+if __name__ == "__main__":
+    main()

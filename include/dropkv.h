@@ -1,0 +1,157 @@
+/*
+ * dropkv.h -- C ABI of the GB300 (sm_103a) DropKV eviction-scoring path.
+ *
+ * The method ("DropKV: Decoupling Residual-Output Perturbation for Near-Optimal
+ * KV-Cache Eviction"; "DropKV: Exact single-entry output-perturbation scoring",
+ * Core equation and Algorithm 1 summary): for every KV head, the last w prompt
+ * queries of each query head in its GQA group attend causally, tail-aligned,
+ * over the n cached keys; with p = softmax(K q / sqrt(d)) and a = sum_j p_j v_j,
+ * each cached token j is scored by its exact single-token output perturbation
+ * s_j = sum_t || p_j / (1 - p_j) (a - v_j) ||^2 ; scores are averaged over the
+ * query heads of the group, max-pooled along the sequence, the last slots are
+ * protected (+inf), the k lowest are evicted and the kept K/V rows compacted.
+ *
+ * Conventions (all entry points):
+ *  - Every buffer is owned by the caller.  Pointers marked "device" are CUDA
+ *    device pointers, 16-byte aligned, densely packed in the stated layout.
+ *    The library allocates no device memory.
+ *  - Calls are asynchronous on `stream` (any CUDA stream of the current
+ *    device; 0 = the legacy default stream).  A host-detectable error returns
+ *    immediately with nothing launched.
+ *  - Errors found on the device (a singular or non-finite score, an invalid
+ *    length or eviction count, a pipeline wait that timed out) are OR-ed into
+ *    the caller's 32-bit device status word (`status`, zeroed by the caller
+ *    before the first call); the call still completes and writes defined
+ *    values.  dropkv_read_status() syncs the stream and reports the word.
+ *  - bf16 inputs are read as stored; arithmetic is fp32 with bf16 operands on
+ *    the tensor cores and fp32 accumulation.
+ */
+#ifndef DROPKV_H
+#define DROPKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define DROPKV_API __attribute__((visibility("default")))
+#else
+#define DROPKV_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DROPKV_OK = 0,
+  DROPKV_ERR_INVALID_ARG = 1,   /* bad shape, pointer, alignment, kernel size or aliasing */
+  DROPKV_ERR_WORKSPACE = 2,     /* workspace missing or smaller than dropkv_workspace_size() */
+  DROPKV_ERR_SINGULAR = 3,      /* some p_j rounded to 1: exact removal is singular (rejected, no epsilon) */
+  DROPKV_ERR_NONFINITE = 4,     /* a score or attention statistic is not finite */
+  DROPKV_ERR_CUDA = 5,          /* a CUDA runtime call failed */
+  DROPKV_ERR_UNSUPPORTED = 6,   /* shape outside the supported range (see dropkv_shape) */
+  DROPKV_ERR_DEVICE_ARG = 7,    /* device-side argument check failed (lengths, eviction counts, capacity) */
+  DROPKV_ERR_TIMEOUT = 8        /* a kernel pipeline wait gave up (flag set instead of hanging) */
+} dropkv_status;
+
+/* Bits of the device status word. */
+#define DROPKV_FLAG_SINGULAR   0x01u
+#define DROPKV_FLAG_NONFINITE  0x02u
+#define DROPKV_FLAG_BAD_LENGTH 0x04u   /* lengths[b] outside [w, n_max] (or < protect) */
+#define DROPKV_FLAG_BAD_K      0x08u   /* evict_k[b] outside [0, n_b - protect] */
+#define DROPKV_FLAG_OVERFLOW   0x10u   /* kept_len[b] > out_rows in dropkv_compact */
+#define DROPKV_FLAG_TIMEOUT    0x20u
+
+/* Problem shape.  Supported: B >= 1; Hq % Hkv == 0; g = Hq / Hkv; R = g * w <= 64;
+ * d a multiple of 8 in [8, 128]; 1 <= w <= n_max < 2^31. */
+typedef struct {
+  int32_t B;       /* batch (sequences) */
+  int32_t Hq;      /* query heads */
+  int32_t Hkv;     /* KV heads */
+  int32_t d;       /* head dimension */
+  int32_t n_max;   /* cache capacity per sequence (padded length) */
+  int32_t w;       /* observation window: tail queries per query head */
+} dropkv_shape;
+
+/* Bytes of device workspace the three calls need for `shape` on the current
+ * device (0 if the shape is invalid or unsupported, or no device is present).
+ * The same workspace may serve dropkv_score and dropkv_select.  After
+ * dropkv_score completes, the workspace starts with the window statistics of
+ * step S1 (U = B * Hkv, R = g * w, row r = h_local * w + t of KV head (b, h),
+ * logits x_j = q.k_j / sqrt(d) over the keys the row sees):
+ *   float lse[U][R]    log sum_j exp(x_j)        (offset 0)
+ *   float a[U][R][d]   sum_j p_j v_j             (offset round_up(4*U*R, 256)) */
+DROPKV_API size_t dropkv_workspace_size(const dropkv_shape* shape);
+
+/* Steps S1-S5: window attention, per-token perturbation score, GQA average,
+ * MaxPool1D and recent-slot protection.
+ *   q_window  device bf16 [B][Hq][w][d]  last w query rows of every query head
+ *   k, v      device bf16 [B][Hkv][n_max][d]  cached keys / values; only rows
+ *             j < lengths[b] are read
+ *   lengths   device int32 [B] (n_b), or NULL for n_b = n_max
+ *   pool_kernel  odd, 1..63: MaxPool1D kernel (stride 1, window clipped to [0, n_b))
+ *   protect   >= 0: slots j >= n_b - protect get +inf after pooling
+ *   scores    device float [B][Hkv][n_max]: final score of slot j < n_b
+ *             (slots >= n_b are not written)
+ *   raw_scores  device float [B][Hkv][n_max] or NULL: GQA-averaged score
+ *             before pooling
+ *   workspace / workspace_bytes  device scratch of dropkv_workspace_size() bytes
+ *   status    device uint32 status word
+ * Sources: "... output-perturbation scoring", Core equation, Algorithm 1
+ * summary, Code mapping (tail-aligned causality, GQA). */
+DROPKV_API dropkv_status dropkv_score(const dropkv_shape* shape, const void* q_window, const void* k, const void* v,
+                           const int32_t* lengths, int32_t pool_kernel, int32_t protect, float* scores,
+                           float* raw_scores, void* workspace, size_t workspace_bytes, uint32_t* status,
+                           cudaStream_t stream);
+
+/* dropkv_score that also records phase_events[0..3] on `stream`: before pass 1
+ * (window attention), between pass 1 and pass 2 (scoring), between pass 2 and
+ * pooling, and after pooling -- for per-kernel timing with CUDA events.  The
+ * events are created by the caller; everything else is as dropkv_score. */
+DROPKV_API dropkv_status dropkv_score_timed(const dropkv_shape* shape, const void* q_window, const void* k,
+                                            const void* v, const int32_t* lengths, int32_t pool_kernel,
+                                            int32_t protect, float* scores, float* raw_scores, void* workspace,
+                                            size_t workspace_bytes, uint32_t* status, cudaStream_t stream,
+                                            cudaEvent_t* phase_events);
+
+/* Step S6: evict the evict_k[b] lowest scores of every KV head (equal scores:
+ * the lower position is evicted first) and list the kept positions.
+ *   scores    device float [B][Hkv][n_max] (as written by dropkv_score)
+ *   lengths   device int32 [B] or NULL (n_max)
+ *   evict_k   device int32 [B]: 0 <= k_b <= n_b - protect (else FLAG_BAD_K, nothing evicted)
+ *   protect   the protect value the scores were made with (bounds k_b)
+ *   kept_idx  device int32 [B][Hkv][n_max]: first n_b - k_b entries of each
+ *             head = kept positions in ascending order; the rest untouched
+ *   kept_len  device int32 [B]: n_b - k_b
+ * Source: "... output-perturbation scoring", Algorithm 1 summary (evict the
+ * smallest scores); "DropKV: Decoupling ...", section 3.2 (bottom-k). */
+DROPKV_API dropkv_status dropkv_select(const dropkv_shape* shape, const float* scores, const int32_t* lengths,
+                            const int32_t* evict_k, int32_t protect, int32_t* kept_idx, int32_t* kept_len,
+                            void* workspace, size_t workspace_bytes, uint32_t* status, cudaStream_t stream);
+
+/* Step S7: gather the kept rows of K and V.
+ *   k, v      device bf16 [B][Hkv][n_max][d]
+ *   kept_idx, kept_len  as written by dropkv_select
+ *   out_rows  row capacity of the outputs per head (>= max_b kept_len[b],
+ *             else FLAG_OVERFLOW and only out_rows rows are copied)
+ *   k_out, v_out  device bf16 [B][Hkv][out_rows][d], must not overlap k or v;
+ *             rows >= kept_len[b] are untouched
+ * Source: "DropKV: Decoupling ...", section 2.2 (eviction removes tokens and
+ * shrinks the resident cache). */
+DROPKV_API dropkv_status dropkv_compact(const dropkv_shape* shape, const void* k, const void* v, const int32_t* kept_idx,
+                             const int32_t* kept_len, int32_t out_rows, void* k_out, void* v_out,
+                             uint32_t* status, cudaStream_t stream);
+
+/* Synchronise `stream`, read the device status word and map it to a status
+ * (the first of SINGULAR, NONFINITE, DEVICE_ARG, TIMEOUT that is set, else OK).
+ * *flags_out (if not NULL) receives the raw word. */
+DROPKV_API dropkv_status dropkv_read_status(const uint32_t* status, cudaStream_t stream, uint32_t* flags_out);
+
+/* Version string of the library build. */
+DROPKV_API const char* dropkv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DROPKV_H */

@@ -1,0 +1,110 @@
+// Internal declarations shared by the library's translation units: problem
+// geometry, the workspace plan, kernel parameter blocks and launchers.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "../../include/dropkv.h"
+
+namespace dropkv {
+
+constexpr int kTile = 128;          // tokens per K/V tile (the MMA M dimension)
+constexpr int kDPad = 128;          // head dimension as staged in shared memory
+constexpr int kMaxR = 64;           // rows (g * w) per KV head supported
+constexpr int kSelChunk = 4096;     // tokens per block in the selection kernels
+constexpr int kHistBins = 4096;     // first-level radix histogram (top 12 key bits)
+constexpr int kCandCap = 8192;      // candidates resolved in shared memory
+constexpr int kMaxPool = 63;
+
+// Geometry derived from dropkv_shape.
+struct Geom {
+  int B, Hq, Hkv, d, n_max, w;
+  int g, R, NR;          // NR: R rounded up to the MMA width instantiated (16, 32 or 64)
+  int U;                 // B * Hkv units (KV heads)
+  int tiles_max;         // ceil(n_max / kTile)
+  int splits1, tpc1;     // pass-1 CTAs per unit and tiles per CTA
+  int splits2, tpc2;     // pass-2 CTAs per unit and tiles per CTA
+  int chunks;            // ceil(n_max / kSelChunk)
+};
+
+// Byte offsets of the workspace regions (all 256-byte aligned).
+struct WsPlan {
+  size_t m, l, a;                // exported statistics (see dropkv.h)
+  size_t m2, aa;                 // max in log2 units, |a|^2
+  size_t ahl;                    // bf16 [U][2][NR][128]: a split into hi + lo parts
+  size_t part_o, part_ml;        // pass-1 partial states
+  size_t tickets;                // u32 [U] pass-1 merge tickets
+  size_t raw;                    // f32 [U][n_max] raw scores when the caller passes none
+  // selection
+  size_t hist;                   // u32 [U][kHistBins]
+  size_t sel_state;              // u32 [U][8]
+  size_t cand;                   // u32 [U][kCandCap][2]
+  size_t cand_cnt;               // u32 [U]
+  size_t sel_tickets;            // u32 [U][2]
+  size_t chunk_kept;             // u32 [U][chunks]
+  size_t chunk_off;              // u32 [U][chunks]
+  size_t sel_zero_begin, sel_zero_end;   // range cleared at the start of dropkv_select
+  size_t total;
+};
+
+bool make_geom(const dropkv_shape* s, int num_sms, Geom* g);
+WsPlan make_plan(const Geom& g);
+
+// Parameter block of the two attention passes.
+struct AttnParams {
+  const __nv_bfloat16* q;        // [B][Hq][w][d]
+  const int32_t* lengths;        // [B] or null
+  int B, Hq, Hkv, d, n_max, w, g, R, U;
+  int splits, tpc;
+  float scale_log2;              // log2(e) / sqrt(d)
+  // workspace
+  float *m, *l, *a, *m2, *aa;
+  __nv_bfloat16* ahl;
+  float *part_o, *part_ml;
+  uint32_t* tickets;
+  float* raw;                    // raw score output [U][n_max]
+  uint32_t* status;
+};
+
+struct PoolParams {
+  const float* raw;
+  float* scores;
+  const int32_t* lengths;
+  int B, Hkv, n_max, w, half, protect;
+  uint32_t* status;
+};
+
+struct SelParams {
+  const float* scores;
+  const int32_t* lengths;
+  const int32_t* evict_k;
+  int32_t* kept_idx;
+  int32_t* kept_len;
+  int B, Hkv, n_max, protect, chunks;
+  uint32_t *hist, *state, *cand, *cand_cnt, *tickets, *chunk_kept, *chunk_off;
+  uint32_t* status;
+};
+
+struct CompactParams {
+  const uint8_t* k;
+  const uint8_t* v;
+  const int32_t* kept_idx;
+  const int32_t* kept_len;
+  uint8_t* k_out;
+  uint8_t* v_out;
+  int B, Hkv, n_max, row_bytes, out_rows;
+  uint32_t* status;
+};
+
+cudaError_t launch_window_attention(const AttnParams& p, int NR, const CUtensorMap& tk, const CUtensorMap& tv,
+                                    int num_ctas_x, cudaStream_t st);
+cudaError_t launch_score(const AttnParams& p, int NR, const CUtensorMap& tk, const CUtensorMap& tv,
+                         cudaStream_t st);
+cudaError_t launch_pool_protect(const PoolParams& p, cudaStream_t st);
+cudaError_t launch_select(const SelParams& p, cudaStream_t st);
+cudaError_t launch_compact(const CompactParams& p, cudaStream_t st);
+
+}  // namespace dropkv

@@ -1,0 +1,79 @@
+"""Comparison rules between the CUDA path and the oracle.
+
+Scores: the required bound is |gpu - ref| <= 2e-3 |ref| + 1e-6 (relative error
+2e-3, absolute 1e-6 for near-zero scores).  Because scores at long context are
+far below 1e-6, the tests also apply a scale-aware bound
+|gpu - ref| <= 2e-3 |ref| + 1e-6 * max_finite(ref of that head), which keeps
+the relative test meaningful there.  +inf (protected) must match exactly.
+
+Kept sets: they must match exactly except for tokens whose oracle score lies
+within the score tolerance of the oracle's k-th smallest score (the band where
+the k-th and (k+1)-th scores are indistinguishable), and the number kept must
+be exact.
+"""
+import numpy as np
+
+RTOL = 2e-3
+ATOL = 1e-6
+
+
+def score_tolerance(ref_row: np.ndarray) -> np.ndarray:
+    finite = np.isfinite(ref_row)
+    scale = float(np.max(ref_row[finite])) if finite.any() else 0.0
+    return RTOL * np.abs(ref_row) + ATOL * scale
+
+
+def check_scores(got: np.ndarray, ref: np.ndarray, lengths, what: str = "scores"):
+    """got/ref [B,H,n_max]; only slots j < n_b are compared.  Returns the worst
+    error as a fraction of the scale-aware tolerance."""
+    worst = 0.0
+    B, H, _ = ref.shape
+    for b in range(B):
+        nb = int(lengths[b])
+        for h in range(H):
+            r, g = ref[b, h, :nb], got[b, h, :nb]
+            inf = np.isinf(r)
+            assert np.array_equal(np.isinf(g), inf), "%s: +inf slots differ (b=%d h=%d)" % (what, b, h)
+            assert np.all(g[inf] == r[inf])
+            fr, fg = r[~inf], g[~inf]
+            assert np.all(np.isfinite(fg)), "%s: non-finite GPU score (b=%d h=%d)" % (what, b, h)
+            err = np.abs(fg - fr)
+            literal = RTOL * np.abs(fr) + ATOL
+            assert np.all(err <= literal), "%s: literal bound violated (b=%d h=%d) max %.3g" % (
+                what, b, h, float(np.max(err / literal)))
+            tol = score_tolerance(r)[~inf]
+            frac = err / np.where(tol > 0, tol, 1e-300)
+            if frac.size:
+                worst = max(worst, float(frac.max()))
+            assert np.all(err <= tol), "%s: scale-aware bound violated (b=%d h=%d) worst %.3g of tol" % (
+                what, b, h, float(frac.max()))
+    return worst
+
+
+def check_kept(kept_gpu: np.ndarray, len_gpu: np.ndarray, kept_ref: np.ndarray, len_ref: np.ndarray,
+               final_ref: np.ndarray, lengths, evict_k):
+    """Exact kept sets outside the tolerance band around the k-th smallest score."""
+    assert np.array_equal(len_gpu, len_ref), (len_gpu, len_ref)
+    B, H, _ = final_ref.shape
+    band_total = 0
+    for b in range(B):
+        nb, kb, kl = int(lengths[b]), int(evict_k[b]), int(len_ref[b])
+        for h in range(H):
+            g = kept_gpu[b, h, :kl]
+            assert np.all(np.diff(g) > 0), "kept indices must be strictly ascending (b=%d h=%d)" % (b, h)
+            assert g.min() >= 0 and g.max() < nb
+            r = kept_ref[b, h, :kl]
+            if np.array_equal(g, r):
+                continue
+            fin = final_ref[b, h, :nb]
+            if kb == 0:
+                raise AssertionError("nothing to evict but kept sets differ (b=%d h=%d)" % (b, h))
+            order = np.lexsort((np.arange(nb), fin))
+            T = fin[order[kb - 1]]
+            tolT = RTOL * abs(T) + ATOL * float(np.max(fin[np.isfinite(fin)]))
+            band = np.abs(fin - T) <= tolT
+            diff = np.setxor1d(g, r)
+            assert np.all(band[diff]), "kept sets differ outside the tolerance band (b=%d h=%d): %s" % (
+                b, h, diff[~band[diff]][:10])
+            band_total += diff.size
+    return band_total

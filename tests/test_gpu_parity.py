@@ -1,0 +1,172 @@
+"""GPU parity of the CUDA path against the oracle, through the C ABI.
+
+Inputs are the seeded workloads; the oracle sees exactly the bf16 values the
+GPU reads.  Every workload runs at its full size, plus reduced sizes that
+still span several tiles with a ragged tail and the edge cases of the method.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from kv_cache_eviction_dropkv_gb300 import DropKV, synth
+from tests._parity import check_kept, check_scores
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda", 0) if torch.cuda.is_available() else None
+SENTINEL = -7.25
+
+
+def _run(wl, poison=True, out_rows=None):
+    s = wl.spec
+    op = DropKV(s.B, s.Hq, s.Hkv, s.d, s.n_max, s.w, s.pool_kernel, s.protect, out_rows=out_rows, device=DEV)
+    k, v = wl.k.clone(), wl.v.clone()
+    if poison:
+        for b in range(s.B):
+            nb = int(wl.lengths[b])
+            k[b, :, nb:] = float("nan")
+            v[b, :, nb:] = float("nan")
+    q, k, v = wl.q.to(DEV), k.to(DEV), v.to(DEV)
+    lengths, ev = wl.lengths.to(DEV), wl.evict_k.to(DEV)
+    op.scores.fill_(SENTINEL)
+    op.raw_scores.fill_(SENTINEL)
+    op.kept_idx.fill_(-5)
+    op.run(q, k, v, lengths, ev)
+    flags = op.check()
+    return op, k, v, flags
+
+
+def _compare(wl, op, kdev, vdev, ref, label):
+    s = wl.spec
+    lengths = wl.lengths.numpy()
+    raw = op.raw_scores.cpu().numpy()
+    fin = op.scores.cpu().numpy()
+    w_raw = check_scores(raw, ref["raw"], lengths, label + " raw")
+    w_fin = check_scores(fin, ref["final"], lengths, label + " final")
+    for b in range(s.B):          # slots past n_b are never written
+        nb = int(lengths[b])
+        assert np.all(fin[b, :, nb:] == SENTINEL) and np.all(raw[b, :, nb:] == SENTINEL)
+    lse, a = (t.cpu().numpy() for t in op.window_stats())
+    ref_lse = (ref["m"] + np.log(ref["l"])).reshape(lse.shape)
+    ref_a = ref["a"].reshape(a.shape)
+    np.testing.assert_allclose(lse, ref_lse, rtol=1e-5, atol=1e-4)
+    scale_a = np.abs(ref_a).max(axis=-1, keepdims=True)
+    assert np.all(np.abs(a - ref_a) <= 1e-4 * scale_a + 1e-6), float(np.max(np.abs(a - ref_a) / scale_a))
+    kept = op.kept_idx.cpu().numpy()
+    kl = op.kept_len.cpu().numpy()
+    # selection is integer work: on the GPU's own scores it must equal a stable sort exactly
+    own_kept, own_len = oracle.select(np.where(np.isnan(fin), np.inf, fin).astype(np.float64), lengths,
+                                      wl.evict_k.numpy(), s.protect)
+    assert np.array_equal(own_len, kl)
+    for b in range(s.B):
+        assert np.array_equal(own_kept[b, :, :kl[b]], kept[b, :, :kl[b]]), "select != stable sort of GPU scores"
+    band = check_kept(kept, kl, ref["kept_idx"], ref["kept_len"], ref["final"], lengths, wl.evict_k.numpy())
+    # compaction: byte-exact gather of the GPU's own kept rows
+    k_out, v_out = op.k_out.cpu(), op.v_out.cpu()
+    kc, vc = kdev.cpu(), vdev.cpu()
+    for b in range(s.B):
+        for h in range(s.Hkv):
+            idx = torch.from_numpy(kept[b, h, :kl[b]].astype(np.int64))
+            assert torch.equal(k_out[b, h, :kl[b]].view(torch.int16), kc[b, h, idx].view(torch.int16))
+            assert torch.equal(v_out[b, h, :kl[b]].view(torch.int16), vc[b, h, idx].view(torch.int16))
+            assert np.all(kept[b, h, kl[b]:] == -5)
+    print("%s: worst raw %.3f / final %.3f of tolerance, %d band tokens" % (label, w_raw, w_fin, band))
+
+
+@pytest.mark.parametrize("seed", [42, 43, 44])
+def test_tiny_workload(seed):
+    wl = synth.make_workload("tiny_d16_n128", seed=seed)
+    s = wl.spec
+    ref = oracle.run_path(wl.q, wl.k, wl.v, wl.lengths, wl.evict_k, s.pool_kernel, s.protect)
+    op, k, v, _ = _run(wl)
+    _compare(wl, op, k, v, ref, "tiny seed %d" % seed)
+
+
+@pytest.mark.parametrize("name,n_max", [
+    ("phi3mini_mha_d96_n4k", 1000),
+    ("llama8b_gqa_d128_n32k", 2 * 128 * 19 + 57),
+    ("qwen_gqa7_b4_ragged_n64k", 3000),
+])
+def test_reduced_sizes_ragged_tail(name, n_max):
+    wl = synth.make_workload(name, n_max=n_max)
+    s = wl.spec
+    ref = oracle.run_path(wl.q, wl.k, wl.v, wl.lengths, wl.evict_k, s.pool_kernel, s.protect)
+    op, k, v, _ = _run(wl)
+    _compare(wl, op, k, v, ref, "%s n=%d" % (name, n_max))
+
+
+@pytest.mark.parametrize("name", [
+    "phi3mini_mha_d96_n4k",
+    "llama8b_gqa_d128_n32k",
+    "llama8b_gqa_d128_n128k",
+    "qwen_gqa7_b4_ragged_n64k",
+])
+def test_full_size_workloads(name):
+    wl = synth.make_workload(name)
+    s = wl.spec
+    ref = oracle.run_path(wl.q, wl.k, wl.v, wl.lengths, wl.evict_k, s.pool_kernel, s.protect)
+    op, k, v, _ = _run(wl)
+    _compare(wl, op, k, v, ref, name)
+
+
+def _custom(B, Hq, Hkv, d, n, w, seed=0, lengths=None):
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal((B, Hq, w, d)).astype(np.float32)
+    k = rng.standard_normal((B, Hkv, n, d)).astype(np.float32)
+    v = rng.standard_normal((B, Hkv, n, d)).astype(np.float32)
+    lens = np.full(B, n, dtype=np.int32) if lengths is None else np.asarray(lengths, dtype=np.int32)
+    return q, k, v, lens
+
+
+def _run_custom(q, k, v, lens, evict, pool, protect):
+    wl = synth.Workload(spec=synth.WorkloadSpec("custom", q.shape[0], q.shape[1], k.shape[1], q.shape[3],
+                                                k.shape[2], q.shape[2], pool, protect, 0, "custom"),
+                        q=synth.bf16_round(q), k=synth.bf16_round(k), v=synth.bf16_round(v),
+                        lengths=torch.from_numpy(lens), evict_k=torch.from_numpy(np.asarray(evict, dtype=np.int32)))
+    ref = oracle.run_path(wl.q, wl.k, wl.v, wl.lengths, wl.evict_k, pool, protect)
+    op, kd, vd, flags = _run(wl)
+    _compare(wl, op, kd, vd, ref, "custom")
+    return op, flags
+
+
+@pytest.mark.parametrize("case", [
+    # (B, Hq, Hkv, d, n, w, pool, protect, evict)
+    (1, 1, 1, 64, 128, 1, 1, 0, [0]),          # w=1, g=1, pool 1, nothing evicted
+    (1, 2, 1, 32, 77, 3, 1, 0, [74]),          # n < one tile, evict every unprotected slot
+    (1, 8, 2, 128, 300, 4, 7, 4, [150]),       # g=4, several tiles, ragged tail
+    (2, 4, 4, 96, 513, 2, 3, 2, [400, 1]),     # MHA, d=96
+    (1, 16, 1, 128, 1025, 4, 5, 4, [1000]),    # R=64 (largest supported group x window)
+    (1, 3, 1, 8, 260, 5, 9, 5, [100]),         # d=8, R=15
+])
+def test_edge_shapes(case):
+    B, Hq, Hkv, d, n, w, pool, protect, evict = case
+    q, k, v, lens = _custom(B, Hq, Hkv, d, n, w, seed=sum(case[:6]))
+    _run_custom(q, k, v, lens, evict, pool, protect)
+
+
+def test_ragged_lengths_with_nan_padding():
+    q, k, v, lens = _custom(3, 4, 2, 64, 700, 4, seed=5, lengths=[700, 129, 333])
+    _run_custom(q, k, v, lens, [600, 100, 0], 5, 4)
+
+
+def test_logit_jump_inside_a_chunk():
+    """Two keys about 20 nats above every other logit, each in the third tile of
+    a different CTA's range: the CTA's running exponent reference has to move
+    mid-range and its accumulator be rescaled.  Each big key ends near p = 0.5."""
+    n = 128 * 152 * 4
+    q, k, v, lens = _custom(1, 1, 1, 64, n, 2, seed=9)
+    q[0, 0, 1] = q[0, 0, 0]
+    qn = q[0, 0, 0] / np.linalg.norm(q[0, 0, 0])
+    big = 20.0 * np.sqrt(64) / np.linalg.norm(q[0, 0, 0])
+    for pos in (128 * (4 * 10 + 2) + 5, 128 * (4 * 50 + 3) + 77):
+        k[0, 0, pos] = big * qn
+    _run_custom(q, k, v, lens, [n // 2], 3, 2)
+
+
+def test_ties_and_protection():
+    """Identical keys and values give equal scores: ties must be evicted lowest position first."""
+    q, k, v, lens = _custom(1, 2, 1, 32, 640, 2, seed=4)
+    k[0, 0, 100:400] = k[0, 0, 100]
+    v[0, 0, 100:400] = v[0, 0, 100]
+    _run_custom(q, k, v, lens, [250], 1, 2)
