@@ -251,6 +251,10 @@ def main():
 
     K = args.steps
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(K)]
+    for row in evs:              # torch creates the CUDA event on its first record()
+        for e in row:
+            e.record(stream)
+    torch.cuda.synchronize()
     sampler = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local])
                            if os.environ.get("CUDA_VISIBLE_DEVICES") else local)
     sampler.start()

@@ -62,6 +62,10 @@ typedef enum {
 #define DROPKV_FLAG_BAD_K      0x08u   /* evict_k[b] outside [0, n_b - protect] */
 #define DROPKV_FLAG_OVERFLOW   0x10u   /* kept_len[b] > out_rows in dropkv_compact */
 #define DROPKV_FLAG_TIMEOUT    0x20u
+#define DROPKV_FLAG_INTERNAL   0x40u   /* a selection consistency check failed (kept count != n_b - k_b) */
+/* Detail bits that accompany DROPKV_FLAG_NONFINITE: where the value appeared. */
+#define DROPKV_FLAG_NONFINITE_STATS 0x100u  /* window statistics (normaliser or |a|^2) */
+#define DROPKV_FLAG_NONFINITE_SCORE 0x200u  /* a token score */
 
 /* Problem shape.  Supported: B >= 1; Hq % Hkv == 0; g = Hq / Hkv; R = g * w <= 64;
  * d a multiple of 8 in [8, 128]; 1 <= w <= n_max < 2^31. */
@@ -144,7 +148,8 @@ DROPKV_API dropkv_status dropkv_compact(const dropkv_shape* shape, const void* k
                              uint32_t* status, cudaStream_t stream);
 
 /* Synchronise `stream`, read the device status word and map it to a status
- * (the first of SINGULAR, NONFINITE, DEVICE_ARG, TIMEOUT that is set, else OK).
+ * (the first of SINGULAR, NONFINITE, DEVICE_ARG, TIMEOUT that is set, else OK;
+ * FLAG_INTERNAL maps to DROPKV_ERR_CUDA).
  * *flags_out (if not NULL) receives the raw word. */
 DROPKV_API dropkv_status dropkv_read_status(const uint32_t* status, cudaStream_t stream, uint32_t* flags_out);
 

@@ -312,6 +312,7 @@ dropkv_status dropkv_read_status(const uint32_t* status, cudaStream_t stream, ui
   if (f & DROPKV_FLAG_NONFINITE) return DROPKV_ERR_NONFINITE;
   if (f & (DROPKV_FLAG_BAD_LENGTH | DROPKV_FLAG_BAD_K | DROPKV_FLAG_OVERFLOW)) return DROPKV_ERR_DEVICE_ARG;
   if (f & DROPKV_FLAG_TIMEOUT) return DROPKV_ERR_TIMEOUT;
+  if (f & DROPKV_FLAG_INTERNAL) return DROPKV_ERR_CUDA;
   return DROPKV_OK;
 }
 

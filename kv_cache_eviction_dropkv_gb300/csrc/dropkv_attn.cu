@@ -7,9 +7,11 @@
 //   S^T [128 tokens x R rows] = K_tile . Q^T        (A = K, K-major; B = Q, K-major)
 //   pass 1: O^T [128 dims x R] += V_tile^T . P^T     (A = V, MN-major; B = P, MN-major)
 //   pass 2: AV^T [128 tokens x R] = V_tile . a^T     (A = V, K-major; B = a_hi, then a_lo)
-// with one TMEM lane per token (or per head dimension for O), so each of the
-// 128 softmax / score threads owns one token and needs no cross-thread
-// reduction on the hot path.
+// with one TMEM lane per token (or per head dimension for O).  Eight worker
+// warps own the 128 lanes twice over (warps w and w + 4 read lane quarter w)
+// and split the R window rows between them, so each worker thread owns one
+// token and half of the rows and needs no cross-thread reduction on the hot
+// path; a TMA warp and an MMA warp feed them through mbarrier rings.
 //
 // Method: "DropKV: Exact single-entry output-perturbation scoring", Core
 // equation (p = softmax(Kq/sqrt d), a = sum_j p_j v_j, Delta_j = p_j/(1-p_j)
@@ -28,10 +30,14 @@
 namespace dropkv {
 namespace {
 
-constexpr int kWorkers = 128;            // warps 0-3: one thread per TMEM lane
-constexpr int kThreads = 192;            // + warp 4 (TMA producer) + warp 5 (MMA issuer, TMEM owner)
+constexpr int kWorkerWarps = 8;          // warps w and w + 4 share TMEM lane quarter w and split the rows
+constexpr int kWorkers = 32 * kWorkerWarps;
+constexpr int kProducerWarp = 8;         // TMA producer
+constexpr int kMmaWarp = 9;              // MMA issuer, TMEM owner
+constexpr int kThreads = 320;
 constexpr int kTileBytes = kTile * kDPad * 2;   // 32 KB: one K or V tile, two SW128 blocks
 constexpr int kHalfTile = kTileBytes / 2;
+constexpr uint32_t kBarWork = 1, kBarAux = 2;    // named barriers among the worker warps
 // Lazy re-referencing of the running softmax maximum (log2 units): the
 // exponentials of a CTA stay relative to one reference until some logit
 // exceeds it by more than this, so e = 2^(y - ref) <= 2^24.
@@ -59,8 +65,8 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// Wait for a TMA copy to land without honouring the abort flag (used only to
-// drain copies in flight before the CTA exits).
+// Wait for a copy or MMA to land without honouring the abort flag (used only
+// to drain work in flight before the CTA exits).
 __device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
   const uint64_t t0 = global_timer_ns();
   while (!mbar_try_wait(bar, parity)) {
@@ -80,13 +86,31 @@ __device__ __forceinline__ void stage_rows_sw128(uint8_t* dst, const __nv_bfloat
   }
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(__nv_bfloat16 lo, __nv_bfloat16 hi) {
-  return (uint32_t)__bfloat16_as_ushort(lo) | ((uint32_t)__bfloat16_as_ushort(hi) << 16);
+// Two fp32 values as bf16 hi parts plus bf16 lo parts (e = hi + lo to ~2^-17).
+__device__ __forceinline__ void split_hi_lo(float e0, float e1, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(e0, e1);
+  const float2 hf = __bfloat1622float2(h);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(e0 - hf.x, e1 - hf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
+// Sum of squares of 8 packed bf16 values.
+__device__ __forceinline__ float sumsq_bf16x8(const uint4 v, float acc) {
+  const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const float lo = __uint_as_float(w4[u] << 16), hi = __uint_as_float(w4[u] & 0xFFFF0000u);
+    acc = fmaf(lo, lo, acc);
+    acc = fmaf(hi, hi, acc);
+  }
+  return acc;
 }
 
 // ============================================================== pass 1
 template <int NR>
 struct Pass1Cfg {
+  static constexpr int HR = NR / 2;                 // rows per worker half
   static constexpr int KS = NR <= 32 ? 3 : 2;       // K ring depth
   static constexpr int VS = 2;                      // V ring depth
   static constexpr int kQBytes = NR * kDPad * 2;
@@ -106,8 +130,8 @@ struct Pass1Small {
   int abort;
   int is_last;
   int pos[kMaxR];          // last key visible to row r (tail-aligned causality)
-  float mref[kMaxR];       // current exponent reference of row r (log2 units)
-  float red[4][kMaxR];     // per-warp reduction scratch
+  float mref[kMaxR];       // exponent reference of row r at the end (log2 units)
+  float red[4][kMaxR];     // per-lane-quarter reduction scratch
 };
 
 template <int NR>
@@ -136,14 +160,18 @@ __device__ void merge_unit(const AttnParams& p, int unit, float* wts, float* Ms,
     }
     Ms[tid] = M;
     Ls[tid] = L;
-    if (!(L > 0.f) || !isfinite(L)) atomicOr(p.status, DROPKV_FLAG_NONFINITE);
+    if (!(L > 0.f) || !isfinite(L)) atomicOr(p.status, DROPKV_FLAG_NONFINITE | DROPKV_FLAG_NONFINITE_STATS);
   }
   __syncthreads();
   float* a_out = p.a + (size_t)unit * R * d;
   for (int idx = tid; idx < R * d; idx += kThreads) {
     const int r = idx / d, c = idx - r * d;
     float acc = 0.f;
-    for (int s = 0; s < S; ++s) acc += po[((size_t)s * R + r) * d + c] * wts[s * R + r];
+    for (int s = 0; s < S; ++s) {
+      // splits without visible keys publish no O partial: never read it
+      const float wgt = wts[s * R + r];
+      if (wgt != 0.f) acc = fmaf(po[((size_t)s * R + r) * d + c], wgt, acc);
+    }
     a_out[idx] = acc / Ls[r];
   }
   __syncthreads();
@@ -169,15 +197,17 @@ __device__ void merge_unit(const AttnParams& p, int unit, float* wts, float* Ms,
     p.l[o] = Ls[tid];
     // exported: log-sum-exp of the natural-unit logits, log(L) + m ln 2
     p.m[o] = (Ms[tid] + log2f(Ls[tid])) * 0.69314718055994531f;
-    if (!isfinite(aa)) atomicOr(p.status, DROPKV_FLAG_NONFINITE);
+    if (!isfinite(aa)) atomicOr(p.status, DROPKV_FLAG_NONFINITE | DROPKV_FLAG_NONFINITE_STATS);
   }
 }
+
 
 template <int NR>
 __global__ void __launch_bounds__(kThreads, 1)
     window_attention_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                             const AttnParams p) {
   using C = Pass1Cfg<NR>;
+  constexpr int HR = C::HR;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
   uint8_t* sK = sm + C::kOffK;
@@ -203,8 +233,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < C::KS; ++i) { mbar_init(&S.kfull[i], 1); mbar_init(&S.kempty[i], 1); }
     for (int i = 0; i < C::VS; ++i) { mbar_init(&S.vfull[i], 1); mbar_init(&S.vempty[i], 1); }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&S.sfull[i], 1); mbar_init(&S.sempty[i], 4);
-      mbar_init(&S.pfull[i], 4); mbar_init(&S.pempty[i], 1);
+      mbar_init(&S.sfull[i], 1); mbar_init(&S.sempty[i], kWorkerWarps);
+      mbar_init(&S.pfull[i], kWorkerWarps); mbar_init(&S.pempty[i], 1);
     }
     mbar_init(&S.ofull, 1);
     mbar_init(&S.drain, 1);
@@ -216,13 +246,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     S.mref[tid] = -INFINITY;
   }
   if (T > 0) {
-    if (warp == 5) tmem_alloc(&S.tmem_base, C::kTmemCols);
+    if (warp == kMmaWarp) tmem_alloc(&S.tmem_base, C::kTmemCols);
     if (tid < kWorkers) {
       const __nv_bfloat16* qsrc = p.q + ((size_t)b * p.Hq + (size_t)h * p.g) * p.w * p.d;
       stage_rows_sw128(sQ, qsrc, NR, R, p.d, p.d, tid, kWorkers);
       fence_proxy_async_smem();
     }
-    if (warp == 4 && lane == 0) { tma_prefetch_desc(&tmk); tma_prefetch_desc(&tmv); }
+    if (warp == kProducerWarp && lane == 0) { tma_prefetch_desc(&tmk); tma_prefetch_desc(&tmv); }
   }
   tc_fence_before();
   __syncthreads();
@@ -231,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tS = tmem, tO = tmem + 2 * NR;    // S buffers at [0, 2NR), O at [2NR, 3NR)
   bool failed = false;
 
-  if (T > 0 && warp == 4) {
+  if (T > 0 && warp == kProducerWarp) {
     // ---------------------------------------------------- TMA producer
     if (lane == 0) {
       int issued_k = 0, issued_v = 0;
@@ -257,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (T > 0 && warp == 5) {
+  } else if (T > 0 && warp == kMmaWarp) {
     // ---------------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t idS = umma_idesc_bf16(128, NR, 0, 0);
@@ -307,108 +337,116 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_drain(&S.drain, 0);
     }
     __syncwarp();
-  } else if (T > 0 && warp < 4) {
+  } else if (T > 0 && warp < kWorkerWarps) {
     // ---------------------------------------------------- softmax workers
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    float lsum[NR];
+    // Thread (quarter wq, half) owns token wq*32 + lane of each tile and rows
+    // [r0, r0 + HR) of the window.
+    const int wq = warp & 3, half = warp >> 2;
+    const int tok = wq * 32 + lane;
+    const int r0 = half * HR;
+    const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+    uint32_t rowmask = 0;
 #pragma unroll
-    for (int r = 0; r < NR; ++r) lsum[r] = 0.f;
+    for (int r = 0; r < HR; ++r) rowmask |= (uint32_t)(r0 + r < R) << r;
+    const float scale = p.scale_log2;
+    const int all_see = nb - p.w;            // keys j <= all_see are visible to every row
+    float lsum[HR], mr[HR];
+#pragma unroll
+    for (int r = 0; r < HR; ++r) { lsum[r] = 0.f; mr[r] = -INFINITY; }
     for (int i = 0; i < T; ++i) {
-      const int tile = t0 + i, sb = i & 1, vs = i % C::VS;
-      const int j = tile * kTile + tid;
-      const bool tail = tile * kTile + kTile > nb;       // tile holds slots past the sequence
+      const int tile0 = (t0 + i) * kTile, sb = i & 1, vs = i % C::VS;
+      const int j = tile0 + tok;
+      const bool full = tile0 + kTile - 1 <= all_see;
+      const bool tail = tile0 + kTile > nb;       // tile holds slots past the sequence
       bool ok = mbar_wait(&S.sfull[sb], (i >> 1) & 1, &S.abort);
       if (ok && i >= 2) ok = mbar_wait(&S.pempty[sb], ((i >> 1) + 1) & 1, &S.abort);
       if (ok && tail) ok = mbar_wait(&S.vfull[vs], (i / C::VS) & 1, &S.abort);
-      if (named_bar_or(1, kWorkers, !ok)) { failed = true; break; }
+      ok = __all_sync(0xffffffffu, ok);
+      if (named_bar_or(kBarWork, kWorkers, !ok)) { failed = true; break; }
       tc_fence_after();
-      float y[NR];
-#pragma unroll
-      for (int c0 = 0; c0 < NR; c0 += 16) tmem_ld16(tS + lane_base + sb * NR + c0, &y[c0]);
+      float sraw[HR];
+      tmem_ld_cols<HR>(tS + lane_base + sb * NR + r0, sraw);
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.sempty[sb]);
 
-      uint64_t vis = 0;
+      uint32_t vis = rowmask;
+      if (!full) {
+        uint32_t v = 0;
+        if (j < nb) {
+#pragma unroll
+          for (int r = 0; r < HR; ++r) v |= (uint32_t)(j <= S.pos[r0 + r]) << r;
+        }
+        vis &= v;
+      }
+      float rel[HR];
       bool need = false;
 #pragma unroll
-      for (int r = 0; r < NR; ++r) {
-        y[r] *= p.scale_log2;
-        const bool v_r = (j < nb) && (j <= S.pos[r]);
-        vis |= (uint64_t)v_r << r;
-        need |= v_r && (y[r] - S.mref[r] > kRescaleLog2);
+      for (int r = 0; r < HR; ++r) {
+        rel[r] = fmaf(sraw[r], scale, -mr[r]);
+        need |= ((vis >> r) & 1u) && rel[r] > kRescaleLog2;
       }
-      if (named_bar_or(1, kWorkers, need)) {
+      if (named_bar_or(kBarWork, kWorkers, need)) {
         // new reference = max(old reference, this tile's max) per row
 #pragma unroll
-        for (int r = 0; r < NR; ++r) {
-          const float v = ((vis >> r) & 1) ? y[r] : -INFINITY;
+        for (int r = 0; r < HR; ++r) {
+          const float v = ((vis >> r) & 1u) ? sraw[r] * scale : -INFINITY;
           const uint32_t u = __reduce_max_sync(0xffffffffu, f2ord(v));
-          if (lane == 0) S.red[warp][r] = ord2f(u);
+          if (lane == 0) S.red[wq][r0 + r] = ord2f(u);
         }
-        named_bar(2, kWorkers);                 // per-warp maxima complete
-        float factor[NR];
-        float my_ref = 0.f;                     // new reference of row `tid` (tid < NR)
+        named_bar(kBarAux, kWorkers);
+        float factor[HR];
 #pragma unroll
-        for (int r = 0; r < NR; ++r) {
-          const float old = S.mref[r];
-          const float nm = fmaxf(fmaxf(fmaxf(S.red[0][r], S.red[1][r]), fmaxf(S.red[2][r], S.red[3][r])), old);
-          factor[r] = (old == -INFINITY) ? 0.f : exp2f(old - nm);
+        for (int r = 0; r < HR; ++r) {
+          const int rr = r0 + r;
+          const float nm = fmaxf(fmaxf(fmaxf(S.red[0][rr], S.red[1][rr]), fmaxf(S.red[2][rr], S.red[3][rr])), mr[r]);
+          factor[r] = (mr[r] == -INFINITY) ? 0.f : ex2_approx(mr[r] - nm);
           lsum[r] *= factor[r];
-          if (r == tid) my_ref = nm;
+          mr[r] = nm;
+          rel[r] = fmaf(sraw[r], scale, -nm);
         }
         if (i > 0) {
-          // rescale the accumulated O (lane = head dimension) once PV of tile i-1 is done
-          const bool okw = mbar_wait(&S.ofull, (i - 1) & 1, &S.abort);
-          if (named_bar_or(2, kWorkers, !okw)) { failed = true; break; }
+          // rescale the accumulated O (lane = head dimension) once PV of tile i-1 is
+          // done; PV(i-2) is known complete (pempty), so ofull is at most one phase
+          // behind and the parity wait is unambiguous
+          bool okw = mbar_wait(&S.ofull, (i - 1) & 1, &S.abort);
+          okw = __all_sync(0xffffffffu, okw);
+          if (named_bar_or(kBarAux, kWorkers, !okw)) { failed = true; break; }
           tc_fence_after();
+          float o[HR];
+          tmem_ld_cols<HR>(tO + lane_base + r0, o);
+          tmem_wait_ld();
 #pragma unroll
-          for (int c0 = 0; c0 < NR; c0 += 16) {
-            float o[16];
-            tmem_ld16(tO + lane_base + c0, o);
-            tmem_wait_ld();
-#pragma unroll
-            for (int q = 0; q < 16; ++q) o[q] *= factor[c0 + q];
-            tmem_st16(tO + lane_base + c0, o);
-          }
+          for (int r = 0; r < HR; ++r) o[r] *= factor[r];
+          tmem_st_cols<HR>(tO + lane_base + r0, o);
           tmem_wait_st();
           tc_fence_before();
         }
-        named_bar(2, kWorkers);                 // every thread has read the old references
-        if (tid < NR) S.mref[tid] = my_ref;
-        named_bar(2, kWorkers);                 // new references visible
       }
       // exponentials relative to the row reference, split into bf16 hi + lo
       uint8_t* phi = sP + (sb * 2 + 0) * C::kPBytes;
       uint8_t* plo = sP + (sb * 2 + 1) * C::kPBytes;
 #pragma unroll
-      for (int r8 = 0; r8 < NR / 8; ++r8) {
+      for (int c8 = 0; c8 < HR / 8; ++c8) {
         uint32_t hp[4], lp[4];
 #pragma unroll
-        for (int q = 0; q < 8; q += 2) {
-          float e2[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int r = r8 * 8 + q + u;
-            const float e = ((vis >> r) & 1) ? exp2f(y[r] - S.mref[r]) : 0.f;
-            lsum[r] += e;
-            e2[u] = e;
-          }
-          const __nv_bfloat16 h0 = __float2bfloat16_rn(e2[0]), h1 = __float2bfloat16_rn(e2[1]);
-          const __nv_bfloat16 l0 = __float2bfloat16_rn(e2[0] - __bfloat162float(h0));
-          const __nv_bfloat16 l1 = __float2bfloat16_rn(e2[1] - __bfloat162float(h1));
-          hp[q >> 1] = pack_bf16x2(h0, h1);
-          lp[q >> 1] = pack_bf16x2(l0, l1);
+        for (int q = 0; q < 4; ++q) {
+          const int r = c8 * 8 + 2 * q;
+          const float e0 = ((vis >> r) & 1u) ? ex2_approx(rel[r]) : 0.f;
+          const float e1 = ((vis >> (r + 1)) & 1u) ? ex2_approx(rel[r + 1]) : 0.f;
+          lsum[r] += e0;
+          lsum[r + 1] += e1;
+          split_hi_lo(e0, e1, hp[q], lp[q]);
         }
-        const uint32_t off = interleave_mn_offset(tid, r8 * 8, NR);
+        const uint32_t off = interleave_mn_offset(tok, r0 + c8 * 8, NR);
         *reinterpret_cast<uint4*>(phi + off) = make_uint4(hp[0], hp[1], hp[2], hp[3]);
         *reinterpret_cast<uint4*>(plo + off) = make_uint4(lp[0], lp[1], lp[2], lp[3]);
       }
-      if (tail && j >= nb) {
+      if (tail && half == 0 && j >= nb) {
         // slots past the sequence may hold anything (NaN): zero their V rows
         // so that 0 * NaN never reaches the PV accumulator
-        uint8_t* vrow = sV + vs * kTileBytes + tid * 128;
+        uint8_t* vrow = sV + vs * kTileBytes + tok * 128;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           *reinterpret_cast<uint4*>(vrow + c * 16) = make_uint4(0, 0, 0, 0);
@@ -420,30 +458,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&S.pfull[sb]);
     }
     // ------------------------------------------------ partial state of this split
+    // The MMA warp commits `drain` once, after its last MMA: a single-phase
+    // wait.  (A parity wait on the per-tile `ofull` barrier would be ambiguous
+    // here, since up to two PV commits may still be outstanding.)
     bool okw = true;
-    if (!failed) okw = mbar_wait(&S.ofull, (T - 1) & 1, &S.abort);
-    if (named_bar_or(1, kWorkers, failed || !okw)) failed = true;
+    if (!failed) okw = mbar_wait(&S.drain, 0, &S.abort);
+    okw = __all_sync(0xffffffffu, okw);
+    if (named_bar_or(kBarWork, kWorkers, failed || !okw)) failed = true;
     const size_t part = (size_t)unit * p.splits + split;
     if (!failed) {
       tc_fence_after();
+      float o[HR];
+      tmem_ld_cols<HR>(tO + lane_base + r0, o);
+      tmem_wait_ld();
       float* po = p.part_o + part * R * p.d;
 #pragma unroll
-      for (int c0 = 0; c0 < NR; c0 += 16) {
-        float o[16];
-        tmem_ld16(tO + lane_base + c0, o);
-        tmem_wait_ld();
-#pragma unroll
-        for (int q = 0; q < 16; ++q)
-          if (c0 + q < R && tid < p.d) po[(size_t)(c0 + q) * p.d + tid] = o[q];
-      }
+      for (int r = 0; r < HR; ++r)
+        if (r0 + r < R && tok < p.d) po[(size_t)(r0 + r) * p.d + tok] = o[r];
       tc_fence_before();
     }
 #pragma unroll
-    for (int r = 0; r < NR; ++r) {
+    for (int r = 0; r < HR; ++r) {
       const float v = warp_sum(lsum[r]);
-      if (lane == 0) S.red[warp][r] = v;
+      if (lane == 0) S.red[wq][r0 + r] = v;
     }
-    named_bar(2, kWorkers);
+    if (wq == 0 && lane == 0) {
+#pragma unroll
+      for (int r = 0; r < HR; ++r) S.mref[r0 + r] = mr[r];
+    }
+    named_bar(kBarAux, kWorkers);
     if (tid < R) {
       float* ml = p.part_ml + (part * R + tid) * 2;
       ml[0] = S.mref[tid];
@@ -462,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (T > 0 && warp == 5) {
+  if (T > 0 && warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
@@ -487,6 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ============================================================== pass 2
 template <int NR>
 struct Pass2Cfg {
+  static constexpr int HR = NR / 2;
   static constexpr int KS = 3;
   static constexpr int VS = NR <= 32 ? 3 : 2;
   static constexpr int kQBytes = NR * kDPad * 2;
@@ -504,8 +548,8 @@ struct Pass2Small {
   uint64_t accfull[2], accempty[2], drain;
   uint32_t tmem_base;
   int abort;
-  int pos[kMaxR];
-  float m2[kMaxR], L[kMaxR], aa[kMaxR];
+  float4 rowc[kMaxR];        // per row: (max in log2 units, normaliser L, |a|^2, last visible key as int bits)
+  float4 xch[2][kTile];      // upper-half partials per token (sum r^2 (|a|^2 - 2 a.v), sum r^2, |v|^2 part, singular)
 };
 
 template <int NR>
@@ -518,6 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                  const AttnParams p) {
   using C = Pass2Cfg<NR>;
+  constexpr int HR = C::HR;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
   uint8_t* sK = sm + C::kOffK;
@@ -540,13 +585,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     for (int i = 0; i < C::KS; ++i) { mbar_init(&S.kfull[i], 1); mbar_init(&S.kempty[i], 1); }
-    for (int i = 0; i < C::VS; ++i) { mbar_init(&S.vfull[i], 1); mbar_init(&S.vempty[i], 5); }
-    for (int i = 0; i < 2; ++i) { mbar_init(&S.accfull[i], 1); mbar_init(&S.accempty[i], 4); }
+    for (int i = 0; i < C::VS; ++i) { mbar_init(&S.vfull[i], 1); mbar_init(&S.vempty[i], kWorkerWarps + 1); }
+    for (int i = 0; i < 2; ++i) { mbar_init(&S.accfull[i], 1); mbar_init(&S.accempty[i], kWorkerWarps); }
     mbar_init(&S.drain, 1);
     S.abort = 0;
     fence_mbar_init();
   }
-  if (warp == 5) tmem_alloc(&S.tmem_base, C::kTmemCols);
+  if (warp == kMmaWarp) tmem_alloc(&S.tmem_base, C::kTmemCols);
   if (tid < kWorkers) {
     const __nv_bfloat16* qsrc = p.q + ((size_t)b * p.Hq + (size_t)h * p.g) * p.w * p.d;
     stage_rows_sw128(sQ, qsrc, NR, R, p.d, p.d, tid, kWorkers);
@@ -556,21 +601,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_proxy_async_smem();
     if (tid < kMaxR) {
       const bool real = tid < R;
-      S.pos[tid] = real ? nb - p.w + (tid % p.w) : -1;
       const size_t o = (size_t)unit * R + tid;
-      S.m2[tid] = real ? p.m2[o] : 0.f;
-      S.L[tid] = real ? p.l[o] : 1.f;
-      S.aa[tid] = real ? p.aa[o] : 0.f;
+      S.rowc[tid] = make_float4(real ? p.m2[o] : 0.f, real ? p.l[o] : 1.f, real ? p.aa[o] : 0.f,
+                                __int_as_float(real ? nb - p.w + (tid % p.w) : -1));
     }
   }
-  if (warp == 4 && lane == 0) { tma_prefetch_desc(&tmk); tma_prefetch_desc(&tmv); }
+  if (warp == kProducerWarp && lane == 0) { tma_prefetch_desc(&tmk); tma_prefetch_desc(&tmv); }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = S.tmem_base;
   bool failed = false;
 
-  if (warp == 4) {
+  if (warp == kProducerWarp) {
     if (lane == 0) {
       int issued_k = 0, issued_v = 0;
       for (int i = 0; i < T; ++i) {
@@ -595,7 +638,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
     if (lane == 0) {
       const uint32_t idS = umma_idesc_bf16(128, NR, 0, 0);
       const uint32_t qaddr = smem_addr(sQ), ahi = smem_addr(sAhi), alo = smem_addr(sAlo);
@@ -632,67 +675,88 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_drain(&S.drain, 0);
     }
     __syncwarp();
-  } else {
+  } else if (warp < kWorkerWarps) {
     // ---------------------------------------------------- score workers
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    // Thread (quarter wq, half) owns token wq*32 + lane, rows [r0, r0 + HR)
+    // and columns [64 half, 64 half + 64) of |v|^2; the upper half hands its
+    // partial sums to the lower half, which writes the score.
+    //   s = (1/g) sum_r r_r^2 (|a_r|^2 - 2 a_r.v + |v|^2),  r_r = e / (L_r - e) = p/(1-p)
+    const int wq = warp & 3, half = warp >> 2;
+    const int tok = wq * 32 + lane;
+    const int r0 = half * HR;
+    const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+    uint32_t rowmask = 0;
+#pragma unroll
+    for (int r = 0; r < HR; ++r) rowmask |= (uint32_t)(r0 + r < R) << r;
+    const float scale = p.scale_log2;
     const float inv_g = 1.0f / (float)p.g;
+    const int all_see = nb - p.w;
     float* raw = p.raw + (size_t)unit * p.n_max;
     uint32_t flags = 0;
     for (int i = 0; i < T; ++i) {
-      const int tile = t0 + i, vs = i % C::VS, ab = i & 1;
-      const int j = tile * kTile + tid;
-      // |v_j|^2 from the staged V row (order of the 128 columns is irrelevant)
+      const int tile0 = (t0 + i) * kTile, vs = i % C::VS, ab = i & 1;
+      const int j = tile0 + tok;
+      const bool full = tile0 + kTile - 1 <= all_see;
       bool ok = mbar_wait(&S.vfull[vs], (i / C::VS) & 1, &S.abort);
-      float vv = 0.f;
+      float vvh = 0.f;
       if (ok) {
-        const uint8_t* vrow = sV + vs * kTileBytes + tid * 128;
+        // this half's 64 columns of the staged V row; chunks visited in a
+        // per-thread rotated order so a warp's reads spread over all banks
+        const uint8_t* vrow = sV + vs * kTileBytes + half * kHalfTile + tok * 128;
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const uint4 raw4 = *reinterpret_cast<const uint4*>(vrow + (c >> 3) * kHalfTile + (c & 7) * 16);
-          const uint32_t w4[4] = {raw4.x, raw4.y, raw4.z, raw4.w};
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const float lo = __uint_as_float(w4[u] << 16), hi = __uint_as_float(w4[u] & 0xFFFF0000u);
-            vv = fmaf(lo, lo, vv);
-            vv = fmaf(hi, hi, vv);
-          }
-        }
+        for (int c = 0; c < 8; ++c)
+          vvh = sumsq_bf16x8(*reinterpret_cast<const uint4*>(vrow + ((c + tok) & 7) * 16), vvh);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.vempty[vs]);
       if (ok) ok = mbar_wait(&S.accfull[ab], (i >> 1) & 1, &S.abort);
-      if (!ok) { failed = true; break; }      // no named barriers in this role: exit per thread
-      tc_fence_after();
-      float sv[NR], av[NR];
+      ok = __all_sync(0xffffffffu, ok);
+      float A = 0.f, W = 0.f;
+      bool singular = false;
+      if (ok) {
+        tc_fence_after();
+        float sv[HR], av[HR];
+        tmem_ld_cols<HR>(tmem + lane_base + ab * 2 * NR + r0, sv);
+        tmem_ld_cols<HR>(tmem + lane_base + ab * 2 * NR + NR + r0, av);
+        tmem_wait_ld();
+        tc_fence_before();
+        uint32_t vis = rowmask;
+        if (!full) {
+          uint32_t v = 0;
+          if (j < nb) {
 #pragma unroll
-      for (int c0 = 0; c0 < NR; c0 += 16) {
-        tmem_ld16(tmem + lane_base + ab * 2 * NR + c0, &sv[c0]);
-        tmem_ld16(tmem + lane_base + ab * 2 * NR + NR + c0, &av[c0]);
-      }
-      tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&S.accempty[ab]);
-      if (j < nb) {
-        float s = 0.f;
-        bool singular = false;
+            for (int r = 0; r < HR; ++r) v |= (uint32_t)(j <= __float_as_int(S.rowc[r0 + r].w)) << r;
+          }
+          vis &= v;
+        }
 #pragma unroll
-        for (int r = 0; r < NR; ++r) {
-          if (j <= S.pos[r]) {
-            const float e = exp2f(sv[r] * p.scale_log2 - S.m2[r]);
-            const float den = S.L[r] - e;           // l (1 - p_j)
-            if (!(den > 0.f)) singular = true;
-            const float ratio = __fdividef(e, den);  // p_j / (1 - p_j)
-            const float dist = fmaxf(fmaf(-2.f, av[r], S.aa[r] + vv), 0.f);   // |a - v_j|^2
-            s = fmaf(ratio * ratio, dist, s);
+        for (int r = 0; r < HR; ++r) {
+          if ((vis >> r) & 1u) {
+            const float4 c = S.rowc[r0 + r];
+            const float e = ex2_approx(fmaf(sv[r], scale, -c.x));
+            const float den = c.y - e;                 // L (1 - p_j)
+            singular |= !(den > 0.f);
+            const float ratio = e * rcp_approx(den);   // p_j / (1 - p_j)
+            const float q = ratio * ratio;
+            A = fmaf(q, fmaf(-2.f, av[r], c.z), A);
+            W += q;
           }
         }
-        s *= inv_g;
-        if (singular) {
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.accempty[ab]);
+      if (half == 1) S.xch[ab][tok] = make_float4(A, W, vvh, singular ? 1.f : 0.f);
+      if (named_bar_or(kBarWork, kWorkers, !ok)) { failed = true; break; }
+      if (half == 0 && j < nb) {
+        const float4 o = S.xch[ab][tok];
+        float s = fmaf(vvh + o.z, W + o.y, A + o.x);
+        if (singular || o.w != 0.f) {
           s = INFINITY;
           flags |= DROPKV_FLAG_SINGULAR;
         } else if (!isfinite(s)) {
-          flags |= DROPKV_FLAG_NONFINITE;
+          flags |= DROPKV_FLAG_NONFINITE | DROPKV_FLAG_NONFINITE_SCORE;
+        } else {
+          s = fmaxf(s, 0.f) * inv_g;   // the exact value is >= 0; rounding may not make it negative
         }
         raw[j] = s;
       }
@@ -702,7 +766,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (failed) S.abort = 1;
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }

@@ -310,7 +310,7 @@ __global__ void __launch_bounds__(kSelThreads) select_cand_kernel(const SelParam
     st[kStKey] = (uint32_t)(thr >> 32);
     st[kStIdx] = (uint32_t)(thr & 0xFFFFFFFFu);
     const uint32_t expect = (uint32_t)(ui.nb - (mode == kModeNormal ? ui.kb : 0));
-    if (carry != expect) atomicOr(p.status, DROPKV_FLAG_NONFINITE);
+    if (carry != expect) atomicOr(p.status, DROPKV_FLAG_INTERNAL);
     p.tickets[unit * 2 + 1] = 0;
   }
 }
