@@ -119,6 +119,27 @@ DROPKV_API dropkv_status dropkv_score_timed(const dropkv_shape* shape, const voi
                                             size_t workspace_bytes, uint32_t* status, cudaStream_t stream,
                                             cudaEvent_t* phase_events);
 
+/* dropkv_score without a workspace argument, for callers that cannot allocate
+ * device memory when they score (a host framework that owns all device memory
+ * through its own pool, or a serving loop that forbids allocations after
+ * start-up).  The paper has no counterpart: this is a deployment variant.
+ *   Scratch: a fixed 16 MiB device array inside the library (held by every GPU
+ *   that loads it until exit), enough for the scoring scratch of every shape
+ *   whose dropkv_workspace_size() scoring part fits (for example B=1, Hkv=8,
+ *   n=128K).  Larger shapes return DROPKV_ERR_WORKSPACE and launch nothing.
+ *   Nothing is allocated: no cudaMalloc, no cudaFree, no allocating library call.
+ *   The first call on a device looks up the array's device address (once per
+ *   device, with that device current); make that first call before any stream
+ *   capture.
+ *   All calls share the array and it keeps the last call's contents: calls
+ *   that overlap on the GPU (concurrent streams, other threads) race and must
+ *   be serialised by the caller.  The window statistics are not exported.
+ * Arguments, outputs and status word are as for dropkv_score. */
+DROPKV_API dropkv_status dropkv_score_noalloc(const dropkv_shape* shape, const void* q_window, const void* k,
+                                              const void* v, const int32_t* lengths, int32_t pool_kernel,
+                                              int32_t protect, float* scores, float* raw_scores, uint32_t* status,
+                                              cudaStream_t stream);
+
 /* Step S6: evict the evict_k[b] lowest scores of every KV head (equal scores:
  * the lower position is evicted first) and list the kept positions.
  *   scores    device float [B][Hkv][n_max] (as written by dropkv_score)

@@ -59,6 +59,8 @@ def lib():
             L.dropkv_score.restype = ctypes.c_int
             L.dropkv_score_timed.argtypes = [SH, P, P, P, P, I32, I32, P, P, P, SZ, P, P, P]
             L.dropkv_score_timed.restype = ctypes.c_int
+            L.dropkv_score_noalloc.argtypes = [SH, P, P, P, P, I32, I32, P, P, P, P]
+            L.dropkv_score_noalloc.restype = ctypes.c_int
             L.dropkv_select.argtypes = [SH, P, P, P, I32, P, P, P, SZ, P, P]
             L.dropkv_select.restype = ctypes.c_int
             L.dropkv_compact.argtypes = [SH, P, P, P, P, I32, P, P, P, P]
@@ -126,6 +128,15 @@ def dropkv_score_timed(shape, q_window, k, v, lengths, pool_kernel, protect, sco
                                     _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(status),
                                     _stream(stream), arr)
     return _check(code, "dropkv_score_timed")
+
+
+def dropkv_score_noalloc(shape, q_window, k, v, lengths, pool_kernel, protect, scores, raw_scores, status,
+                         stream=None):
+    """dropkv_score with the library's fixed scratch array instead of a workspace (allocates nothing)."""
+    code = lib().dropkv_score_noalloc(ctypes.byref(shape), _ptr(q_window), _ptr(k), _ptr(v), _ptr(lengths),
+                                      int(pool_kernel), int(protect), _ptr(scores), _ptr(raw_scores),
+                                      _ptr(status), _stream(stream))
+    return _check(code, "dropkv_score_noalloc")
 
 
 def dropkv_select(shape, scores, lengths, evict_k, protect, kept_idx, kept_len, workspace, status, stream=None):

@@ -16,8 +16,8 @@ def test_library_exports_every_declared_symbol():
     path = _build.build_library()
     lib = ctypes.CDLL(path)
     declared = B.declared_functions()
-    assert set(declared) == {"dropkv_workspace_size", "dropkv_score", "dropkv_score_timed", "dropkv_select",
-                             "dropkv_compact", "dropkv_read_status", "dropkv_version"}
+    assert set(declared) == {"dropkv_workspace_size", "dropkv_score", "dropkv_score_timed", "dropkv_score_noalloc",
+                             "dropkv_select", "dropkv_compact", "dropkv_read_status", "dropkv_version"}
     for name in declared:
         assert hasattr(lib, name), name
     out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True, check=True).stdout
