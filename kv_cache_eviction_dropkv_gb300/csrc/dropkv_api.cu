@@ -120,10 +120,10 @@ WsPlan make_plan(const Geom& g) {
   w.ahl = take((size_t)g.U * 2 * kMaxR * kDPad * 2);
   w.part_o = take((size_t)g.U * g.splits1 * g.R * g.d * 4);
   w.part_ml = take((size_t)g.U * g.splits1 * g.R * 2 * 4);
-  w.tickets = take((size_t)g.U * 4);
   w.raw = take((size_t)g.U * g.n_max * 4);
   w.sel_zero_begin = off;
   w.hist = take((size_t)g.U * kHistBins * 4);
+  w.hist2 = take((size_t)g.U * kHistBins * 4);
   w.cand_cnt = take((size_t)g.U * 4);
   w.sel_tickets = take((size_t)g.U * 2 * 4);
   w.chunk_kept = take((size_t)g.U * g.chunks * 4);
@@ -194,11 +194,9 @@ dropkv_status score_impl(const dropkv_shape* shape, const void* q_window, const 
   p.ahl = reinterpret_cast<__nv_bfloat16*>(ws + w.ahl);
   p.part_o = reinterpret_cast<float*>(ws + w.part_o);
   p.part_ml = reinterpret_cast<float*>(ws + w.part_ml);
-  p.tickets = reinterpret_cast<uint32_t*>(ws + w.tickets);
   p.raw = raw_scores ? raw_scores : reinterpret_cast<float*>(ws + w.raw);
   p.status = status;
 
-  if (cudaMemsetAsync(p.tickets, 0, (size_t)g.U * 4, stream) != cudaSuccess) return DROPKV_ERR_CUDA;
   if (ev && cudaEventRecord(ev[0], stream) != cudaSuccess) return DROPKV_ERR_CUDA;
   p.splits = g.splits1;
   p.tpc = g.tpc1;
@@ -265,6 +263,7 @@ dropkv_status dropkv_select(const dropkv_shape* shape, const float* scores, cons
   p.kept_len = kept_len;
   p.B = g.B; p.Hkv = g.Hkv; p.n_max = g.n_max; p.protect = protect; p.chunks = g.chunks;
   p.hist = reinterpret_cast<uint32_t*>(ws + w.hist);
+  p.hist2 = reinterpret_cast<uint32_t*>(ws + w.hist2);
   p.state = reinterpret_cast<uint32_t*>(ws + w.sel_state);
   p.cand = reinterpret_cast<uint32_t*>(ws + w.cand);
   p.cand_cnt = reinterpret_cast<uint32_t*>(ws + w.cand_cnt);

@@ -1,4 +1,4 @@
-// Pass 1 (window attention with split-K and a last-CTA merge) and pass 2
+// Pass 1 (window attention with split-K, then a merge of the splits) and pass 2
 // (streaming per-token perturbation score) of the DropKV scoring path.
 //
 // Both passes stream 128-token K/V tiles of one KV head through TMA into
@@ -107,28 +107,51 @@ __device__ __forceinline__ float sumsq_bf16x8(const uint4 v, float acc) {
   return acc;
 }
 
+// TMA producer of one ring: streams the tiles [t0, t0 + T) of one tensor into
+// a ring of DEPTH 32 KB stages.  K and V rings are driven by different lanes
+// of the producer warp, so each can run ahead of the consumers by its own depth.
+template <int DEPTH>
+__device__ __forceinline__ void stream_ring(uint8_t* ring, uint64_t* full, uint64_t* empty, const CUtensorMap* map,
+                                            int t0, int T, int unit, volatile int* abort, uint32_t* status) {
+  int issued = 0;
+  bool ok = true;
+  for (int i = 0; i < T; ++i) {
+    const int s = i % DEPTH;
+    if (i >= DEPTH && !mbar_wait(&empty[s], ((i / DEPTH) + 1) & 1, abort)) { ok = false; break; }
+    mbar_arrive_expect_tx(&full[s], kTileBytes);
+    tma_load_3d(ring + s * kTileBytes, map, &full[s], 0, (t0 + i) * kTile, unit);
+    tma_load_3d(ring + s * kTileBytes + kHalfTile, map, &full[s], 64, (t0 + i) * kTile, unit);
+    ++issued;
+  }
+  if (!ok) {
+    *abort = 1;
+    atomicOr(status, DROPKV_FLAG_TIMEOUT);
+    for (int i = max(0, issued - DEPTH); i < issued; ++i) mbar_drain(&full[i % DEPTH], (i / DEPTH) & 1);
+  }
+}
+
 // ============================================================== pass 1
 template <int NR>
 struct Pass1Cfg {
   static constexpr int HR = NR / 2;                 // rows per worker half
-  static constexpr int KS = NR <= 32 ? 3 : 2;       // K ring depth
-  static constexpr int VS = 2;                      // V ring depth
+  static constexpr int KS = NR <= 16 ? 3 : 2;       // K ring depth (K is released right after S = K Q^T)
+  static constexpr int VS = 3;                      // V ring depth (V is held until PV completes)
+  static constexpr int PB = NR <= 32 ? 2 : 1;       // P buffers
   static constexpr int kQBytes = NR * kDPad * 2;
   static constexpr int kPBytes = kTile * NR * 2;    // one of (hi, lo) of one P buffer
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + KS * kTileBytes;
   static constexpr int kOffQ = kOffV + VS * kTileBytes;
-  static constexpr int kOffP = kOffQ + kQBytes;     // [buffer 0, 1][hi, lo]
-  static constexpr int kOffSmall = kOffP + 4 * kPBytes;
+  static constexpr int kOffP = kOffQ + kQBytes;     // [buffer][hi, lo]
+  static constexpr int kOffSmall = kOffP + 2 * PB * kPBytes;
   static constexpr uint32_t kTmemCols = (3 * NR <= 64) ? 64u : (3 * NR <= 128 ? 128u : 256u);
 };
 
 struct Pass1Small {
-  uint64_t kfull[3], kempty[3], vfull[2], vempty[2];
+  uint64_t kfull[3], kempty[3], vfull[3], vempty[3];
   uint64_t sfull[2], sempty[2], pfull[2], pempty[2], ofull, drain;
   uint32_t tmem_base;
   int abort;
-  int is_last;
   int pos[kMaxR];          // last key visible to row r (tail-aligned causality)
   float mref[kMaxR];       // exponent reference of row r at the end (log2 units)
   float red[4][kMaxR];     // per-lane-quarter reduction scratch
@@ -139,68 +162,102 @@ constexpr int pass1_smem_bytes() {
   return Pass1Cfg<NR>::kOffSmall + (int)sizeof(Pass1Small) + 1024;
 }
 
-// Merge the split-K partial states of one KV head (executed by the last CTA).
-// m = max_s m_s;  L = sum_s l_s 2^(m_s - m);  a = sum_s O_s 2^(m_s - m) / L.
-__device__ void merge_unit(const AttnParams& p, int unit, float* wts, float* Ms, float* Ls, int tid) {
-  const int S = p.splits, R = p.R, d = p.d;
-  const float* ml = p.part_ml + (size_t)unit * S * R * 2;
-  const float* po = p.part_o + (size_t)unit * S * R * d;
-  if (tid < R) {
-    float M = -INFINITY;
-    for (int s = 0; s < S; ++s) {
-      const float ls = ml[((size_t)s * R + tid) * 2 + 1];
-      if (ls > 0.f) M = fmaxf(M, ml[((size_t)s * R + tid) * 2]);
-    }
-    float L = 0.f;
-    for (int s = 0; s < S; ++s) {
-      const float ms = ml[((size_t)s * R + tid) * 2], ls = ml[((size_t)s * R + tid) * 2 + 1];
-      const float wgt = (ls > 0.f) ? exp2f(ms - M) : 0.f;
-      wts[s * R + tid] = wgt;
-      L += ls * wgt;
-    }
-    Ms[tid] = M;
-    Ls[tid] = L;
-    if (!(L > 0.f) || !isfinite(L)) atomicOr(p.status, DROPKV_FLAG_NONFINITE | DROPKV_FLAG_NONFINITE_STATS);
-  }
-  __syncthreads();
-  float* a_out = p.a + (size_t)unit * R * d;
-  for (int idx = tid; idx < R * d; idx += kThreads) {
-    const int r = idx / d, c = idx - r * d;
-    float acc = 0.f;
-    for (int s = 0; s < S; ++s) {
-      // splits without visible keys publish no O partial: never read it
-      const float wgt = wts[s * R + r];
-      if (wgt != 0.f) acc = fmaf(po[((size_t)s * R + r) * d + c], wgt, acc);
-    }
-    a_out[idx] = acc / Ls[r];
-  }
-  __syncthreads();
-  // |a|^2, the hi/lo bf16 split of a (zero-padded to [NR pad 64][128]), and the stats
+// Merge of the split-K partial states (its own small kernel: it sits on the
+// critical path, so it is spread over many CTAs with all loads in flight).
+//   m = max_s m_s;  L = sum_s l_s 2^(m_s - m);  a = sum_s O_s 2^(m_s - m) / L.
+// CTA (row group, KV head): warp w takes row r = 4 * group + w, lane c the
+// float4 column c of a; every split of that column is loaded before any is
+// used.  Also writes |a|^2, the bf16 hi/lo split of a (zero rows past R and
+// zero columns past d) and the exported log-sum-exp.
+constexpr int kMergeRows = 4;                 // rows per CTA (one warp each)
+constexpr int kMergeThreads = 32 * kMergeRows;
+constexpr int kMergeBatch = 32;               // splits loaded ahead per lane
+
+__global__ void __launch_bounds__(kMergeThreads) merge_splits_kernel(const AttnParams p) {
+  __shared__ float wts_s[kMergeRows][kMergeBatch];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int unit = blockIdx.y, r = blockIdx.x * kMergeRows + warp;
+  const int b = unit / p.Hkv;
+  const int nb = p.lengths ? p.lengths[b] : p.n_max;
+  if (nb < p.w || nb > p.n_max) return;          // flagged by pass 1
+  const int S = p.splits, R = p.R, d = p.d, D4 = d >> 2;
   __nv_bfloat16* ahl = p.ahl + (size_t)unit * 2 * kMaxR * kDPad;
-  for (int idx = tid; idx < kMaxR * kDPad; idx += kThreads) {
-    const int r = idx / kDPad, c = idx - r * kDPad;
-    const float x = (r < R && c < d) ? a_out[r * d + c] : 0.f;
-    const __nv_bfloat16 hi = __float2bfloat16_rn(x);
-    const __nv_bfloat16 lo = __float2bfloat16_rn(x - __bfloat162float(hi));
-    ahl[idx] = hi;
-    ahl[kMaxR * kDPad + idx] = lo;
+  if (r >= R) {
+    // padding rows of the MMA operand: zero (32 lanes x 4 columns = 128)
+    reinterpret_cast<uint2*>(ahl + (size_t)r * kDPad)[lane] = make_uint2(0u, 0u);
+    reinterpret_cast<uint2*>(ahl + (size_t)(kMaxR + r) * kDPad)[lane] = make_uint2(0u, 0u);
+    return;
   }
-  if (tid < R) {
-    float aa = 0.f;
-    for (int c = 0; c < d; ++c) {
-      const float x = a_out[tid * d + c];
-      aa = fmaf(x, x, aa);
+  const float2* ml = reinterpret_cast<const float2*>(p.part_ml) + (size_t)unit * S * R;
+  // row maximum and normaliser over the splits (lanes stride the splits)
+  float M = -INFINITY;
+  for (int s = lane; s < S; s += 32) {
+    const float2 v = __ldcg(ml + (size_t)s * R + r);
+    if (v.y > 0.f) M = fmaxf(M, v.x);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float L = 0.f;
+  for (int s = lane; s < S; s += 32) {
+    const float2 v = __ldcg(ml + (size_t)s * R + r);
+    if (v.y > 0.f) L = fmaf(v.y, exp2f(v.x - M), L);
+  }
+  L = warp_sum(L);
+  // a for this lane's float4 column
+  const float4* po4 = reinterpret_cast<const float4*>(p.part_o + (size_t)unit * S * R * d);
+  const size_t split_stride = (size_t)R * D4;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s0 = 0; s0 < S; s0 += kMergeBatch) {
+    // weights of this batch of splits (0 for splits without visible keys,
+    // whose O partial is never written and so never read)
+    {
+      const int s = s0 + lane;
+      float wgt = 0.f;
+      if (s < S) {
+        const float2 v = __ldcg(ml + (size_t)s * R + r);
+        wgt = (v.y > 0.f) ? exp2f(v.x - M) : 0.f;
+      }
+      wts_s[warp][lane] = wgt;
     }
-    const size_t o = (size_t)unit * R + tid;
+    __syncwarp();
+    float4 o[kMergeBatch];
+#pragma unroll
+    for (int u = 0; u < kMergeBatch; ++u)
+      o[u] = (lane < D4 && s0 + u < S && wts_s[warp][u] != 0.f)
+                 ? __ldcg(po4 + (size_t)(s0 + u) * split_stride + (size_t)r * D4 + lane)
+                 : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int u = 0; u < kMergeBatch; ++u) {
+      const float wgt = wts_s[warp][u];
+      acc.x = fmaf(o[u].x, wgt, acc.x);
+      acc.y = fmaf(o[u].y, wgt, acc.y);
+      acc.z = fmaf(o[u].z, wgt, acc.z);
+      acc.w = fmaf(o[u].w, wgt, acc.w);
+    }
+    __syncwarp();
+  }
+  const float inv = 1.0f / L;
+  const float4 a = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+  if (lane < D4) reinterpret_cast<float4*>(p.a + ((size_t)unit * R + r) * d)[lane] = a;
+  const float aa = warp_sum(lane < D4 ? a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w : 0.f);
+  // hi/lo bf16 split of the row (columns >= d are zero)
+  uint32_t h01, l01, h23, l23;
+  split_hi_lo(a.x, a.y, h01, l01);
+  split_hi_lo(a.z, a.w, h23, l23);
+  if (lane >= D4) h01 = l01 = h23 = l23 = 0u;
+  reinterpret_cast<uint2*>(ahl + (size_t)r * kDPad)[lane] = make_uint2(h01, h23);
+  reinterpret_cast<uint2*>(ahl + (size_t)(kMaxR + r) * kDPad)[lane] = make_uint2(l01, l23);
+  if (lane == 0) {
+    const size_t o = (size_t)unit * R + r;
     p.aa[o] = aa;
-    p.m2[o] = Ms[tid];
-    p.l[o] = Ls[tid];
+    p.m2[o] = M;
+    p.l[o] = L;
     // exported: log-sum-exp of the natural-unit logits, log(L) + m ln 2
-    p.m[o] = (Ms[tid] + log2f(Ls[tid])) * 0.69314718055994531f;
-    if (!isfinite(aa)) atomicOr(p.status, DROPKV_FLAG_NONFINITE | DROPKV_FLAG_NONFINITE_STATS);
+    p.m[o] = (M + log2f(L)) * 0.69314718055994531f;
+    if (!(L > 0.f) || !isfinite(L) || !isfinite(aa))
+      atomicOr(p.status, DROPKV_FLAG_NONFINITE | DROPKV_FLAG_NONFINITE_STATS);
   }
 }
-
 
 template <int NR>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -232,10 +289,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     for (int i = 0; i < C::KS; ++i) { mbar_init(&S.kfull[i], 1); mbar_init(&S.kempty[i], 1); }
     for (int i = 0; i < C::VS; ++i) { mbar_init(&S.vfull[i], 1); mbar_init(&S.vempty[i], 1); }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&S.sfull[i], 1); mbar_init(&S.sempty[i], kWorkerWarps);
-      mbar_init(&S.pfull[i], kWorkerWarps); mbar_init(&S.pempty[i], 1);
-    }
+    for (int i = 0; i < 2; ++i) { mbar_init(&S.sfull[i], 1); mbar_init(&S.sempty[i], kWorkerWarps); }
+    for (int i = 0; i < C::PB; ++i) { mbar_init(&S.pfull[i], kWorkerWarps); mbar_init(&S.pempty[i], 1); }
     mbar_init(&S.ofull, 1);
     mbar_init(&S.drain, 1);
     S.abort = 0;
@@ -262,30 +317,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   bool failed = false;
 
   if (T > 0 && warp == kProducerWarp) {
-    // ---------------------------------------------------- TMA producer
-    if (lane == 0) {
-      int issued_k = 0, issued_v = 0;
-      for (int i = 0; i < T; ++i) {
-        const int y = (t0 + i) * kTile;
-        const int ks = i % C::KS, vs = i % C::VS;
-        if (i >= C::KS && !mbar_wait(&S.kempty[ks], ((i / C::KS) + 1) & 1, &S.abort)) { failed = true; break; }
-        mbar_arrive_expect_tx(&S.kfull[ks], kTileBytes);
-        tma_load_3d(sK + ks * kTileBytes, &tmk, &S.kfull[ks], 0, y, unit);
-        tma_load_3d(sK + ks * kTileBytes + kHalfTile, &tmk, &S.kfull[ks], 64, y, unit);
-        ++issued_k;
-        if (i >= C::VS && !mbar_wait(&S.vempty[vs], ((i / C::VS) + 1) & 1, &S.abort)) { failed = true; break; }
-        mbar_arrive_expect_tx(&S.vfull[vs], kTileBytes);
-        tma_load_3d(sV + vs * kTileBytes, &tmv, &S.vfull[vs], 0, y, unit);
-        tma_load_3d(sV + vs * kTileBytes + kHalfTile, &tmv, &S.vfull[vs], 64, y, unit);
-        ++issued_v;
-      }
-      if (failed) {
-        S.abort = 1;
-        atomicOr(p.status, DROPKV_FLAG_TIMEOUT);
-        for (int i = max(0, issued_k - C::KS); i < issued_k; ++i) mbar_drain(&S.kfull[i % C::KS], (i / C::KS) & 1);
-        for (int i = max(0, issued_v - C::VS); i < issued_v; ++i) mbar_drain(&S.vfull[i % C::VS], (i / C::VS) & 1);
-      }
-    }
+    // ---------------------------------------------------- TMA producer: lane 0 K, lane 1 V
+    if (lane == 0) stream_ring<C::KS>(sK, S.kfull, S.kempty, &tmk, t0, T, unit, &S.abort, p.status);
+    else if (lane == 1) stream_ring<C::VS>(sV, S.vfull, S.vempty, &tmv, t0, T, unit, &S.abort, p.status);
     __syncwarp();
   } else if (T > 0 && warp == kMmaWarp) {
     // ---------------------------------------------------- MMA issuer
@@ -310,8 +344,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = issue_S(0);
       for (int i = 0; ok && i < T; ++i) {
         if (i + 1 < T && !(ok = issue_S(i + 1))) break;
-        const int pb = i & 1, vs = i % C::VS;
-        if (!mbar_wait(&S.pfull[pb], (i >> 1) & 1, &S.abort)) { ok = false; break; }
+        const int pb = i % C::PB, vs = i % C::VS;
+        if (!mbar_wait(&S.pfull[pb], (i / C::PB) & 1, &S.abort)) { ok = false; break; }
         if (!mbar_wait(&S.vfull[vs], (i / C::VS) & 1, &S.abort)) { ok = false; break; }
         tc_fence_after();
         const uint32_t vb = smem_addr(sV + vs * kTileBytes);
@@ -354,20 +388,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int r = 0; r < HR; ++r) { lsum[r] = 0.f; mr[r] = -INFINITY; }
     for (int i = 0; i < T; ++i) {
-      const int tile0 = (t0 + i) * kTile, sb = i & 1, vs = i % C::VS;
+      const int tile0 = (t0 + i) * kTile, sb = i & 1, vs = i % C::VS, pb = i % C::PB;
       const int j = tile0 + tok;
       const bool full = tile0 + kTile - 1 <= all_see;
       const bool tail = tile0 + kTile > nb;       // tile holds slots past the sequence
-      bool ok = mbar_wait(&S.sfull[sb], (i >> 1) & 1, &S.abort);
-      if (ok && i >= 2) ok = mbar_wait(&S.pempty[sb], ((i >> 1) + 1) & 1, &S.abort);
-      if (ok && tail) ok = mbar_wait(&S.vfull[vs], (i / C::VS) & 1, &S.abort);
-      ok = __all_sync(0xffffffffu, ok);
-      if (named_bar_or(kBarWork, kWorkers, !ok)) { failed = true; break; }
-      tc_fence_after();
+      bool ok = __all_sync(0xffffffffu, mbar_wait(&S.sfull[sb], (i >> 1) & 1, &S.abort));
       float sraw[HR];
-      tmem_ld_cols<HR>(tS + lane_base + sb * NR + r0, sraw);
-      tmem_wait_ld();
-      tc_fence_before();
+      if (ok) {
+        tc_fence_after();
+        tmem_ld_cols<HR>(tS + lane_base + sb * NR + r0, sraw);
+        tmem_wait_ld();
+        tc_fence_before();
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.sempty[sb]);
 
@@ -387,7 +419,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         rel[r] = fmaf(sraw[r], scale, -mr[r]);
         need |= ((vis >> r) & 1u) && rel[r] > kRescaleLog2;
       }
-      if (named_bar_or(kBarWork, kWorkers, need)) {
+      // this tile's P buffer must be free (PV of tile i - PB done); the tail tile's V must have landed
+      if (ok && i >= C::PB) ok = mbar_wait(&S.pempty[pb], ((i / C::PB) + 1) & 1, &S.abort);
+      if (ok && tail) ok = mbar_wait(&S.vfull[vs], (i / C::VS) & 1, &S.abort);
+      ok = __all_sync(0xffffffffu, ok);
+      // one barrier per tile in the common case: it carries both "some wait
+      // failed" and "some logit outgrew its reference"
+      if (named_bar_or(kBarWork, kWorkers, !ok || need)) {
+        if (named_bar_or(kBarAux, kWorkers, !ok)) { failed = true; break; }
         // new reference = max(old reference, this tile's max) per row
 #pragma unroll
         for (int r = 0; r < HR; ++r) {
@@ -425,8 +464,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // exponentials relative to the row reference, split into bf16 hi + lo
-      uint8_t* phi = sP + (sb * 2 + 0) * C::kPBytes;
-      uint8_t* plo = sP + (sb * 2 + 1) * C::kPBytes;
+      uint8_t* phi = sP + (pb * 2 + 0) * C::kPBytes;
+      uint8_t* plo = sP + (pb * 2 + 1) * C::kPBytes;
 #pragma unroll
       for (int c8 = 0; c8 < HR / 8; ++c8) {
         uint32_t hp[4], lp[4];
@@ -455,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&S.pfull[sb]);
+      if (lane == 0) mbar_arrive(&S.pfull[pb]);
     }
     // ------------------------------------------------ partial state of this split
     // The MMA warp commits `drain` once, after its last MMA: a single-phase
@@ -509,30 +548,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
-  // ---------------------------------------------------- split-K merge ticket
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    const uint32_t t = atomicAdd(&p.tickets[unit], 1u);
-    S.is_last = (t == (uint32_t)p.splits - 1);
-  }
-  __syncthreads();
-  if (S.is_last) {
-    __threadfence();
-    float* wts = reinterpret_cast<float*>(sK);                     // [splits][R]
-    float* Ms = wts + (size_t)p.splits * R;
-    float* Ls = Ms + kMaxR;
-    merge_unit(p, unit, wts, Ms, Ls, tid);
-    if (tid == 0) p.tickets[unit] = 0;
-  }
+  // the partial states are merged by merge_splits_kernel
 }
 
 // ============================================================== pass 2
 template <int NR>
 struct Pass2Cfg {
   static constexpr int HR = NR / 2;
-  static constexpr int KS = 3;
-  static constexpr int VS = NR <= 32 ? 3 : 2;
+  static constexpr int KS = 2;                      // K is released right after S = K Q^T
+  static constexpr int VS = NR <= 32 ? 4 : 3;       // V is held until A.V^T and |v|^2 are done
   static constexpr int kQBytes = NR * kDPad * 2;
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + KS * kTileBytes;
@@ -544,7 +568,7 @@ struct Pass2Cfg {
 };
 
 struct Pass2Small {
-  uint64_t kfull[3], kempty[3], vfull[3], vempty[3];
+  uint64_t kfull[2], kempty[2], vfull[4], vempty[4];
   uint64_t accfull[2], accempty[2], drain;
   uint32_t tmem_base;
   int abort;
@@ -614,29 +638,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   bool failed = false;
 
   if (warp == kProducerWarp) {
-    if (lane == 0) {
-      int issued_k = 0, issued_v = 0;
-      for (int i = 0; i < T; ++i) {
-        const int y = (t0 + i) * kTile;
-        const int ks = i % C::KS, vs = i % C::VS;
-        if (i >= C::KS && !mbar_wait(&S.kempty[ks], ((i / C::KS) + 1) & 1, &S.abort)) { failed = true; break; }
-        mbar_arrive_expect_tx(&S.kfull[ks], kTileBytes);
-        tma_load_3d(sK + ks * kTileBytes, &tmk, &S.kfull[ks], 0, y, unit);
-        tma_load_3d(sK + ks * kTileBytes + kHalfTile, &tmk, &S.kfull[ks], 64, y, unit);
-        ++issued_k;
-        if (i >= C::VS && !mbar_wait(&S.vempty[vs], ((i / C::VS) + 1) & 1, &S.abort)) { failed = true; break; }
-        mbar_arrive_expect_tx(&S.vfull[vs], kTileBytes);
-        tma_load_3d(sV + vs * kTileBytes, &tmv, &S.vfull[vs], 0, y, unit);
-        tma_load_3d(sV + vs * kTileBytes + kHalfTile, &tmv, &S.vfull[vs], 64, y, unit);
-        ++issued_v;
-      }
-      if (failed) {
-        S.abort = 1;
-        atomicOr(p.status, DROPKV_FLAG_TIMEOUT);
-        for (int i = max(0, issued_k - C::KS); i < issued_k; ++i) mbar_drain(&S.kfull[i % C::KS], (i / C::KS) & 1);
-        for (int i = max(0, issued_v - C::VS); i < issued_v; ++i) mbar_drain(&S.vfull[i % C::VS], (i / C::VS) & 1);
-      }
-    }
+    // TMA producer: lane 0 K, lane 1 V
+    if (lane == 0) stream_ring<C::KS>(sK, S.kfull, S.kempty, &tmk, t0, T, unit, &S.abort, p.status);
+    else if (lane == 1) stream_ring<C::VS>(sV, S.vfull, S.vempty, &tmv, t0, T, unit, &S.abort, p.status);
     __syncwarp();
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
@@ -779,6 +783,9 @@ cudaError_t launch_pass1_t(const AttnParams& p, const CUtensorMap& tk, const CUt
   cudaError_t e = cudaFuncSetAttribute(window_attention_kernel<NR>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   window_attention_kernel<NR><<<dim3(p.splits, p.U), kThreads, smem, st>>>(tk, tv, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  merge_splits_kernel<<<dim3(kMaxR / kMergeRows, p.U), kMergeThreads, 0, st>>>(p);
   return cudaGetLastError();
 }
 

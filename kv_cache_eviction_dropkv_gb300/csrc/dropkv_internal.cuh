@@ -14,7 +14,7 @@ namespace dropkv {
 constexpr int kTile = 128;          // tokens per K/V tile (the MMA M dimension)
 constexpr int kDPad = 128;          // head dimension as staged in shared memory
 constexpr int kMaxR = 64;           // rows (g * w) per KV head supported
-constexpr int kSelChunk = 4096;     // tokens per block in the selection kernels
+constexpr int kSelChunk = 16384;    // tokens per block in the selection kernels
 constexpr int kHistBins = 4096;     // first-level radix histogram (top 12 key bits)
 constexpr int kCandCap = 8192;      // candidates resolved in shared memory
 constexpr int kMaxPool = 63;
@@ -36,10 +36,10 @@ struct WsPlan {
   size_t m2, aa;                 // max in log2 units, |a|^2
   size_t ahl;                    // bf16 [U][2][NR][128]: a split into hi + lo parts
   size_t part_o, part_ml;        // pass-1 partial states
-  size_t tickets;                // u32 [U] pass-1 merge tickets
   size_t raw;                    // f32 [U][n_max] raw scores when the caller passes none
   // selection
   size_t hist;                   // u32 [U][kHistBins]
+  size_t hist2;                  // u32 [U][kHistBins] (second level)
   size_t sel_state;              // u32 [U][8]
   size_t cand;                   // u32 [U][kCandCap][2]
   size_t cand_cnt;               // u32 [U]
@@ -64,7 +64,6 @@ struct AttnParams {
   float *m, *l, *a, *m2, *aa;
   __nv_bfloat16* ahl;
   float *part_o, *part_ml;
-  uint32_t* tickets;
   float* raw;                    // raw score output [U][n_max]
   uint32_t* status;
 };
@@ -84,7 +83,7 @@ struct SelParams {
   int32_t* kept_idx;
   int32_t* kept_len;
   int B, Hkv, n_max, protect, chunks;
-  uint32_t *hist, *state, *cand, *cand_cnt, *tickets, *chunk_kept, *chunk_off;
+  uint32_t *hist, *hist2, *state, *cand, *cand_cnt, *tickets, *chunk_kept, *chunk_off;
   uint32_t* status;
 };
 

@@ -11,10 +11,11 @@
 // position first and exactly k_b slots are evicted.
 //   1. select_hist:  histogram of the top 12 key bits per KV head (all CTAs),
 //                    the last CTA of a head locates the bin holding rank k.
-//   2. select_cand:  CTAs count the slots above that bin per chunk and gather
-//                    the bin's members; the last CTA resolves the remaining
-//                    52 bits of (key, position) in shared memory and turns the
-//                    per-chunk kept counts into output offsets.
+//   2. select_cand:  CTAs count the slots above that bin per chunk, gather the
+//                    bin's members and histogram their next 12 bits; the last
+//                    CTA finds the 24-bit prefix of the k-th pair, ranks the
+//                    few members sharing it and turns the per-chunk kept
+//                    counts into output offsets.
 //   3. select_write: each chunk writes its kept positions in ascending order.
 #include <cuda_runtime.h>
 
@@ -24,15 +25,17 @@ namespace dropkv {
 namespace {
 
 constexpr int kSelThreads = 256;
-constexpr int kPerThread = kSelChunk / kSelThreads;   // 16
 constexpr int kPoolTile = 2048;
 constexpr int kPoolThreads = 256;
 
 enum : uint32_t { kModeNormal = 0, kModeKeepAll = 1, kModeSkip = 2 };
 enum { kStMode = 0, kStBin = 1, kStRank = 2, kStCount = 3, kStKey = 4, kStIdx = 5 };
 
+// Order-preserving map of a float to an unsigned key (-0.0 is taken as +0.0,
+// so equal scores compare equal and fall to the position tie-break).
 __device__ __forceinline__ uint32_t f2ord(float f) {
-  const uint32_t u = __float_as_uint(f);
+  uint32_t u = __float_as_uint(f);
+  if (u == 0x80000000u) u = 0u;
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
@@ -110,6 +113,75 @@ __device__ __forceinline__ UnitInfo unit_info(const SelParams& p, int b) {
   return u;
 }
 
+// Four consecutive scores starting at slot j (j % 4 == 0); slots >= nb read as
+// +inf and are masked by the caller.  Vector loads when rows are 16-byte aligned.
+__device__ __forceinline__ float4 load4(const float* row, int j, int nb, bool vec) {
+  if (vec && j + 3 < nb) return __ldg(reinterpret_cast<const float4*>(row + j));
+  float4 v;
+  v.x = (j < nb) ? __ldg(row + j) : INFINITY;
+  v.y = (j + 1 < nb) ? __ldg(row + j + 1) : INFINITY;
+  v.z = (j + 2 < nb) ? __ldg(row + j + 2) : INFINITY;
+  v.w = (j + 3 < nb) ? __ldg(row + j + 3) : INFINITY;
+  return v;
+}
+
+// Shared-memory histogram increments for four consecutive slots: runs of
+// equal bins (pooling repeats values over neighbouring slots) are added once.
+constexpr uint32_t kNoBin = 0xFFFFFFFFu;
+__device__ __forceinline__ void hist_add4(uint32_t* h, uint32_t b0, uint32_t b1, uint32_t b2, uint32_t b3) {
+  uint32_t cur = b0, cnt = 1;
+  const uint32_t nxt[3] = {b1, b2, b3};
+#pragma unroll
+  for (int i = 0; i < 3; ++i) {
+    if (nxt[i] == cur) {
+      ++cnt;
+    } else {
+      if (cur != kNoBin) atomicAdd(&h[cur], cnt);
+      cur = nxt[i];
+      cnt = 1;
+    }
+  }
+  if (cur != kNoBin) atomicAdd(&h[cur], cnt);
+}
+
+constexpr int kVec = kSelChunk / (4 * kSelThreads);   // float4 loads per thread per chunk
+
+// The bin of a kHistBins histogram (global memory) that holds the k-th
+// (1-based) item, the rank of that item inside the bin and the bin's count.
+__device__ void find_bin(const uint32_t* gh, uint32_t k, uint32_t* scratch, uint32_t& bin, uint32_t& rank,
+                         uint32_t& count) {
+  __shared__ uint32_t s_bin, s_rank, s_count;
+  constexpr int per = kHistBins / kSelThreads;
+  uint32_t cnt[per];
+  uint32_t local = 0;
+#pragma unroll
+  for (int q = 0; q < per; ++q) {
+    cnt[q] = __ldcg(&gh[threadIdx.x * per + q]);
+    local += cnt[q];
+  }
+  uint32_t total;
+  const uint32_t before = block_exclusive_scan<kSelThreads>(local, scratch, &total);
+  if (before < k && k <= before + local) {
+    uint32_t c = before;
+    for (int q = 0; q < per; ++q) {
+      if (c + cnt[q] >= k) {
+        s_bin = threadIdx.x * per + q;
+        s_rank = k - c;
+        s_count = cnt[q];
+        break;
+      }
+      c += cnt[q];
+    }
+  }
+  __syncthreads();
+  bin = s_bin;
+  rank = s_rank;
+  count = s_count;
+  __syncthreads();
+}
+
+// Level 1: histogram of the top 12 bits of the score keys of every KV head;
+// the last CTA of a head finds the bin that holds the k_b-th smallest key.
 __global__ void __launch_bounds__(kSelThreads) select_hist_kernel(const SelParams p) {
   __shared__ uint32_t sh[kHistBins];
   __shared__ uint32_t scratch[32];
@@ -129,10 +201,16 @@ __global__ void __launch_bounds__(kSelThreads) select_hist_kernel(const SelParam
   if (j0 >= ui.nb) return;
   for (int i = threadIdx.x; i < kHistBins; i += kSelThreads) sh[i] = 0;
   __syncthreads();
-  const float* sc = p.scores + (size_t)unit * p.n_max;
-  for (int i = 0; i < kPerThread; ++i) {
-    const int j = j0 + i * kSelThreads + threadIdx.x;
-    if (j < ui.nb) atomicAdd(&sh[f2ord(sc[j]) >> 20], 1u);
+  const float* row = p.scores + (size_t)unit * p.n_max;
+  const bool vec = (p.n_max & 3) == 0;
+  float4 xv[kVec];   // load phase: all of this thread's slots in flight at once
+#pragma unroll
+  for (int v = 0; v < kVec; ++v) xv[v] = load4(row, j0 + (v * kSelThreads + threadIdx.x) * 4, ui.nb, vec);
+#pragma unroll
+  for (int v = 0; v < kVec; ++v) {
+    const int j = j0 + (v * kSelThreads + threadIdx.x) * 4;
+    hist_add4(sh, j < ui.nb ? f2ord(xv[v].x) >> 20 : kNoBin, j + 1 < ui.nb ? f2ord(xv[v].y) >> 20 : kNoBin,
+              j + 2 < ui.nb ? f2ord(xv[v].z) >> 20 : kNoBin, j + 3 < ui.nb ? f2ord(xv[v].w) >> 20 : kNoBin);
   }
   __syncthreads();
   uint32_t* gh = p.hist + (size_t)unit * kHistBins;
@@ -147,28 +225,13 @@ __global__ void __launch_bounds__(kSelThreads) select_hist_kernel(const SelParam
   __syncthreads();
   if (!is_last) return;
   __threadfence();
-  // last CTA of this head: find the bin holding the kb-th smallest key
-  uint32_t cnt[kHistBins / kSelThreads];
-  uint32_t local = 0;
-  for (int q = 0; q < kHistBins / kSelThreads; ++q) {
-    cnt[q] = __ldcg(&gh[threadIdx.x * (kHistBins / kSelThreads) + q]);
-    local += cnt[q];
-  }
-  uint32_t total;
-  const uint32_t before = block_exclusive_scan<kSelThreads>(local, scratch, &total);
   if (ui.mode == kModeNormal) {
-    const uint32_t k = (uint32_t)ui.kb;
-    if (before < k && k <= before + local) {
-      uint32_t c = before;
-      for (int q = 0; q < kHistBins / kSelThreads; ++q) {
-        if (c + cnt[q] >= k) {
-          st[kStBin] = threadIdx.x * (kHistBins / kSelThreads) + q;
-          st[kStRank] = k - c;
-          st[kStCount] = cnt[q];
-          break;
-        }
-        c += cnt[q];
-      }
+    uint32_t bin, rank, count;
+    find_bin(gh, (uint32_t)ui.kb, scratch, bin, rank, count);
+    if (threadIdx.x == 0) {
+      st[kStBin] = bin;
+      st[kStRank] = rank;
+      st[kStCount] = count;
     }
   }
   if (threadIdx.x == 0) {
@@ -178,22 +241,19 @@ __global__ void __launch_bounds__(kSelThreads) select_hist_kernel(const SelParam
 }
 
 // Radix select of the rank-th (1-based) smallest 64-bit composite among `n`
-// items whose top 12 bits are already fixed; `get(i)` returns item i.
-// Resolves bits 51..0 with 8-bit digits; returns the selected composite.
+// items whose bits [known_lo, 64) all equal those of `prefix`; `get(i)`
+// returns item i.  Resolves the remaining bits with 8-bit digits.
 template <typename Get>
-__device__ uint64_t radix_select_52(int n, uint32_t rank, uint64_t prefix, Get get, uint32_t* hist,
-                                    uint32_t* scratch) {
+__device__ uint64_t radix_select(int n, uint32_t rank, uint64_t prefix, int known_lo, Get get, uint32_t* hist,
+                                 uint32_t* scratch) {
   __shared__ uint64_t s_prefix;
   __shared__ uint32_t s_rank, s_count;
   if (threadIdx.x == 0) { s_prefix = prefix; s_rank = rank; s_count = (uint32_t)n; }
   __syncthreads();
-  const int shifts[7] = {44, 36, 28, 20, 12, 4, 0};
-  const int widths[7] = {8, 8, 8, 8, 8, 8, 4};
-  int known_lo = 52;   // bits [known_lo, 64) are fixed
-  for (int pass = 0; pass < 7; ++pass) {
-    const int sh = shifts[pass], wb = widths[pass];
+  while (known_lo > 0) {
     const uint64_t pre = s_prefix;
     if (s_count == 1) break;
+    const int wb = known_lo < 8 ? known_lo : 8, sh = known_lo - wb;
     for (int i = threadIdx.x; i < 256; i += kSelThreads) hist[i] = 0;
     __syncthreads();
     for (int i = threadIdx.x; i < n; i += kSelThreads) {
@@ -201,8 +261,7 @@ __device__ uint64_t radix_select_52(int n, uint32_t rank, uint64_t prefix, Get g
       if ((v >> known_lo) == (pre >> known_lo)) atomicAdd(&hist[(v >> sh) & ((1u << wb) - 1)], 1u);
     }
     __syncthreads();
-    // 256 bins, one per thread: find the digit holding s_rank
-    const uint32_t c = hist[threadIdx.x];
+    const uint32_t c = hist[threadIdx.x];          // 256 bins, one per thread
     uint32_t total;
     const uint32_t before = block_exclusive_scan<kSelThreads>(c, scratch, &total);
     const uint32_t r = s_rank;
@@ -229,10 +288,20 @@ __device__ uint64_t radix_select_52(int n, uint32_t rank, uint64_t prefix, Get g
   return out;
 }
 
+constexpr uint32_t kBruteForce = 1024;   // resolve at most this many survivors by direct ranking
+
+// Level 2: every CTA counts its slots above the bin (kept for sure), gathers
+// the bin's members and histograms their next 12 key bits; the last CTA of a
+// head locates the 24-bit prefix of the k-th pair, ranks the few members that
+// share it directly (radix on larger tie sets), and turns the per-chunk kept
+// counts into output offsets.
 __global__ void __launch_bounds__(kSelThreads) select_cand_kernel(const SelParams p) {
+  __shared__ uint32_t sh2[kHistBins];
   __shared__ uint32_t scratch[32];
   __shared__ uint32_t hist[256];
   __shared__ int is_last;
+  __shared__ uint32_t n2_s;
+  __shared__ uint64_t thr_s;
   extern __shared__ uint64_t cand_s[];     // kCandCap composites (last CTA only)
   const int chunk = blockIdx.x, unit = blockIdx.y, b = unit / p.Hkv;
   const UnitInfo ui = unit_info(p, b);
@@ -242,24 +311,62 @@ __global__ void __launch_bounds__(kSelThreads) select_cand_kernel(const SelParam
   uint32_t* st = p.state + (size_t)unit * 8;
   const uint32_t mode = ui.mode;
   const uint32_t bin = __ldcg(&st[kStBin]), count1 = __ldcg(&st[kStCount]);
-  const float* sc = p.scores + (size_t)unit * p.n_max;
+  const bool gather = mode == kModeNormal && count1 <= (uint32_t)kCandCap;
+  const float* row = p.scores + (size_t)unit * p.n_max;
+  const bool vec = (p.n_max & 3) == 0;
   uint32_t* cand = p.cand + (size_t)unit * kCandCap * 2;
-  uint32_t def = 0;
-  for (int i = 0; i < kPerThread; ++i) {
-    const int j = j0 + i * kSelThreads + threadIdx.x;
-    if (j >= ui.nb) break;
-    if (mode == kModeKeepAll) { ++def; continue; }
-    const uint32_t key = f2ord(sc[j]), top = key >> 20;
-    if (top > bin) {
-      ++def;
-    } else if (top == bin && count1 <= (uint32_t)kCandCap) {
-      const uint32_t slot = atomicAdd(&p.cand_cnt[unit], 1u);
-      if (slot < (uint32_t)kCandCap) { cand[slot * 2] = key; cand[slot * 2 + 1] = (uint32_t)j; }
+  for (int i = threadIdx.x; i < kHistBins; i += kSelThreads) sh2[i] = 0;
+  __syncthreads();
+  uint32_t def = 0, nmem = 0;
+  float4 xv[kVec];   // load phase: all of this thread's slots in flight at once
+#pragma unroll
+  for (int v = 0; v < kVec; ++v) xv[v] = load4(row, j0 + (v * kSelThreads + threadIdx.x) * 4, ui.nb, vec);
+#pragma unroll
+  for (int v = 0; v < kVec; ++v) {
+    const int j = j0 + (v * kSelThreads + threadIdx.x) * 4;
+    const float xs[4] = {xv[v].x, xv[v].y, xv[v].z, xv[v].w};
+    uint32_t b2[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const bool valid = j + u < ui.nb;
+      const uint32_t key = f2ord(xs[u]), top = key >> 20;
+      const bool member = valid && mode == kModeNormal && top == bin;
+      def += valid && (mode == kModeKeepAll || top > bin);
+      nmem += member;
+      b2[u] = member ? (key >> 8) & 0xFFFu : kNoBin;
     }
+    hist_add4(sh2, b2[0], b2[1], b2[2], b2[3]);
   }
   uint32_t total;
   block_exclusive_scan<kSelThreads>(def, scratch, &total);
   if (threadIdx.x == 0) atomicAdd(&p.chunk_kept[(size_t)unit * p.chunks + chunk], total);
+  if (gather) {
+    // members of the bin: one range reservation per CTA, then plain stores
+    uint32_t nblk;
+    const uint32_t before = block_exclusive_scan<kSelThreads>(nmem, scratch, &nblk);
+    __shared__ uint32_t base_s;
+    if (threadIdx.x == 0) base_s = nblk ? atomicAdd(&p.cand_cnt[unit], nblk) : 0u;
+    __syncthreads();
+    uint32_t slot = base_s + before;
+#pragma unroll
+    for (int v = 0; v < kVec; ++v) {
+      const int j = j0 + (v * kSelThreads + threadIdx.x) * 4;
+      const float xs[4] = {xv[v].x, xv[v].y, xv[v].z, xv[v].w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const uint32_t key = f2ord(xs[u]);
+        if (j + u < ui.nb && (key >> 20) == bin) {
+          if (slot < (uint32_t)kCandCap) { cand[slot * 2] = key; cand[slot * 2 + 1] = (uint32_t)(j + u); }
+          ++slot;
+        }
+      }
+    }
+  }
+  if (mode == kModeNormal) {
+    uint32_t* gh2 = p.hist2 + (size_t)unit * kHistBins;
+    for (int i = threadIdx.x; i < kHistBins; i += kSelThreads)
+      if (sh2[i]) atomicAdd(&gh2[i], sh2[i]);
+  }
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -272,21 +379,61 @@ __global__ void __launch_bounds__(kSelThreads) select_cand_kernel(const SelParam
 
   uint64_t thr = 0;   // composite (key << 32 | position) of the k-th smallest slot
   if (mode == kModeNormal) {
-    const uint32_t rank = __ldcg(&st[kStRank]);
-    const uint64_t prefix = (uint64_t)bin << 52;
-    if (count1 <= (uint32_t)kCandCap) {
-      const int n = (int)count1;
-      for (int i = threadIdx.x; i < n; i += kSelThreads)
-        cand_s[i] = ((uint64_t)__ldcg(&cand[i * 2]) << 32) | __ldcg(&cand[i * 2 + 1]);
+    const uint32_t rank1 = __ldcg(&st[kStRank]);
+    uint32_t bin2, rank2, count2;
+    find_bin(p.hist2 + (size_t)unit * kHistBins, rank1, scratch, bin2, rank2, count2);
+    const uint32_t pre24 = (bin << 12) | bin2;
+    if (gather) {
+      // members sharing the 24-bit prefix of the k-th key
+      if (threadIdx.x == 0) n2_s = 0;
       __syncthreads();
-      thr = radix_select_52(n, rank, prefix, [&](int i) { return cand_s[i]; }, hist, scratch);
-      // kept members of the bin, per chunk
-      for (int i = threadIdx.x; i < n; i += kSelThreads)
-        if (cand_s[i] > thr) atomicAdd(&p.chunk_kept[(size_t)unit * p.chunks + (int)(cand_s[i] & 0xFFFFFFFFu) / kSelChunk], 1u);
+      for (int i = threadIdx.x; i < (int)count1; i += kSelThreads) {
+        const uint32_t key = __ldcg(&cand[i * 2]);
+        if ((key >> 8) == pre24) {
+          const uint32_t slot = atomicAdd(&n2_s, 1u);
+          cand_s[slot] = ((uint64_t)key << 32) | __ldcg(&cand[i * 2 + 1]);
+        }
+      }
+      __syncthreads();
+      const int n2 = (int)n2_s;
+      if ((uint32_t)n2 <= kBruteForce) {
+        // direct ranking: the member with exactly rank2 - 1 smaller members
+        for (int i = threadIdx.x; i < n2; i += kSelThreads) {
+          const uint64_t c = cand_s[i];
+          uint32_t below = 0;
+          for (int q = 0; q < n2; ++q) below += cand_s[q] < c;
+          if (below == rank2 - 1) thr_s = c;
+        }
+        __syncthreads();
+        thr = thr_s;
+      } else {
+        thr = radix_select(n2, rank2, (uint64_t)pre24 << 40, 40, [&](int i) { return cand_s[i]; }, hist, scratch);
+      }
+      // kept members of the level-1 bin, per chunk (counted in shared memory
+      // when the chunk count allows, reusing the level-2 histogram's space)
+      const int nchunks_b = ceil_div(ui.nb, kSelChunk);
+      const bool local_counts = nchunks_b <= kHistBins;
+      if (local_counts) {
+        for (int i = threadIdx.x; i < nchunks_b; i += kSelThreads) sh2[i] = 0;
+        __syncthreads();
+      }
+      for (int i = threadIdx.x; i < (int)count1; i += kSelThreads) {
+        const uint64_t c = ((uint64_t)__ldcg(&cand[i * 2]) << 32) | __ldcg(&cand[i * 2 + 1]);
+        if (c > thr) {
+          const int ch = (int)(c & 0xFFFFFFFFu) / kSelChunk;
+          if (local_counts) atomicAdd(&sh2[ch], 1u);
+          else atomicAdd(&p.chunk_kept[(size_t)unit * p.chunks + ch], 1u);
+        }
+      }
+      if (local_counts) {
+        __syncthreads();
+        for (int i = threadIdx.x; i < nchunks_b; i += kSelThreads)
+          if (sh2[i]) atomicAdd(&p.chunk_kept[(size_t)unit * p.chunks + i], sh2[i]);
+      }
     } else {
       // large bin: resolve directly over the head's scores (slow path)
-      auto get = [&](int j) -> uint64_t { return ((uint64_t)f2ord(__ldcg(&sc[j])) << 32) | (uint32_t)j; };
-      thr = radix_select_52(ui.nb, rank, prefix, get, hist, scratch);
+      auto get = [&](int j) -> uint64_t { return ((uint64_t)f2ord(__ldcg(&row[j])) << 32) | (uint32_t)j; };
+      thr = radix_select(ui.nb, rank2, (uint64_t)pre24 << 40, 40, get, hist, scratch);
       for (int j = threadIdx.x; j < ui.nb; j += kSelThreads) {
         const uint64_t v = get(j);
         if ((v >> 52) == bin && v > thr) atomicAdd(&p.chunk_kept[(size_t)unit * p.chunks + j / kSelChunk], 1u);
@@ -315,6 +462,7 @@ __global__ void __launch_bounds__(kSelThreads) select_cand_kernel(const SelParam
   }
 }
 
+// Level 3: each chunk writes its kept positions in ascending order.
 __global__ void __launch_bounds__(kSelThreads) select_write_kernel(const SelParams p) {
   __shared__ uint32_t scratch[32];
   const int chunk = blockIdx.x, unit = blockIdx.y, b = unit / p.Hkv, h = unit - b * p.Hkv;
@@ -326,26 +474,36 @@ __global__ void __launch_bounds__(kSelThreads) select_write_kernel(const SelPara
   if (j0 >= ui.nb) return;
   const uint32_t* st = p.state + (size_t)unit * 8;
   const uint64_t thr = ((uint64_t)__ldcg(&st[kStKey]) << 32) | __ldcg(&st[kStIdx]);
-  const float* sc = p.scores + (size_t)unit * p.n_max;
-  // each thread owns 16 consecutive slots so the output stays in position order
-  const int jt = j0 + threadIdx.x * kPerThread;
-  uint32_t keepmask = 0, cnt = 0;
+  const float* row = p.scores + (size_t)unit * p.n_max;
+  const bool vec = (p.n_max & 3) == 0;
+  // each thread owns kPerThread consecutive slots so the output stays in position order
+  constexpr int kPer = kSelChunk / kSelThreads;
+  const int jt = j0 + threadIdx.x * kPer;
+  uint64_t keepmask = 0;
+  uint32_t cnt = 0;
+  float4 xv[kPer / 4];   // load phase: all of this thread's slots in flight at once
 #pragma unroll
-  for (int q = 0; q < kPerThread; ++q) {
-    const int j = jt + q;
-    bool keep = false;
-    if (j < ui.nb) {
-      keep = (ui.mode == kModeKeepAll) || ((((uint64_t)f2ord(sc[j]) << 32) | (uint32_t)j) > thr);
+  for (int q4 = 0; q4 < kPer / 4; ++q4) xv[q4] = load4(row, jt + q4 * 4, ui.nb, vec);
+#pragma unroll
+  for (int q4 = 0; q4 < kPer / 4; ++q4) {
+    const int j = jt + q4 * 4;
+    const float xs[4] = {xv[q4].x, xv[q4].y, xv[q4].z, xv[q4].w};
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const bool keep = (j + u < ui.nb) &&
+                        ((ui.mode == kModeKeepAll) || ((((uint64_t)f2ord(xs[u]) << 32) | (uint32_t)(j + u)) > thr));
+      keepmask |= (uint64_t)keep << (q4 * 4 + u);
+      cnt += keep;
     }
-    keepmask |= (uint32_t)keep << q;
-    cnt += keep;
   }
   uint32_t total;
   const uint32_t before = block_exclusive_scan<kSelThreads>(cnt, scratch, &total);
   int32_t* out = p.kept_idx + (size_t)unit * p.n_max + __ldcg(&p.chunk_off[(size_t)unit * p.chunks + chunk]) + before;
-#pragma unroll
-  for (int q = 0; q < kPerThread; ++q)
-    if ((keepmask >> q) & 1) *out++ = jt + q;
+  while (keepmask) {
+    const int q = __ffsll((long long)keepmask) - 1;
+    *out++ = jt + q;
+    keepmask &= keepmask - 1;
+  }
 }
 
 // ------------------------------------------------------------ compaction
