@@ -31,7 +31,7 @@ from kv_cache_eviction_dropkv_gb300 import synth  # noqa: E402
 
 METRIC = "DropKV scored tokens/s and ms per layer at n=128K; achieved HBM GB/s vs peak"
 UNIT = "tokens/s"
-KERNELS_PER_STEP = 7      # window attention, score, pool+protect, 3 selection kernels, compaction
+KERNELS_PER_STEP = 9      # window attention, split merge, score, pool+protect, 4 selection kernels, compaction
 L2_FLUSH_BYTES = 256 << 20
 FALLBACK_HBM_GBS = 6800.0
 
@@ -258,10 +258,12 @@ def main():
     op.check(stream)
 
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(K)]
-    for row in evs:              # torch creates the CUDA event on its first record()
-        for e in row:
-            e.record(stream)
+    # timed steps: one event pair per step (events between the kernels of a
+    # step would serialise their programmatic dependent launches)
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    for e in ev0 + ev1:          # torch creates the CUDA event on its first record()
+        e.record(stream)
     torch.cuda.synchronize()
     sampler = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local])
                            if os.environ.get("CUDA_VISIBLE_DEVICES") else local)
@@ -272,21 +274,35 @@ def main():
     wall0 = time.perf_counter()
     for i in range(K):
         flush_l2(i)
-        e = evs[i]
-        e[0].record(stream)
-        step(e)
-        e[6].record(stream)
+        ev0[i].record(stream)
+        step()
+        ev1[i].record(stream)
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     wall = time.perf_counter() - wall0
     clocks = sampler.stop()
     op.check(stream)
+    t_step = [ev0[i].elapsed_time(ev1[i]) for i in range(K)]
+
+    # per-kernel phases, in separate steps with events at the phase boundaries
+    KP = max(3, min(K, 50))
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(KP)]
+    for row in evs:
+        for e in row:
+            e.record(stream)
+    torch.cuda.synchronize()
+    for i in range(KP):
+        flush_l2(i)
+        evs[i][0].record(stream)
+        step(evs[i])
+        evs[i][6].record(stream)
+    torch.cuda.synchronize()
+    op.check(stream)
 
     def ms(a, b):
-        return [evs[i][a].elapsed_time(evs[i][b]) for i in range(K)]
+        return [evs[i][a].elapsed_time(evs[i][b]) for i in range(KP)]
 
-    t_step = ms(0, 6)
     phases = {"window_attention": ms(1, 2), "score": ms(2, 3), "pool_protect": ms(3, 4),
               "select": ms(4, 5), "compact": ms(5, 6)}
     step_ms = sum(t_step) / K
@@ -298,7 +314,7 @@ def main():
 
     nbytes = workload_bytes(spec, lengths_np, kept_np)
     peak, peak_kind = measured_peaks()
-    phase_ms = {kname: sum(v_) / K for kname, v_ in phases.items()}
+    phase_ms = {kname: sum(v_) / KP for kname, v_ in phases.items()}
     dom = max(("window_attention", "score"), key=lambda kk: phase_ms[kk])
     achieved = nbytes[dom] / (phase_ms[dom] / 1e3) / 1e9
     roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -314,7 +330,8 @@ def main():
             "roofline": roofline,
             "path_roofline": {"achieved": path_gbs, "peak": peak, "unit": "GB/s", "frac": path_gbs / peak,
                               "algorithmic_bytes_per_step": nbytes["path"]},
-            "phases_ms": phase_ms, "wall_s_timed": wall, "gpu_launches": KERNELS_PER_STEP * K,
+            "phases_ms": phase_ms, "phases_note": "per-kernel times from %d separate steps with events at the phase boundaries (window_attention includes the split merge)" % KP,
+            "wall_s_timed": wall, "gpu_launches": KERNELS_PER_STEP * K,
             "clocks": clocks}
 
     if not args.no_e2e:

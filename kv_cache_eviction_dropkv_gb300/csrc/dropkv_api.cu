@@ -253,8 +253,6 @@ dropkv_status dropkv_select(const dropkv_shape* shape, const float* scores, cons
   const WsPlan w = make_plan(g);
   if (!workspace || workspace_bytes < w.total || !aligned16(workspace)) return DROPKV_ERR_WORKSPACE;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  if (cudaMemsetAsync(ws + w.sel_zero_begin, 0, w.sel_zero_end - w.sel_zero_begin, stream) != cudaSuccess)
-    return DROPKV_ERR_CUDA;
   SelParams p{};
   p.scores = scores;
   p.lengths = lengths;
@@ -271,7 +269,9 @@ dropkv_status dropkv_select(const dropkv_shape* shape, const float* scores, cons
   p.chunk_kept = reinterpret_cast<uint32_t*>(ws + w.chunk_kept);
   p.chunk_off = reinterpret_cast<uint32_t*>(ws + w.chunk_off);
   p.status = status;
-  return launch_select(p, stream) == cudaSuccess ? DROPKV_OK : DROPKV_ERR_CUDA;
+  return launch_select(p, w.sel_zero_end - w.sel_zero_begin, ws + w.sel_zero_begin, stream) == cudaSuccess
+             ? DROPKV_OK
+             : DROPKV_ERR_CUDA;
 }
 
 dropkv_status dropkv_compact(const dropkv_shape* shape, const void* k, const void* v, const int32_t* kept_idx,

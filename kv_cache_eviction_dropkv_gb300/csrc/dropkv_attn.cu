@@ -178,6 +178,8 @@ __global__ void __launch_bounds__(kMergeThreads) merge_splits_kernel(const AttnP
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int unit = blockIdx.y, r = blockIdx.x * kMergeRows + warp;
   const int b = unit / p.Hkv;
+  grid_dep_wait();                                // the partials come from pass 1
+  grid_dep_launch();
   const int nb = p.lengths ? p.lengths[b] : p.n_max;
   if (nb < p.w || nb > p.n_max) return;          // flagged by pass 1
   const int S = p.splits, R = p.R, d = p.d, D4 = d >> 2;
@@ -278,6 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int b = unit / p.Hkv, h = unit - b * p.Hkv;
   const int nb = p.lengths ? p.lengths[b] : p.n_max;
   if (nb < p.w || nb > p.n_max) {           // invalid length: the unit is skipped
+    grid_dep_wait();
     if (tid == 0 && split == 0 && h == 0) atomicOr(p.status, DROPKV_FLAG_BAD_LENGTH);
     return;
   }
@@ -315,6 +318,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = S.tmem_base;
   const uint32_t tS = tmem, tO = tmem + 2 * NR;    // S buffers at [0, 2NR), O at [2NR, 3NR)
   bool failed = false;
+  // Streaming reads only the caller's inputs, so the next kernel may be
+  // scheduled now; the writes of the partial states come after grid_dep_wait().
+  grid_dep_launch();
 
   if (T > 0 && warp == kProducerWarp) {
     // ---------------------------------------------------- TMA producer: lane 0 K, lane 1 V
@@ -500,6 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The MMA warp commits `drain` once, after its last MMA: a single-phase
     // wait.  (A parity wait on the per-tile `ofull` barrier would be ambiguous
     // here, since up to two PV commits may still be outstanding.)
+    grid_dep_wait();                              // earlier kernels are done before we write
     bool okw = true;
     if (!failed) okw = mbar_wait(&S.drain, 0, &S.abort);
     okw = __all_sync(0xffffffffu, okw);
@@ -535,6 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (T == 0) {
     // empty split (past the end of a shorter sequence): publish an empty state
+    grid_dep_wait();
     const size_t part = (size_t)unit * p.splits + split;
     for (int idx = tid; idx < R; idx += kThreads) {
       p.part_ml[(part * R + idx) * 2] = -INFINITY;
@@ -569,7 +577,7 @@ struct Pass2Cfg {
 
 struct Pass2Small {
   uint64_t kfull[2], kempty[2], vfull[4], vempty[4];
-  uint64_t accfull[2], accempty[2], drain;
+  uint64_t accfull[2], accempty[2], drain, aready;
   uint32_t tmem_base;
   int abort;
   float4 rowc[kMaxR];        // per row: (max in log2 units, normaliser L, |a|^2, last visible key as int bits)
@@ -612,6 +620,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < C::VS; ++i) { mbar_init(&S.vfull[i], 1); mbar_init(&S.vempty[i], kWorkerWarps + 1); }
     for (int i = 0; i < 2; ++i) { mbar_init(&S.accfull[i], 1); mbar_init(&S.accempty[i], kWorkerWarps); }
     mbar_init(&S.drain, 1);
+    mbar_init(&S.aready, 1);
     S.abort = 0;
     fence_mbar_init();
   }
@@ -619,16 +628,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid < kWorkers) {
     const __nv_bfloat16* qsrc = p.q + ((size_t)b * p.Hq + (size_t)h * p.g) * p.w * p.d;
     stage_rows_sw128(sQ, qsrc, NR, R, p.d, p.d, tid, kWorkers);
-    const __nv_bfloat16* ahl = p.ahl + (size_t)unit * 2 * kMaxR * kDPad;
-    stage_rows_sw128(sAhi, ahl, NR, NR, kDPad, kDPad, tid, kWorkers);
-    stage_rows_sw128(sAlo, ahl + kMaxR * kDPad, NR, NR, kDPad, kDPad, tid, kWorkers);
     fence_proxy_async_smem();
-    if (tid < kMaxR) {
-      const bool real = tid < R;
-      const size_t o = (size_t)unit * R + tid;
-      S.rowc[tid] = make_float4(real ? p.m2[o] : 0.f, real ? p.l[o] : 1.f, real ? p.aa[o] : 0.f,
-                                __int_as_float(real ? nb - p.w + (tid % p.w) : -1));
-    }
   }
   if (warp == kProducerWarp && lane == 0) { tma_prefetch_desc(&tmk); tma_prefetch_desc(&tmv); }
   tc_fence_before();
@@ -636,6 +636,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = S.tmem_base;
   bool failed = false;
+  // K, V and Q are the caller's inputs: streaming and S = K Q^T start at once;
+  // the merged statistics of pass 1 are staged by the workers after
+  // grid_dep_wait() and released to the MMA warp through `aready`.
+  grid_dep_launch();
 
   if (warp == kProducerWarp) {
     // TMA producer: lane 0 K, lane 1 V
@@ -658,6 +662,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < 8; ++s)
           umma_bf16(dS, desc_kmajor_sw128(kb, kTile, s), desc_kmajor_sw128(qaddr, NR, s), idS, s > 0);
         umma_commit(&S.kempty[ks]);
+        if (i == 0 && !mbar_wait(&S.aready, 0, &S.abort)) { ok = false; break; }
         if (!mbar_wait(&S.vfull[vs], (i / C::VS) & 1, &S.abort)) { ok = false; break; }
         tc_fence_after();
         const uint32_t vb = smem_addr(sV + vs * kTileBytes);
@@ -697,6 +702,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int all_see = nb - p.w;
     float* raw = p.raw + (size_t)unit * p.n_max;
     uint32_t flags = 0;
+    grid_dep_wait();                              // a, |a|^2, m and L come from the merge
+    {
+      const __nv_bfloat16* ahl = p.ahl + (size_t)unit * 2 * kMaxR * kDPad;
+      stage_rows_sw128(sAhi, ahl, NR, NR, kDPad, kDPad, tid, kWorkers);
+      stage_rows_sw128(sAlo, ahl + kMaxR * kDPad, NR, NR, kDPad, kDPad, tid, kWorkers);
+      fence_proxy_async_smem();
+      if (tid < kMaxR) {
+        const bool real = tid < R;
+        const size_t o = (size_t)unit * R + tid;
+        S.rowc[tid] = make_float4(real ? p.m2[o] : 0.f, real ? p.l[o] : 1.f, real ? p.aa[o] : 0.f,
+                                  __int_as_float(real ? nb - p.w + (tid % p.w) : -1));
+      }
+      named_bar(kBarWork, kWorkers);
+      if (tid == 0) mbar_arrive(&S.aready);
+    }
     for (int i = 0; i < T; ++i) {
       const int tile0 = (t0 + i) * kTile, vs = i % C::VS, ab = i & 1;
       const int j = tile0 + tok;
@@ -782,11 +802,9 @@ cudaError_t launch_pass1_t(const AttnParams& p, const CUtensorMap& tk, const CUt
   static_assert(smem <= 232448, "pass-1 shared memory exceeds the per-CTA limit");
   cudaError_t e = cudaFuncSetAttribute(window_attention_kernel<NR>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  window_attention_kernel<NR><<<dim3(p.splits, p.U), kThreads, smem, st>>>(tk, tv, p);
-  e = cudaGetLastError();
+  e = launch_pdl(window_attention_kernel<NR>, dim3(p.splits, p.U), dim3(kThreads), smem, st, tk, tv, p);
   if (e != cudaSuccess) return e;
-  merge_splits_kernel<<<dim3(kMaxR / kMergeRows, p.U), kMergeThreads, 0, st>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(merge_splits_kernel, dim3(kMaxR / kMergeRows, p.U), dim3(kMergeThreads), 0, st, p);
 }
 
 template <int NR>
@@ -795,8 +813,7 @@ cudaError_t launch_pass2_t(const AttnParams& p, const CUtensorMap& tk, const CUt
   static_assert(smem <= 232448, "pass-2 shared memory exceeds the per-CTA limit");
   cudaError_t e = cudaFuncSetAttribute(score_kernel<NR>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  score_kernel<NR><<<dim3(p.splits, p.U), kThreads, smem, st>>>(tk, tv, p);
-  return cudaGetLastError();
+  return launch_pdl(score_kernel<NR>, dim3(p.splits, p.U), dim3(kThreads), smem, st, tk, tv, p);
 }
 
 }  // namespace

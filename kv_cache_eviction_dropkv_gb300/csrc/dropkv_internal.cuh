@@ -3,6 +3,7 @@
 #pragma once
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -98,12 +99,32 @@ struct CompactParams {
   uint32_t* status;
 };
 
+// Launch with programmatic dependent launch: the kernel may be scheduled
+// while its predecessor in the stream is finishing.  Every kernel of the
+// library calls grid_dep_wait() before it reads anything an earlier kernel
+// wrote and before its first global write, so stream order is preserved.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 cudaError_t launch_window_attention(const AttnParams& p, int NR, const CUtensorMap& tk, const CUtensorMap& tv,
                                     int num_ctas_x, cudaStream_t st);
 cudaError_t launch_score(const AttnParams& p, int NR, const CUtensorMap& tk, const CUtensorMap& tv,
                          cudaStream_t st);
 cudaError_t launch_pool_protect(const PoolParams& p, cudaStream_t st);
-cudaError_t launch_select(const SelParams& p, cudaStream_t st);
+cudaError_t launch_select(const SelParams& p, size_t zero_bytes, void* zero_base, cudaStream_t st);
 cudaError_t launch_compact(const CompactParams& p, cudaStream_t st);
 
 }  // namespace dropkv

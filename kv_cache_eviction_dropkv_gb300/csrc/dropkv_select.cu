@@ -19,7 +19,10 @@
 //   3. select_write: each chunk writes its kept positions in ascending order.
 #include <cuda_runtime.h>
 
+#include <algorithm>
+
 #include "dropkv_internal.cuh"
+#include "sm103_ptx.cuh"
 
 namespace dropkv {
 namespace {
@@ -73,6 +76,8 @@ __device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* s
 // ------------------------------------------------------------ pool + protect
 __global__ void __launch_bounds__(kPoolThreads) pool_protect_kernel(const PoolParams p) {
   __shared__ float buf[kPoolTile + 2 * (kMaxPool / 2)];
+  grid_dep_wait();          // the raw scores come from pass 2
+  grid_dep_launch();
   const int unit = blockIdx.y, b = unit / p.Hkv;
   const int nb = p.lengths ? p.lengths[b] : p.n_max;
   if (nb < p.w || nb > p.n_max) return;
@@ -180,12 +185,23 @@ __device__ void find_bin(const uint32_t* gh, uint32_t k, uint32_t* scratch, uint
   __syncthreads();
 }
 
+// Clears the selection counters and histograms (they are accumulated with
+// atomics by the kernels that follow).
+__global__ void __launch_bounds__(256) select_zero_kernel(uint4* base, size_t n16) {
+  grid_dep_wait();
+  grid_dep_launch();
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n16; i += (size_t)gridDim.x * blockDim.x)
+    base[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+
 // Level 1: histogram of the top 12 bits of the score keys of every KV head;
 // the last CTA of a head finds the bin that holds the k_b-th smallest key.
 __global__ void __launch_bounds__(kSelThreads) select_hist_kernel(const SelParams p) {
   __shared__ uint32_t sh[kHistBins];
   __shared__ uint32_t scratch[32];
   __shared__ int is_last;
+  grid_dep_wait();
+  grid_dep_launch();
   const int chunk = blockIdx.x, unit = blockIdx.y, b = unit / p.Hkv, h = unit - b * p.Hkv;
   const UnitInfo ui = unit_info(p, b);
   uint32_t* st = p.state + (size_t)unit * 8;
@@ -303,6 +319,8 @@ __global__ void __launch_bounds__(kSelThreads) select_cand_kernel(const SelParam
   __shared__ uint32_t n2_s;
   __shared__ uint64_t thr_s;
   extern __shared__ uint64_t cand_s[];     // kCandCap composites (last CTA only)
+  grid_dep_wait();
+  grid_dep_launch();
   const int chunk = blockIdx.x, unit = blockIdx.y, b = unit / p.Hkv;
   const UnitInfo ui = unit_info(p, b);
   if (ui.mode == kModeSkip) return;
@@ -465,6 +483,8 @@ __global__ void __launch_bounds__(kSelThreads) select_cand_kernel(const SelParam
 // Level 3: each chunk writes its kept positions in ascending order.
 __global__ void __launch_bounds__(kSelThreads) select_write_kernel(const SelParams p) {
   __shared__ uint32_t scratch[32];
+  grid_dep_wait();
+  grid_dep_launch();
   const int chunk = blockIdx.x, unit = blockIdx.y, b = unit / p.Hkv, h = unit - b * p.Hkv;
   const UnitInfo ui = unit_info(p, b);
   if (chunk == 0 && h == 0 && threadIdx.x == 0)
@@ -512,6 +532,8 @@ constexpr int kRowsPerWarp = 2;
 constexpr int kRowsPerBlock = (kCompactThreads / 32) * kRowsPerWarp;
 
 __global__ void __launch_bounds__(kCompactThreads) compact_kernel(const CompactParams p) {
+  grid_dep_wait();          // kept_idx / kept_len come from the selection
+  grid_dep_launch();
   const int unit = blockIdx.y, b = unit / p.Hkv, h = unit - b * p.Hkv;
   int kl = p.kept_len[b];
   if (kl > p.out_rows) {
@@ -544,30 +566,30 @@ __global__ void __launch_bounds__(kCompactThreads) compact_kernel(const CompactP
 
 cudaError_t launch_pool_protect(const PoolParams& p, cudaStream_t st) {
   dim3 grid((p.n_max + kPoolTile - 1) / kPoolTile, p.B * p.Hkv);
-  pool_protect_kernel<<<grid, kPoolThreads, 0, st>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(pool_protect_kernel, grid, dim3(kPoolThreads), 0, st, p);
 }
 
-cudaError_t launch_select(const SelParams& p, cudaStream_t st) {
+cudaError_t launch_select(const SelParams& p, size_t zero_bytes, void* zero_base, cudaStream_t st) {
+  const size_t n16 = zero_bytes / 16;
+  const int zb = (int)std::min<size_t>((n16 + 255) / 256, 1024);
+  cudaError_t e = launch_pdl(select_zero_kernel, dim3(zb > 0 ? zb : 1), dim3(256), 0, st,
+                             reinterpret_cast<uint4*>(zero_base), n16);
+  if (e != cudaSuccess) return e;
   dim3 grid(p.chunks, p.B * p.Hkv);
-  select_hist_kernel<<<grid, kSelThreads, 0, st>>>(p);
-  cudaError_t e = cudaGetLastError();
+  e = launch_pdl(select_hist_kernel, grid, dim3(kSelThreads), 0, st, p);
   if (e != cudaSuccess) return e;
   const int dyn = kCandCap * (int)sizeof(uint64_t);
   e = cudaFuncSetAttribute(select_cand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
   if (e != cudaSuccess) return e;
-  select_cand_kernel<<<grid, kSelThreads, dyn, st>>>(p);
-  e = cudaGetLastError();
+  e = launch_pdl(select_cand_kernel, grid, dim3(kSelThreads), (size_t)dyn, st, p);
   if (e != cudaSuccess) return e;
-  select_write_kernel<<<grid, kSelThreads, 0, st>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(select_write_kernel, grid, dim3(kSelThreads), 0, st, p);
 }
 
 cudaError_t launch_compact(const CompactParams& p, cudaStream_t st) {
   if (p.out_rows <= 0) return cudaSuccess;
   dim3 grid((p.out_rows + kRowsPerBlock - 1) / kRowsPerBlock, p.B * p.Hkv);
-  compact_kernel<<<grid, kCompactThreads, 0, st>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(compact_kernel, grid, dim3(kCompactThreads), 0, st, p);
 }
 
 }  // namespace dropkv
