@@ -31,7 +31,16 @@ from kv_cache_eviction_dropkv_gb300 import synth  # noqa: E402
 
 METRIC = "DropKV scored tokens/s and ms per layer at n=128K; achieved HBM GB/s vs peak"
 UNIT = "tokens/s"
-KERNELS_PER_STEP = 9      # window attention, split merge, score, pool+protect, 4 selection kernels, compaction
+SEL_CHUNK = 16384         # slots per CTA in the selection kernels
+CLUSTER_MAX_CHUNKS = 8    # heads of up to 8 chunks are selected by one cluster launch
+
+
+def kernels_per_step(n_max):
+    """Kernels one step launches: window attention, split merge, score,
+    pool+protect, the selection (one cluster launch, or clear + 3 radix
+    kernels for heads longer than 8 chunks) and compaction."""
+    chunks = -(-n_max // SEL_CHUNK)
+    return 4 + (1 if chunks <= CLUSTER_MAX_CHUNKS else 4) + 1
 L2_FLUSH_BYTES = 256 << 20
 FALLBACK_HBM_GBS = 6800.0
 
@@ -331,7 +340,7 @@ def main():
             "path_roofline": {"achieved": path_gbs, "peak": peak, "unit": "GB/s", "frac": path_gbs / peak,
                               "algorithmic_bytes_per_step": nbytes["path"]},
             "phases_ms": phase_ms, "phases_note": "per-kernel times from %d separate steps with events at the phase boundaries (window_attention includes the split merge)" % KP,
-            "wall_s_timed": wall, "gpu_launches": KERNELS_PER_STEP * K,
+            "wall_s_timed": wall, "gpu_launches": kernels_per_step(spec.n_max) * K,
             "clocks": clocks}
 
     if not args.no_e2e:

@@ -17,6 +17,7 @@
 //                    few members sharing it and turns the per-chunk kept
 //                    counts into output offsets.
 //   3. select_write: each chunk writes its kept positions in ascending order.
+#include <cooperative_groups.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -526,6 +527,200 @@ __global__ void __launch_bounds__(kSelThreads) select_write_kernel(const SelPara
   }
 }
 
+// ------------------------------------------------------------ cluster selection
+// The whole selection of a KV head inside one thread-block cluster: one CTA
+// per 16384-slot chunk (up to 8 chunks), 1024 threads holding 16 consecutive
+// slots each in registers.  The k-th pair (T, t) is found digit by digit —
+// key bits 31..20, 19..8, 7..0, then the tie rank among slots whose key is T —
+// with each digit's histogram merged across the cluster through distributed
+// shared memory; no global scratch and a single launch.
+namespace cg = cooperative_groups;
+constexpr int kClThreads = 1024;
+constexpr int kClPer = kSelChunk / kClThreads;   // 16 consecutive slots per thread
+constexpr int kClMax = 8;                        // portable cluster size
+
+// CTA r of the cluster sums bins [r*BINS/C, (r+1)*BINS/C) of every CTA's
+// `hist` and writes the sums into every CTA's `merged`.
+template <int BINS>
+__device__ __forceinline__ void cluster_merge(cg::cluster_group& cl, uint32_t* hist, uint32_t* merged, int C, int r) {
+  const int lo = r * BINS / C, hi = (r + 1) * BINS / C;
+  for (int i = lo + (int)threadIdx.x; i < hi; i += kClThreads) {
+    uint32_t s = 0;
+    for (int src = 0; src < C; ++src) s += cl.map_shared_rank(hist, src)[i];
+    for (int dst = 0; dst < C; ++dst) cl.map_shared_rank(merged, dst)[i] = s;
+  }
+}
+
+// Bin of a shared-memory histogram that holds the k-th (1-based) item, the
+// item's rank inside the bin and the bin's count.
+template <int BINS>
+__device__ __forceinline__ void cluster_find_bin(const uint32_t* h, uint32_t k, uint32_t* scratch, uint32_t* bc,
+                                                 uint32_t& bin, uint32_t& rank, uint32_t& count) {
+  constexpr int per = BINS >= kClThreads ? BINS / kClThreads : 1;
+  const int base = (int)threadIdx.x * per;
+  uint32_t cnt[per];
+  uint32_t local = 0;
+#pragma unroll
+  for (int q = 0; q < per; ++q) {
+    cnt[q] = (base + q < BINS) ? h[base + q] : 0u;
+    local += cnt[q];
+  }
+  if (threadIdx.x == 0) { bc[0] = 0; bc[1] = 1; bc[2] = 0; }
+  uint32_t total;
+  const uint32_t before = block_exclusive_scan<kClThreads>(local, scratch, &total);
+  if (before < k && k <= before + local) {
+    uint32_t c = before;
+#pragma unroll
+    for (int q = 0; q < per; ++q) {
+      if (c < k && k <= c + cnt[q]) { bc[0] = base + q; bc[1] = k - c; bc[2] = cnt[q]; }
+      c += cnt[q];
+    }
+  }
+  __syncthreads();
+  bin = bc[0];
+  rank = bc[1];
+  count = bc[2];
+  __syncthreads();
+}
+
+// Run-aggregated shared-memory histogram of this thread's slots: slot u adds
+// to bin `digit(key)` when u < nv and `member(key)`.
+template <typename Member, typename Digit>
+__device__ __forceinline__ void cluster_hist_add(uint32_t* hist, const uint32_t (&key)[kClPer], int nv, Member member,
+                                                 Digit digit) {
+  uint32_t cur = kNoBin, cnt = 0;
+#pragma unroll
+  for (int u = 0; u < kClPer; ++u) {
+    const uint32_t bn = (u < nv && member(key[u])) ? digit(key[u]) : kNoBin;
+    if (bn == cur) {
+      ++cnt;
+    } else {
+      if (cur != kNoBin) atomicAdd(&hist[cur], cnt);
+      cur = bn;
+      cnt = 1;
+    }
+  }
+  if (cur != kNoBin) atomicAdd(&hist[cur], cnt);
+}
+
+__global__ void __launch_bounds__(kClThreads, 1) select_cluster_kernel(const SelParams p) {
+  __shared__ uint32_t hist[kHistBins];
+  __shared__ uint32_t merged[kHistBins];
+  __shared__ uint32_t scratch[32];
+  __shared__ uint32_t bc[3];
+  __shared__ uint32_t xch[2 * kClMax];   // (slots above T, slots equal to T) of every CTA of the cluster
+  cg::cluster_group cl = cg::this_cluster();
+  grid_dep_wait();
+  grid_dep_launch();
+  // the cluster spans blockIdx.x, so the cluster rank is the chunk index
+  const int C = (int)gridDim.x, r = (int)cl.block_rank(), unit = blockIdx.y, b = unit / p.Hkv,
+            h = unit - b * p.Hkv;
+  const UnitInfo ui = unit_info(p, b);
+  if (r == 0 && h == 0 && threadIdx.x == 0) {
+    if (ui.mode == kModeSkip) atomicOr(p.status, DROPKV_FLAG_BAD_LENGTH);
+    else if (ui.kb < 0 || ui.kb > ui.nb - p.protect) atomicOr(p.status, DROPKV_FLAG_BAD_K);
+    p.kept_len[b] = (ui.mode == kModeSkip) ? 0 : ui.nb - (ui.mode == kModeNormal ? ui.kb : 0);
+  }
+  const int nb = (ui.mode == kModeSkip) ? 0 : ui.nb;
+  const int jt = r * kSelChunk + (int)threadIdx.x * kClPer;
+  const int nv = min(max(nb - jt, 0), kClPer);
+  int32_t* out_row = p.kept_idx + (size_t)unit * p.n_max;
+  if (ui.mode != kModeNormal) {
+    // nothing evicted: kept slot j sits at index j (the branch is uniform over the cluster)
+    for (int u = 0; u < nv; ++u) out_row[jt + u] = jt + u;
+    return;
+  }
+  const float* row = p.scores + (size_t)unit * p.n_max;
+  const bool vec = (p.n_max & 3) == 0;
+  uint32_t key[kClPer];
+#pragma unroll
+  for (int q4 = 0; q4 < kClPer / 4; ++q4) {
+    const float4 x = load4(row, jt + q4 * 4, nb, vec);
+    key[q4 * 4 + 0] = f2ord(x.x);
+    key[q4 * 4 + 1] = f2ord(x.y);
+    key[q4 * 4 + 2] = f2ord(x.z);
+    key[q4 * 4 + 3] = f2ord(x.w);
+  }
+
+  // digit 1: key bits 31..20
+  for (int i = threadIdx.x; i < kHistBins; i += kClThreads) hist[i] = 0;
+  __syncthreads();
+  cluster_hist_add(hist, key, nv, [](uint32_t) { return true; }, [](uint32_t k) { return k >> 20; });
+  cl.sync();
+  cluster_merge<kHistBins>(cl, hist, merged, C, r);
+  cl.sync();
+  uint32_t bin1, rank1, cnt1;
+  cluster_find_bin<kHistBins>(merged, (uint32_t)ui.kb, scratch, bc, bin1, rank1, cnt1);
+
+  // digit 2: key bits 19..8 of the members of bin1
+  for (int i = threadIdx.x; i < kHistBins; i += kClThreads) hist[i] = 0;
+  __syncthreads();
+  cluster_hist_add(hist, key, nv, [bin1](uint32_t k) { return (k >> 20) == bin1; },
+                   [](uint32_t k) { return (k >> 8) & 0xFFFu; });
+  cl.sync();
+  cluster_merge<kHistBins>(cl, hist, merged, C, r);
+  cl.sync();
+  uint32_t bin2, rank2, cnt2;
+  cluster_find_bin<kHistBins>(merged, rank1, scratch, bc, bin2, rank2, cnt2);
+  const uint32_t pre24 = (bin1 << 12) | bin2;
+
+  // digit 3: key bits 7..0 of the members sharing the 24-bit prefix
+  for (int i = threadIdx.x; i < 256; i += kClThreads) hist[i] = 0;
+  __syncthreads();
+  cluster_hist_add(hist, key, nv, [pre24](uint32_t k) { return (k >> 8) == pre24; },
+                   [](uint32_t k) { return k & 0xFFu; });
+  cl.sync();
+  cluster_merge<256>(cl, hist, merged, C, r);
+  cl.sync();
+  uint32_t bin3, rank3, cnt3;
+  cluster_find_bin<256>(merged, rank2, scratch, bc, bin3, rank3, cnt3);
+  const uint32_t T = (pre24 << 8) | bin3;
+
+  // tie rank: the slots with key T are evicted in position order up to rank3
+  uint32_t above = 0, ties = 0;
+#pragma unroll
+  for (int u = 0; u < kClPer; ++u) {
+    above += (u < nv && key[u] > T);
+    ties += (u < nv && key[u] == T);
+  }
+  uint32_t packed_total;   // (above << 16 | ties); a chunk holds at most 16384 slots
+  const uint32_t packed_before = block_exclusive_scan<kClThreads>((above << 16) | ties, scratch, &packed_total);
+  if (threadIdx.x < (unsigned)C) {
+    uint32_t* dst = cl.map_shared_rank(xch, (int)threadIdx.x);
+    dst[2 * r] = packed_total >> 16;
+    dst[2 * r + 1] = packed_total & 0xFFFFu;
+  }
+  cl.sync();   // last access to another CTA's shared memory is before this point
+  // offsets of this CTA among the ties and among the kept slots of the head
+  uint32_t tie_pre = 0, kept_pre = 0, tie_off = 0, kept_off = 0;
+  for (int s = 0; s < C; ++s) {
+    const uint32_t a = xch[2 * s], t = xch[2 * s + 1];
+    const int past = (int)(tie_pre + t) - (int)rank3;   // ties of CTA s ranked after rank3
+    if (s == r) { tie_off = tie_pre; kept_off = kept_pre; }
+    tie_pre += t;
+    kept_pre += a + (uint32_t)min(max(past, 0), (int)t);
+  }
+  if (r == 0 && threadIdx.x == 0 && kept_pre != (uint32_t)(nb - ui.kb)) atomicOr(p.status, DROPKV_FLAG_INTERNAL);
+  uint32_t tr = tie_off + (packed_before & 0xFFFFu);   // ties before this thread's slots
+  uint32_t keepmask = 0, cnt = 0;
+#pragma unroll
+  for (int u = 0; u < kClPer; ++u) {
+    const bool eq = u < nv && key[u] == T;
+    tr += eq;
+    const bool keep = u < nv && (key[u] > T || (eq && tr > rank3));
+    keepmask |= (uint32_t)keep << u;
+    cnt += keep;
+  }
+  uint32_t total;
+  const uint32_t before = block_exclusive_scan<kClThreads>(cnt, scratch, &total);
+  int32_t* out = out_row + kept_off + before;
+  while (keepmask) {
+    const int q = __ffs((int)keepmask) - 1;
+    *out++ = jt + q;
+    keepmask &= keepmask - 1;
+  }
+}
+
 // ------------------------------------------------------------ compaction
 constexpr int kCompactThreads = 256;
 constexpr int kRowsPerWarp = 2;
@@ -570,12 +765,31 @@ cudaError_t launch_pool_protect(const PoolParams& p, cudaStream_t st) {
 }
 
 cudaError_t launch_select(const SelParams& p, size_t zero_bytes, void* zero_base, cudaStream_t st) {
+  dim3 grid(p.chunks, p.B * p.Hkv);
+  if (p.chunks <= kClMax) {
+    // one cluster per KV head: no global counters to clear
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kClThreads);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)p.chunks;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, select_cluster_kernel, p);
+    if (e == cudaSuccess) return e;
+    (void)cudaGetLastError();   // clusters refused on this device: take the multi-kernel path
+  }
   const size_t n16 = zero_bytes / 16;
   const int zb = (int)std::min<size_t>((n16 + 255) / 256, 1024);
   cudaError_t e = launch_pdl(select_zero_kernel, dim3(zb > 0 ? zb : 1), dim3(256), 0, st,
                              reinterpret_cast<uint4*>(zero_base), n16);
   if (e != cudaSuccess) return e;
-  dim3 grid(p.chunks, p.B * p.Hkv);
   e = launch_pdl(select_hist_kernel, grid, dim3(kSelThreads), 0, st, p);
   if (e != cudaSuccess) return e;
   const int dyn = kCandCap * (int)sizeof(uint64_t);

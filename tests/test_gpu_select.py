@@ -1,9 +1,12 @@
 """Bit-exact parity of dropkv_select with the oracle's stable sort, on crafted
-score arrays that drive every branch of the radix selection: few ties, a
-24-bit prefix shared by a few slots (direct ranking), large tie sets (radix
-over positions), a level-1 bin larger than the candidate buffer (direct pass
-over the scores), signed zeros, ragged lengths and the k = 0 / k = n - protect
-edges.  Selection is integer work, so the kept sets must be identical."""
+score arrays that drive every branch of both selection paths: heads of up to
+eight 16384-slot chunks are selected inside one thread-block cluster (digit
+histograms merged across the cluster, ties ranked by position across its
+CTAs); longer heads take the multi-kernel radix path (few ties, a 24-bit
+prefix shared by a few slots, large tie sets, a level-1 bin larger than the
+candidate buffer).  Also signed zeros, ragged lengths and the k = 0 /
+k = n - protect edges.  Selection is integer work, so the kept sets must be
+identical."""
 import numpy as np
 import pytest
 import torch
@@ -99,3 +102,45 @@ def test_noaligned_rows():
     n = 16387                                   # rows not 16-byte aligned: scalar loads
     s = rng.random((2, 2, n)).astype(np.float32)
     _check(s, [n, 16385], [8000, 16000], 1)
+
+
+@pytest.mark.parametrize("n", [40000, 70000, 90000, 110000, 131072])
+def test_every_cluster_size(n):
+    """3, 5, 6, 7 and 8 chunks per head: one cluster per KV head of that size."""
+    rng = np.random.default_rng(n + 7)
+    s = (rng.lognormal(0.0, 3.0, (2, 2, n))).astype(np.float32)
+    lengths = [n, n - 16385]
+    s = _protect(s, lengths, 8)
+    _check(s, lengths, [(n - 8) * 19 // 20, (lengths[1] - 8) // 3], 8)
+
+
+def test_ties_straddle_cluster_ctas():
+    """Equal scores in every chunk of a 5-chunk head, cut in the middle of them."""
+    rng = np.random.default_rng(11)
+    n = 80000
+    s = (rng.random((1, 2, n)) + 2.0).astype(np.float32)
+    s[0, :, ::7] = np.float32(2.5)
+    below = int(np.sum(s[0, 0] < 2.5))
+    _check(s, [n], [below + int(np.sum(s[0, 0] == 2.5)) // 2 + 3], 0)
+
+
+@pytest.mark.parametrize("case", ["random", "prefix", "ties2000", "ties12000"])
+def test_multi_kernel_path(case):
+    """Heads longer than eight chunks use the multi-kernel radix selection."""
+    rng = np.random.default_rng(5)
+    n = 150000
+    if case == "random":
+        s = (rng.standard_normal((2, 2, n)) ** 2).astype(np.float32)
+        lengths = [n, 140001]
+        s = _protect(s, lengths, 8)
+        _check(s, lengths, [(n - 8) * 9 // 10, 70000], 8)
+        return
+    s = (rng.random((1, 2, n)) + 2.0).astype(np.float32)
+    if case == "prefix":
+        s[0, 0, 100:140] = np.float32(2.5) + np.arange(40, dtype=np.float32) * np.float32(2 ** -22)
+        _check(s, [n], [int(np.sum(s[0, 0] < 2.5)) + 17], 0)
+        return
+    n_tied = int(case[4:])
+    pos = rng.choice(n, n_tied, replace=False)
+    s[0, :, pos] = np.float32(2.5)
+    _check(s, [n], [int(np.sum(s[0, 0] < 2.5)) + n_tied // 3], 0)
