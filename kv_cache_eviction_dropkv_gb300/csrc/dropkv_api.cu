@@ -96,6 +96,7 @@ bool make_geom(const dropkv_shape* s, int num_sms, Geom* g) {
   // One CTA per SM: spread the U * tiles_max tiles over about num_sms CTAs.
   const long long total = (long long)g->U * g->tiles_max;
   g->tpc1 = (int)std::max<long long>(1, (total + num_sms - 1) / num_sms);
+  g->tpc1 = std::max(g->tpc1, ceil_div_i(g->tiles_max, kMaxSplits));
   g->splits1 = ceil_div_i(g->tiles_max, g->tpc1);
   g->tpc2 = g->tpc1;
   g->splits2 = g->splits1;

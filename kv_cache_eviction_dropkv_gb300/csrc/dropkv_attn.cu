@@ -165,22 +165,24 @@ constexpr int pass1_smem_bytes() {
 // Merge of the split-K partial states (its own small kernel: it sits on the
 // critical path, so it is spread over many CTAs with all loads in flight).
 //   m = max_s m_s;  L = sum_s l_s 2^(m_s - m);  a = sum_s O_s 2^(m_s - m) / L.
-// CTA (row group, KV head): warp w takes row r = 4 * group + w, lane c the
-// float4 column c of a; every split of that column is loaded before any is
-// used.  Also writes |a|^2, the bf16 hi/lo split of a (zero rows past R and
-// zero columns past d) and the exported log-sum-exp.
+// CTA (row group, KV head): warp w takes row r = 4 * group + w.  Lane c holds
+// the (m, l) of splits c, c + 32, ... and float4 column c of every split's O,
+// all requested in one round trip.  Also writes |a|^2, the bf16 hi/lo split
+// of a (zero rows past R and zero columns past d) and the exported
+// log-sum-exp.
 constexpr int kMergeRows = 4;                 // rows per CTA (one warp each)
 constexpr int kMergeThreads = 32 * kMergeRows;
-constexpr int kMergeBatch = 32;               // splits loaded ahead per lane
+constexpr int kMergeSplitRegs = kMaxSplits / 32;
+static_assert(kMergeSplitRegs * 32 == kMaxSplits, "split states are held 32 per register slot");
 
 __global__ void __launch_bounds__(kMergeThreads) merge_splits_kernel(const AttnParams p) {
-  __shared__ float wts_s[kMergeRows][kMergeBatch];
+  __shared__ float wts_s[kMergeRows][32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int unit = blockIdx.y, r = blockIdx.x * kMergeRows + warp;
   const int b = unit / p.Hkv;
+  const int nb = p.lengths ? p.lengths[b] : p.n_max;   // a caller input: read before the wait
   grid_dep_wait();                                // the partials come from pass 1
   grid_dep_launch();
-  const int nb = p.lengths ? p.lengths[b] : p.n_max;
   if (nb < p.w || nb > p.n_max) return;          // flagged by pass 1
   const int S = p.splits, R = p.R, d = p.d, D4 = d >> 2;
   __nv_bfloat16* ahl = p.ahl + (size_t)unit * 2 * kMaxR * kDPad;
@@ -191,52 +193,61 @@ __global__ void __launch_bounds__(kMergeThreads) merge_splits_kernel(const AttnP
     return;
   }
   const float2* ml = reinterpret_cast<const float2*>(p.part_ml) + (size_t)unit * S * R;
-  // row maximum and normaliser over the splits (lanes stride the splits)
-  float M = -INFINITY;
-  for (int s = lane; s < S; s += 32) {
-    const float2 v = __ldcg(ml + (size_t)s * R + r);
-    if (v.y > 0.f) M = fmaxf(M, v.x);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  float L = 0.f;
-  for (int s = lane; s < S; s += 32) {
-    const float2 v = __ldcg(ml + (size_t)s * R + r);
-    if (v.y > 0.f) L = fmaf(v.y, exp2f(v.x - M), L);
-  }
-  L = warp_sum(L);
-  // a for this lane's float4 column
   const float4* po4 = reinterpret_cast<const float4*>(p.part_o + (size_t)unit * S * R * d);
   const size_t split_stride = (size_t)R * D4;
+  // one round trip: the (m, l) of every split and the O column of the first
+  // 32 splits are all requested before any is used (the O partial of a split
+  // without visible keys is never written; its weight is 0 and it is dropped
+  // by a select, not a multiply, so whatever it holds cannot leak in)
+  float2 v[kMergeSplitRegs];
+#pragma unroll
+  for (int q = 0; q < kMergeSplitRegs; ++q) {
+    const int s = q * 32 + lane;
+    v[q] = (s < S) ? __ldcg(ml + (size_t)s * R + r) : make_float2(-INFINITY, 0.f);
+  }
+  float4 o[32];
+#pragma unroll
+  for (int u = 0; u < 32; ++u)
+    o[u] = (lane < D4 && u < S) ? __ldcg(po4 + (size_t)u * split_stride + (size_t)r * D4 + lane)
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+  float M = -INFINITY;
+#pragma unroll
+  for (int q = 0; q < kMergeSplitRegs; ++q)
+    if (v[q].y > 0.f) M = fmaxf(M, v[q].x);
+#pragma unroll
+  for (int o2 = 16; o2 > 0; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o2));
+  float wgt[kMergeSplitRegs];
+  float L = 0.f;
+#pragma unroll
+  for (int q = 0; q < kMergeSplitRegs; ++q) {
+    wgt[q] = (v[q].y > 0.f) ? exp2f(v[q].x - M) : 0.f;
+    L = fmaf(v[q].y, wgt[q], L);
+  }
+  L = warp_sum(L);
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int s0 = 0; s0 < S; s0 += kMergeBatch) {
-    // weights of this batch of splits (0 for splits without visible keys,
-    // whose O partial is never written and so never read)
-    {
-      const int s = s0 + lane;
-      float wgt = 0.f;
-      if (s < S) {
-        const float2 v = __ldcg(ml + (size_t)s * R + r);
-        wgt = (v.y > 0.f) ? exp2f(v.x - M) : 0.f;
+#pragma unroll
+  for (int q = 0; q < kMergeSplitRegs; ++q) {
+    if (q * 32 >= S) break;
+    __syncwarp();
+    wts_s[warp][lane] = wgt[q];
+    __syncwarp();
+    if (q > 0) {
+#pragma unroll
+      for (int u = 0; u < 32; ++u)
+        o[u] = (lane < D4 && q * 32 + u < S)
+                   ? __ldcg(po4 + (size_t)(q * 32 + u) * split_stride + (size_t)r * D4 + lane)
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < 32; ++u) {
+      const float wu = wts_s[warp][u];
+      if (wu != 0.f) {
+        acc.x = fmaf(o[u].x, wu, acc.x);
+        acc.y = fmaf(o[u].y, wu, acc.y);
+        acc.z = fmaf(o[u].z, wu, acc.z);
+        acc.w = fmaf(o[u].w, wu, acc.w);
       }
-      wts_s[warp][lane] = wgt;
     }
-    __syncwarp();
-    float4 o[kMergeBatch];
-#pragma unroll
-    for (int u = 0; u < kMergeBatch; ++u)
-      o[u] = (lane < D4 && s0 + u < S && wts_s[warp][u] != 0.f)
-                 ? __ldcg(po4 + (size_t)(s0 + u) * split_stride + (size_t)r * D4 + lane)
-                 : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int u = 0; u < kMergeBatch; ++u) {
-      const float wgt = wts_s[warp][u];
-      acc.x = fmaf(o[u].x, wgt, acc.x);
-      acc.y = fmaf(o[u].y, wgt, acc.y);
-      acc.z = fmaf(o[u].z, wgt, acc.z);
-      acc.w = fmaf(o[u].w, wgt, acc.w);
-    }
-    __syncwarp();
   }
   const float inv = 1.0f / L;
   const float4 a = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
@@ -636,13 +647,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = S.tmem_base;
   bool failed = false;
-  // K, V and Q are the caller's inputs: streaming and S = K Q^T start at once;
-  // the merged statistics of pass 1 are staged by the workers after
-  // grid_dep_wait() and released to the MMA warp through `aready`.
+  // The merged statistics of pass 1 are staged by the workers after
+  // grid_dep_wait() and released to the MMA warp through `aready`.  The
+  // producer also waits: streaming K and V while the merge runs would only
+  // slow the merge's loads, on which every worker waits.
   grid_dep_launch();
 
   if (warp == kProducerWarp) {
     // TMA producer: lane 0 K, lane 1 V
+    grid_dep_wait();
     if (lane == 0) stream_ring<C::KS>(sK, S.kfull, S.kempty, &tmk, t0, T, unit, &S.abort, p.status);
     else if (lane == 1) stream_ring<C::VS>(sV, S.vfull, S.vempty, &tmv, t0, T, unit, &S.abort, p.status);
     __syncwarp();

@@ -15,6 +15,7 @@ namespace dropkv {
 constexpr int kTile = 128;          // tokens per K/V tile (the MMA M dimension)
 constexpr int kDPad = 128;          // head dimension as staged in shared memory
 constexpr int kMaxR = 64;           // rows (g * w) per KV head supported
+constexpr int kMaxSplits = 160;    // split-K partial states per KV head (merge holds 5 per lane)
 constexpr int kSelChunk = 16384;    // tokens per block in the selection kernels
 constexpr int kHistBins = 4096;     // first-level radix histogram (top 12 key bits)
 constexpr int kCandCap = 8192;      // candidates resolved in shared memory

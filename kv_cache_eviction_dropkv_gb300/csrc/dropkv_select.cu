@@ -531,40 +531,53 @@ __global__ void __launch_bounds__(kSelThreads) select_write_kernel(const SelPara
 // The whole selection of a KV head inside one thread-block cluster: one CTA
 // per 16384-slot chunk (up to 8 chunks), 1024 threads holding 16 consecutive
 // slots each in registers.  The k-th pair (T, t) is found digit by digit —
-// key bits 31..20, 19..8, 7..0, then the tie rank among slots whose key is T —
-// with each digit's histogram merged across the cluster through distributed
-// shared memory; no global scratch and a single launch.
+// key bits 31..20, 19..8, 7..0, then the tie rank among slots whose key is T.
+// Each digit's histogram is built in shared memory, then added bin range by
+// bin range into the CTA that owns the range (distributed shared memory
+// atomics), so one cluster barrier per digit completes it; every CTA then
+// reads the merged bins it needs from their owners.  No global scratch and a
+// single launch.
 namespace cg = cooperative_groups;
 constexpr int kClThreads = 1024;
 constexpr int kClPer = kSelChunk / kClThreads;   // 16 consecutive slots per thread
 constexpr int kClMax = 8;                        // portable cluster size
 
-// CTA r of the cluster sums bins [r*BINS/C, (r+1)*BINS/C) of every CTA's
-// `hist` and writes the sums into every CTA's `merged`.
+struct ClusterSmem {
+  uint32_t hist[kHistBins];   // this CTA's histogram of the current digit
+  uint32_t mg1[kHistBins];    // merged digit-1 bins (the owned range is used)
+  uint32_t mg2[kHistBins];    // merged digit-2 bins
+  uint32_t mg3[256];          // merged digit-3 bins
+  uint32_t scratch[32];
+  uint32_t bc[3];
+  uint32_t xch[2 * kClMax];   // (slots above T, slots equal to T) of every CTA of the cluster
+};
+
+__device__ __forceinline__ int cl_owner(int bin, int bins, int C) { return (int)(((long long)bin * C) / bins); }
+
+// Adds the nonzero bins of the local histogram into the owners' merged copy.
 template <int BINS>
-__device__ __forceinline__ void cluster_merge(cg::cluster_group& cl, uint32_t* hist, uint32_t* merged, int C, int r) {
-  const int lo = r * BINS / C, hi = (r + 1) * BINS / C;
-  for (int i = lo + (int)threadIdx.x; i < hi; i += kClThreads) {
-    uint32_t s = 0;
-    for (int src = 0; src < C; ++src) s += cl.map_shared_rank(hist, src)[i];
-    for (int dst = 0; dst < C; ++dst) cl.map_shared_rank(merged, dst)[i] = s;
+__device__ __forceinline__ void cluster_push(cg::cluster_group& cl, const uint32_t* hist, uint32_t* merged, int C) {
+  for (int i = threadIdx.x; i < BINS; i += kClThreads) {
+    const uint32_t c = hist[i];
+    if (c) atomicAdd(cl.map_shared_rank(merged, cl_owner(i, BINS, C)) + i, c);
   }
 }
 
-// Bin of a shared-memory histogram that holds the k-th (1-based) item, the
-// item's rank inside the bin and the bin's count.
+// Bin of the merged histogram (read from the owners) that holds the k-th
+// (1-based) item, the item's rank inside the bin and the bin's count.
 template <int BINS>
-__device__ __forceinline__ void cluster_find_bin(const uint32_t* h, uint32_t k, uint32_t* scratch, uint32_t* bc,
-                                                 uint32_t& bin, uint32_t& rank, uint32_t& count) {
+__device__ __forceinline__ void cluster_find_bin(cg::cluster_group& cl, uint32_t* merged, int C, uint32_t k,
+                                                 uint32_t* scratch, uint32_t* bc, uint32_t& bin, uint32_t& rank,
+                                                 uint32_t& count) {
   constexpr int per = BINS >= kClThreads ? BINS / kClThreads : 1;
   const int base = (int)threadIdx.x * per;
   uint32_t cnt[per];
   uint32_t local = 0;
 #pragma unroll
-  for (int q = 0; q < per; ++q) {
-    cnt[q] = (base + q < BINS) ? h[base + q] : 0u;
-    local += cnt[q];
-  }
+  for (int q = 0; q < per; ++q)
+    cnt[q] = (base + q < BINS) ? cl.map_shared_rank(merged, cl_owner(base + q, BINS, C))[base + q] : 0u;
+#pragma unroll
+  for (int q = 0; q < per; ++q) local += cnt[q];
   if (threadIdx.x == 0) { bc[0] = 0; bc[1] = 1; bc[2] = 0; }
   uint32_t total;
   const uint32_t before = block_exclusive_scan<kClThreads>(local, scratch, &total);
@@ -604,28 +617,32 @@ __device__ __forceinline__ void cluster_hist_add(uint32_t* hist, const uint32_t 
 }
 
 __global__ void __launch_bounds__(kClThreads, 1) select_cluster_kernel(const SelParams p) {
-  __shared__ uint32_t hist[kHistBins];
-  __shared__ uint32_t merged[kHistBins];
-  __shared__ uint32_t scratch[32];
-  __shared__ uint32_t bc[3];
-  __shared__ uint32_t xch[2 * kClMax];   // (slots above T, slots equal to T) of every CTA of the cluster
+  extern __shared__ __align__(16) uint8_t cl_smem_raw[];
+  ClusterSmem& S = *reinterpret_cast<ClusterSmem*>(cl_smem_raw);
   cg::cluster_group cl = cg::this_cluster();
-  grid_dep_wait();
-  grid_dep_launch();
   // the cluster spans blockIdx.x, so the cluster rank is the chunk index
   const int C = (int)gridDim.x, r = (int)cl.block_rank(), unit = blockIdx.y, b = unit / p.Hkv,
             h = unit - b * p.Hkv;
+  // lengths and k are caller inputs that no kernel of the path writes: read
+  // them, and clear the merge bins, while the scores are still being made
   const UnitInfo ui = unit_info(p, b);
+  const bool normal = ui.mode == kModeNormal;
+  if (normal) {
+    for (int i = threadIdx.x; i < kHistBins; i += kClThreads) S.hist[i] = S.mg1[i] = S.mg2[i] = 0u;
+    if (threadIdx.x < 256) S.mg3[threadIdx.x] = 0u;
+  }
+  grid_dep_wait();
+  grid_dep_launch();
   if (r == 0 && h == 0 && threadIdx.x == 0) {
     if (ui.mode == kModeSkip) atomicOr(p.status, DROPKV_FLAG_BAD_LENGTH);
     else if (ui.kb < 0 || ui.kb > ui.nb - p.protect) atomicOr(p.status, DROPKV_FLAG_BAD_K);
-    p.kept_len[b] = (ui.mode == kModeSkip) ? 0 : ui.nb - (ui.mode == kModeNormal ? ui.kb : 0);
+    p.kept_len[b] = (ui.mode == kModeSkip) ? 0 : ui.nb - (normal ? ui.kb : 0);
   }
   const int nb = (ui.mode == kModeSkip) ? 0 : ui.nb;
   const int jt = r * kSelChunk + (int)threadIdx.x * kClPer;
   const int nv = min(max(nb - jt, 0), kClPer);
   int32_t* out_row = p.kept_idx + (size_t)unit * p.n_max;
-  if (ui.mode != kModeNormal) {
+  if (!normal) {
     // nothing evicted: kept slot j sits at index j (the branch is uniform over the cluster)
     for (int u = 0; u < nv; ++u) out_row[jt + u] = jt + u;
     return;
@@ -641,39 +658,38 @@ __global__ void __launch_bounds__(kClThreads, 1) select_cluster_kernel(const Sel
     key[q4 * 4 + 2] = f2ord(x.z);
     key[q4 * 4 + 3] = f2ord(x.w);
   }
+  __syncthreads();   // cleared bins
 
   // digit 1: key bits 31..20
-  for (int i = threadIdx.x; i < kHistBins; i += kClThreads) hist[i] = 0;
-  __syncthreads();
-  cluster_hist_add(hist, key, nv, [](uint32_t) { return true; }, [](uint32_t k) { return k >> 20; });
-  cl.sync();
-  cluster_merge<kHistBins>(cl, hist, merged, C, r);
+  cluster_hist_add(S.hist, key, nv, [](uint32_t) { return true; }, [](uint32_t k) { return k >> 20; });
+  cl.sync();         // every CTA running, its bins cleared and its histogram complete
+  cluster_push<kHistBins>(cl, S.hist, S.mg1, C);
   cl.sync();
   uint32_t bin1, rank1, cnt1;
-  cluster_find_bin<kHistBins>(merged, (uint32_t)ui.kb, scratch, bc, bin1, rank1, cnt1);
+  cluster_find_bin<kHistBins>(cl, S.mg1, C, (uint32_t)ui.kb, S.scratch, S.bc, bin1, rank1, cnt1);
 
   // digit 2: key bits 19..8 of the members of bin1
-  for (int i = threadIdx.x; i < kHistBins; i += kClThreads) hist[i] = 0;
+  for (int i = threadIdx.x; i < kHistBins; i += kClThreads) S.hist[i] = 0;
   __syncthreads();
-  cluster_hist_add(hist, key, nv, [bin1](uint32_t k) { return (k >> 20) == bin1; },
+  cluster_hist_add(S.hist, key, nv, [bin1](uint32_t k) { return (k >> 20) == bin1; },
                    [](uint32_t k) { return (k >> 8) & 0xFFFu; });
-  cl.sync();
-  cluster_merge<kHistBins>(cl, hist, merged, C, r);
+  __syncthreads();
+  cluster_push<kHistBins>(cl, S.hist, S.mg2, C);
   cl.sync();
   uint32_t bin2, rank2, cnt2;
-  cluster_find_bin<kHistBins>(merged, rank1, scratch, bc, bin2, rank2, cnt2);
+  cluster_find_bin<kHistBins>(cl, S.mg2, C, rank1, S.scratch, S.bc, bin2, rank2, cnt2);
   const uint32_t pre24 = (bin1 << 12) | bin2;
 
   // digit 3: key bits 7..0 of the members sharing the 24-bit prefix
-  for (int i = threadIdx.x; i < 256; i += kClThreads) hist[i] = 0;
+  for (int i = threadIdx.x; i < 256; i += kClThreads) S.hist[i] = 0;
   __syncthreads();
-  cluster_hist_add(hist, key, nv, [pre24](uint32_t k) { return (k >> 8) == pre24; },
+  cluster_hist_add(S.hist, key, nv, [pre24](uint32_t k) { return (k >> 8) == pre24; },
                    [](uint32_t k) { return k & 0xFFu; });
-  cl.sync();
-  cluster_merge<256>(cl, hist, merged, C, r);
+  __syncthreads();
+  cluster_push<256>(cl, S.hist, S.mg3, C);
   cl.sync();
   uint32_t bin3, rank3, cnt3;
-  cluster_find_bin<256>(merged, rank2, scratch, bc, bin3, rank3, cnt3);
+  cluster_find_bin<256>(cl, S.mg3, C, rank2, S.scratch, S.bc, bin3, rank3, cnt3);
   const uint32_t T = (pre24 << 8) | bin3;
 
   // tie rank: the slots with key T are evicted in position order up to rank3
@@ -684,9 +700,9 @@ __global__ void __launch_bounds__(kClThreads, 1) select_cluster_kernel(const Sel
     ties += (u < nv && key[u] == T);
   }
   uint32_t packed_total;   // (above << 16 | ties); a chunk holds at most 16384 slots
-  const uint32_t packed_before = block_exclusive_scan<kClThreads>((above << 16) | ties, scratch, &packed_total);
+  const uint32_t packed_before = block_exclusive_scan<kClThreads>((above << 16) | ties, S.scratch, &packed_total);
   if (threadIdx.x < (unsigned)C) {
-    uint32_t* dst = cl.map_shared_rank(xch, (int)threadIdx.x);
+    uint32_t* dst = cl.map_shared_rank(S.xch, (int)threadIdx.x);
     dst[2 * r] = packed_total >> 16;
     dst[2 * r + 1] = packed_total & 0xFFFFu;
   }
@@ -694,7 +710,7 @@ __global__ void __launch_bounds__(kClThreads, 1) select_cluster_kernel(const Sel
   // offsets of this CTA among the ties and among the kept slots of the head
   uint32_t tie_pre = 0, kept_pre = 0, tie_off = 0, kept_off = 0;
   for (int s = 0; s < C; ++s) {
-    const uint32_t a = xch[2 * s], t = xch[2 * s + 1];
+    const uint32_t a = S.xch[2 * s], t = S.xch[2 * s + 1];
     const int past = (int)(tie_pre + t) - (int)rank3;   // ties of CTA s ranked after rank3
     if (s == r) { tie_off = tie_pre; kept_off = kept_pre; }
     tie_pre += t;
@@ -712,7 +728,7 @@ __global__ void __launch_bounds__(kClThreads, 1) select_cluster_kernel(const Sel
     cnt += keep;
   }
   uint32_t total;
-  const uint32_t before = block_exclusive_scan<kClThreads>(cnt, scratch, &total);
+  const uint32_t before = block_exclusive_scan<kClThreads>(cnt, S.scratch, &total);
   int32_t* out = out_row + kept_off + before;
   while (keepmask) {
     const int q = __ffs((int)keepmask) - 1;
@@ -772,6 +788,7 @@ cudaError_t launch_select(const SelParams& p, size_t zero_bytes, void* zero_base
     cfg.gridDim = grid;
     cfg.blockDim = dim3(kClThreads);
     cfg.stream = st;
+    cfg.dynamicSmemBytes = sizeof(ClusterSmem);
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)p.chunks;
@@ -781,7 +798,9 @@ cudaError_t launch_select(const SelParams& p, size_t zero_bytes, void* zero_base
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, select_cluster_kernel, p);
+    cudaError_t e = cudaFuncSetAttribute(select_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)sizeof(ClusterSmem));
+    if (e == cudaSuccess) e = cudaLaunchKernelEx(&cfg, select_cluster_kernel, p);
     if (e == cudaSuccess) return e;
     (void)cudaGetLastError();   // clusters refused on this device: take the multi-kernel path
   }
