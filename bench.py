@@ -36,11 +36,12 @@ CLUSTER_MAX_CHUNKS = 8    # heads of up to 8 chunks are selected by one cluster 
 
 
 def kernels_per_step(n_max):
-    """Kernels one step launches: window attention, split merge, score,
-    pool+protect, the selection (one cluster launch, or clear + 3 radix
-    kernels for heads longer than 8 chunks) and compaction."""
+    """Kernels one dropkv_evict step launches: window attention, split merge,
+    score, then either one cluster selection that also pools, or (heads
+    longer than 8 chunks) pool+protect, clear and 3 radix kernels; then
+    compaction."""
     chunks = -(-n_max // SEL_CHUNK)
-    return 4 + (1 if chunks <= CLUSTER_MAX_CHUNKS else 4) + 1
+    return 3 + (1 if chunks <= CLUSTER_MAX_CHUNKS else 5) + 1
 L2_FLUSH_BYTES = 256 << 20
 FALLBACK_HBM_GBS = 6800.0
 
@@ -88,7 +89,11 @@ def workload_bytes(spec, lengths, kept):
     p1 = U_tok * kv
     p2 = U_tok * (kv + 4)                                 # + raw score write
     pool = U_tok * 8
-    sel = U_tok * 4 * 3 + spec.Hkv * int(sum(kept)) * 4   # hist, candidates, write passes + kept idx
+    # selection: the cluster kernel selects from the pooled scores it has just
+    # made in shared memory (pool's 8 B cover its reads and writes); the
+    # multi-kernel path for heads longer than 8 chunks reads the scores 3 times
+    sel_passes = 0 if -(-spec.n_max // SEL_CHUNK) <= CLUSTER_MAX_CHUNKS else 3
+    sel = U_tok * 4 * sel_passes + spec.Hkv * int(sum(kept)) * 4
     comp = spec.Hkv * int(sum(kept)) * (4 + 2 * 2 * spec.d * 2)
     return {"window_attention": p1, "score": p2, "pool_protect": pool, "select": sel, "compact": comp,
             "path": p1 + p2 + pool + sel + comp}
@@ -256,9 +261,9 @@ def main():
             op.run(q, k, v, lengths, ev, stream=stream, keep_raw=False)
         else:
             B.dropkv_score_timed(op.shape, q, k, v, lengths, op.pool_kernel, op.protect, op.scores, None,
-                                 op.workspace, op.status, events[1:5], stream)
+                                 op.workspace, op.status, events[1:6], stream)
             op.select(lengths, ev, stream)
-            events[5].record(stream)
+            events[6].record(stream)
             op.compact(k, v, stream)
 
     for w in range(max(3, args.warmup)):
@@ -296,7 +301,7 @@ def main():
 
     # per-kernel phases, in separate steps with events at the phase boundaries
     KP = max(3, min(K, 50))
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(KP)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(KP)]
     for row in evs:
         for e in row:
             e.record(stream)
@@ -305,15 +310,15 @@ def main():
         flush_l2(i)
         evs[i][0].record(stream)
         step(evs[i])
-        evs[i][6].record(stream)
+        evs[i][7].record(stream)
     torch.cuda.synchronize()
     op.check(stream)
 
     def ms(a, b):
         return [evs[i][a].elapsed_time(evs[i][b]) for i in range(KP)]
 
-    phases = {"window_attention": ms(1, 2), "score": ms(2, 3), "pool_protect": ms(3, 4),
-              "select": ms(4, 5), "compact": ms(5, 6)}
+    phases = {"window_attention": ms(1, 2), "split_merge": ms(2, 3), "score": ms(3, 4), "pool_protect": ms(4, 5),
+              "select": ms(5, 6), "compact": ms(6, 7)}
     step_ms = sum(t_step) / K
     if world > 1:
         t = torch.tensor([step_ms], device=dev)
@@ -339,7 +344,7 @@ def main():
             "roofline": roofline,
             "path_roofline": {"achieved": path_gbs, "peak": peak, "unit": "GB/s", "frac": path_gbs / peak,
                               "algorithmic_bytes_per_step": nbytes["path"]},
-            "phases_ms": phase_ms, "phases_note": "per-kernel times from %d separate steps with events at the phase boundaries (window_attention includes the split merge)" % KP,
+            "phases_ms": phase_ms, "phases_note": "per-kernel times from %d separate steps with events at the phase boundaries, run as the three separate calls (pooling in its own kernel; the timed step pools inside the selection)" % KP,
             "wall_s_timed": wall, "gpu_launches": kernels_per_step(spec.n_max) * K,
             "clocks": clocks}
 

@@ -88,8 +88,9 @@ typedef struct {
  *   float a[U][R][d]   sum_j p_j v_j             (offset round_up(4*U*R, 256)) */
 DROPKV_API size_t dropkv_workspace_size(const dropkv_shape* shape);
 
-/* Steps S1-S5: window attention, per-token perturbation score, GQA average,
- * MaxPool1D and recent-slot protection.
+/* Steps S1-S4: window attention with its split-K merge, per-token
+ * perturbation score with the GQA average, MaxPool1D and recent-slot
+ * protection.
  *   q_window  device bf16 [B][Hq][w][d]  last w query rows of every query head
  *   k, v      device bf16 [B][Hkv][n_max][d]  cached keys / values; only rows
  *             j < lengths[b] are read
@@ -109,10 +110,11 @@ DROPKV_API dropkv_status dropkv_score(const dropkv_shape* shape, const void* q_w
                            float* raw_scores, void* workspace, size_t workspace_bytes, uint32_t* status,
                            cudaStream_t stream);
 
-/* dropkv_score that also records phase_events[0..3] on `stream`: before pass 1
- * (window attention), between pass 1 and pass 2 (scoring), between pass 2 and
- * pooling, and after pooling -- for per-kernel timing with CUDA events.  The
- * events are created by the caller; everything else is as dropkv_score. */
+/* dropkv_score that also records phase_events[0..4] on `stream`: before pass 1
+ * (window attention), between pass 1 and the split-K merge, between the merge
+ * and pass 2 (scoring), between pass 2 and pooling, and after pooling -- for
+ * per-kernel timing with CUDA events.  The events are created by the caller;
+ * everything else is as dropkv_score. */
 DROPKV_API dropkv_status dropkv_score_timed(const dropkv_shape* shape, const void* q_window, const void* k,
                                             const void* v, const int32_t* lengths, int32_t pool_kernel,
                                             int32_t protect, float* scores, float* raw_scores, void* workspace,
@@ -140,7 +142,7 @@ DROPKV_API dropkv_status dropkv_score_noalloc(const dropkv_shape* shape, const v
                                               int32_t protect, float* scores, float* raw_scores, uint32_t* status,
                                               cudaStream_t stream);
 
-/* Step S6: evict the evict_k[b] lowest scores of every KV head (equal scores:
+/* Step S5: evict the evict_k[b] lowest scores of every KV head (equal scores:
  * the lower position is evicted first) and list the kept positions.
  *   scores    device float [B][Hkv][n_max] (as written by dropkv_score)
  *   lengths   device int32 [B] or NULL (n_max)
@@ -155,7 +157,7 @@ DROPKV_API dropkv_status dropkv_select(const dropkv_shape* shape, const float* s
                             const int32_t* evict_k, int32_t protect, int32_t* kept_idx, int32_t* kept_len,
                             void* workspace, size_t workspace_bytes, uint32_t* status, cudaStream_t stream);
 
-/* Step S7: gather the kept rows of K and V.
+/* Step S6: gather the kept rows of K and V.
  *   k, v      device bf16 [B][Hkv][n_max][d]
  *   kept_idx, kept_len  as written by dropkv_select
  *   out_rows  row capacity of the outputs per head (>= max_b kept_len[b],
@@ -167,6 +169,20 @@ DROPKV_API dropkv_status dropkv_select(const dropkv_shape* shape, const float* s
 DROPKV_API dropkv_status dropkv_compact(const dropkv_shape* shape, const void* k, const void* v, const int32_t* kept_idx,
                              const int32_t* kept_len, int32_t out_rows, void* k_out, void* v_out,
                              uint32_t* status, cudaStream_t stream);
+
+/* Steps S1-S6 in one call: dropkv_score, dropkv_select and (when k_out and
+ * v_out are given) dropkv_compact, with the same arguments, outputs and
+ * results as those three calls in sequence.  Every argument is checked before
+ * anything is launched.  Heads of at most 8 * 16384 slots have MaxPool1D and
+ * protection done inside the selection kernel (the pooled scores are still
+ * written to `scores`), one launch fewer than the separate calls.
+ *   k_out, v_out  both NULL (no compaction; out_rows ignored) or both set
+ * Sources: as for the three calls. */
+DROPKV_API dropkv_status dropkv_evict(const dropkv_shape* shape, const void* q_window, const void* k, const void* v,
+                                      const int32_t* lengths, const int32_t* evict_k, int32_t pool_kernel,
+                                      int32_t protect, float* scores, float* raw_scores, int32_t* kept_idx,
+                                      int32_t* kept_len, int32_t out_rows, void* k_out, void* v_out, void* workspace,
+                                      size_t workspace_bytes, uint32_t* status, cudaStream_t stream);
 
 /* Synchronise `stream`, read the device status word and map it to a status
  * (the first of SINGULAR, NONFINITE, DEVICE_ARG, TIMEOUT that is set, else OK;

@@ -65,6 +65,8 @@ def lib():
             L.dropkv_select.restype = ctypes.c_int
             L.dropkv_compact.argtypes = [SH, P, P, P, P, I32, P, P, P, P]
             L.dropkv_compact.restype = ctypes.c_int
+            L.dropkv_evict.argtypes = [SH, P, P, P, P, P, I32, I32, P, P, P, P, I32, P, P, P, SZ, P, P]
+            L.dropkv_evict.restype = ctypes.c_int
             L.dropkv_read_status.argtypes = [P, P, ctypes.POINTER(ctypes.c_uint32)]
             L.dropkv_read_status.restype = ctypes.c_int
             L.dropkv_version.argtypes = []
@@ -121,8 +123,10 @@ def dropkv_score(shape, q_window, k, v, lengths, pool_kernel, protect, scores, r
 
 def dropkv_score_timed(shape, q_window, k, v, lengths, pool_kernel, protect, scores, raw_scores, workspace,
                        status, events, stream=None):
-    """dropkv_score recording 4 torch.cuda.Event objects at its phase boundaries."""
-    arr = (ctypes.c_void_p * 4)(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    """dropkv_score recording 5 torch.cuda.Event objects at its phase boundaries."""
+    if len(events) != 5:
+        raise ValueError("dropkv_score_timed records 5 events")
+    arr = (ctypes.c_void_p * 5)(*[ctypes.c_void_p(e.cuda_event) for e in events])
     code = lib().dropkv_score_timed(ctypes.byref(shape), _ptr(q_window), _ptr(k), _ptr(v), _ptr(lengths),
                                     int(pool_kernel), int(protect), _ptr(scores), _ptr(raw_scores),
                                     _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(status),
@@ -150,6 +154,15 @@ def dropkv_compact(shape, k, v, kept_idx, kept_len, out_rows, k_out, v_out, stat
     code = lib().dropkv_compact(ctypes.byref(shape), _ptr(k), _ptr(v), _ptr(kept_idx), _ptr(kept_len),
                                 int(out_rows), _ptr(k_out), _ptr(v_out), _ptr(status), _stream(stream))
     return _check(code, "dropkv_compact")
+
+
+def dropkv_evict(shape, q_window, k, v, lengths, evict_k, pool_kernel, protect, scores, raw_scores, kept_idx,
+                 kept_len, out_rows, k_out, v_out, workspace, status, stream=None):
+    code = lib().dropkv_evict(ctypes.byref(shape), _ptr(q_window), _ptr(k), _ptr(v), _ptr(lengths), _ptr(evict_k),
+                              int(pool_kernel), int(protect), _ptr(scores), _ptr(raw_scores), _ptr(kept_idx),
+                              _ptr(kept_len), int(out_rows), _ptr(k_out), _ptr(v_out), _ptr(workspace),
+                              workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream))
+    return _check(code, "dropkv_evict")
 
 
 def dropkv_read_status(status, stream=None):

@@ -62,6 +62,13 @@ class DropKV:
                          self.status, stream)
 
     def run(self, q, k, v, lengths, evict_k, stream=None, keep_raw=True):
+        """The whole step in one library call (dropkv_evict)."""
+        B.dropkv_evict(self.shape, q, k, v, lengths, evict_k, self.pool_kernel, self.protect, self.scores,
+                       self.raw_scores if keep_raw else None, self.kept_idx, self.kept_len, self.out_rows,
+                       self.k_out, self.v_out, self.workspace, self.status, stream)
+
+    def run_separate(self, q, k, v, lengths, evict_k, stream=None, keep_raw=True):
+        """The same step as three library calls (score, select, compact)."""
         self.score(q, k, v, lengths, stream, keep_raw)
         self.select(lengths, evict_k, stream)
         self.compact(k, v, stream)

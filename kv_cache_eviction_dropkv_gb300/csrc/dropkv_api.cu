@@ -156,7 +156,7 @@ namespace {
 dropkv_status score_impl(const dropkv_shape* shape, const void* q_window, const void* k, const void* v,
                          const int32_t* lengths, int32_t pool_kernel, int32_t protect, float* scores,
                          float* raw_scores, void* workspace, size_t workspace_bytes, uint32_t* status,
-                         cudaStream_t stream, cudaEvent_t* ev) {
+                         cudaStream_t stream, cudaEvent_t* ev, PoolParams* defer_pool = nullptr) {
   const int sms = current_sms(nullptr);
   if (sms <= 0) return DROPKV_ERR_CUDA;
   if (!shape) return DROPKV_ERR_INVALID_ARG;
@@ -203,10 +203,12 @@ dropkv_status score_impl(const dropkv_shape* shape, const void* q_window, const 
   p.tpc = g.tpc1;
   if (launch_window_attention(p, g.NR, tk, tv, g.splits1, stream) != cudaSuccess) return DROPKV_ERR_CUDA;
   if (ev && cudaEventRecord(ev[1], stream) != cudaSuccess) return DROPKV_ERR_CUDA;
+  if (launch_merge(p, stream) != cudaSuccess) return DROPKV_ERR_CUDA;
+  if (ev && cudaEventRecord(ev[2], stream) != cudaSuccess) return DROPKV_ERR_CUDA;
   p.splits = g.splits2;
   p.tpc = g.tpc2;
   if (launch_score(p, g.NR, tk, tv, stream) != cudaSuccess) return DROPKV_ERR_CUDA;
-  if (ev && cudaEventRecord(ev[2], stream) != cudaSuccess) return DROPKV_ERR_CUDA;
+  if (ev && cudaEventRecord(ev[3], stream) != cudaSuccess) return DROPKV_ERR_CUDA;
 
   PoolParams pp{};
   pp.raw = p.raw;
@@ -216,9 +218,77 @@ dropkv_status score_impl(const dropkv_shape* shape, const void* q_window, const 
   pp.half = pool_kernel / 2;
   pp.protect = protect;
   pp.status = status;
+  if (defer_pool) {   // the caller's selection pools (dropkv_evict)
+    *defer_pool = pp;
+    return DROPKV_OK;
+  }
   if (launch_pool_protect(pp, stream) != cudaSuccess) return DROPKV_ERR_CUDA;
-  if (ev && cudaEventRecord(ev[3], stream) != cudaSuccess) return DROPKV_ERR_CUDA;
+  if (ev && cudaEventRecord(ev[4], stream) != cudaSuccess) return DROPKV_ERR_CUDA;
   return DROPKV_OK;
+}
+
+dropkv_status select_impl(const dropkv_shape* shape, const float* scores, const int32_t* lengths,
+                          const int32_t* evict_k, int32_t protect, int32_t* kept_idx, int32_t* kept_len,
+                          void* workspace, size_t workspace_bytes, uint32_t* status, cudaStream_t stream,
+                          const PoolParams* pool, bool check_only = false) {
+  const int sms = current_sms(nullptr);
+  if (sms <= 0) return DROPKV_ERR_CUDA;
+  Geom g;
+  if (!shape || !make_geom(shape, sms, &g)) return DROPKV_ERR_INVALID_ARG;
+  if (!scores || !evict_k || !kept_idx || !kept_len || !status || protect < 0) return DROPKV_ERR_INVALID_ARG;
+  if (!aligned16(scores) || !aligned16(kept_idx)) return DROPKV_ERR_INVALID_ARG;
+  const WsPlan w = make_plan(g);
+  if (!workspace || workspace_bytes < w.total || !aligned16(workspace)) return DROPKV_ERR_WORKSPACE;
+  if (check_only) return DROPKV_OK;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  SelParams p{};
+  p.scores = scores;
+  p.lengths = lengths;
+  p.evict_k = evict_k;
+  p.kept_idx = kept_idx;
+  p.kept_len = kept_len;
+  p.B = g.B; p.Hkv = g.Hkv; p.n_max = g.n_max; p.protect = protect; p.chunks = g.chunks;
+  p.hist = reinterpret_cast<uint32_t*>(ws + w.hist);
+  p.hist2 = reinterpret_cast<uint32_t*>(ws + w.hist2);
+  p.state = reinterpret_cast<uint32_t*>(ws + w.sel_state);
+  p.cand = reinterpret_cast<uint32_t*>(ws + w.cand);
+  p.cand_cnt = reinterpret_cast<uint32_t*>(ws + w.cand_cnt);
+  p.tickets = reinterpret_cast<uint32_t*>(ws + w.sel_tickets);
+  p.chunk_kept = reinterpret_cast<uint32_t*>(ws + w.chunk_kept);
+  p.chunk_off = reinterpret_cast<uint32_t*>(ws + w.chunk_off);
+  p.status = status;
+  if (pool) p.pool = *pool;
+  return launch_select(p, w.sel_zero_end - w.sel_zero_begin, ws + w.sel_zero_begin, stream) == cudaSuccess
+             ? DROPKV_OK
+             : DROPKV_ERR_CUDA;
+}
+
+dropkv_status compact_impl(const dropkv_shape* shape, const void* k, const void* v, const int32_t* kept_idx,
+                           const int32_t* kept_len, int32_t out_rows, void* k_out, void* v_out, uint32_t* status,
+                           cudaStream_t stream, bool check_only) {
+  const int sms = current_sms(nullptr);
+  if (sms <= 0) return DROPKV_ERR_CUDA;
+  Geom g;
+  if (!shape || !make_geom(shape, sms, &g)) return DROPKV_ERR_INVALID_ARG;
+  if (!k || !v || !kept_idx || !kept_len || !k_out || !v_out || !status || out_rows < 0)
+    return DROPKV_ERR_INVALID_ARG;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_out) || !aligned16(v_out)) return DROPKV_ERR_INVALID_ARG;
+  const size_t in_bytes = (size_t)g.U * g.n_max * g.d * 2, out_bytes = (size_t)g.U * out_rows * g.d * 2;
+  if (out_rows > 0 && (ranges_overlap(k_out, out_bytes, k, in_bytes) || ranges_overlap(k_out, out_bytes, v, in_bytes) ||
+                       ranges_overlap(v_out, out_bytes, k, in_bytes) || ranges_overlap(v_out, out_bytes, v, in_bytes) ||
+                       ranges_overlap(k_out, out_bytes, v_out, out_bytes)))
+    return DROPKV_ERR_INVALID_ARG;
+  if (check_only) return DROPKV_OK;
+  CompactParams p{};
+  p.k = static_cast<const uint8_t*>(k);
+  p.v = static_cast<const uint8_t*>(v);
+  p.kept_idx = kept_idx;
+  p.kept_len = kept_len;
+  p.k_out = static_cast<uint8_t*>(k_out);
+  p.v_out = static_cast<uint8_t*>(v_out);
+  p.B = g.B; p.Hkv = g.Hkv; p.n_max = g.n_max; p.row_bytes = g.d * 2; p.out_rows = out_rows;
+  p.status = status;
+  return launch_compact(p, stream) == cudaSuccess ? DROPKV_OK : DROPKV_ERR_CUDA;
 }
 
 }  // namespace
@@ -245,61 +315,38 @@ dropkv_status dropkv_score_timed(const dropkv_shape* shape, const void* q_window
 dropkv_status dropkv_select(const dropkv_shape* shape, const float* scores, const int32_t* lengths,
                             const int32_t* evict_k, int32_t protect, int32_t* kept_idx, int32_t* kept_len,
                             void* workspace, size_t workspace_bytes, uint32_t* status, cudaStream_t stream) {
-  const int sms = current_sms(nullptr);
-  if (sms <= 0) return DROPKV_ERR_CUDA;
-  Geom g;
-  if (!shape || !make_geom(shape, sms, &g)) return DROPKV_ERR_INVALID_ARG;
-  if (!scores || !evict_k || !kept_idx || !kept_len || !status || protect < 0) return DROPKV_ERR_INVALID_ARG;
-  if (!aligned16(scores) || !aligned16(kept_idx)) return DROPKV_ERR_INVALID_ARG;
-  const WsPlan w = make_plan(g);
-  if (!workspace || workspace_bytes < w.total || !aligned16(workspace)) return DROPKV_ERR_WORKSPACE;
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  SelParams p{};
-  p.scores = scores;
-  p.lengths = lengths;
-  p.evict_k = evict_k;
-  p.kept_idx = kept_idx;
-  p.kept_len = kept_len;
-  p.B = g.B; p.Hkv = g.Hkv; p.n_max = g.n_max; p.protect = protect; p.chunks = g.chunks;
-  p.hist = reinterpret_cast<uint32_t*>(ws + w.hist);
-  p.hist2 = reinterpret_cast<uint32_t*>(ws + w.hist2);
-  p.state = reinterpret_cast<uint32_t*>(ws + w.sel_state);
-  p.cand = reinterpret_cast<uint32_t*>(ws + w.cand);
-  p.cand_cnt = reinterpret_cast<uint32_t*>(ws + w.cand_cnt);
-  p.tickets = reinterpret_cast<uint32_t*>(ws + w.sel_tickets);
-  p.chunk_kept = reinterpret_cast<uint32_t*>(ws + w.chunk_kept);
-  p.chunk_off = reinterpret_cast<uint32_t*>(ws + w.chunk_off);
-  p.status = status;
-  return launch_select(p, w.sel_zero_end - w.sel_zero_begin, ws + w.sel_zero_begin, stream) == cudaSuccess
-             ? DROPKV_OK
-             : DROPKV_ERR_CUDA;
+  return select_impl(shape, scores, lengths, evict_k, protect, kept_idx, kept_len, workspace, workspace_bytes, status,
+                     stream, nullptr);
 }
 
 dropkv_status dropkv_compact(const dropkv_shape* shape, const void* k, const void* v, const int32_t* kept_idx,
                              const int32_t* kept_len, int32_t out_rows, void* k_out, void* v_out,
                              uint32_t* status, cudaStream_t stream) {
-  const int sms = current_sms(nullptr);
-  if (sms <= 0) return DROPKV_ERR_CUDA;
-  Geom g;
-  if (!shape || !make_geom(shape, sms, &g)) return DROPKV_ERR_INVALID_ARG;
-  if (!k || !v || !kept_idx || !kept_len || !k_out || !v_out || !status || out_rows < 0)
-    return DROPKV_ERR_INVALID_ARG;
-  if (!aligned16(k) || !aligned16(v) || !aligned16(k_out) || !aligned16(v_out)) return DROPKV_ERR_INVALID_ARG;
-  const size_t in_bytes = (size_t)g.U * g.n_max * g.d * 2, out_bytes = (size_t)g.U * out_rows * g.d * 2;
-  if (out_rows > 0 && (ranges_overlap(k_out, out_bytes, k, in_bytes) || ranges_overlap(k_out, out_bytes, v, in_bytes) ||
-                       ranges_overlap(v_out, out_bytes, k, in_bytes) || ranges_overlap(v_out, out_bytes, v, in_bytes) ||
-                       ranges_overlap(k_out, out_bytes, v_out, out_bytes)))
-    return DROPKV_ERR_INVALID_ARG;
-  CompactParams p{};
-  p.k = static_cast<const uint8_t*>(k);
-  p.v = static_cast<const uint8_t*>(v);
-  p.kept_idx = kept_idx;
-  p.kept_len = kept_len;
-  p.k_out = static_cast<uint8_t*>(k_out);
-  p.v_out = static_cast<uint8_t*>(v_out);
-  p.B = g.B; p.Hkv = g.Hkv; p.n_max = g.n_max; p.row_bytes = g.d * 2; p.out_rows = out_rows;
-  p.status = status;
-  return launch_compact(p, stream) == cudaSuccess ? DROPKV_OK : DROPKV_ERR_CUDA;
+  return compact_impl(shape, k, v, kept_idx, kept_len, out_rows, k_out, v_out, status, stream, false);
+}
+
+dropkv_status dropkv_evict(const dropkv_shape* shape, const void* q_window, const void* k, const void* v,
+                           const int32_t* lengths, const int32_t* evict_k, int32_t pool_kernel, int32_t protect,
+                           float* scores, float* raw_scores, int32_t* kept_idx, int32_t* kept_len, int32_t out_rows,
+                           void* k_out, void* v_out, void* workspace, size_t workspace_bytes, uint32_t* status,
+                           cudaStream_t stream) {
+  // every argument is checked before anything is launched
+  dropkv_status st = select_impl(shape, scores, lengths, evict_k, protect, kept_idx, kept_len, workspace,
+                                 workspace_bytes, status, stream, nullptr, /*check_only=*/true);
+  if (st != DROPKV_OK) return st;
+  if ((k_out == nullptr) != (v_out == nullptr)) return DROPKV_ERR_INVALID_ARG;
+  if (k_out) {
+    st = compact_impl(shape, k, v, kept_idx, kept_len, out_rows, k_out, v_out, status, stream, true);
+    if (st != DROPKV_OK) return st;
+  }
+  PoolParams pool{};
+  st = score_impl(shape, q_window, k, v, lengths, pool_kernel, protect, scores, raw_scores, workspace,
+                  workspace_bytes, status, stream, nullptr, &pool);
+  if (st != DROPKV_OK) return st;
+  st = select_impl(shape, scores, lengths, evict_k, protect, kept_idx, kept_len, workspace, workspace_bytes, status,
+                   stream, &pool);
+  if (st != DROPKV_OK || !k_out) return st;
+  return compact_impl(shape, k, v, kept_idx, kept_len, out_rows, k_out, v_out, status, stream, false);
 }
 
 dropkv_status dropkv_read_status(const uint32_t* status, cudaStream_t stream, uint32_t* flags_out) {

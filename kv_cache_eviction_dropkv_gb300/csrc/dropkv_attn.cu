@@ -815,9 +815,7 @@ cudaError_t launch_pass1_t(const AttnParams& p, const CUtensorMap& tk, const CUt
   static_assert(smem <= 232448, "pass-1 shared memory exceeds the per-CTA limit");
   cudaError_t e = cudaFuncSetAttribute(window_attention_kernel<NR>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(window_attention_kernel<NR>, dim3(p.splits, p.U), dim3(kThreads), smem, st, tk, tv, p);
-  if (e != cudaSuccess) return e;
-  return launch_pdl(merge_splits_kernel, dim3(kMaxR / kMergeRows, p.U), dim3(kMergeThreads), 0, st, p);
+  return launch_pdl(window_attention_kernel<NR>, dim3(p.splits, p.U), dim3(kThreads), smem, st, tk, tv, p);
 }
 
 template <int NR>
@@ -839,6 +837,10 @@ cudaError_t launch_window_attention(const AttnParams& p, int NR, const CUtensorM
     case 64: return launch_pass1_t<64>(p, tk, tv, st);
     default: return cudaErrorInvalidValue;
   }
+}
+
+cudaError_t launch_merge(const AttnParams& p, cudaStream_t st) {
+  return launch_pdl(merge_splits_kernel, dim3(kMaxR / kMergeRows, p.U), dim3(kMergeThreads), 0, st, p);
 }
 
 cudaError_t launch_score(const AttnParams& p, int NR, const CUtensorMap& tk, const CUtensorMap& tv,

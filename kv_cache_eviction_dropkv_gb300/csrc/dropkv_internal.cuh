@@ -87,6 +87,9 @@ struct SelParams {
   int B, Hkv, n_max, protect, chunks;
   uint32_t *hist, *hist2, *state, *cand, *cand_cnt, *tickets, *chunk_kept, *chunk_off;
   uint32_t* status;
+  // Optional pooling stage (pool.raw != nullptr): the selection first pools
+  // pool.raw into pool.scores (== scores) as pool_protect_kernel would.
+  PoolParams pool;
 };
 
 struct CompactParams {
@@ -122,6 +125,7 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 
 cudaError_t launch_window_attention(const AttnParams& p, int NR, const CUtensorMap& tk, const CUtensorMap& tv,
                                     int num_ctas_x, cudaStream_t st);
+cudaError_t launch_merge(const AttnParams& p, cudaStream_t st);
 cudaError_t launch_score(const AttnParams& p, int NR, const CUtensorMap& tk, const CUtensorMap& tv,
                          cudaStream_t st);
 cudaError_t launch_pool_protect(const PoolParams& p, cudaStream_t st);

@@ -122,6 +122,7 @@ extern "C" dropkv_status dropkv_score_noalloc(const dropkv_shape* shape, const v
   p.splits = g.splits1;
   p.tpc = g.tpc1;
   if (launch_window_attention(p, g.NR, tk, tv, g.splits1, stream) != cudaSuccess) return DROPKV_ERR_CUDA;
+  if (launch_merge(p, stream) != cudaSuccess) return DROPKV_ERR_CUDA;
   p.splits = g.splits2;
   p.tpc = g.tpc2;
   if (launch_score(p, g.NR, tk, tv, stream) != cudaSuccess) return DROPKV_ERR_CUDA;

@@ -551,6 +551,13 @@ struct ClusterSmem {
   uint32_t bc[3];
   uint32_t xch[2 * kClMax];   // (slots above T, slots equal to T) of every CTA of the cluster
 };
+// Extra shared memory when the selection also pools: the chunk's raw scores
+// with a halo of kClHalo >= kMaxPool / 2 slots on each side (a multiple of 4,
+// so the chunk itself is 16-byte aligned for vector copies).
+constexpr int kClHalo = 32;
+static_assert(kClHalo >= kMaxPool / 2 && kClHalo % 4 == 0, "pooling halo");
+constexpr int kClPoolFloats = kSelChunk + 2 * kClHalo;
+constexpr size_t kClPoolOff = (sizeof(ClusterSmem) + 15) & ~size_t(15);   // 16-byte aligned for float4 reads
 
 __device__ __forceinline__ int cl_owner(int bin, int bins, int C) { return (int)(((long long)bin * C) / bins); }
 
@@ -642,21 +649,100 @@ __global__ void __launch_bounds__(kClThreads, 1) select_cluster_kernel(const Sel
   const int jt = r * kSelChunk + (int)threadIdx.x * kClPer;
   const int nv = min(max(nb - jt, 0), kClPer);
   int32_t* out_row = p.kept_idx + (size_t)unit * p.n_max;
+  const bool vec = (p.n_max & 3) == 0;
+  uint32_t key[kClPer];
+  bool have_keys = false;
+  if (p.pool.raw) {
+    // MaxPool1D (window clipped to [0, n_b)) then protection of the last
+    // `protect` slots, as pool_protect_kernel; skipped for lengths that
+    // kernel rejects (the window statistics flag them)
+    const int pnb = p.lengths ? p.lengths[b] : p.n_max;
+    if (pnb >= p.pool.w && pnb <= p.n_max) {
+      // buf[i] = raw[j0 - kClHalo + i]; -inf outside [0, n_b)
+      float* buf = reinterpret_cast<float*>(cl_smem_raw + kClPoolOff);
+      const int half = p.pool.half, j0 = r * kSelChunk;
+      const float* raw = p.pool.raw + (size_t)unit * p.n_max;
+      float4 x[kClPer / 4];
+#pragma unroll
+      for (int q = 0; q < kClPer / 4; ++q) {
+        const int j = j0 + 4 * ((int)threadIdx.x + q * kClThreads);
+        if (vec && j + 3 < pnb) {
+          x[q] = __ldg(reinterpret_cast<const float4*>(raw + j));
+        } else {
+          x[q].x = (j < pnb) ? __ldg(raw + j) : -INFINITY;
+          x[q].y = (j + 1 < pnb) ? __ldg(raw + j + 1) : -INFINITY;
+          x[q].z = (j + 2 < pnb) ? __ldg(raw + j + 2) : -INFINITY;
+          x[q].w = (j + 3 < pnb) ? __ldg(raw + j + 3) : -INFINITY;
+        }
+      }
+      if (threadIdx.x < 2 * kClHalo) {
+        const int i = threadIdx.x < kClHalo ? (int)threadIdx.x : kSelChunk + (int)threadIdx.x;
+        const int jj = j0 - kClHalo + i;
+        buf[i] = (jj >= 0 && jj < pnb) ? __ldg(raw + jj) : -INFINITY;
+      }
+#pragma unroll
+      for (int q = 0; q < kClPer / 4; ++q)
+        *reinterpret_cast<float4*>(buf + kClHalo + 4 * ((int)threadIdx.x + q * kClThreads)) = x[q];
+      __syncthreads();
+      // this thread's 16 consecutive slots, from the 16 + 2 * half values around them
+      const int base = kClHalo + (int)threadIdx.x * kClPer;
+      float pv[kClPer];
+      if (half <= 4) {
+        float wv[kClPer + 8];
+#pragma unroll
+        for (int c = 0; c < (kClPer + 8) / 4; ++c) {
+          const float4 t = *reinterpret_cast<const float4*>(buf + base - 4 + 4 * c);
+          wv[4 * c] = t.x; wv[4 * c + 1] = t.y; wv[4 * c + 2] = t.z; wv[4 * c + 3] = t.w;
+        }
+#pragma unroll
+        for (int u = 0; u < kClPer; ++u) {
+          float m = wv[4 + u];
+#pragma unroll
+          for (int t = 1; t <= 4; ++t)
+            if (t <= half) m = fmaxf(m, fmaxf(wv[4 + u - t], wv[4 + u + t]));
+          pv[u] = m;
+        }
+      } else {
+#pragma unroll
+        for (int u = 0; u < kClPer; ++u) {
+          float m = buf[base + u - half];
+          for (int t = 1; t <= 2 * half; ++t) m = fmaxf(m, buf[base + u - half + t]);
+          pv[u] = m;
+        }
+      }
+      const int first_protected = pnb - p.protect;
+      float* out = p.pool.scores + (size_t)unit * p.n_max + jt;
+#pragma unroll
+      for (int u = 0; u < kClPer; ++u) pv[u] = (jt + u >= first_protected) ? INFINITY : pv[u];
+      if (vec && jt + kClPer <= pnb) {
+#pragma unroll
+        for (int q = 0; q < kClPer / 4; ++q)
+          reinterpret_cast<float4*>(out)[q] = make_float4(pv[4 * q], pv[4 * q + 1], pv[4 * q + 2], pv[4 * q + 3]);
+      } else {
+#pragma unroll
+        for (int u = 0; u < kClPer; ++u)
+          if (jt + u < pnb) out[u] = pv[u];
+      }
+#pragma unroll
+      for (int u = 0; u < kClPer; ++u) key[u] = f2ord(pv[u]);
+      have_keys = true;
+    }
+  }
   if (!normal) {
     // nothing evicted: kept slot j sits at index j (the branch is uniform over the cluster)
     for (int u = 0; u < nv; ++u) out_row[jt + u] = jt + u;
     return;
   }
-  const float* row = p.scores + (size_t)unit * p.n_max;
-  const bool vec = (p.n_max & 3) == 0;
-  uint32_t key[kClPer];
+  if (!have_keys) {
+    const float* row = p.scores + (size_t)unit * p.n_max;
 #pragma unroll
-  for (int q4 = 0; q4 < kClPer / 4; ++q4) {
-    const float4 x = load4(row, jt + q4 * 4, nb, vec);
-    key[q4 * 4 + 0] = f2ord(x.x);
-    key[q4 * 4 + 1] = f2ord(x.y);
-    key[q4 * 4 + 2] = f2ord(x.z);
-    key[q4 * 4 + 3] = f2ord(x.w);
+    for (int q4 = 0; q4 < kClPer / 4; ++q4) {
+      const float4 x = load4(row, jt + q4 * 4, nb, vec);
+      key[q4 * 4 + 0] = f2ord(x.x);
+      key[q4 * 4 + 1] = f2ord(x.y);
+      key[q4 * 4 + 2] = f2ord(x.z);
+      key[q4 * 4 + 3] = f2ord(x.w);
+    }
   }
   __syncthreads();   // cleared bins
 
@@ -788,7 +874,8 @@ cudaError_t launch_select(const SelParams& p, size_t zero_bytes, void* zero_base
     cfg.gridDim = grid;
     cfg.blockDim = dim3(kClThreads);
     cfg.stream = st;
-    cfg.dynamicSmemBytes = sizeof(ClusterSmem);
+    const size_t smem = p.pool.raw ? kClPoolOff + kClPoolFloats * sizeof(float) : sizeof(ClusterSmem);
+    cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)p.chunks;
@@ -799,10 +886,14 @@ cudaError_t launch_select(const SelParams& p, size_t zero_bytes, void* zero_base
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     cudaError_t e = cudaFuncSetAttribute(select_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)sizeof(ClusterSmem));
+                                         (int)(kClPoolOff + kClPoolFloats * sizeof(float)));
     if (e == cudaSuccess) e = cudaLaunchKernelEx(&cfg, select_cluster_kernel, p);
     if (e == cudaSuccess) return e;
     (void)cudaGetLastError();   // clusters refused on this device: take the multi-kernel path
+  }
+  if (p.pool.raw) {
+    const cudaError_t e = launch_pool_protect(p.pool, st);
+    if (e != cudaSuccess) return e;
   }
   const size_t n16 = zero_bytes / 16;
   const int zb = (int)std::min<size_t>((n16 + 255) / 256, 1024);

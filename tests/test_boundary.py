@@ -17,7 +17,8 @@ def test_library_exports_every_declared_symbol():
     lib = ctypes.CDLL(path)
     declared = B.declared_functions()
     assert set(declared) == {"dropkv_workspace_size", "dropkv_score", "dropkv_score_timed", "dropkv_score_noalloc",
-                             "dropkv_select", "dropkv_compact", "dropkv_read_status", "dropkv_version"}
+                             "dropkv_select", "dropkv_compact", "dropkv_evict", "dropkv_read_status",
+                             "dropkv_version"}
     for name in declared:
         assert hasattr(lib, name), name
     out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True, check=True).stdout
@@ -95,6 +96,18 @@ def test_host_validation_rejects_without_launch():
                                B._ptr(op.kept_len), 10, B._ptr(k), B._ptr(op.v_out), B._ptr(op.status),
                                B._stream(None))
     assert r == 1
+    # the one-call path checks every argument before it launches anything
+    op.kept_len.fill_(-3)
+    evict = lambda **kw: B.lib().dropkv_evict(
+        ctypes.byref(op.shape), B._ptr(q), B._ptr(k), B._ptr(v), B._ptr(lengths), kw.get("ev", B._ptr(ev)),
+        kw.get("pool", 5), 8, B._ptr(op.scores), None, B._ptr(op.kept_idx), B._ptr(op.kept_len), 10,
+        kw.get("k_out", B._ptr(op.k_out)), kw.get("v_out", B._ptr(op.v_out)), B._ptr(op.workspace),
+        kw.get("ws", op.workspace.numel()), B._ptr(op.status), B._stream(None))
+    assert [evict(v_out=None), evict(k_out=B._ptr(k)), evict(ev=None), evict(pool=2),
+            evict(ws=op.workspace.numel() - 1)] == [1, 1, 1, 1, 2]
+    torch.cuda.synchronize()
+    assert torch.all(op.scores == 3.0) and torch.all(op.kept_len == -3)
+    assert int(op.status.item()) == 0
 
 
 @gpu

@@ -170,3 +170,31 @@ def test_ties_and_protection():
     k[0, 0, 100:400] = k[0, 0, 100]
     v[0, 0, 100:400] = v[0, 0, 100]
     _run_custom(q, k, v, lens, [250], 1, 2)
+
+
+@pytest.mark.parametrize("name,n_max,pool", [("tiny_d16_n128", None, None), ("phi3mini_mha_d96_n4k", None, None),
+                                              ("qwen_gqa7_b4_ragged_n64k", None, None),
+                                              ("llama8b_gqa_d128_n32k", 40000, 63),
+                                              ("llama8b_gqa_d128_n32k", 140000, None)])
+def test_one_call_equals_three_calls(name, n_max, pool):
+    """dropkv_evict (pooling inside the cluster selection for heads of at most
+    8 chunks; pool kernel + multi-kernel selection beyond) writes exactly what
+    dropkv_score, dropkv_select and dropkv_compact write in sequence."""
+    wl = synth.make_workload(name, n_max=n_max) if n_max else synth.make_workload(name)
+    s = wl.spec
+    kappa = pool or s.pool_kernel
+    q, k, v = wl.q.to(DEV), wl.k.to(DEV), wl.v.to(DEV)
+    lengths, ev = wl.lengths.to(DEV), wl.evict_k.to(DEV)
+    outs = []
+    for fused in (True, False):
+        op = DropKV(s.B, s.Hq, s.Hkv, s.d, s.n_max, s.w, kappa, s.protect, device=DEV)
+        for t in (op.scores, op.raw_scores):
+            t.fill_(SENTINEL)
+        op.kept_idx.fill_(-5)
+        op.k_out.zero_()
+        op.v_out.zero_()
+        (op.run if fused else op.run_separate)(q, k, v, lengths, ev)
+        op.check()
+        outs.append([t.clone() for t in (op.scores, op.raw_scores, op.kept_idx, op.kept_len, op.k_out, op.v_out)])
+    for a, b in zip(*outs):
+        assert torch.equal(a.view(torch.int8), b.view(torch.int8))
