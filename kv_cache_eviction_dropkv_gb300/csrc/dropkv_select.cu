@@ -17,7 +17,6 @@
 //                    few members sharing it and turns the per-chunk kept
 //                    counts into output offsets.
 //   3. select_write: each chunk writes its kept positions in ascending order.
-#include <cooperative_groups.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -532,19 +531,18 @@ __global__ void __launch_bounds__(kSelThreads) select_write_kernel(const SelPara
 // per 16384-slot chunk (up to 8 chunks), 1024 threads holding 16 consecutive
 // slots each in registers.  The k-th pair (T, t) is found digit by digit —
 // key bits 31..20, 19..8, 7..0, then the tie rank among slots whose key is T.
-// Each digit's histogram is built in shared memory, then added bin range by
-// bin range into the CTA that owns the range (distributed shared memory
-// atomics), so one cluster barrier per digit completes it; every CTA then
-// reads the merged bins it needs from their owners.  No global scratch and a
-// single launch.
-namespace cg = cooperative_groups;
+// Each digit's histogram is built in shared memory, then its nonzero bins are
+// added into every CTA's merged copy with distributed-shared-memory
+// reductions (fire and forget), so one cluster barrier per digit completes
+// the merged histogram in every CTA and the k-th item's bin is found from
+// local shared memory.  No global scratch and a single launch.
 constexpr int kClThreads = 1024;
 constexpr int kClPer = kSelChunk / kClThreads;   // 16 consecutive slots per thread
 constexpr int kClMax = 8;                        // portable cluster size
 
 struct ClusterSmem {
   uint32_t hist[kHistBins];   // this CTA's histogram of the current digit
-  uint32_t mg1[kHistBins];    // merged digit-1 bins (the owned range is used)
+  uint32_t mg1[kHistBins];    // merged digit-1 bins (the sums of every CTA's histogram)
   uint32_t mg2[kHistBins];    // merged digit-2 bins
   uint32_t mg3[256];          // merged digit-3 bins
   uint32_t scratch[32];
@@ -559,32 +557,57 @@ static_assert(kClHalo >= kMaxPool / 2 && kClHalo % 4 == 0, "pooling halo");
 constexpr int kClPoolFloats = kSelChunk + 2 * kClHalo;
 constexpr size_t kClPoolOff = (sizeof(ClusterSmem) + 15) & ~size_t(15);   // 16-byte aligned for float4 reads
 
-__device__ __forceinline__ int cl_owner(int bin, int bins, int C) { return (int)(((long long)bin * C) / bins); }
+// Cluster barrier halves (every thread of every CTA of the cluster arrives;
+// release / acquire order the shared-memory accesses around it).
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_barrier() {
+  cluster_arrive();
+  cluster_wait();
+}
 
-// Adds the nonzero bins of the local histogram into the owners' merged copy.
+// Address of `local` (this CTA's shared memory) in the shared memory of the
+// cluster's CTA `rank`.
+__device__ __forceinline__ uint32_t cluster_map(const void* local, uint32_t rank) {
+  uint32_t out;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(smem_addr(local)), "r"(rank));
+  return out;
+}
+__device__ __forceinline__ void cluster_red_add(uint32_t addr, uint32_t v) {
+  asm volatile("red.shared::cluster.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void cluster_store(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// Adds the nonzero bins of the local histogram into every CTA's merged copy.
 template <int BINS>
-__device__ __forceinline__ void cluster_push(cg::cluster_group& cl, const uint32_t* hist, uint32_t* merged, int C) {
+__device__ __forceinline__ void cluster_push(const uint32_t* hist, uint32_t* merged, int C) {
   for (int i = threadIdx.x; i < BINS; i += kClThreads) {
     const uint32_t c = hist[i];
-    if (c) atomicAdd(cl.map_shared_rank(merged, cl_owner(i, BINS, C)) + i, c);
+    if (c)
+      for (int dst = 0; dst < C; ++dst) cluster_red_add(cluster_map(merged + i, (uint32_t)dst), c);
   }
 }
 
-// Bin of the merged histogram (read from the owners) that holds the k-th
-// (1-based) item, the item's rank inside the bin and the bin's count.
+// Bin of the merged shared-memory histogram that holds the k-th (1-based)
+// item, the item's rank inside the bin and the bin's count.
 template <int BINS>
-__device__ __forceinline__ void cluster_find_bin(cg::cluster_group& cl, uint32_t* merged, int C, uint32_t k,
-                                                 uint32_t* scratch, uint32_t* bc, uint32_t& bin, uint32_t& rank,
-                                                 uint32_t& count) {
+__device__ __forceinline__ void cluster_find_bin(const uint32_t* merged, uint32_t k, uint32_t* scratch, uint32_t* bc,
+                                                 uint32_t& bin, uint32_t& rank, uint32_t& count) {
   constexpr int per = BINS >= kClThreads ? BINS / kClThreads : 1;
   const int base = (int)threadIdx.x * per;
   uint32_t cnt[per];
   uint32_t local = 0;
 #pragma unroll
-  for (int q = 0; q < per; ++q)
-    cnt[q] = (base + q < BINS) ? cl.map_shared_rank(merged, cl_owner(base + q, BINS, C))[base + q] : 0u;
-#pragma unroll
-  for (int q = 0; q < per; ++q) local += cnt[q];
+  for (int q = 0; q < per; ++q) {
+    cnt[q] = (base + q < BINS) ? merged[base + q] : 0u;
+    local += cnt[q];
+  }
   if (threadIdx.x == 0) { bc[0] = 0; bc[1] = 1; bc[2] = 0; }
   uint32_t total;
   const uint32_t before = block_exclusive_scan<kClThreads>(local, scratch, &total);
@@ -626,10 +649,9 @@ __device__ __forceinline__ void cluster_hist_add(uint32_t* hist, const uint32_t 
 __global__ void __launch_bounds__(kClThreads, 1) select_cluster_kernel(const SelParams p) {
   extern __shared__ __align__(16) uint8_t cl_smem_raw[];
   ClusterSmem& S = *reinterpret_cast<ClusterSmem*>(cl_smem_raw);
-  cg::cluster_group cl = cg::this_cluster();
-  // the cluster spans blockIdx.x, so the cluster rank is the chunk index
-  const int C = (int)gridDim.x, r = (int)cl.block_rank(), unit = blockIdx.y, b = unit / p.Hkv,
-            h = unit - b * p.Hkv;
+  // the cluster spans blockIdx.x (its dimension is gridDim.x), so the rank
+  // of a CTA in its cluster is its chunk index
+  const int C = (int)gridDim.x, r = (int)blockIdx.x, unit = blockIdx.y, b = unit / p.Hkv, h = unit - b * p.Hkv;
   // lengths and k are caller inputs that no kernel of the path writes: read
   // them, and clear the merge bins, while the scores are still being made
   const UnitInfo ui = unit_info(p, b);
@@ -637,6 +659,9 @@ __global__ void __launch_bounds__(kClThreads, 1) select_cluster_kernel(const Sel
   if (normal) {
     for (int i = threadIdx.x; i < kHistBins; i += kClThreads) S.hist[i] = S.mg1[i] = S.mg2[i] = 0u;
     if (threadIdx.x < 256) S.mg3[threadIdx.x] = 0u;
+    // first barrier, split: arrive now (bins cleared), wait before the first
+    // access to another CTA, so its latency hides behind the loads
+    cluster_arrive();
   }
   grid_dep_wait();
   grid_dep_launch();
@@ -748,11 +773,12 @@ __global__ void __launch_bounds__(kClThreads, 1) select_cluster_kernel(const Sel
 
   // digit 1: key bits 31..20
   cluster_hist_add(S.hist, key, nv, [](uint32_t) { return true; }, [](uint32_t k) { return k >> 20; });
-  cl.sync();         // every CTA running, its bins cleared and its histogram complete
-  cluster_push<kHistBins>(cl, S.hist, S.mg1, C);
-  cl.sync();
+  __syncthreads();
+  cluster_wait();    // every CTA of the cluster running, its merged bins cleared
+  cluster_push<kHistBins>(S.hist, S.mg1, C);
+  cluster_barrier();
   uint32_t bin1, rank1, cnt1;
-  cluster_find_bin<kHistBins>(cl, S.mg1, C, (uint32_t)ui.kb, S.scratch, S.bc, bin1, rank1, cnt1);
+  cluster_find_bin<kHistBins>(S.mg1, (uint32_t)ui.kb, S.scratch, S.bc, bin1, rank1, cnt1);
 
   // digit 2: key bits 19..8 of the members of bin1
   for (int i = threadIdx.x; i < kHistBins; i += kClThreads) S.hist[i] = 0;
@@ -760,10 +786,10 @@ __global__ void __launch_bounds__(kClThreads, 1) select_cluster_kernel(const Sel
   cluster_hist_add(S.hist, key, nv, [bin1](uint32_t k) { return (k >> 20) == bin1; },
                    [](uint32_t k) { return (k >> 8) & 0xFFFu; });
   __syncthreads();
-  cluster_push<kHistBins>(cl, S.hist, S.mg2, C);
-  cl.sync();
+  cluster_push<kHistBins>(S.hist, S.mg2, C);
+  cluster_barrier();
   uint32_t bin2, rank2, cnt2;
-  cluster_find_bin<kHistBins>(cl, S.mg2, C, rank1, S.scratch, S.bc, bin2, rank2, cnt2);
+  cluster_find_bin<kHistBins>(S.mg2, rank1, S.scratch, S.bc, bin2, rank2, cnt2);
   const uint32_t pre24 = (bin1 << 12) | bin2;
 
   // digit 3: key bits 7..0 of the members sharing the 24-bit prefix
@@ -772,10 +798,10 @@ __global__ void __launch_bounds__(kClThreads, 1) select_cluster_kernel(const Sel
   cluster_hist_add(S.hist, key, nv, [pre24](uint32_t k) { return (k >> 8) == pre24; },
                    [](uint32_t k) { return k & 0xFFu; });
   __syncthreads();
-  cluster_push<256>(cl, S.hist, S.mg3, C);
-  cl.sync();
+  cluster_push<256>(S.hist, S.mg3, C);
+  cluster_barrier();
   uint32_t bin3, rank3, cnt3;
-  cluster_find_bin<256>(cl, S.mg3, C, rank2, S.scratch, S.bc, bin3, rank3, cnt3);
+  cluster_find_bin<256>(S.mg3, rank2, S.scratch, S.bc, bin3, rank3, cnt3);
   const uint32_t T = (pre24 << 8) | bin3;
 
   // tie rank: the slots with key T are evicted in position order up to rank3
@@ -788,11 +814,10 @@ __global__ void __launch_bounds__(kClThreads, 1) select_cluster_kernel(const Sel
   uint32_t packed_total;   // (above << 16 | ties); a chunk holds at most 16384 slots
   const uint32_t packed_before = block_exclusive_scan<kClThreads>((above << 16) | ties, S.scratch, &packed_total);
   if (threadIdx.x < (unsigned)C) {
-    uint32_t* dst = cl.map_shared_rank(S.xch, (int)threadIdx.x);
-    dst[2 * r] = packed_total >> 16;
-    dst[2 * r + 1] = packed_total & 0xFFFFu;
+    cluster_store(cluster_map(S.xch + 2 * r, threadIdx.x), packed_total >> 16);
+    cluster_store(cluster_map(S.xch + 2 * r + 1, threadIdx.x), packed_total & 0xFFFFu);
   }
-  cl.sync();   // last access to another CTA's shared memory is before this point
+  cluster_barrier();   // last access to another CTA's shared memory is before this point
   // offsets of this CTA among the ties and among the kept slots of the head
   uint32_t tie_pre = 0, kept_pre = 0, tie_off = 0, kept_off = 0;
   for (int s = 0; s < C; ++s) {
@@ -803,19 +828,20 @@ __global__ void __launch_bounds__(kClThreads, 1) select_cluster_kernel(const Sel
     kept_pre += a + (uint32_t)min(max(past, 0), (int)t);
   }
   if (r == 0 && threadIdx.x == 0 && kept_pre != (uint32_t)(nb - ui.kb)) atomicOr(p.status, DROPKV_FLAG_INTERNAL);
-  uint32_t tr = tie_off + (packed_before & 0xFFFFu);   // ties before this thread's slots
-  uint32_t keepmask = 0, cnt = 0;
+  // kept slots of the earlier threads of this CTA: all their slots above T,
+  // and their ties ranked after rank3 (tie ranks tie_off + 1 .. tie_off + tb)
+  const uint32_t ab = packed_before >> 16, tb = packed_before & 0xFFFFu;
+  const int tb_kept = min(max((int)(tie_off + tb) - (int)rank3, 0), (int)tb);
+  uint32_t tr = tie_off + tb;   // tie rank before this thread's slots
+  uint32_t keepmask = 0;
 #pragma unroll
   for (int u = 0; u < kClPer; ++u) {
     const bool eq = u < nv && key[u] == T;
     tr += eq;
     const bool keep = u < nv && (key[u] > T || (eq && tr > rank3));
     keepmask |= (uint32_t)keep << u;
-    cnt += keep;
   }
-  uint32_t total;
-  const uint32_t before = block_exclusive_scan<kClThreads>(cnt, S.scratch, &total);
-  int32_t* out = out_row + kept_off + before;
+  int32_t* out = out_row + kept_off + ab + (uint32_t)tb_kept;
   while (keepmask) {
     const int q = __ffs((int)keepmask) - 1;
     *out++ = jt + q;
