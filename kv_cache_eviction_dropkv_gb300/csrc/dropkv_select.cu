@@ -681,7 +681,7 @@ __global__ void __launch_bounds__(kClThreads, 1) select_cluster_kernel(const Sel
     // MaxPool1D (window clipped to [0, n_b)) then protection of the last
     // `protect` slots, as pool_protect_kernel; skipped for lengths that
     // kernel rejects (the window statistics flag them)
-    const int pnb = p.lengths ? p.lengths[b] : p.n_max;
+    const int pnb = ui.nb;   // lengths[b] (or n_max), read before the wait
     if (pnb >= p.pool.w && pnb <= p.n_max) {
       // buf[i] = raw[j0 - kClHalo + i]; -inf outside [0, n_b)
       float* buf = reinterpret_cast<float*>(cl_smem_raw + kClPoolOff);
