@@ -65,6 +65,9 @@ def _load():
             lib.oracle_score.argtypes = [ctypes.POINTER(_Shape), ctypes.c_int, P, P, P, P,
                                          ctypes.c_int, ctypes.c_int, P, P, P, P, P, ctypes.c_int, P]
             lib.oracle_score.restype = ctypes.c_int
+            lib.oracle_score_kind.argtypes = [ctypes.POINTER(_Shape), ctypes.c_int, ctypes.c_int, P, P, P, P,
+                                              ctypes.c_int, ctypes.c_int, P, P, P, P, P, ctypes.c_int, P]
+            lib.oracle_score_kind.restype = ctypes.c_int
             lib.oracle_select.argtypes = [ctypes.POINTER(_Shape), P, P, P, ctypes.c_int, P, P]
             lib.oracle_select.restype = ctypes.c_int
             lib.oracle_compact.argtypes = [ctypes.POINTER(_Shape), ctypes.c_int, P, P, P, P,
@@ -87,7 +90,7 @@ class use_library:
         _load()
         self.saved = _lib
         lib = ctypes.CDLL(self.path)
-        for name in ("oracle_score", "oracle_select", "oracle_compact"):
+        for name in ("oracle_score", "oracle_score_kind", "oracle_select", "oracle_compact"):
             getattr(lib, name).argtypes = getattr(self.saved, name).argtypes
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
@@ -139,12 +142,17 @@ def default_threads() -> int:
     return max(1, os.cpu_count() or 1)
 
 
+KINDS = {"dropkv": 0, "snapkv": 1}
+
+
 def score(q, k, v, lengths=None, pool_kernel: int = 1, protect: int = 0,
-          nthreads: Optional[int] = None, want_stats: bool = True) -> dict:
+          nthreads: Optional[int] = None, want_stats: bool = True, kind: str = "dropkv") -> dict:
     """Run steps S1-S5.  q [B,Hq,w,d]; k, v [B,Hkv,n_max,d]; lengths [B] (None: n_max).
 
     Returns dict with m, l [B,Hq,w], a [B,Hq,w,d] (if want_stats), raw and final
-    [B,Hkv,n_max] (NaN beyond n_b).  Raises SingularInput for p_j == 1."""
+    [B,Hkv,n_max] (NaN beyond n_b).  Raises SingularInput for p_j == 1 (DropKV
+    kind only).  kind "snapkv" scores each key by the window sum of its
+    attention probabilities instead of the perturbation."""
     qa, dt_q = _as_input(q)
     ka, dt_k = _as_input(k)
     va, dt_v = _as_input(v)
@@ -164,10 +172,10 @@ def score(q, k, v, lengths=None, pool_kernel: int = 1, protect: int = 0,
     fin = np.empty((B, Hkv, n_max))
     su = np.zeros(1, dtype=np.int32)
     nt = nthreads if nthreads is not None else default_threads()
-    st = _load().oracle_score(ctypes.byref(shape), dt_q, _ptr(qa), _ptr(ka), _ptr(va), _ptr(lens),
-                              pool_kernel, protect,
-                              _ptr(m) if want_stats else None, _ptr(l) if want_stats else None,
-                              _ptr(a) if want_stats else None, _ptr(raw), _ptr(fin), nt, _ptr(su))
+    st = _load().oracle_score_kind(ctypes.byref(shape), KINDS[kind], dt_q, _ptr(qa), _ptr(ka), _ptr(va),
+                                   _ptr(lens), pool_kernel, protect,
+                                   _ptr(m) if want_stats else None, _ptr(l) if want_stats else None,
+                                   _ptr(a) if want_stats else None, _ptr(raw), _ptr(fin), nt, _ptr(su))
     if st == SINGULAR:
         raise SingularInput("p_j == 1 in unit %d" % int(su[0]))
     if st != OK:
@@ -208,9 +216,9 @@ def compact(k, v, kept_idx, kept_len, out_rows: int):
     return k_out, v_out
 
 
-def run_path(q, k, v, lengths, evict_k, pool_kernel, protect, out_rows=None, nthreads=None):
+def run_path(q, k, v, lengths, evict_k, pool_kernel, protect, out_rows=None, nthreads=None, kind="dropkv"):
     """S1-S7 end to end; the kept K/V are gathered from the bf16 inputs."""
-    sc = score(q, k, v, lengths, pool_kernel, protect, nthreads=nthreads)
+    sc = score(q, k, v, lengths, pool_kernel, protect, nthreads=nthreads, kind=kind)
     kept, kl = select(sc["final"], lengths, evict_k, protect)
     rows = int(out_rows) if out_rows is not None else int(kl.max())
     kb, _ = _as_input(k)

@@ -36,6 +36,11 @@
  *       (same page, Algorithm 1 summary: evict the smallest scores; "DropKV:
  *       Decoupling ...", section 2.2: eviction shrinks the resident cache).
  *  [S7] the kept K/V rows are gathered in that order (byte copies).
+ *
+ * Score kind SnapKV (the attention-only baseline of "DropKV: Decoupling ...",
+ * Appendix B, Table 14: MaxPool1d over the window sum of p_j): step S3 becomes
+ * s_j = sum_t p_j^(t) and the singular rule S2 does not apply (nothing is
+ * divided by 1 - p_j); S1, S4-S7 are unchanged.
  */
 #include <math.h>
 #include <pthread.h>
@@ -63,7 +68,7 @@ typedef struct {
     int dtype;
     const void *q, *k, *v;
     const int32_t* lengths;
-    int pool_kernel, protect;
+    int pool_kernel, protect, kind;
     double *m_out, *l_out, *a_out, *raw_out, *final_out;
     /* work distribution */
     int next_unit;
@@ -128,7 +133,7 @@ static int score_unit(score_job* job, int unit, double* x, double* e, double* qr
             for (int j = 0; j <= pos; ++j) {
                 const double p = e[j] / l;
                 /* S2: a probability rounded to 1 is rejected */
-                if (p == 1.0) return ORACLE_SINGULAR;
+                if (p == 1.0 && job->kind == ORACLE_KIND_DROPKV) return ORACLE_SINGULAR;
                 for (int c = 0; c < d; ++c)
                     a[c] += p * load_elem(job->v, job->dtype, kv_base + (size_t)j * d + c);
             }
@@ -137,6 +142,11 @@ static int score_unit(score_job* job, int unit, double* x, double* e, double* qr
             if (job->a_out)
                 for (int c = 0; c < d; ++c) job->a_out[row * d + c] = a[c];
 
+            if (job->kind == ORACLE_KIND_SNAPKV) {
+                /* SnapKV: the attention probability of every visible key */
+                for (int j = 0; j <= pos; ++j) s_head[j] += e[j] / l;
+                continue;
+            }
             /* S3: ||p_j / (1 - p_j) (a - v_j)||^2 for every visible key */
             for (int j = 0; j <= pos; ++j) {
                 const double p = e[j] / l;
@@ -205,11 +215,12 @@ static int check_shape(const oracle_shape* s) {
     return 1;
 }
 
-int oracle_score(const oracle_shape* s, int dtype, const void* q, const void* k, const void* v,
-                 const int32_t* lengths, int pool_kernel, int protect,
-                 double* m_out, double* l_out, double* a_out, double* raw_out, double* final_out,
-                 int nthreads, int32_t* singular_unit) {
+int oracle_score_kind(const oracle_shape* s, int kind, int dtype, const void* q, const void* k, const void* v,
+                      const int32_t* lengths, int pool_kernel, int protect,
+                      double* m_out, double* l_out, double* a_out, double* raw_out, double* final_out,
+                      int nthreads, int32_t* singular_unit) {
     if (singular_unit) *singular_unit = -1;
+    if (kind != ORACLE_KIND_DROPKV && kind != ORACLE_KIND_SNAPKV) return ORACLE_INVALID;
     if (!check_shape(s) || !q || !k || !v || !lengths || !raw_out || !final_out) return ORACLE_INVALID;
     if (dtype != ORACLE_F64 && dtype != ORACLE_BF16) return ORACLE_INVALID;
     if (pool_kernel < 1 || pool_kernel % 2 == 0 || protect < 0) return ORACLE_INVALID;
@@ -219,7 +230,7 @@ int oracle_score(const oracle_shape* s, int dtype, const void* q, const void* k,
     score_job job;
     memset(&job, 0, sizeof job);
     job.s = s; job.dtype = dtype; job.q = q; job.k = k; job.v = v; job.lengths = lengths;
-    job.pool_kernel = pool_kernel; job.protect = protect;
+    job.pool_kernel = pool_kernel; job.protect = protect; job.kind = kind;
     job.m_out = m_out; job.l_out = l_out; job.a_out = a_out;
     job.raw_out = raw_out; job.final_out = final_out;
     job.status = ORACLE_OK; job.singular_unit = -1;
@@ -238,6 +249,14 @@ int oracle_score(const oracle_shape* s, int dtype, const void* q, const void* k,
     pthread_mutex_destroy(&job.lock);
     if (singular_unit) *singular_unit = job.singular_unit;
     return job.status;
+}
+
+int oracle_score(const oracle_shape* s, int dtype, const void* q, const void* k, const void* v,
+                 const int32_t* lengths, int pool_kernel, int protect,
+                 double* m_out, double* l_out, double* a_out, double* raw_out, double* final_out,
+                 int nthreads, int32_t* singular_unit) {
+    return oracle_score_kind(s, ORACLE_KIND_DROPKV, dtype, q, k, v, lengths, pool_kernel, protect, m_out, l_out,
+                             a_out, raw_out, final_out, nthreads, singular_unit);
 }
 
 /* S6: order by (final score, position), evict the first k_b. */

@@ -12,6 +12,7 @@ typedef struct { int32_t B, Hq, Hkv, d, n_max, w; } oracle_shape;
 
 enum { ORACLE_OK = 0, ORACLE_INVALID = 1, ORACLE_SINGULAR = 3, ORACLE_NOMEM = 9 };
 enum { ORACLE_F64 = 0, ORACLE_BF16 = 1 };
+enum { ORACLE_KIND_DROPKV = 0, ORACLE_KIND_SNAPKV = 1 };
 
 /* Window attention + scores.  q [B,Hq,w,d], k/v [B,Hkv,n_max,d] (fp64 values or
  * bf16 bit patterns, per dtype).  m/l [B,Hq,w], a [B,Hq,w,d] (nullable),
@@ -21,6 +22,13 @@ int oracle_score(const oracle_shape* s, int dtype, const void* q, const void* k,
                  const int32_t* lengths, int pool_kernel, int protect,
                  double* m_out, double* l_out, double* a_out, double* raw_out, double* final_out,
                  int nthreads, int32_t* singular_unit);
+
+/* oracle_score with a score kind: ORACLE_KIND_DROPKV (the perturbation score,
+ * as oracle_score) or ORACLE_KIND_SNAPKV (window sum of p_j, no singular rule). */
+int oracle_score_kind(const oracle_shape* s, int kind, int dtype, const void* q, const void* k, const void* v,
+                      const int32_t* lengths, int pool_kernel, int protect,
+                      double* m_out, double* l_out, double* a_out, double* raw_out, double* final_out,
+                      int nthreads, int32_t* singular_unit);
 
 /* Bottom-k eviction: kept_idx [B,Hkv,n_max] (first kept_len[b] entries, ascending). */
 int oracle_select(const oracle_shape* s, const double* final_scores, const int32_t* lengths,

@@ -25,6 +25,10 @@ MUTATIONS = {
     "tie_break_reversed": ("return (a->idx > b->idx) - (a->idx < b->idx);",
                            "return (a->idx < b->idx) - (a->idx > b->idx);"),
     "square_not_taken": ("s_head[j] += ratio * ratio * dist;", "s_head[j] += ratio * dist;"),
+    "snapkv_unnormalised": ("for (int j = 0; j <= pos; ++j) s_head[j] += e[j] / l;",
+                            "for (int j = 0; j <= pos; ++j) s_head[j] += e[j];"),
+    "snapkv_singular_rule": ("if (p == 1.0 && job->kind == ORACLE_KIND_DROPKV) return ORACLE_SINGULAR;",
+                             "if (p == 1.0) return ORACLE_SINGULAR;"),
 }
 
 
@@ -35,6 +39,8 @@ def _run_pins():
     pins.test_window_attention_vs_sdpa(42)
     pins.test_pool_vs_max_pool1d_and_protection(3)
     pins.test_select_vs_stable_sort_with_ties(0)
+    pins.test_snapkv_raw_vs_torch_softmax(42)
+    pins.test_snapkv_has_no_singular_rule()
 
 
 def test_unmodified_source_passes(tmp_path):

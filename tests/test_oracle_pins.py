@@ -359,3 +359,65 @@ def test_theorem1_bound_exhaustive():
     assert applied >= total // 2
     print("proxy ratio median %.4f p95 %.4f max %.4f; bound applied on %d/%d triples" % (
         np.median(ratios), np.percentile(ratios, 95), np.max(ratios), applied, total))
+
+
+# ------------------------------------------------------------ SnapKV score kind
+def _snapkv_reference(q, k, v, lengths):
+    """Window sum of torch's fp64 softmax over the tail-causal logits, averaged
+    over the query heads of each group (SnapKV's per-token score before
+    pooling, "DropKV: Decoupling ...", Table 14)."""
+    B, Hq, w, d = q.shape
+    Hkv, n = k.shape[1], k.shape[2]
+    g = Hq // Hkv
+    qt, kt = torch.from_numpy(np.ascontiguousarray(q)), torch.from_numpy(np.ascontiguousarray(k))
+    raw = np.full((B, Hkv, n), np.nan)
+    for b in range(B):
+        nb = int(lengths[b])
+        mask = torch.zeros(w, nb, dtype=torch.bool)
+        for t in range(w):
+            mask[t, :nb - w + t + 1] = True
+        for h in range(Hkv):
+            logits = (qt[b, h * g:(h + 1) * g] @ kt[b, h, :nb].T) / math.sqrt(d)      # [g, w, nb]
+            p = torch.softmax(logits.masked_fill(~mask, float("-inf")), dim=-1)
+            raw[b, h, :nb] = p.sum(dim=1).mean(dim=0).numpy()
+    return raw
+
+
+@pytest.mark.parametrize("seed", SEEDS)
+def test_snapkv_raw_vs_torch_softmax(seed):
+    wl = synth.make_workload("tiny_d16_n128", seed=seed)
+    q, k, v = (x.astype(np.float64) for x in (wl.q32, wl.k32, wl.v32))
+    lengths = wl.lengths.numpy()
+    res = oracle.score(q, k, v, lengths, 1, 0, kind="snapkv")
+    ref = _snapkv_reference(q, k, v, lengths)
+    np.testing.assert_allclose(res["raw"], ref, rtol=1e-12, atol=1e-15)
+
+
+def test_snapkv_ragged_gqa7_vs_torch_softmax():
+    q, k, v = _gauss((2, 14, 3, 8), (2, 2, 40, 8), 21)
+    lengths = np.array([40, 23], dtype=np.int32)
+    res = oracle.score(q, k, v, lengths, 1, 0, kind="snapkv")
+    np.testing.assert_allclose(res["raw"], _snapkv_reference(q, k, v, lengths), rtol=1e-12, atol=1e-15)
+    assert np.all(np.isnan(res["raw"][1, :, 23:]))
+
+
+def test_snapkv_window_mass_is_w():
+    """Each window row's probabilities sum to 1, so a KV head's raw SnapKV
+    scores sum to w (a mean over the group of w rows each)."""
+    q, k, v = _gauss((2, 8, 5, 16), (2, 2, 96, 16), 4)
+    lengths = np.array([96, 61], dtype=np.int32)
+    res = oracle.score(q, k, v, lengths, 1, 0, kind="snapkv")
+    for b in range(2):
+        np.testing.assert_allclose(np.sum(res["raw"][b, :, :lengths[b]], axis=-1), 5.0, rtol=1e-13)
+
+
+def test_snapkv_has_no_singular_rule():
+    """The input DropKV rejects (p_j == 1) is an ordinary SnapKV input: the
+    dominant key scores w, every other key 0 (e^-2000 underflows)."""
+    q, k, v = _gauss((1, 1, 2, 16), (1, 1, 32, 16), 9)
+    q[..., 0] = 100.0
+    k[0, 0, 5, 0] = 100.0
+    k[0, 0, np.arange(32) != 5, 0] = 0.0
+    res = oracle.score(q, k, v, np.array([32], dtype=np.int32), kind="snapkv")
+    assert res["raw"][0, 0, 5] == 2.0
+    assert np.all(res["raw"][0, 0, np.arange(32) != 5] == 0.0)
