@@ -55,6 +55,8 @@ def parse_args():
     ap.add_argument("--workload", default=synth.HEADLINE, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--score", choices=["dropkv", "snapkv"], default="dropkv",
+                    help="score kind: the DropKV perturbation score (default) or the SnapKV baseline")
     return ap.parse_args()
 
 
@@ -74,18 +76,19 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def config_of(spec, lengths):
-    return {"workload": spec.name, "B": spec.B, "Hq": spec.Hq, "Hkv": spec.Hkv, "d": spec.d, "n_max": spec.n_max,
+def config_of(spec, lengths, score="dropkv"):
+    return {"workload": spec.name, "score": score, "B": spec.B, "Hq": spec.Hq, "Hkv": spec.Hkv, "d": spec.d, "n_max": spec.n_max,
             "n_tokens": int(sum(lengths)), "w": spec.w, "pool_kernel": spec.pool_kernel, "protect": spec.protect,
             "budget_pct_kept": spec.budget_pct, "inputs": "bf16",
             "l2": "inputs larger than L2 (K+V %.0f MB); between steps a 256 MB write flushes L2 and a 256 MB read cleans it" % (
                 2 * spec.B * spec.Hkv * spec.n_max * spec.d * 2 / 1e6)}
 
 
-def workload_bytes(spec, lengths, kept):
-    """Algorithmic bytes of the two-pass structure (byte model)."""
+def workload_bytes(spec, lengths, kept, score="dropkv"):
+    """Algorithmic bytes of the two-pass structure (byte model).
+    The SnapKV score reads only K in both passes."""
     U_tok = spec.Hkv * int(sum(lengths))                  # head-tokens
-    kv = 4 * spec.d                                       # K + V bytes per head-token
+    kv = (4 if score == "dropkv" else 2) * spec.d         # K (+ V) bytes per head-token
     p1 = U_tok * kv
     p2 = U_tok * (kv + 4)                                 # + raw score write
     pool = U_tok * 8
@@ -173,42 +176,53 @@ class ClockSampler:
 
 
 def run_reference(args, spec, wl):
-    """Reference arm: the fp64 CPU oracle on the host cores, same workload and metric."""
+    """Reference arm: the fp64 CPU oracle on the host cores, same workload,
+    metric and unit.  Each step is a bounded sample of the layer: one query
+    head of one KV head over all of its sequence's tokens (the oracle's unit of
+    independent work), cycling through the layer's (sequence, KV head, query
+    head) triples; it counts n_b / Hq scored tokens, the share of the layer's
+    tokens that one query head's scoring represents."""
     import oracle
     lengths = wl.lengths.numpy()
-    units = int(sum(lengths))
-    cores = min(spec.B * spec.Hkv, os.cpu_count() or 1)
+    g = spec.Hq // spec.Hkv
+    triples = [(b, h, hl) for b in range(spec.B) for h in range(spec.Hkv) for hl in range(g)]
 
-    def step():
-        oracle.run_path(wl.q, wl.k, wl.v, wl.lengths, wl.evict_k, spec.pool_kernel, spec.protect, nthreads=cores)
+    def step(i):
+        b, h, hl = triples[i % len(triples)]
+        hq = h * g + hl
+        oracle.run_path(wl.q[b:b + 1, hq:hq + 1], wl.k[b:b + 1, h:h + 1], wl.v[b:b + 1, h:h + 1],
+                        wl.lengths[b:b + 1], wl.evict_k[b:b + 1], spec.pool_kernel, spec.protect, nthreads=1,
+                        kind=args.score)
+        return int(lengths[b]) / spec.Hq
 
-    for _ in range(args.warmup):
-        step()
-    times = []
-    for _ in range(args.steps):
+    for i in range(args.warmup):
+        step(i)
+    times, units = [], 0.0
+    for i in range(args.steps):
         t0 = time.perf_counter()
-        step()
+        units += step(args.warmup + i)
         times.append(time.perf_counter() - t0)
     total = sum(times)
-    value = units * len(times) / total
-    sample = "the full layer (%d KV heads x %d tokens) per step, fp64, %d threads over KV heads" % (
-        spec.B * spec.Hkv, units, cores)
+    value = units / total
+    sample = ("per step one query head of one KV head over all n_b tokens (1/%d of the layer's scoring work), "
+              "fp64, 1 thread" % spec.Hq)
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded generator; stands in for RULER/LongBench layers)",
-            "config": config_of(spec, lengths),
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+            "config": config_of(spec, lengths, args.score),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
 
 
-def cpu_baseline(spec, wl):
+def cpu_baseline(spec, wl, score="dropkv"):
     import oracle
     cores = min(spec.B * spec.Hkv, os.cpu_count() or 1)
     units = int(wl.lengths.sum())
     t0 = time.perf_counter()
-    oracle.run_path(wl.q, wl.k, wl.v, wl.lengths, wl.evict_k, spec.pool_kernel, spec.protect, nthreads=cores)
+    oracle.run_path(wl.q, wl.k, wl.v, wl.lengths, wl.evict_k, spec.pool_kernel, spec.protect, nthreads=cores,
+                    kind=score)
     dt = time.perf_counter() - t0
     return {"value": units / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": "one full layer (%d KV heads, %d tokens), fp64, %.1f s on %d threads" % (
@@ -242,7 +256,7 @@ def main():
     kept_np = wl.kept_len()
     units = int(sum(lengths_np))
     op = DropKV(spec.B, spec.Hq, spec.Hkv, spec.d, spec.n_max, spec.w, spec.pool_kernel, spec.protect,
-                out_rows=int(kept_np.max()), device=dev)
+                out_rows=int(kept_np.max()), device=dev, kind=args.score)
     q, k, v = wl.q.to(dev), wl.k.to(dev), wl.v.to(dev)
     lengths, ev = wl.lengths.to(dev), wl.evict_k.to(dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -261,7 +275,7 @@ def main():
             op.run(q, k, v, lengths, ev, stream=stream, keep_raw=False)
         else:
             B.dropkv_score_timed(op.shape, q, k, v, lengths, op.pool_kernel, op.protect, op.scores, None,
-                                 op.workspace, op.status, events[1:6], stream)
+                                 op.workspace, op.status, events[1:6], stream, kind=args.score)
             op.select(lengths, ev, stream)
             events[6].record(stream)
             op.compact(k, v, stream)
@@ -326,21 +340,21 @@ def main():
         step_ms = float(t.item())
     value = units * world / (step_ms / 1e3)
 
-    nbytes = workload_bytes(spec, lengths_np, kept_np)
+    nbytes = workload_bytes(spec, lengths_np, kept_np, args.score)
     peak, peak_kind = measured_peaks()
     phase_ms = {kname: sum(v_) / KP for kname, v_ in phases.items()}
     dom = max(("window_attention", "score"), key=lambda kk: phase_ms[kk])
     achieved = nbytes[dom] / (phase_ms[dom] / 1e3) / 1e9
     roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "peak_source": peak_kind,
-                "traffic": recorded_traffic(dom, spec.name),
+                "traffic": recorded_traffic(dom, spec.name if args.score == "dropkv" else spec.name + ":" + args.score),
                 "algorithmic_bytes_per_launch": nbytes[dom]}
     path_gbs = nbytes["path"] / (step_ms / 1e3) / 1e9
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
             "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f32", "data": "synthetic (seeded generator; stands in for RULER/LongBench layers)",
-            "config": dict(config_of(spec, lengths_np), parallelism="one independent layer per GPU"),
+            "config": dict(config_of(spec, lengths_np, args.score), parallelism="one independent layer per GPU"),
             "roofline": roofline,
             "path_roofline": {"achieved": path_gbs, "peak": peak, "unit": "GB/s", "frac": path_gbs / peak,
                               "algorithmic_bytes_per_step": nbytes["path"]},
@@ -352,7 +366,7 @@ def main():
         line["e2e"] = e2e_leg(op, wl, dev, stream, args, world)
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(spec, wl)
+        line["cpu_baseline"] = cpu_baseline(spec, wl, args.score)
     if rank == 0:
         print(json.dumps(line))
     if world > 1:

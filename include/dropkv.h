@@ -67,6 +67,12 @@ typedef enum {
 #define DROPKV_FLAG_NONFINITE_STATS 0x100u  /* window statistics (normaliser or |a|^2) */
 #define DROPKV_FLAG_NONFINITE_SCORE 0x200u  /* a token score */
 
+/* Score kinds of dropkv_score_ex / dropkv_evict_ex. */
+#define DROPKV_SCORE_DROPKV 0   /* s_j = sum_t ||p_j / (1 - p_j) (a - v_j)||^2 (the method) */
+#define DROPKV_SCORE_SNAPKV 1   /* s_j = sum_t p_j: the attention-only baseline ("DropKV: Decoupling ...",
+                                 * Appendix B, Table 14, SnapKV row), same window, GQA mean,
+                                 * pooling, protection, selection and compaction; reads K only */
+
 /* Problem shape.  Supported: B >= 1; Hq % Hkv == 0; g = Hq / Hkv; R = g * w <= 64;
  * d a multiple of 8 in [8, 128]; 1 <= w <= n_max < 2^31. */
 typedef struct {
@@ -110,16 +116,16 @@ DROPKV_API dropkv_status dropkv_score(const dropkv_shape* shape, const void* q_w
                            float* raw_scores, void* workspace, size_t workspace_bytes, uint32_t* status,
                            cudaStream_t stream);
 
-/* dropkv_score that also records phase_events[0..4] on `stream`: before pass 1
- * (window attention), between pass 1 and the split-K merge, between the merge
- * and pass 2 (scoring), between pass 2 and pooling, and after pooling -- for
- * per-kernel timing with CUDA events.  The events are created by the caller;
- * everything else is as dropkv_score. */
-DROPKV_API dropkv_status dropkv_score_timed(const dropkv_shape* shape, const void* q_window, const void* k,
-                                            const void* v, const int32_t* lengths, int32_t pool_kernel,
-                                            int32_t protect, float* scores, float* raw_scores, void* workspace,
-                                            size_t workspace_bytes, uint32_t* status, cudaStream_t stream,
-                                            cudaEvent_t* phase_events);
+/* dropkv_score_ex that also records phase_events[0..4] on `stream`: before
+ * pass 1 (window attention), between pass 1 and the split-K merge, between the
+ * merge and pass 2 (scoring), between pass 2 and pooling, and after pooling --
+ * for per-kernel timing with CUDA events.  The events are created by the
+ * caller; everything else is as dropkv_score_ex. */
+DROPKV_API dropkv_status dropkv_score_timed(const dropkv_shape* shape, int32_t score_kind, const void* q_window,
+                                            const void* k, const void* v, const int32_t* lengths,
+                                            int32_t pool_kernel, int32_t protect, float* scores, float* raw_scores,
+                                            void* workspace, size_t workspace_bytes, uint32_t* status,
+                                            cudaStream_t stream, cudaEvent_t* phase_events);
 
 /* dropkv_score without a workspace argument, for callers that cannot allocate
  * device memory when they score (a host framework that owns all device memory
@@ -183,6 +189,22 @@ DROPKV_API dropkv_status dropkv_evict(const dropkv_shape* shape, const void* q_w
                                       int32_t protect, float* scores, float* raw_scores, int32_t* kept_idx,
                                       int32_t* kept_len, int32_t out_rows, void* k_out, void* v_out, void* workspace,
                                       size_t workspace_bytes, uint32_t* status, cudaStream_t stream);
+
+/* dropkv_score and dropkv_evict with a score kind (DROPKV_SCORE_DROPKV or
+ * DROPKV_SCORE_SNAPKV; anything else is DROPKV_ERR_INVALID_ARG).  With
+ * DROPKV_SCORE_SNAPKV the singular rule does not apply (nothing is divided by
+ * 1 - p_j), V is read only by the compaction, and the workspace exports lse
+ * but not a.  Everything else is as for the calls without the kind. */
+DROPKV_API dropkv_status dropkv_score_ex(const dropkv_shape* shape, int32_t score_kind, const void* q_window,
+                                         const void* k, const void* v, const int32_t* lengths, int32_t pool_kernel,
+                                         int32_t protect, float* scores, float* raw_scores, void* workspace,
+                                         size_t workspace_bytes, uint32_t* status, cudaStream_t stream);
+DROPKV_API dropkv_status dropkv_evict_ex(const dropkv_shape* shape, int32_t score_kind, const void* q_window,
+                                         const void* k, const void* v, const int32_t* lengths, const int32_t* evict_k,
+                                         int32_t pool_kernel, int32_t protect, float* scores, float* raw_scores,
+                                         int32_t* kept_idx, int32_t* kept_len, int32_t out_rows, void* k_out,
+                                         void* v_out, void* workspace, size_t workspace_bytes, uint32_t* status,
+                                         cudaStream_t stream);
 
 /* Synchronise `stream`, read the device status word and map it to a status
  * (the first of SINGULAR, NONFINITE, DEVICE_ARG, TIMEOUT that is set, else OK;

@@ -57,7 +57,7 @@ def lib():
             L.dropkv_workspace_size.restype = SZ
             L.dropkv_score.argtypes = [SH, P, P, P, P, I32, I32, P, P, P, SZ, P, P]
             L.dropkv_score.restype = ctypes.c_int
-            L.dropkv_score_timed.argtypes = [SH, P, P, P, P, I32, I32, P, P, P, SZ, P, P, P]
+            L.dropkv_score_timed.argtypes = [SH, I32, P, P, P, P, I32, I32, P, P, P, SZ, P, P, P]
             L.dropkv_score_timed.restype = ctypes.c_int
             L.dropkv_score_noalloc.argtypes = [SH, P, P, P, P, I32, I32, P, P, P, P]
             L.dropkv_score_noalloc.restype = ctypes.c_int
@@ -67,6 +67,10 @@ def lib():
             L.dropkv_compact.restype = ctypes.c_int
             L.dropkv_evict.argtypes = [SH, P, P, P, P, P, I32, I32, P, P, P, P, I32, P, P, P, SZ, P, P]
             L.dropkv_evict.restype = ctypes.c_int
+            L.dropkv_evict_ex.argtypes = [SH, I32, P, P, P, P, P, I32, I32, P, P, P, P, I32, P, P, P, SZ, P, P]
+            L.dropkv_evict_ex.restype = ctypes.c_int
+            L.dropkv_score_ex.argtypes = [SH, I32, P, P, P, P, I32, I32, P, P, P, SZ, P, P]
+            L.dropkv_score_ex.restype = ctypes.c_int
             L.dropkv_read_status.argtypes = [P, P, ctypes.POINTER(ctypes.c_uint32)]
             L.dropkv_read_status.restype = ctypes.c_int
             L.dropkv_version.argtypes = []
@@ -122,12 +126,13 @@ def dropkv_score(shape, q_window, k, v, lengths, pool_kernel, protect, scores, r
 
 
 def dropkv_score_timed(shape, q_window, k, v, lengths, pool_kernel, protect, scores, raw_scores, workspace,
-                       status, events, stream=None):
+                       status, events, stream=None, kind="dropkv"):
     """dropkv_score recording 5 torch.cuda.Event objects at its phase boundaries."""
     if len(events) != 5:
         raise ValueError("dropkv_score_timed records 5 events")
     arr = (ctypes.c_void_p * 5)(*[ctypes.c_void_p(e.cuda_event) for e in events])
-    code = lib().dropkv_score_timed(ctypes.byref(shape), _ptr(q_window), _ptr(k), _ptr(v), _ptr(lengths),
+    code = lib().dropkv_score_timed(ctypes.byref(shape), SCORE_KINDS[kind], _ptr(q_window), _ptr(k), _ptr(v),
+                                    _ptr(lengths),
                                     int(pool_kernel), int(protect), _ptr(scores), _ptr(raw_scores),
                                     _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(status),
                                     _stream(stream), arr)
@@ -163,6 +168,28 @@ def dropkv_evict(shape, q_window, k, v, lengths, evict_k, pool_kernel, protect, 
                               _ptr(kept_len), int(out_rows), _ptr(k_out), _ptr(v_out), _ptr(workspace),
                               workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream))
     return _check(code, "dropkv_evict")
+
+
+SCORE_KINDS = {"dropkv": 0, "snapkv": 1}
+
+
+def dropkv_score_ex(shape, kind, q_window, k, v, lengths, pool_kernel, protect, scores, raw_scores, workspace,
+                    status, stream=None):
+    code = lib().dropkv_score_ex(ctypes.byref(shape), SCORE_KINDS[kind], _ptr(q_window), _ptr(k), _ptr(v),
+                                 _ptr(lengths), int(pool_kernel), int(protect), _ptr(scores), _ptr(raw_scores),
+                                 _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(status),
+                                 _stream(stream))
+    return _check(code, "dropkv_score_ex")
+
+
+def dropkv_evict_ex(shape, kind, q_window, k, v, lengths, evict_k, pool_kernel, protect, scores, raw_scores,
+                    kept_idx, kept_len, out_rows, k_out, v_out, workspace, status, stream=None):
+    code = lib().dropkv_evict_ex(ctypes.byref(shape), SCORE_KINDS[kind], _ptr(q_window), _ptr(k), _ptr(v),
+                                 _ptr(lengths), _ptr(evict_k), int(pool_kernel), int(protect), _ptr(scores),
+                                 _ptr(raw_scores), _ptr(kept_idx), _ptr(kept_len), int(out_rows), _ptr(k_out),
+                                 _ptr(v_out), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                 _ptr(status), _stream(stream))
+    return _check(code, "dropkv_evict_ex")
 
 
 def dropkv_read_status(status, stream=None):

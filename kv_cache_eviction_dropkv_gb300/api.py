@@ -19,7 +19,12 @@ class DropKV:
     scores, kept indices and lengths and the compacted K/V."""
 
     def __init__(self, B_: int, Hq: int, Hkv: int, d: int, n_max: int, w: int, pool_kernel: int = 5,
-                 protect: Optional[int] = None, out_rows: Optional[int] = None, device=None):
+                 protect: Optional[int] = None, out_rows: Optional[int] = None, device=None, kind: str = "dropkv"):
+        """kind: "dropkv" (the perturbation score) or "snapkv" (window sum of
+        attention probabilities, the attention-only baseline)."""
+        if kind not in B.SCORE_KINDS:
+            raise ValueError("kind must be one of %s" % sorted(B.SCORE_KINDS))
+        self.kind = kind
         self.shape = B.make_shape(B_, Hq, Hkv, d, n_max, w)
         self.device = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
         self.pool_kernel = int(pool_kernel)
@@ -50,8 +55,8 @@ class DropKV:
         return lse, a
 
     def score(self, q, k, v, lengths=None, stream=None, keep_raw=True):
-        B.dropkv_score(self.shape, q, k, v, lengths, self.pool_kernel, self.protect, self.scores,
-                       self.raw_scores if keep_raw else None, self.workspace, self.status, stream)
+        B.dropkv_score_ex(self.shape, self.kind, q, k, v, lengths, self.pool_kernel, self.protect, self.scores,
+                          self.raw_scores if keep_raw else None, self.workspace, self.status, stream)
 
     def select(self, lengths, evict_k, stream=None):
         B.dropkv_select(self.shape, self.scores, lengths, evict_k, self.protect, self.kept_idx, self.kept_len,
@@ -63,9 +68,9 @@ class DropKV:
 
     def run(self, q, k, v, lengths, evict_k, stream=None, keep_raw=True):
         """The whole step in one library call (dropkv_evict)."""
-        B.dropkv_evict(self.shape, q, k, v, lengths, evict_k, self.pool_kernel, self.protect, self.scores,
-                       self.raw_scores if keep_raw else None, self.kept_idx, self.kept_len, self.out_rows,
-                       self.k_out, self.v_out, self.workspace, self.status, stream)
+        B.dropkv_evict_ex(self.shape, self.kind, q, k, v, lengths, evict_k, self.pool_kernel, self.protect,
+                          self.scores, self.raw_scores if keep_raw else None, self.kept_idx, self.kept_len,
+                          self.out_rows, self.k_out, self.v_out, self.workspace, self.status, stream)
 
     def run_separate(self, q, k, v, lengths, evict_k, stream=None, keep_raw=True):
         """The same step as three library calls (score, select, compact)."""

@@ -156,7 +156,8 @@ namespace {
 dropkv_status score_impl(const dropkv_shape* shape, const void* q_window, const void* k, const void* v,
                          const int32_t* lengths, int32_t pool_kernel, int32_t protect, float* scores,
                          float* raw_scores, void* workspace, size_t workspace_bytes, uint32_t* status,
-                         cudaStream_t stream, cudaEvent_t* ev, PoolParams* defer_pool = nullptr) {
+                         cudaStream_t stream, cudaEvent_t* ev, PoolParams* defer_pool = nullptr,
+                         int kind = DROPKV_SCORE_DROPKV) {
   const int sms = current_sms(nullptr);
   if (sms <= 0) return DROPKV_ERR_CUDA;
   if (!shape) return DROPKV_ERR_INVALID_ARG;
@@ -172,6 +173,7 @@ dropkv_status score_impl(const dropkv_shape* shape, const void* q_window, const 
     return DROPKV_ERR_INVALID_ARG;
   if (pool_kernel < 1 || pool_kernel > kMaxPool || pool_kernel % 2 == 0 || protect < 0)
     return DROPKV_ERR_INVALID_ARG;
+  if (kind != DROPKV_SCORE_DROPKV && kind != DROPKV_SCORE_SNAPKV) return DROPKV_ERR_INVALID_ARG;
   const WsPlan w = make_plan(g);
   if (!workspace || workspace_bytes < w.total || !aligned16(workspace)) return DROPKV_ERR_WORKSPACE;
   const size_t score_bytes = (size_t)g.U * g.n_max * 4;
@@ -197,6 +199,7 @@ dropkv_status score_impl(const dropkv_shape* shape, const void* q_window, const 
   p.part_ml = reinterpret_cast<float*>(ws + w.part_ml);
   p.raw = raw_scores ? raw_scores : reinterpret_cast<float*>(ws + w.raw);
   p.status = status;
+  p.kind = kind == DROPKV_SCORE_SNAPKV ? kKindSnapKV : kKindDropKV;
 
   if (ev && cudaEventRecord(ev[0], stream) != cudaSuccess) return DROPKV_ERR_CUDA;
   p.splits = g.splits1;
@@ -303,13 +306,13 @@ dropkv_status dropkv_score(const dropkv_shape* shape, const void* q_window, cons
                     workspace_bytes, status, stream, nullptr);
 }
 
-dropkv_status dropkv_score_timed(const dropkv_shape* shape, const void* q_window, const void* k, const void* v,
-                                 const int32_t* lengths, int32_t pool_kernel, int32_t protect, float* scores,
-                                 float* raw_scores, void* workspace, size_t workspace_bytes, uint32_t* status,
-                                 cudaStream_t stream, cudaEvent_t* phase_events) {
+dropkv_status dropkv_score_timed(const dropkv_shape* shape, int32_t score_kind, const void* q_window, const void* k,
+                                 const void* v, const int32_t* lengths, int32_t pool_kernel, int32_t protect,
+                                 float* scores, float* raw_scores, void* workspace, size_t workspace_bytes,
+                                 uint32_t* status, cudaStream_t stream, cudaEvent_t* phase_events) {
   if (!phase_events) return DROPKV_ERR_INVALID_ARG;
   return score_impl(shape, q_window, k, v, lengths, pool_kernel, protect, scores, raw_scores, workspace,
-                    workspace_bytes, status, stream, phase_events);
+                    workspace_bytes, status, stream, phase_events, nullptr, score_kind);
 }
 
 dropkv_status dropkv_select(const dropkv_shape* shape, const float* scores, const int32_t* lengths,
@@ -325,11 +328,11 @@ dropkv_status dropkv_compact(const dropkv_shape* shape, const void* k, const voi
   return compact_impl(shape, k, v, kept_idx, kept_len, out_rows, k_out, v_out, status, stream, false);
 }
 
-dropkv_status dropkv_evict(const dropkv_shape* shape, const void* q_window, const void* k, const void* v,
-                           const int32_t* lengths, const int32_t* evict_k, int32_t pool_kernel, int32_t protect,
-                           float* scores, float* raw_scores, int32_t* kept_idx, int32_t* kept_len, int32_t out_rows,
-                           void* k_out, void* v_out, void* workspace, size_t workspace_bytes, uint32_t* status,
-                           cudaStream_t stream) {
+dropkv_status dropkv_evict_ex(const dropkv_shape* shape, int32_t score_kind, const void* q_window, const void* k,
+                              const void* v, const int32_t* lengths, const int32_t* evict_k, int32_t pool_kernel,
+                              int32_t protect, float* scores, float* raw_scores, int32_t* kept_idx,
+                              int32_t* kept_len, int32_t out_rows, void* k_out, void* v_out, void* workspace,
+                              size_t workspace_bytes, uint32_t* status, cudaStream_t stream) {
   // every argument is checked before anything is launched
   dropkv_status st = select_impl(shape, scores, lengths, evict_k, protect, kept_idx, kept_len, workspace,
                                  workspace_bytes, status, stream, nullptr, /*check_only=*/true);
@@ -341,12 +344,30 @@ dropkv_status dropkv_evict(const dropkv_shape* shape, const void* q_window, cons
   }
   PoolParams pool{};
   st = score_impl(shape, q_window, k, v, lengths, pool_kernel, protect, scores, raw_scores, workspace,
-                  workspace_bytes, status, stream, nullptr, &pool);
+                  workspace_bytes, status, stream, nullptr, &pool, score_kind);
   if (st != DROPKV_OK) return st;
   st = select_impl(shape, scores, lengths, evict_k, protect, kept_idx, kept_len, workspace, workspace_bytes, status,
                    stream, &pool);
   if (st != DROPKV_OK || !k_out) return st;
   return compact_impl(shape, k, v, kept_idx, kept_len, out_rows, k_out, v_out, status, stream, false);
+}
+
+dropkv_status dropkv_evict(const dropkv_shape* shape, const void* q_window, const void* k, const void* v,
+                           const int32_t* lengths, const int32_t* evict_k, int32_t pool_kernel, int32_t protect,
+                           float* scores, float* raw_scores, int32_t* kept_idx, int32_t* kept_len, int32_t out_rows,
+                           void* k_out, void* v_out, void* workspace, size_t workspace_bytes, uint32_t* status,
+                           cudaStream_t stream) {
+  return dropkv_evict_ex(shape, DROPKV_SCORE_DROPKV, q_window, k, v, lengths, evict_k, pool_kernel, protect, scores,
+                         raw_scores, kept_idx, kept_len, out_rows, k_out, v_out, workspace, workspace_bytes, status,
+                         stream);
+}
+
+dropkv_status dropkv_score_ex(const dropkv_shape* shape, int32_t score_kind, const void* q_window, const void* k,
+                              const void* v, const int32_t* lengths, int32_t pool_kernel, int32_t protect,
+                              float* scores, float* raw_scores, void* workspace, size_t workspace_bytes,
+                              uint32_t* status, cudaStream_t stream) {
+  return score_impl(shape, q_window, k, v, lengths, pool_kernel, protect, scores, raw_scores, workspace,
+                    workspace_bytes, status, stream, nullptr, nullptr, score_kind);
 }
 
 dropkv_status dropkv_read_status(const uint32_t* status, cudaStream_t stream, uint32_t* flags_out) {

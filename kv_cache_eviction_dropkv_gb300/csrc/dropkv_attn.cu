@@ -131,11 +131,17 @@ __device__ __forceinline__ void stream_ring(uint8_t* ring, uint64_t* full, uint6
 }
 
 // ============================================================== pass 1
-template <int NR>
+constexpr int kMaxStages = 6;   // ring stages of one tensor (mbarrier arrays)
+
+// STATS: statistics only (no V): the V ring's stages go to K, keeping the
+// bytes in flight per SM (V keeps one unused stage so the ring arithmetic holds).
+template <int NR, bool STATS = false>
 struct Pass1Cfg {
   static constexpr int HR = NR / 2;                 // rows per worker half
-  static constexpr int KS = NR <= 16 ? 3 : 2;       // K ring depth (K is released right after S = K Q^T)
-  static constexpr int VS = 3;                      // V ring depth (V is held until PV completes)
+  static constexpr int KS0 = NR <= 16 ? 3 : 2;      // K ring depth (K is released right after S = K Q^T)
+  static constexpr int VS0 = 3;                     // V ring depth (V is held until PV completes)
+  static constexpr int KS = STATS ? KS0 + VS0 - 1 : KS0;
+  static constexpr int VS = STATS ? 1 : VS0;
   static constexpr int PB = NR <= 32 ? 2 : 1;       // P buffers
   static constexpr int kQBytes = NR * kDPad * 2;
   static constexpr int kPBytes = kTile * NR * 2;    // one of (hi, lo) of one P buffer
@@ -145,10 +151,11 @@ struct Pass1Cfg {
   static constexpr int kOffP = kOffQ + kQBytes;     // [buffer][hi, lo]
   static constexpr int kOffSmall = kOffP + 2 * PB * kPBytes;
   static constexpr uint32_t kTmemCols = (3 * NR <= 64) ? 64u : (3 * NR <= 128 ? 128u : 256u);
+  static_assert(KS <= kMaxStages && VS <= kMaxStages, "ring depth");
 };
 
 struct Pass1Small {
-  uint64_t kfull[3], kempty[3], vfull[3], vempty[3];
+  uint64_t kfull[kMaxStages], kempty[kMaxStages], vfull[kMaxStages], vempty[kMaxStages];
   uint64_t sfull[2], sempty[2], pfull[2], pempty[2], ofull, drain;
   uint32_t tmem_base;
   int abort;
@@ -157,9 +164,9 @@ struct Pass1Small {
   float red[4][kMaxR];     // per-lane-quarter reduction scratch
 };
 
-template <int NR>
+template <int NR, bool STATS>
 constexpr int pass1_smem_bytes() {
-  return Pass1Cfg<NR>::kOffSmall + (int)sizeof(Pass1Small) + 1024;
+  return Pass1Cfg<NR, STATS>::kOffSmall + (int)sizeof(Pass1Small) + 1024;
 }
 
 // Merge of the split-K partial states (its own small kernel: it sits on the
@@ -205,11 +212,12 @@ __global__ void __launch_bounds__(kMergeThreads) merge_splits_kernel(const AttnP
     const int s = q * 32 + lane;
     v[q] = (s < S) ? __ldcg(ml + (size_t)s * R + r) : make_float2(-INFINITY, 0.f);
   }
+  const bool stats_only = p.kind == kKindSnapKV;   // no O partials were written
   float4 o[32];
 #pragma unroll
   for (int u = 0; u < 32; ++u)
-    o[u] = (lane < D4 && u < S) ? __ldcg(po4 + (size_t)u * split_stride + (size_t)r * D4 + lane)
-                                : make_float4(0.f, 0.f, 0.f, 0.f);
+    o[u] = (!stats_only && lane < D4 && u < S) ? __ldcg(po4 + (size_t)u * split_stride + (size_t)r * D4 + lane)
+                                               : make_float4(0.f, 0.f, 0.f, 0.f);
   float M = -INFINITY;
 #pragma unroll
   for (int q = 0; q < kMergeSplitRegs; ++q)
@@ -224,6 +232,16 @@ __global__ void __launch_bounds__(kMergeThreads) merge_splits_kernel(const AttnP
     L = fmaf(v[q].y, wgt[q], L);
   }
   L = warp_sum(L);
+  if (stats_only) {
+    if (lane == 0) {
+      const size_t o2 = (size_t)unit * R + r;
+      p.m2[o2] = M;
+      p.l[o2] = L;
+      p.m[o2] = (M + log2f(L)) * 0.69314718055994531f;
+      if (!(L > 0.f) || !isfinite(L)) atomicOr(p.status, DROPKV_FLAG_NONFINITE | DROPKV_FLAG_NONFINITE_STATS);
+    }
+    return;
+  }
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
   for (int q = 0; q < kMergeSplitRegs; ++q) {
@@ -272,11 +290,13 @@ __global__ void __launch_bounds__(kMergeThreads) merge_splits_kernel(const AttnP
   }
 }
 
-template <int NR>
+// STATS: the softmax statistics (m, l) only -- no V, no P V^T, no O partial
+// (the SnapKV score needs the normaliser of every window row, not a).
+template <int NR, bool STATS>
 __global__ void __launch_bounds__(kThreads, 1)
     window_attention_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                             const AttnParams p) {
-  using C = Pass1Cfg<NR>;
+  using C = Pass1Cfg<NR, STATS>;
   constexpr int HR = C::HR;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
@@ -321,7 +341,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       stage_rows_sw128(sQ, qsrc, NR, R, p.d, p.d, tid, kWorkers);
       fence_proxy_async_smem();
     }
-    if (warp == kProducerWarp && lane == 0) { tma_prefetch_desc(&tmk); tma_prefetch_desc(&tmv); }
+    if (warp == kProducerWarp && lane == 0) {
+      tma_prefetch_desc(&tmk);
+      if (!STATS) tma_prefetch_desc(&tmv);
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -336,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (T > 0 && warp == kProducerWarp) {
     // ---------------------------------------------------- TMA producer: lane 0 K, lane 1 V
     if (lane == 0) stream_ring<C::KS>(sK, S.kfull, S.kempty, &tmk, t0, T, unit, &S.abort, p.status);
-    else if (lane == 1) stream_ring<C::VS>(sV, S.vfull, S.vempty, &tmv, t0, T, unit, &S.abort, p.status);
+    else if (lane == 1 && !STATS) stream_ring<C::VS>(sV, S.vfull, S.vempty, &tmv, t0, T, unit, &S.abort, p.status);
     __syncwarp();
   } else if (T > 0 && warp == kMmaWarp) {
     // ---------------------------------------------------- MMA issuer
@@ -361,6 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = issue_S(0);
       for (int i = 0; ok && i < T; ++i) {
         if (i + 1 < T && !(ok = issue_S(i + 1))) break;
+        if (STATS) continue;
         const int pb = i % C::PB, vs = i % C::VS;
         if (!mbar_wait(&S.pfull[pb], (i / C::PB) & 1, &S.abort)) { ok = false; break; }
         if (!mbar_wait(&S.vfull[vs], (i / C::VS) & 1, &S.abort)) { ok = false; break; }
@@ -437,8 +461,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         need |= ((vis >> r) & 1u) && rel[r] > kRescaleLog2;
       }
       // this tile's P buffer must be free (PV of tile i - PB done); the tail tile's V must have landed
-      if (ok && i >= C::PB) ok = mbar_wait(&S.pempty[pb], ((i / C::PB) + 1) & 1, &S.abort);
-      if (ok && tail) ok = mbar_wait(&S.vfull[vs], (i / C::VS) & 1, &S.abort);
+      if (!STATS && ok && i >= C::PB) ok = mbar_wait(&S.pempty[pb], ((i / C::PB) + 1) & 1, &S.abort);
+      if (!STATS && ok && tail) ok = mbar_wait(&S.vfull[vs], (i / C::VS) & 1, &S.abort);
       ok = __all_sync(0xffffffffu, ok);
       // one barrier per tile in the common case: it carries both "some wait
       // failed" and "some logit outgrew its reference"
@@ -462,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mr[r] = nm;
           rel[r] = fmaf(sraw[r], scale, -nm);
         }
-        if (i > 0) {
+        if (!STATS && i > 0) {
           // rescale the accumulated O (lane = head dimension) once PV of tile i-1 is
           // done; PV(i-2) is known complete (pempty), so ofull is at most one phase
           // behind and the parity wait is unambiguous
@@ -479,6 +503,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_wait_st();
           tc_fence_before();
         }
+      }
+      if (STATS) {
+        // the normaliser only
+#pragma unroll
+        for (int r = 0; r < HR; ++r)
+          if ((vis >> r) & 1u) lsum[r] += ex2_approx(rel[r]);
+        continue;
       }
       // exponentials relative to the row reference, split into bf16 hi + lo
       uint8_t* phi = sP + (pb * 2 + 0) * C::kPBytes;
@@ -523,7 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     okw = __all_sync(0xffffffffu, okw);
     if (named_bar_or(kBarWork, kWorkers, failed || !okw)) failed = true;
     const size_t part = (size_t)unit * p.splits + split;
-    if (!failed) {
+    if (!STATS && !failed) {
       tc_fence_after();
       float o[HR];
       tmem_ld_cols<HR>(tO + lane_base + r0, o);
@@ -571,11 +602,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ============================================================== pass 2
-template <int NR>
+// SNAP: K only; the V ring's stages go to K (V keeps one unused stage).
+template <int NR, bool SNAP = false>
 struct Pass2Cfg {
   static constexpr int HR = NR / 2;
-  static constexpr int KS = 2;                      // K is released right after S = K Q^T
-  static constexpr int VS = NR <= 32 ? 4 : 3;       // V is held until A.V^T and |v|^2 are done
+  static constexpr int KS0 = 2;                     // K is released right after S = K Q^T
+  static constexpr int VS0 = NR <= 32 ? 4 : 3;      // V is held until A.V^T and |v|^2 are done
+  static constexpr int KS = SNAP ? KS0 + VS0 - 1 : KS0;
+  static constexpr int VS = SNAP ? 1 : VS0;
   static constexpr int kQBytes = NR * kDPad * 2;
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + KS * kTileBytes;
@@ -584,10 +618,11 @@ struct Pass2Cfg {
   static constexpr int kOffAlo = kOffAhi + kQBytes;
   static constexpr int kOffSmall = kOffAlo + kQBytes;
   static constexpr uint32_t kTmemCols = (4 * NR <= 64) ? 64u : (4 * NR <= 128 ? 128u : 256u);
+  static_assert(KS <= kMaxStages && VS <= kMaxStages, "ring depth");
 };
 
 struct Pass2Small {
-  uint64_t kfull[2], kempty[2], vfull[4], vempty[4];
+  uint64_t kfull[kMaxStages], kempty[kMaxStages], vfull[kMaxStages], vempty[kMaxStages];
   uint64_t accfull[2], accempty[2], drain, aready;
   uint32_t tmem_base;
   int abort;
@@ -595,16 +630,17 @@ struct Pass2Small {
   float4 xch[2][kTile];      // upper-half partials per token (sum r^2 (|a|^2 - 2 a.v), sum r^2, |v|^2 part, singular)
 };
 
-template <int NR>
+template <int NR, bool SNAP>
 constexpr int pass2_smem_bytes() {
-  return Pass2Cfg<NR>::kOffSmall + (int)sizeof(Pass2Small) + 1024;
+  return Pass2Cfg<NR, SNAP>::kOffSmall + (int)sizeof(Pass2Small) + 1024;
 }
 
-template <int NR>
+// SNAP: the SnapKV score (1/g) sum_r p_r from K alone -- no V, no A V^T.
+template <int NR, bool SNAP>
 __global__ void __launch_bounds__(kThreads, 1)
     score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                  const AttnParams p) {
-  using C = Pass2Cfg<NR>;
+  using C = Pass2Cfg<NR, SNAP>;
   constexpr int HR = C::HR;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
@@ -641,7 +677,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     stage_rows_sw128(sQ, qsrc, NR, R, p.d, p.d, tid, kWorkers);
     fence_proxy_async_smem();
   }
-  if (warp == kProducerWarp && lane == 0) { tma_prefetch_desc(&tmk); tma_prefetch_desc(&tmv); }
+  if (warp == kProducerWarp && lane == 0) {
+    tma_prefetch_desc(&tmk);
+    if (!SNAP) tma_prefetch_desc(&tmv);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -657,7 +696,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // TMA producer: lane 0 K, lane 1 V
     grid_dep_wait();
     if (lane == 0) stream_ring<C::KS>(sK, S.kfull, S.kempty, &tmk, t0, T, unit, &S.abort, p.status);
-    else if (lane == 1) stream_ring<C::VS>(sV, S.vfull, S.vempty, &tmv, t0, T, unit, &S.abort, p.status);
+    else if (lane == 1 && !SNAP) stream_ring<C::VS>(sV, S.vfull, S.vempty, &tmv, t0, T, unit, &S.abort, p.status);
     __syncwarp();
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
@@ -675,6 +714,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < 8; ++s)
           umma_bf16(dS, desc_kmajor_sw128(kb, kTile, s), desc_kmajor_sw128(qaddr, NR, s), idS, s > 0);
         umma_commit(&S.kempty[ks]);
+        if (SNAP) {
+          umma_commit(&S.accfull[ab]);
+          continue;
+        }
         if (i == 0 && !mbar_wait(&S.aready, 0, &S.abort)) { ok = false; break; }
         if (!mbar_wait(&S.vfull[vs], (i / C::VS) & 1, &S.abort)) { ok = false; break; }
         tc_fence_after();
@@ -717,14 +760,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t flags = 0;
     grid_dep_wait();                              // a, |a|^2, m and L come from the merge
     {
-      const __nv_bfloat16* ahl = p.ahl + (size_t)unit * 2 * kMaxR * kDPad;
-      stage_rows_sw128(sAhi, ahl, NR, NR, kDPad, kDPad, tid, kWorkers);
-      stage_rows_sw128(sAlo, ahl + kMaxR * kDPad, NR, NR, kDPad, kDPad, tid, kWorkers);
-      fence_proxy_async_smem();
+      if (!SNAP) {
+        const __nv_bfloat16* ahl = p.ahl + (size_t)unit * 2 * kMaxR * kDPad;
+        stage_rows_sw128(sAhi, ahl, NR, NR, kDPad, kDPad, tid, kWorkers);
+        stage_rows_sw128(sAlo, ahl + kMaxR * kDPad, NR, NR, kDPad, kDPad, tid, kWorkers);
+        fence_proxy_async_smem();
+      }
       if (tid < kMaxR) {
         const bool real = tid < R;
         const size_t o = (size_t)unit * R + tid;
-        S.rowc[tid] = make_float4(real ? p.m2[o] : 0.f, real ? p.l[o] : 1.f, real ? p.aa[o] : 0.f,
+        S.rowc[tid] = make_float4(real ? p.m2[o] : 0.f, real ? p.l[o] : 1.f, (real && !SNAP) ? p.aa[o] : 0.f,
                                   __int_as_float(real ? nb - p.w + (tid % p.w) : -1));
       }
       named_bar(kBarWork, kWorkers);
@@ -734,9 +779,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int tile0 = (t0 + i) * kTile, vs = i % C::VS, ab = i & 1;
       const int j = tile0 + tok;
       const bool full = tile0 + kTile - 1 <= all_see;
-      bool ok = mbar_wait(&S.vfull[vs], (i / C::VS) & 1, &S.abort);
+      bool ok = SNAP ? true : mbar_wait(&S.vfull[vs], (i / C::VS) & 1, &S.abort);
       float vvh = 0.f;
-      if (ok) {
+      if (!SNAP && ok) {
         // this half's 64 columns of the staged V row; chunks visited in a
         // per-thread rotated order so a warp's reads spread over all banks
         const uint8_t* vrow = sV + vs * kTileBytes + half * kHalfTile + tok * 128;
@@ -745,7 +790,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           vvh = sumsq_bf16x8(*reinterpret_cast<const uint4*>(vrow + ((c + tok) & 7) * 16), vvh);
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&S.vempty[vs]);
+      if (!SNAP && lane == 0) mbar_arrive(&S.vempty[vs]);
       if (ok) ok = mbar_wait(&S.accfull[ab], (i >> 1) & 1, &S.abort);
       ok = __all_sync(0xffffffffu, ok);
       float A = 0.f, W = 0.f;
@@ -754,7 +799,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         float sv[HR], av[HR];
         tmem_ld_cols<HR>(tmem + lane_base + ab * 2 * NR + r0, sv);
-        tmem_ld_cols<HR>(tmem + lane_base + ab * 2 * NR + NR + r0, av);
+        if (!SNAP) tmem_ld_cols<HR>(tmem + lane_base + ab * 2 * NR + NR + r0, av);
         tmem_wait_ld();
         tc_fence_before();
         uint32_t vis = rowmask;
@@ -768,6 +813,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 #pragma unroll
         for (int r = 0; r < HR; ++r) {
+          if (SNAP) {
+            // SnapKV: A accumulates p_j = e / L over the visible rows
+            if ((vis >> r) & 1u) {
+              const float4 c = S.rowc[r0 + r];
+              A = fmaf(ex2_approx(fmaf(sv[r], scale, -c.x)), rcp_approx(c.y), A);
+            }
+            continue;
+          }
           if ((vis >> r) & 1u) {
             const float4 c = S.rowc[r0 + r];
             const float e = ex2_approx(fmaf(sv[r], scale, -c.x));
@@ -784,7 +837,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&S.accempty[ab]);
       if (half == 1) S.xch[ab][tok] = make_float4(A, W, vvh, singular ? 1.f : 0.f);
       if (named_bar_or(kBarWork, kWorkers, !ok)) { failed = true; break; }
-      if (half == 0 && j < nb) {
+      if (SNAP && half == 0 && j < nb) {
+        float s = (A + S.xch[ab][tok].x) * inv_g;
+        if (!isfinite(s)) flags |= DROPKV_FLAG_NONFINITE | DROPKV_FLAG_NONFINITE_SCORE;
+        raw[j] = s;
+      } else if (half == 0 && j < nb) {
         const float4 o = S.xch[ab][tok];
         float s = fmaf(vvh + o.z, W + o.y, A + o.x);
         if (singular || o.w != 0.f) {
@@ -809,32 +866,34 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int NR>
+template <int NR, bool SNAP>
 cudaError_t launch_pass1_t(const AttnParams& p, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t st) {
-  constexpr int smem = pass1_smem_bytes<NR>();
+  constexpr int smem = pass1_smem_bytes<NR, SNAP>();
   static_assert(smem <= 232448, "pass-1 shared memory exceeds the per-CTA limit");
-  cudaError_t e = cudaFuncSetAttribute(window_attention_kernel<NR>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = cudaFuncSetAttribute(window_attention_kernel<NR, SNAP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(window_attention_kernel<NR>, dim3(p.splits, p.U), dim3(kThreads), smem, st, tk, tv, p);
+  return launch_pdl(window_attention_kernel<NR, SNAP>, dim3(p.splits, p.U), dim3(kThreads), smem, st, tk, tv, p);
 }
 
-template <int NR>
+template <int NR, bool SNAP>
 cudaError_t launch_pass2_t(const AttnParams& p, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t st) {
-  constexpr int smem = pass2_smem_bytes<NR>();
+  constexpr int smem = pass2_smem_bytes<NR, SNAP>();
   static_assert(smem <= 232448, "pass-2 shared memory exceeds the per-CTA limit");
-  cudaError_t e = cudaFuncSetAttribute(score_kernel<NR>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = cudaFuncSetAttribute(score_kernel<NR, SNAP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(score_kernel<NR>, dim3(p.splits, p.U), dim3(kThreads), smem, st, tk, tv, p);
+  return launch_pdl(score_kernel<NR, SNAP>, dim3(p.splits, p.U), dim3(kThreads), smem, st, tk, tv, p);
 }
 
 }  // namespace
 
 cudaError_t launch_window_attention(const AttnParams& p, int NR, const CUtensorMap& tk, const CUtensorMap& tv,
                                     int, cudaStream_t st) {
+  const bool snap = p.kind == kKindSnapKV;
   switch (NR) {
-    case 16: return launch_pass1_t<16>(p, tk, tv, st);
-    case 32: return launch_pass1_t<32>(p, tk, tv, st);
-    case 64: return launch_pass1_t<64>(p, tk, tv, st);
+    case 16: return snap ? launch_pass1_t<16, true>(p, tk, tv, st) : launch_pass1_t<16, false>(p, tk, tv, st);
+    case 32: return snap ? launch_pass1_t<32, true>(p, tk, tv, st) : launch_pass1_t<32, false>(p, tk, tv, st);
+    case 64: return snap ? launch_pass1_t<64, true>(p, tk, tv, st) : launch_pass1_t<64, false>(p, tk, tv, st);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -845,10 +904,11 @@ cudaError_t launch_merge(const AttnParams& p, cudaStream_t st) {
 
 cudaError_t launch_score(const AttnParams& p, int NR, const CUtensorMap& tk, const CUtensorMap& tv,
                          cudaStream_t st) {
+  const bool snap = p.kind == kKindSnapKV;
   switch (NR) {
-    case 16: return launch_pass2_t<16>(p, tk, tv, st);
-    case 32: return launch_pass2_t<32>(p, tk, tv, st);
-    case 64: return launch_pass2_t<64>(p, tk, tv, st);
+    case 16: return snap ? launch_pass2_t<16, true>(p, tk, tv, st) : launch_pass2_t<16, false>(p, tk, tv, st);
+    case 32: return snap ? launch_pass2_t<32, true>(p, tk, tv, st) : launch_pass2_t<32, false>(p, tk, tv, st);
+    case 64: return snap ? launch_pass2_t<64, true>(p, tk, tv, st) : launch_pass2_t<64, false>(p, tk, tv, st);
     default: return cudaErrorInvalidValue;
   }
 }

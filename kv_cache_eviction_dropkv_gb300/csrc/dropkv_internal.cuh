@@ -56,6 +56,10 @@ bool make_geom(const dropkv_shape* s, int num_sms, Geom* g);
 WsPlan make_plan(const Geom& g);
 
 // Parameter block of the two attention passes.
+// Score kinds (DROPKV_SCORE_* of the C ABI).
+constexpr int kKindDropKV = 0;   // exact single-token output perturbation
+constexpr int kKindSnapKV = 1;   // window sum of attention probabilities
+
 struct AttnParams {
   const __nv_bfloat16* q;        // [B][Hq][w][d]
   const int32_t* lengths;        // [B] or null
@@ -68,6 +72,7 @@ struct AttnParams {
   float *part_o, *part_ml;
   float* raw;                    // raw score output [U][n_max]
   uint32_t* status;
+  int kind;                      // kKindDropKV or kKindSnapKV
 };
 
 struct PoolParams {
