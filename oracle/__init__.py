@@ -73,6 +73,11 @@ def _load():
             lib.oracle_compact.argtypes = [ctypes.POINTER(_Shape), ctypes.c_int, P, P, P, P,
                                            ctypes.c_int, P, P]
             lib.oracle_compact.restype = ctypes.c_int
+            lib.oracle_select_layer.argtypes = [ctypes.POINTER(_Shape), P, P, P, ctypes.c_int, P, P]
+            lib.oracle_select_layer.restype = ctypes.c_int
+            lib.oracle_compact_heads.argtypes = [ctypes.POINTER(_Shape), ctypes.c_int, P, P, P, P,
+                                                 ctypes.c_int, P, P]
+            lib.oracle_compact_heads.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -90,7 +95,8 @@ class use_library:
         _load()
         self.saved = _lib
         lib = ctypes.CDLL(self.path)
-        for name in ("oracle_score", "oracle_score_kind", "oracle_select", "oracle_compact"):
+        for name in ("oracle_score", "oracle_score_kind", "oracle_select", "oracle_compact", "oracle_select_layer",
+                     "oracle_compact_heads"):
             getattr(lib, name).argtypes = getattr(self.saved, name).argtypes
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
@@ -197,6 +203,54 @@ def select(final, lengths, evict_k, protect: int = 0):
     if st != OK:
         raise OracleError("oracle_select failed with status %d" % st)
     return kept, kl
+
+
+def select_layer(final, lengths, evict_total, protect: int = 0):
+    """Layer-wide bottom-k (AdaDropKV): per sequence, evict the evict_total[b]
+    smallest (score, head, position) over all KV heads.  Returns (kept_idx
+    [B,Hkv,n_max] int32, first kept_len[b,h] valid; kept_len [B,Hkv])."""
+    fin = np.ascontiguousarray(final, dtype=np.float64)
+    B, Hkv, n_max = fin.shape
+    lens = np.ascontiguousarray(np.asarray(lengths), dtype=np.int32)
+    et = np.ascontiguousarray(np.asarray(evict_total), dtype=np.int32)
+    kept = np.full((B, Hkv, n_max), -1, dtype=np.int32)
+    kl = np.zeros((B, Hkv), dtype=np.int32)
+    shape = _Shape(B, Hkv, Hkv, 1, n_max, 1)
+    st = _load().oracle_select_layer(ctypes.byref(shape), _ptr(fin), _ptr(lens), _ptr(et), protect,
+                                     _ptr(kept), _ptr(kl))
+    if st != OK:
+        raise OracleError("oracle_select_layer failed with status %d" % st)
+    return kept, kl
+
+
+def compact_heads(k, v, kept_idx, kept_len, out_rows: int):
+    """Gather with a kept count per KV head (kept_len [B,Hkv])."""
+    ka = np.ascontiguousarray(k)
+    va = np.ascontiguousarray(v)
+    B, Hkv, n_max, d = ka.shape
+    idx = np.ascontiguousarray(kept_idx, dtype=np.int32)
+    kl = np.ascontiguousarray(kept_len, dtype=np.int32)
+    k_out = np.zeros((B, Hkv, out_rows, d), dtype=ka.dtype)
+    v_out = np.zeros((B, Hkv, out_rows, d), dtype=va.dtype)
+    shape = _Shape(B, Hkv, Hkv, d, n_max, 1)
+    st = _load().oracle_compact_heads(ctypes.byref(shape), ka.dtype.itemsize, _ptr(ka), _ptr(va), _ptr(idx),
+                                      _ptr(kl), out_rows, _ptr(k_out), _ptr(v_out))
+    if st != OK:
+        raise OracleError("oracle_compact_heads failed with status %d" % st)
+    return k_out, v_out
+
+
+def run_path_layer(q, k, v, lengths, evict_total, pool_kernel, protect, out_rows=None, nthreads=None,
+                   kind="dropkv"):
+    """S1-S5, the layer-wide selection and the per-head gather."""
+    sc = score(q, k, v, lengths, pool_kernel, protect, nthreads=nthreads, kind=kind)
+    kept, kl = select_layer(sc["final"], lengths, evict_total, protect)
+    rows = int(out_rows) if out_rows is not None else int(kl.max())
+    kb, _ = _as_input(k)
+    vb, _ = _as_input(v)
+    k_out, v_out = compact_heads(kb, vb, kept, kl, rows)
+    sc.update(kept_idx=kept, kept_len=kl, k_out=k_out, v_out=v_out)
+    return sc
 
 
 def compact(k, v, kept_idx, kept_len, out_rows: int):

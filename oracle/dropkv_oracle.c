@@ -37,6 +37,13 @@
  *       Decoupling ...", section 2.2: eviction shrinks the resident cache).
  *  [S7] the kept K/V rows are gathered in that order (byte copies).
  *
+ * Layer-wide selection (AdaDropKV: DropKV scores with an adaptive head
+ * budget, "DropKV: Decoupling ...", section 5.3 and Appendix A.3; the pages
+ * give no allocation rule, so the plainest one is taken): for each sequence,
+ * the scores of all its KV heads form one pool; the evict_total[b] smallest
+ * (score, head, position) triples are evicted, so each head keeps its own
+ * number of slots.  Each head's kept positions are listed ascending.
+ *
  * Score kind SnapKV (the attention-only baseline of "DropKV: Decoupling ...",
  * Appendix B, Table 14: MaxPool1d over the window sum of p_j): step S3 becomes
  * s_j = sum_t p_j^(t) and the singular rule S2 does not apply (nothing is
@@ -300,6 +307,70 @@ int oracle_select(const oracle_shape* s, const double* final_scores, const int32
         }
     }
     free(tmp);
+    return ORACLE_OK;
+}
+
+/* Layer-wide S6: one pool per sequence over all its KV heads; ties go to the
+ * lower head, then the lower position.  kept_len is [B][Hkv]. */
+int oracle_select_layer(const oracle_shape* s, const double* final_scores, const int32_t* lengths,
+                        const int32_t* evict_total, int protect, int32_t* kept_idx, int32_t* kept_len) {
+    if (!check_shape(s) || !final_scores || !lengths || !evict_total || !kept_idx || !kept_len)
+        return ORACLE_INVALID;
+    for (int b = 0; b < s->B; ++b) {
+        if (lengths[b] < 1 || lengths[b] > s->n_max) return ORACLE_INVALID;
+        if (evict_total[b] < 0 || evict_total[b] > s->Hkv * (lengths[b] - protect)) return ORACLE_INVALID;
+    }
+    const size_t n_max = (size_t)s->n_max;
+    keyed* tmp = (keyed*)malloc((size_t)s->Hkv * n_max * sizeof(keyed));
+    char* keep = (char*)malloc((size_t)s->Hkv * n_max);
+    if (!tmp || !keep) { free(tmp); free(keep); return ORACLE_NOMEM; }
+    for (int b = 0; b < s->B; ++b) {
+        const int nb = lengths[b];
+        size_t m = 0;
+        for (int h = 0; h < s->Hkv; ++h) {
+            const double* fin = final_scores + ((size_t)b * s->Hkv + h) * n_max;
+            for (int j = 0; j < nb; ++j) {
+                tmp[m].key = fin[j];
+                tmp[m].idx = (int32_t)((size_t)h * n_max + (size_t)j);
+                ++m;
+            }
+        }
+        qsort(tmp, m, sizeof(keyed), cmp_keyed);
+        memset(keep, 0, (size_t)s->Hkv * n_max);
+        for (size_t i = (size_t)evict_total[b]; i < m; ++i) keep[tmp[i].idx] = 1;
+        for (int h = 0; h < s->Hkv; ++h) {
+            int32_t* out = kept_idx + ((size_t)b * s->Hkv + h) * n_max;
+            int c = 0;
+            for (int j = 0; j < nb; ++j)
+                if (keep[(size_t)h * n_max + (size_t)j]) out[c++] = j;
+            kept_len[(size_t)b * s->Hkv + h] = c;
+        }
+    }
+    free(tmp);
+    free(keep);
+    return ORACLE_OK;
+}
+
+/* S7 with a kept count per KV head (kept_len [B][Hkv]). */
+int oracle_compact_heads(const oracle_shape* s, int elem_bytes, const void* k, const void* v,
+                         const int32_t* kept_idx, const int32_t* kept_len, int out_rows,
+                         void* k_out, void* v_out) {
+    if (!check_shape(s) || elem_bytes < 1 || !k || !v || !kept_idx || !kept_len || !k_out || !v_out)
+        return ORACLE_INVALID;
+    const size_t row_bytes = (size_t)s->d * elem_bytes;
+    const size_t n_max = (size_t)s->n_max;
+    for (int u = 0; u < s->B * s->Hkv; ++u)
+        if (kept_len[u] < 0 || kept_len[u] > out_rows) return ORACLE_INVALID;
+    for (size_t unit = 0; unit < (size_t)s->B * s->Hkv; ++unit) {
+        const int32_t* idx = kept_idx + unit * n_max;
+        for (int i = 0; i < kept_len[unit]; ++i) {
+            if (idx[i] < 0 || (size_t)idx[i] >= n_max) return ORACLE_INVALID;
+            const size_t src = (unit * n_max + (size_t)idx[i]) * row_bytes;
+            const size_t dst = (unit * (size_t)out_rows + (size_t)i) * row_bytes;
+            memcpy((char*)k_out + dst, (const char*)k + src, row_bytes);
+            memcpy((char*)v_out + dst, (const char*)v + src, row_bytes);
+        }
+    }
     return ORACLE_OK;
 }
 

@@ -34,6 +34,16 @@ int oracle_score_kind(const oracle_shape* s, int kind, int dtype, const void* q,
 int oracle_select(const oracle_shape* s, const double* final_scores, const int32_t* lengths,
                   const int32_t* evict_k, int protect, int32_t* kept_idx, int32_t* kept_len);
 
+/* Layer-wide bottom-k: per sequence, evict the evict_total[b] smallest
+ * (score, head, position) over all KV heads; kept_len [B,Hkv]. */
+int oracle_select_layer(const oracle_shape* s, const double* final_scores, const int32_t* lengths,
+                        const int32_t* evict_total, int protect, int32_t* kept_idx, int32_t* kept_len);
+
+/* Gather with a kept count per KV head (kept_len [B,Hkv]). */
+int oracle_compact_heads(const oracle_shape* s, int elem_bytes, const void* k, const void* v,
+                         const int32_t* kept_idx, const int32_t* kept_len, int out_rows,
+                         void* k_out, void* v_out);
+
 /* Gather of kept rows: k_out/v_out [B,Hkv,out_rows,d] of elem_bytes elements. */
 int oracle_compact(const oracle_shape* s, int elem_bytes, const void* k, const void* v,
                    const int32_t* kept_idx, const int32_t* kept_len, int out_rows,

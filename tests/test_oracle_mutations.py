@@ -29,6 +29,10 @@ MUTATIONS = {
                             "for (int j = 0; j <= pos; ++j) s_head[j] += e[j];"),
     "snapkv_singular_rule": ("if (p == 1.0 && job->kind == ORACLE_KIND_DROPKV) return ORACLE_SINGULAR;",
                              "if (p == 1.0) return ORACLE_SINGULAR;"),
+    "layer_evicts_one_more": ("for (size_t i = (size_t)evict_total[b]; i < m; ++i) keep[tmp[i].idx] = 1;",
+                              "for (size_t i = (size_t)evict_total[b] + 1; i < m; ++i) keep[tmp[i].idx] = 1;"),
+    "layer_ties_by_position_first": ("tmp[m].idx = (int32_t)((size_t)h * n_max + (size_t)j);",
+                                     "tmp[m].idx = (int32_t)((size_t)j * s->Hkv + (size_t)h);"),
 }
 
 
@@ -41,6 +45,7 @@ def _run_pins():
     pins.test_select_vs_stable_sort_with_ties(0)
     pins.test_snapkv_raw_vs_torch_softmax(42)
     pins.test_snapkv_has_no_singular_rule()
+    pins.test_select_layer_vs_stable_sort(0)
 
 
 def test_unmodified_source_passes(tmp_path):

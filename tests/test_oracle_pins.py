@@ -421,3 +421,71 @@ def test_snapkv_has_no_singular_rule():
     res = oracle.score(q, k, v, np.array([32], dtype=np.int32), kind="snapkv")
     assert res["raw"][0, 0, 5] == 2.0
     assert np.all(res["raw"][0, 0, np.arange(32) != 5] == 0.0)
+
+
+# ------------------------------------------------------------ layer-wide selection
+def _layer_reference(fin, lengths, evict_total):
+    """torch's stable sort over each sequence's scores laid out head after
+    head (ties keep that order: lower head, then lower position)."""
+    B, H, n = fin.shape
+    kept = {}
+    for b in range(B):
+        nb = int(lengths[b])
+        flat = torch.from_numpy(np.ascontiguousarray(fin[b, :, :nb]).reshape(-1))
+        order = torch.sort(flat, stable=True).indices.numpy()
+        keep = np.sort(order[int(evict_total[b]):])
+        for h in range(H):
+            sel = keep[(keep >= h * nb) & (keep < (h + 1) * nb)] - h * nb
+            kept[(b, h)] = sel.astype(np.int32)
+    return kept
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_select_layer_vs_stable_sort(seed):
+    rng = np.random.default_rng(seed)
+    B, H, n = 3, 4, 300
+    fin = rng.integers(0, 50, size=(B, H, n)).astype(np.float64)        # many ties across heads
+    lengths = np.array([300, 123, 41], dtype=np.int32)
+    protect = 3
+    for b in range(B):
+        fin[b, :, lengths[b] - protect:lengths[b]] = np.inf
+        fin[b, :, lengths[b]:] = np.nan
+    evict_total = np.array([H * (300 - protect), 200, 0], dtype=np.int32)
+    kept, kl = oracle.select_layer(fin, lengths, evict_total, protect)
+    ref = _layer_reference(fin, lengths, evict_total)
+    for b in range(B):
+        assert int(kl[b].sum()) == H * int(lengths[b]) - int(evict_total[b])
+        for h in range(H):
+            assert np.array_equal(kept[b, h, :kl[b, h]], ref[(b, h)])
+            assert set(range(lengths[b] - protect, lengths[b])) <= set(kept[b, h, :kl[b, h]].tolist())
+
+
+def test_select_layer_brute_force():
+    """Rank every (score, head, position) triple by counting the ones below it."""
+    rng = np.random.default_rng(7)
+    H, n = 3, 20
+    fin = rng.integers(0, 6, size=(1, H, n)).astype(np.float64)
+    for e in (0, 1, 17, 30, H * n):
+        kept, kl = oracle.select_layer(fin, [n], [e], 0)
+        trip = [(fin[0, h, j], h, j) for h in range(H) for j in range(n)]
+        evicted = {(h, j) for (s, h, j) in trip if sum(t < (s, h, j) for t in trip) < e}
+        for h in range(H):
+            want = [j for j in range(n) if (h, j) not in evicted]
+            assert kept[0, h, :kl[0, h]].tolist() == want
+
+
+def test_compact_heads_byte_exact():
+    rng = np.random.default_rng(3)
+    k = rng.integers(0, 2 ** 16, size=(2, 3, 50, 8), dtype=np.uint16)
+    v = rng.integers(0, 2 ** 16, size=(2, 3, 50, 8), dtype=np.uint16)
+    kept = np.full((2, 3, 50), -1, dtype=np.int32)
+    kl = np.array([[5, 0, 50], [1, 2, 3]], dtype=np.int32)
+    for b in range(2):
+        for h in range(3):
+            kept[b, h, :kl[b, h]] = np.sort(rng.choice(50, kl[b, h], replace=False))
+    ko, vo = oracle.compact_heads(k, v, kept, kl, 50)
+    for b in range(2):
+        for h in range(3):
+            idx = kept[b, h, :kl[b, h]]
+            assert np.array_equal(ko[b, h, :kl[b, h]], k[b, h, idx])
+            assert np.array_equal(vo[b, h, :kl[b, h]], v[b, h, idx])
