@@ -35,11 +35,13 @@ SEL_CHUNK = 16384         # slots per CTA in the selection kernels
 CLUSTER_MAX_CHUNKS = 8    # heads of up to 8 chunks are selected by one cluster launch
 
 
-def kernels_per_step(n_max):
-    """Kernels one dropkv_evict step launches: window attention, split merge,
-    score, then either one cluster selection that also pools, or (heads
-    longer than 8 chunks) pool+protect, clear and 3 radix kernels; then
-    compaction."""
+def kernels_per_step(n_max, select="head"):
+    """Kernels one step launches: window attention, split merge, score, then
+    either one cluster selection that also pools, or (heads longer than 8
+    chunks) pool+protect, clear and 3 radix kernels; then compaction.  The
+    layer-wide selection: pool+protect, clear and 5 kernels."""
+    if select == "layer":
+        return 3 + 1 + 6 + 1
     chunks = -(-n_max // SEL_CHUNK)
     return 3 + (1 if chunks <= CLUSTER_MAX_CHUNKS else 5) + 1
 L2_FLUSH_BYTES = 256 << 20
@@ -57,6 +59,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--score", choices=["dropkv", "snapkv"], default="dropkv",
                     help="score kind: the DropKV perturbation score (default) or the SnapKV baseline")
+    ap.add_argument("--select", choices=["head", "layer"], default="head",
+                    help="bottom-k per KV head (default) or one pool per sequence over its KV heads (AdaDropKV)")
     return ap.parse_args()
 
 
@@ -76,15 +80,15 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def config_of(spec, lengths, score="dropkv"):
-    return {"workload": spec.name, "score": score, "B": spec.B, "Hq": spec.Hq, "Hkv": spec.Hkv, "d": spec.d, "n_max": spec.n_max,
+def config_of(spec, lengths, score="dropkv", select="head"):
+    return {"workload": spec.name, "score": score, "select": select, "B": spec.B, "Hq": spec.Hq, "Hkv": spec.Hkv, "d": spec.d, "n_max": spec.n_max,
             "n_tokens": int(sum(lengths)), "w": spec.w, "pool_kernel": spec.pool_kernel, "protect": spec.protect,
             "budget_pct_kept": spec.budget_pct, "inputs": "bf16",
             "l2": "inputs larger than L2 (K+V %.0f MB); between steps a 256 MB write flushes L2 and a 256 MB read cleans it" % (
                 2 * spec.B * spec.Hkv * spec.n_max * spec.d * 2 / 1e6)}
 
 
-def workload_bytes(spec, lengths, kept, score="dropkv"):
+def workload_bytes(spec, lengths, kept, score="dropkv", select="head"):
     """Algorithmic bytes of the two-pass structure (byte model).
     The SnapKV score reads only K in both passes."""
     U_tok = spec.Hkv * int(sum(lengths))                  # head-tokens
@@ -96,6 +100,8 @@ def workload_bytes(spec, lengths, kept, score="dropkv"):
     # made in shared memory (pool's 8 B cover its reads and writes); the
     # multi-kernel path for heads longer than 8 chunks reads the scores 3 times
     sel_passes = 0 if -(-spec.n_max // SEL_CHUNK) <= CLUSTER_MAX_CHUNKS else 3
+    if select == "layer":
+        sel_passes = 5                                    # three digit histograms, counts, write
     sel = U_tok * 4 * sel_passes + spec.Hkv * int(sum(kept)) * 4
     comp = spec.Hkv * int(sum(kept)) * (4 + 2 * 2 * spec.d * 2)
     return {"window_attention": p1, "score": p2, "pool_protect": pool, "select": sel, "compact": comp,
@@ -255,10 +261,14 @@ def main():
     lengths_np = wl.lengths.numpy()
     kept_np = wl.kept_len()
     units = int(sum(lengths_np))
+    layer = args.select == "layer"
+    # the layer-wide selection keeps a data-dependent count per head: room for n_max rows
     op = DropKV(spec.B, spec.Hq, spec.Hkv, spec.d, spec.n_max, spec.w, spec.pool_kernel, spec.protect,
-                out_rows=int(kept_np.max()), device=dev, kind=args.score)
+                out_rows=spec.n_max if layer else int(kept_np.max()), device=dev, kind=args.score)
     q, k, v = wl.q.to(dev), wl.k.to(dev), wl.v.to(dev)
     lengths, ev = wl.lengths.to(dev), wl.evict_k.to(dev)
+    if layer:
+        ev = ev * spec.Hkv            # the same total budget as per-head selection
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     clean = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
@@ -272,13 +282,22 @@ def main():
 
     def step(events=None):
         if events is None:
-            op.run(q, k, v, lengths, ev, stream=stream, keep_raw=False)
+            if layer:
+                op.run_layer(q, k, v, lengths, ev, stream=stream, keep_raw=False)
+            else:
+                op.run(q, k, v, lengths, ev, stream=stream, keep_raw=False)
         else:
             B.dropkv_score_timed(op.shape, q, k, v, lengths, op.pool_kernel, op.protect, op.scores, None,
                                  op.workspace, op.status, events[1:6], stream, kind=args.score)
-            op.select(lengths, ev, stream)
+            if layer:
+                op.select_layer(lengths, ev, stream)
+            else:
+                op.select(lengths, ev, stream)
             events[6].record(stream)
-            op.compact(k, v, stream)
+            if layer:
+                op.compact_heads(k, v, stream)
+            else:
+                op.compact(k, v, stream)
 
     for w in range(max(3, args.warmup)):
         flush_l2(w)
@@ -340,7 +359,7 @@ def main():
         step_ms = float(t.item())
     value = units * world / (step_ms / 1e3)
 
-    nbytes = workload_bytes(spec, lengths_np, kept_np, args.score)
+    nbytes = workload_bytes(spec, lengths_np, kept_np, args.score, args.select)
     peak, peak_kind = measured_peaks()
     phase_ms = {kname: sum(v_) / KP for kname, v_ in phases.items()}
     dom = max(("window_attention", "score"), key=lambda kk: phase_ms[kk])
@@ -354,12 +373,13 @@ def main():
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
             "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f32", "data": "synthetic (seeded generator; stands in for RULER/LongBench layers)",
-            "config": dict(config_of(spec, lengths_np, args.score), parallelism="one independent layer per GPU"),
+            "config": dict(config_of(spec, lengths_np, args.score, args.select),
+                           parallelism="one independent layer per GPU"),
             "roofline": roofline,
             "path_roofline": {"achieved": path_gbs, "peak": peak, "unit": "GB/s", "frac": path_gbs / peak,
                               "algorithmic_bytes_per_step": nbytes["path"]},
             "phases_ms": phase_ms, "phases_note": "per-kernel times from %d separate steps with events at the phase boundaries, run as the three separate calls (pooling in its own kernel; the timed step pools inside the selection)" % KP,
-            "wall_s_timed": wall, "gpu_launches": kernels_per_step(spec.n_max) * K,
+            "wall_s_timed": wall, "gpu_launches": kernels_per_step(spec.n_max, args.select) * K,
             "clocks": clocks}
 
     if not args.no_e2e:
@@ -389,7 +409,10 @@ def e2e_leg(op, wl, dev, stream, args, world):
     def one():
         for src, dst in ((hq, dq), (hk, dk), (hv, dv), (hl, dl), (he, de)):
             dst.copy_(src, non_blocking=True)
-        op.run(dq, dk, dv, dl, de, stream=stream, keep_raw=False)
+        if args.select == "layer":
+            op.run_layer(dq, dk, dv, dl, de * op.shape.Hkv, stream=stream, keep_raw=False)
+        else:
+            op.run(dq, dk, dv, dl, de, stream=stream, keep_raw=False)
         for src, dst in zip(outs, houts):
             dst.copy_(src, non_blocking=True)
 

@@ -176,6 +176,32 @@ DROPKV_API dropkv_status dropkv_compact(const dropkv_shape* shape, const void* k
                              const int32_t* kept_len, int32_t out_rows, void* k_out, void* v_out,
                              uint32_t* status, cudaStream_t stream);
 
+/* Step S5 with one pool per sequence (the adaptive head budget of AdaDropKV,
+ * "DropKV: Decoupling ...", section 5.3 and Appendix A.3; the pages give no
+ * allocation rule, so the plainest is taken): the scores of all KV heads of
+ * sequence b compete, and the evict_total[b] smallest (score, head, position)
+ * triples are evicted (equal scores: the lower head, then the lower position,
+ * goes first), so each head keeps its own number of slots.
+ *   scores    device float [B][Hkv][n_max] (as written by dropkv_score)
+ *   lengths   device int32 [B] or NULL (n_max)
+ *   evict_total  device int32 [B]: 0 <= e_b <= Hkv (n_b - protect) (else
+ *             FLAG_BAD_K and nothing evicted); Hkv * k_b gives the same total
+ *             budget as dropkv_select
+ *   kept_idx  device int32 [B][Hkv][n_max]: first kept_len[b][h] entries of
+ *             each head = kept positions ascending; the rest untouched
+ *   kept_len  device int32 [B][Hkv]
+ * Requires Hkv * n_max < 2^31. */
+DROPKV_API dropkv_status dropkv_select_layer(const dropkv_shape* shape, const float* scores, const int32_t* lengths,
+                                             const int32_t* evict_total, int32_t protect, int32_t* kept_idx,
+                                             int32_t* kept_len, void* workspace, size_t workspace_bytes,
+                                             uint32_t* status, cudaStream_t stream);
+
+/* dropkv_compact with a kept count per KV head: kept_len is [B][Hkv] (as
+ * written by dropkv_select_layer); everything else as dropkv_compact. */
+DROPKV_API dropkv_status dropkv_compact_heads(const dropkv_shape* shape, const void* k, const void* v,
+                                              const int32_t* kept_idx, const int32_t* kept_len, int32_t out_rows,
+                                              void* k_out, void* v_out, uint32_t* status, cudaStream_t stream);
+
 /* Steps S1-S6 in one call: dropkv_score, dropkv_select and (when k_out and
  * v_out are given) dropkv_compact, with the same arguments, outputs and
  * results as those three calls in sequence.  Every argument is checked before

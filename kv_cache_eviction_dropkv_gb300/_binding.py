@@ -71,6 +71,10 @@ def lib():
             L.dropkv_evict_ex.restype = ctypes.c_int
             L.dropkv_score_ex.argtypes = [SH, I32, P, P, P, P, I32, I32, P, P, P, SZ, P, P]
             L.dropkv_score_ex.restype = ctypes.c_int
+            L.dropkv_select_layer.argtypes = [SH, P, P, P, I32, P, P, P, SZ, P, P]
+            L.dropkv_select_layer.restype = ctypes.c_int
+            L.dropkv_compact_heads.argtypes = [SH, P, P, P, P, I32, P, P, P, P]
+            L.dropkv_compact_heads.restype = ctypes.c_int
             L.dropkv_read_status.argtypes = [P, P, ctypes.POINTER(ctypes.c_uint32)]
             L.dropkv_read_status.restype = ctypes.c_int
             L.dropkv_version.argtypes = []
@@ -190,6 +194,20 @@ def dropkv_evict_ex(shape, kind, q_window, k, v, lengths, evict_k, pool_kernel, 
                                  _ptr(v_out), _ptr(workspace), workspace.numel() * workspace.element_size(),
                                  _ptr(status), _stream(stream))
     return _check(code, "dropkv_evict_ex")
+
+
+def dropkv_select_layer(shape, scores, lengths, evict_total, protect, kept_idx, kept_len, workspace, status,
+                        stream=None):
+    code = lib().dropkv_select_layer(ctypes.byref(shape), _ptr(scores), _ptr(lengths), _ptr(evict_total),
+                                     int(protect), _ptr(kept_idx), _ptr(kept_len), _ptr(workspace),
+                                     workspace.numel() * workspace.element_size(), _ptr(status), _stream(stream))
+    return _check(code, "dropkv_select_layer")
+
+
+def dropkv_compact_heads(shape, k, v, kept_idx, kept_len, out_rows, k_out, v_out, status, stream=None):
+    code = lib().dropkv_compact_heads(ctypes.byref(shape), _ptr(k), _ptr(v), _ptr(kept_idx), _ptr(kept_len),
+                                      int(out_rows), _ptr(k_out), _ptr(v_out), _ptr(status), _stream(stream))
+    return _check(code, "dropkv_compact_heads")
 
 
 def dropkv_read_status(status, stream=None):

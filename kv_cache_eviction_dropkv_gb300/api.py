@@ -41,6 +41,7 @@ class DropKV:
             self.raw_scores = torch.empty(B_, Hkv, n_max, dtype=torch.float32, device=dev)
             self.kept_idx = torch.empty(B_, Hkv, n_max, dtype=torch.int32, device=dev)
             self.kept_len = torch.empty(B_, dtype=torch.int32, device=dev)
+            self.kept_len_heads = torch.empty(B_, Hkv, dtype=torch.int32, device=dev)
             self.k_out = torch.empty(B_, Hkv, self.out_rows, d, dtype=torch.bfloat16, device=dev)
             self.v_out = torch.empty(B_, Hkv, self.out_rows, d, dtype=torch.bfloat16, device=dev)
 
@@ -77,6 +78,22 @@ class DropKV:
         self.score(q, k, v, lengths, stream, keep_raw)
         self.select(lengths, evict_k, stream)
         self.compact(k, v, stream)
+
+    def select_layer(self, lengths, evict_total, stream=None):
+        """Layer-wide selection (one pool per sequence over its KV heads):
+        kept_idx per head, counts in kept_len_heads [B, Hkv]."""
+        B.dropkv_select_layer(self.shape, self.scores, lengths, evict_total, self.protect, self.kept_idx,
+                              self.kept_len_heads, self.workspace, self.status, stream)
+
+    def compact_heads(self, k, v, stream=None):
+        B.dropkv_compact_heads(self.shape, k, v, self.kept_idx, self.kept_len_heads, self.out_rows, self.k_out,
+                               self.v_out, self.status, stream)
+
+    def run_layer(self, q, k, v, lengths, evict_total, stream=None, keep_raw=True):
+        """Score, layer-wide selection and per-head compaction (AdaDropKV reading)."""
+        self.score(q, k, v, lengths, stream, keep_raw)
+        self.select_layer(lengths, evict_total, stream)
+        self.compact_heads(k, v, stream)
 
     def check(self, stream=None):
         """Sync and raise if the device status word reports an error."""

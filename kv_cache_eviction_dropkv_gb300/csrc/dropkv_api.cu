@@ -132,6 +132,13 @@ WsPlan make_plan(const Geom& g) {
   w.sel_state = take((size_t)g.U * 8 * 4);
   w.cand = take((size_t)g.U * kCandCap * 2 * 4);
   w.chunk_off = take((size_t)g.U * g.chunks * 4);
+  w.layer_zero_begin = off;
+  w.layer_h1 = take((size_t)g.B * kHistBins * 4);
+  w.layer_h2 = take((size_t)g.B * kHistBins * 4);
+  w.layer_h3 = take((size_t)g.B * 256 * 4);
+  w.layer_zero_end = off;
+  w.layer_state = take((size_t)g.B * 8 * 4);
+  w.layer_counts = take((size_t)g.U * g.chunks * 2 * 4);
   w.total = off;
   return w;
 }
@@ -268,7 +275,7 @@ dropkv_status select_impl(const dropkv_shape* shape, const float* scores, const 
 
 dropkv_status compact_impl(const dropkv_shape* shape, const void* k, const void* v, const int32_t* kept_idx,
                            const int32_t* kept_len, int32_t out_rows, void* k_out, void* v_out, uint32_t* status,
-                           cudaStream_t stream, bool check_only) {
+                           cudaStream_t stream, bool check_only, bool per_head = false) {
   const int sms = current_sms(nullptr);
   if (sms <= 0) return DROPKV_ERR_CUDA;
   Geom g;
@@ -291,6 +298,7 @@ dropkv_status compact_impl(const dropkv_shape* shape, const void* k, const void*
   p.v_out = static_cast<uint8_t*>(v_out);
   p.B = g.B; p.Hkv = g.Hkv; p.n_max = g.n_max; p.row_bytes = g.d * 2; p.out_rows = out_rows;
   p.status = status;
+  p.per_head = per_head ? 1 : 0;
   return launch_compact(p, stream) == cudaSuccess ? DROPKV_OK : DROPKV_ERR_CUDA;
 }
 
@@ -368,6 +376,44 @@ dropkv_status dropkv_score_ex(const dropkv_shape* shape, int32_t score_kind, con
                               uint32_t* status, cudaStream_t stream) {
   return score_impl(shape, q_window, k, v, lengths, pool_kernel, protect, scores, raw_scores, workspace,
                     workspace_bytes, status, stream, nullptr, nullptr, score_kind);
+}
+
+dropkv_status dropkv_select_layer(const dropkv_shape* shape, const float* scores, const int32_t* lengths,
+                                  const int32_t* evict_total, int32_t protect, int32_t* kept_idx, int32_t* kept_len,
+                                  void* workspace, size_t workspace_bytes, uint32_t* status, cudaStream_t stream) {
+  const int sms = current_sms(nullptr);
+  if (sms <= 0) return DROPKV_ERR_CUDA;
+  Geom g;
+  if (!shape || !make_geom(shape, sms, &g)) return DROPKV_ERR_INVALID_ARG;
+  if (!scores || !evict_total || !kept_idx || !kept_len || !status || protect < 0) return DROPKV_ERR_INVALID_ARG;
+  if (!aligned16(scores) || !aligned16(kept_idx)) return DROPKV_ERR_INVALID_ARG;
+  if ((long long)g.Hkv * g.n_max >= (1LL << 31)) return DROPKV_ERR_UNSUPPORTED;
+  const WsPlan w = make_plan(g);
+  if (!workspace || workspace_bytes < w.total || !aligned16(workspace)) return DROPKV_ERR_WORKSPACE;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  LayerSelParams p{};
+  p.scores = scores;
+  p.lengths = lengths;
+  p.evict_total = evict_total;
+  p.kept_idx = kept_idx;
+  p.kept_len = kept_len;
+  p.B = g.B; p.Hkv = g.Hkv; p.n_max = g.n_max; p.protect = protect; p.chunks = g.chunks;
+  p.h1 = reinterpret_cast<uint32_t*>(ws + w.layer_h1);
+  p.h2 = reinterpret_cast<uint32_t*>(ws + w.layer_h2);
+  p.h3 = reinterpret_cast<uint32_t*>(ws + w.layer_h3);
+  p.state = reinterpret_cast<uint32_t*>(ws + w.layer_state);
+  p.counts = reinterpret_cast<uint32_t*>(ws + w.layer_counts);
+  p.status = status;
+  return launch_select_layer(p, w.layer_zero_end - w.layer_zero_begin, ws + w.layer_zero_begin, stream) ==
+                 cudaSuccess
+             ? DROPKV_OK
+             : DROPKV_ERR_CUDA;
+}
+
+dropkv_status dropkv_compact_heads(const dropkv_shape* shape, const void* k, const void* v, const int32_t* kept_idx,
+                                   const int32_t* kept_len, int32_t out_rows, void* k_out, void* v_out,
+                                   uint32_t* status, cudaStream_t stream) {
+  return compact_impl(shape, k, v, kept_idx, kept_len, out_rows, k_out, v_out, status, stream, false, true);
 }
 
 dropkv_status dropkv_read_status(const uint32_t* status, cudaStream_t stream, uint32_t* flags_out) {

@@ -48,6 +48,11 @@ struct WsPlan {
   size_t sel_tickets;            // u32 [U][2]
   size_t chunk_kept;             // u32 [U][chunks]
   size_t chunk_off;              // u32 [U][chunks]
+  size_t layer_zero_begin;       // layer-wide selection: h1, h2 [B][4096], h3 [B][256] (cleared per call)
+  size_t layer_h1, layer_h2, layer_h3;
+  size_t layer_zero_end;
+  size_t layer_state;            // u32 [B][8]
+  size_t layer_counts;           // u32 [B][Hkv][chunks][2]
   size_t sel_zero_begin, sel_zero_end;   // range cleared at the start of dropkv_select
   size_t total;
 };
@@ -106,6 +111,21 @@ struct CompactParams {
   uint8_t* v_out;
   int B, Hkv, n_max, row_bytes, out_rows;
   uint32_t* status;
+  int per_head;                  // kept_len is [B][Hkv] (layer-wide selection), else [B]
+};
+
+// Layer-wide selection: one pool per sequence over all its KV heads.
+struct LayerSelParams {
+  const float* scores;           // [B][Hkv][n_max]
+  const int32_t* lengths;        // [B] or null
+  const int32_t* evict_total;    // [B]
+  int32_t* kept_idx;             // [B][Hkv][n_max]
+  int32_t* kept_len;             // [B][Hkv]
+  int B, Hkv, n_max, protect, chunks;   // chunks per head
+  uint32_t *h1, *h2, *h3;        // [B][4096], [B][4096], [B][256] (cleared before the first kernel)
+  uint32_t* state;               // [B][8]
+  uint32_t* counts;              // [B][Hkv][chunks][2]: slots above T, slots equal to T
+  uint32_t* status;
 };
 
 // Launch with programmatic dependent launch: the kernel may be scheduled
@@ -135,6 +155,7 @@ cudaError_t launch_score(const AttnParams& p, int NR, const CUtensorMap& tk, con
                          cudaStream_t st);
 cudaError_t launch_pool_protect(const PoolParams& p, cudaStream_t st);
 cudaError_t launch_select(const SelParams& p, size_t zero_bytes, void* zero_base, cudaStream_t st);
+cudaError_t launch_select_layer(const LayerSelParams& p, size_t zero_bytes, void* zero_base, cudaStream_t st);
 cudaError_t launch_compact(const CompactParams& p, cudaStream_t st);
 
 }  // namespace dropkv

@@ -849,6 +849,269 @@ __global__ void __launch_bounds__(kClThreads, 1) select_cluster_kernel(const Sel
   }
 }
 
+// ------------------------------------------------------------ layer-wide selection
+// The adaptive head budget of AdaDropKV ("DropKV: Decoupling ...", section 5.3
+// and Appendix A.3), read as one pool per sequence: the scores of all its KV
+// heads compete, and the evict_total[b] smallest (score, head, position)
+// triples are evicted, so each head keeps its own number of slots.  Grid
+// (chunks, Hkv, B): one 16384-slot chunk of one head per CTA, 64 consecutive
+// slots per thread.  The k-th triple is found digit by digit (key bits
+// 31..20, 19..8, 7..0, then the tie rank among equal keys in head-major
+// order) over five kernels whose boundaries order the global histograms, so
+// nothing waits on another CTA; the last kernel turns per-chunk counts into
+// per-head output offsets.
+enum { kLsBin1 = 0, kLsRank1 = 1, kLsPre24 = 2, kLsRank2 = 3, kLsKey = 4, kLsRank3 = 5 };
+constexpr int kLsPer = kSelChunk / kSelThreads;   // 64 consecutive slots per thread
+
+struct LayerInfo {
+  int nb, e;
+  uint32_t mode;
+};
+
+__device__ __forceinline__ LayerInfo layer_info(const LayerSelParams& p, int b) {
+  LayerInfo u;
+  u.nb = p.lengths ? p.lengths[b] : p.n_max;
+  u.e = p.evict_total[b];
+  if (u.nb < 1 || u.nb > p.n_max || u.nb < p.protect) u.mode = kModeSkip;
+  else if (u.e <= 0 || (long long)u.e > (long long)p.Hkv * (u.nb - p.protect)) u.mode = kModeKeepAll;
+  else u.mode = kModeNormal;
+  return u;
+}
+
+// Keys of this thread's slots j0 + 64 t + [0, 64) (slots >= nb are masked by nv).
+__device__ __forceinline__ int layer_keys(const LayerSelParams& p, int b, int h, int j0, int nb,
+                                          uint32_t (&key)[kLsPer]) {
+  const float* row = p.scores + ((size_t)b * p.Hkv + h) * p.n_max;
+  const bool vec = (p.n_max & 3) == 0;
+  const int jt = j0 + (int)threadIdx.x * kLsPer;
+#pragma unroll
+  for (int q4 = 0; q4 < kLsPer / 4; ++q4) {
+    const float4 x = load4(row, jt + q4 * 4, nb, vec);
+    key[q4 * 4 + 0] = f2ord(x.x);
+    key[q4 * 4 + 1] = f2ord(x.y);
+    key[q4 * 4 + 2] = f2ord(x.z);
+    key[q4 * 4 + 3] = f2ord(x.w);
+  }
+  return min(max(nb - jt, 0), kLsPer);
+}
+
+// Run-aggregated shared-memory histogram of the slots u < nv with member(key).
+template <typename Member, typename Digit>
+__device__ __forceinline__ void layer_hist_add(uint32_t* hist, const uint32_t (&key)[kLsPer], int nv, Member member,
+                                               Digit digit) {
+  uint32_t cur = kNoBin, cnt = 0;
+#pragma unroll
+  for (int u = 0; u < kLsPer; ++u) {
+    const uint32_t bn = (u < nv && member(key[u])) ? digit(key[u]) : kNoBin;
+    if (bn == cur) {
+      ++cnt;
+    } else {
+      if (cur != kNoBin) atomicAdd(&hist[cur], cnt);
+      cur = bn;
+      cnt = 1;
+    }
+  }
+  if (cur != kNoBin) atomicAdd(&hist[cur], cnt);
+}
+
+template <int BINS>
+__device__ __forceinline__ void layer_flush(const uint32_t* sh, uint32_t* gh) {
+  __syncthreads();
+  for (int i = threadIdx.x; i < BINS; i += kSelThreads)
+    if (sh[i]) atomicAdd(&gh[i], sh[i]);
+}
+
+// Digit 1 (key bits 31..20) of every head of the sequence into one histogram.
+__global__ void __launch_bounds__(kSelThreads) layer_hist1_kernel(const LayerSelParams p) {
+  __shared__ uint32_t sh[kHistBins];
+  grid_dep_wait();
+  grid_dep_launch();
+  const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const LayerInfo li = layer_info(p, b);
+  if (chunk == 0 && h == 0 && threadIdx.x == 0) {
+    if (li.mode == kModeSkip) atomicOr(p.status, DROPKV_FLAG_BAD_LENGTH);
+    else if (li.e < 0 || (long long)li.e > (long long)p.Hkv * (li.nb - p.protect)) atomicOr(p.status, DROPKV_FLAG_BAD_K);
+  }
+  const int j0 = chunk * kSelChunk;
+  if (li.mode != kModeNormal || j0 >= li.nb) return;
+  for (int i = threadIdx.x; i < kHistBins; i += kSelThreads) sh[i] = 0;
+  __syncthreads();
+  uint32_t key[kLsPer];
+  const int nv = layer_keys(p, b, h, j0, li.nb, key);
+  layer_hist_add(sh, key, nv, [](uint32_t) { return true; }, [](uint32_t k) { return k >> 20; });
+  layer_flush<kHistBins>(sh, p.h1 + (size_t)b * kHistBins);
+}
+
+// Digit 2 (key bits 19..8) of the members of the k-th key's digit-1 bin.
+__global__ void __launch_bounds__(kSelThreads) layer_hist2_kernel(const LayerSelParams p) {
+  __shared__ uint32_t sh[kHistBins];
+  __shared__ uint32_t scratch[32];
+  grid_dep_wait();
+  grid_dep_launch();
+  const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const LayerInfo li = layer_info(p, b);
+  const int j0 = chunk * kSelChunk;
+  if (li.mode != kModeNormal || j0 >= li.nb) return;
+  uint32_t bin1, rank1, cnt1;
+  find_bin(p.h1 + (size_t)b * kHistBins, (uint32_t)li.e, scratch, bin1, rank1, cnt1);
+  if (chunk == 0 && h == 0 && threadIdx.x == 0) {
+    p.state[b * 8 + kLsBin1] = bin1;
+    p.state[b * 8 + kLsRank1] = rank1;
+  }
+  for (int i = threadIdx.x; i < kHistBins; i += kSelThreads) sh[i] = 0;
+  __syncthreads();
+  uint32_t key[kLsPer];
+  const int nv = layer_keys(p, b, h, j0, li.nb, key);
+  layer_hist_add(sh, key, nv, [bin1](uint32_t k) { return (k >> 20) == bin1; },
+                 [](uint32_t k) { return (k >> 8) & 0xFFFu; });
+  layer_flush<kHistBins>(sh, p.h2 + (size_t)b * kHistBins);
+}
+
+// Digit 3 (key bits 7..0) of the members sharing the k-th key's 24-bit prefix.
+__global__ void __launch_bounds__(kSelThreads) layer_hist3_kernel(const LayerSelParams p) {
+  __shared__ uint32_t sh[256];
+  __shared__ uint32_t scratch[32];
+  grid_dep_wait();
+  grid_dep_launch();
+  const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const LayerInfo li = layer_info(p, b);
+  const int j0 = chunk * kSelChunk;
+  if (li.mode != kModeNormal || j0 >= li.nb) return;
+  const uint32_t bin1 = __ldcg(&p.state[b * 8 + kLsBin1]), rank1 = __ldcg(&p.state[b * 8 + kLsRank1]);
+  uint32_t bin2, rank2, cnt2;
+  find_bin(p.h2 + (size_t)b * kHistBins, rank1, scratch, bin2, rank2, cnt2);
+  const uint32_t pre24 = (bin1 << 12) | bin2;
+  if (chunk == 0 && h == 0 && threadIdx.x == 0) {
+    p.state[b * 8 + kLsPre24] = pre24;
+    p.state[b * 8 + kLsRank2] = rank2;
+  }
+  sh[threadIdx.x] = 0;   // 256 threads, 256 bins
+  __syncthreads();
+  uint32_t key[kLsPer];
+  const int nv = layer_keys(p, b, h, j0, li.nb, key);
+  layer_hist_add(sh, key, nv, [pre24](uint32_t k) { return (k >> 8) == pre24; }, [](uint32_t k) { return k & 0xFFu; });
+  layer_flush<256>(sh, p.h3 + (size_t)b * 256);
+}
+
+// The k-th key T and its rank among the equal keys; per chunk, the slots
+// above T and equal to T (written for every chunk, zero past the sequence).
+__global__ void __launch_bounds__(kSelThreads) layer_count_kernel(const LayerSelParams p) {
+  static_assert(kSelThreads == 256, "one digit-3 bin per thread");
+  __shared__ uint32_t scratch[32];
+  __shared__ uint32_t t_s, r_s;
+  grid_dep_wait();
+  grid_dep_launch();
+  const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const LayerInfo li = layer_info(p, b);
+  if (li.mode != kModeNormal) return;
+  const int j0 = chunk * kSelChunk;
+  uint32_t* cnt_out = p.counts + (((size_t)b * p.Hkv + h) * p.chunks + chunk) * 2;
+  if (j0 >= li.nb) {
+    if (threadIdx.x == 0) { cnt_out[0] = 0; cnt_out[1] = 0; }
+    return;
+  }
+  const uint32_t pre24 = __ldcg(&p.state[b * 8 + kLsPre24]), rank2 = __ldcg(&p.state[b * 8 + kLsRank2]);
+  const uint32_t c3 = __ldcg(&p.h3[(size_t)b * 256 + threadIdx.x]);
+  if (threadIdx.x == 0) { t_s = pre24 << 8; r_s = 1; }
+  uint32_t total;
+  const uint32_t before = block_exclusive_scan<kSelThreads>(c3, scratch, &total);
+  if (before < rank2 && rank2 <= before + c3) {
+    t_s = (pre24 << 8) | threadIdx.x;
+    r_s = rank2 - before;
+  }
+  __syncthreads();
+  const uint32_t T = t_s, rank3 = r_s;
+  if (chunk == 0 && h == 0 && threadIdx.x == 0) {
+    p.state[b * 8 + kLsKey] = T;
+    p.state[b * 8 + kLsRank3] = rank3;
+  }
+  uint32_t key[kLsPer];
+  const int nv = layer_keys(p, b, h, j0, li.nb, key);
+  uint32_t above = 0, ties = 0;
+#pragma unroll
+  for (int u = 0; u < kLsPer; ++u) {
+    above += (u < nv && key[u] > T);
+    ties += (u < nv && key[u] == T);
+  }
+  uint32_t packed_total;   // (above << 16) | ties; a chunk holds at most 16384 slots
+  block_exclusive_scan<kSelThreads>((above << 16) | ties, scratch, &packed_total);
+  if (threadIdx.x == 0) {
+    cnt_out[0] = packed_total >> 16;
+    cnt_out[1] = packed_total & 0xFFFFu;
+  }
+}
+
+// Kept positions of every head, ascending, and the per-head kept counts.
+__global__ void __launch_bounds__(kSelThreads) layer_write_kernel(const LayerSelParams p) {
+  __shared__ uint32_t scratch[32];
+  __shared__ uint32_t tie_off_s, head_off_s;
+  grid_dep_wait();
+  grid_dep_launch();
+  const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const LayerInfo li = layer_info(p, b);
+  const int j0 = chunk * kSelChunk;
+  int32_t* out_row = p.kept_idx + ((size_t)b * p.Hkv + h) * p.n_max;
+  int32_t* kept_len = p.kept_len + (size_t)b * p.Hkv + h;
+  if (li.mode == kModeSkip) {
+    if (chunk == 0 && threadIdx.x == 0) *kept_len = 0;
+    return;
+  }
+  if (li.mode == kModeKeepAll) {
+    if (chunk == 0 && threadIdx.x == 0) *kept_len = li.nb;
+    for (int j = j0 + threadIdx.x; j < min(j0 + kSelChunk, li.nb); j += kSelThreads) out_row[j] = j;
+    return;
+  }
+  const uint32_t T = __ldcg(&p.state[b * 8 + kLsKey]), rank3 = __ldcg(&p.state[b * 8 + kLsRank3]);
+  if (threadIdx.x == 0) {
+    // walk the chunks in head-major order: tie offset of this chunk, kept
+    // slots of this head before it, and (chunk 0) the head's kept count
+    const uint32_t* cnt = p.counts + (size_t)b * p.Hkv * p.chunks * 2;
+    uint32_t tie_pre = 0, head_kept = 0, all_kept = 0, my_tie = 0, my_off = 0;
+    for (int hh = 0; hh < p.Hkv; ++hh) {
+      head_kept = 0;
+      for (int c = 0; c < p.chunks; ++c) {
+        const uint32_t a = __ldcg(&cnt[((size_t)hh * p.chunks + c) * 2]);
+        const uint32_t t = __ldcg(&cnt[((size_t)hh * p.chunks + c) * 2 + 1]);
+        if (hh == h && c == chunk) { my_tie = tie_pre; my_off = head_kept; }
+        const int past = (int)(tie_pre + t) - (int)rank3;   // ties of this chunk ranked after rank3
+        const uint32_t kept_c = a + (uint32_t)min(max(past, 0), (int)t);
+        tie_pre += t;
+        head_kept += kept_c;
+      }
+      if (hh == h && chunk == 0) *kept_len = (int32_t)head_kept;
+      all_kept += head_kept;
+    }
+    if (h == 0 && chunk == 0 && (long long)all_kept != (long long)p.Hkv * li.nb - li.e)
+      atomicOr(p.status, DROPKV_FLAG_INTERNAL);
+    tie_off_s = my_tie;
+    head_off_s = my_off;
+  }
+  __syncthreads();
+  if (j0 >= li.nb) return;
+  uint32_t key[kLsPer];
+  const int nv = layer_keys(p, b, h, j0, li.nb, key);
+  const int jt = j0 + (int)threadIdx.x * kLsPer;
+  uint32_t above = 0, ties = 0;
+#pragma unroll
+  for (int u = 0; u < kLsPer; ++u) {
+    above += (u < nv && key[u] > T);
+    ties += (u < nv && key[u] == T);
+  }
+  uint32_t packed_total;
+  const uint32_t packed_before = block_exclusive_scan<kSelThreads>((above << 16) | ties, scratch, &packed_total);
+  const uint32_t ab = packed_before >> 16, tb = packed_before & 0xFFFFu;
+  const uint32_t tie_off = tie_off_s;
+  const int tb_kept = min(max((int)(tie_off + tb) - (int)rank3, 0), (int)tb);
+  int32_t* out = out_row + head_off_s + ab + (uint32_t)tb_kept;
+  uint32_t tr = tie_off + tb;   // tie rank before this thread's slots
+#pragma unroll
+  for (int u = 0; u < kLsPer; ++u) {
+    const bool eq = u < nv && key[u] == T;
+    tr += eq;
+    if (u < nv && (key[u] > T || (eq && tr > rank3))) *out++ = jt + u;
+  }
+}
+
 // ------------------------------------------------------------ compaction
 constexpr int kCompactThreads = 256;
 constexpr int kRowsPerWarp = 2;
@@ -858,29 +1121,38 @@ __global__ void __launch_bounds__(kCompactThreads) compact_kernel(const CompactP
   grid_dep_wait();          // kept_idx / kept_len come from the selection
   grid_dep_launch();
   const int unit = blockIdx.y, b = unit / p.Hkv, h = unit - b * p.Hkv;
-  int kl = p.kept_len[b];
+  int kl = p.per_head ? p.kept_len[unit] : p.kept_len[b];
   if (kl > p.out_rows) {
-    if (blockIdx.x == 0 && h == 0 && threadIdx.x == 0) atomicOr(p.status, DROPKV_FLAG_OVERFLOW);
+    if (blockIdx.x == 0 && (h == 0 || p.per_head) && threadIdx.x == 0) atomicOr(p.status, DROPKV_FLAG_OVERFLOW);
     kl = p.out_rows;
   }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cpr = p.row_bytes / 16;          // 16-byte chunks per row
   const int32_t* idx = p.kept_idx + (size_t)unit * p.n_max;
-  for (int rr = 0; rr < kRowsPerWarp; ++rr) {
-    const int i = blockIdx.x * kRowsPerBlock + warp * kRowsPerWarp + rr;
-    if (i >= kl) break;
-    const int src = __ldg(&idx[i]);
-    if (src < 0 || src >= p.n_max) {
-      if (lane == 0) atomicOr(p.status, DROPKV_FLAG_BAD_LENGTH);
-      continue;
-    }
-    const size_t so = ((size_t)unit * p.n_max + src) * p.row_bytes;
-    const size_t dof = ((size_t)unit * p.out_rows + i) * p.row_bytes;
-    for (int c = lane; c < 2 * cpr; c += 32) {
-      const bool is_v = c >= cpr;
-      const int cc = is_v ? c - cpr : c;
-      const uint4 val = __ldg(reinterpret_cast<const uint4*>((is_v ? p.v : p.k) + so) + cc);
-      *(reinterpret_cast<uint4*>((is_v ? p.v_out : p.k_out) + dof) + cc) = val;
+  // grid-stride over the head's kept rows: the grid is sized for the GPU,
+  // not for out_rows (which may be far above the kept count).  A row is at
+  // most 2 x 16 chunks of 16 bytes (K and V, d <= 128): lane c moves chunk c
+  // of both of the warp's rows, loads first.
+  static_assert(kRowsPerWarp == 2, "two rows per warp and iteration");
+  const bool is_v = lane >= cpr;
+  const int cc = is_v ? lane - cpr : lane;
+  const uint8_t* src_base = is_v ? p.v : p.k;
+  uint8_t* dst_base = is_v ? p.v_out : p.k_out;
+  for (int i0 = blockIdx.x * kRowsPerBlock + warp * kRowsPerWarp; i0 < kl; i0 += gridDim.x * kRowsPerBlock) {
+    const int i1 = i0 + 1;
+    int s0 = __ldg(&idx[i0]);
+    int s1 = i1 < kl ? __ldg(&idx[i1]) : 0;
+    // an index outside the cache is flagged and its row skipped (clamped so the load stays in bounds)
+    const bool bad0 = s0 < 0 || s0 >= p.n_max, bad1 = s1 < 0 || s1 >= p.n_max;
+    if ((bad0 || bad1) && lane == 0) atomicOr(p.status, DROPKV_FLAG_BAD_LENGTH);
+    s0 = min(max(s0, 0), p.n_max - 1);
+    s1 = min(max(s1, 0), p.n_max - 1);
+    if (lane < 2 * cpr) {
+      const uint4 a = __ldg(reinterpret_cast<const uint4*>(src_base + ((size_t)unit * p.n_max + s0) * p.row_bytes) + cc);
+      const uint4 c = __ldg(reinterpret_cast<const uint4*>(src_base + ((size_t)unit * p.n_max + s1) * p.row_bytes) + cc);
+      if (!bad0) *(reinterpret_cast<uint4*>(dst_base + ((size_t)unit * p.out_rows + i0) * p.row_bytes) + cc) = a;
+      if (!bad1 && i1 < kl)
+        *(reinterpret_cast<uint4*>(dst_base + ((size_t)unit * p.out_rows + i1) * p.row_bytes) + cc) = c;
     }
   }
 }
@@ -936,9 +1208,30 @@ cudaError_t launch_select(const SelParams& p, size_t zero_bytes, void* zero_base
   return launch_pdl(select_write_kernel, grid, dim3(kSelThreads), 0, st, p);
 }
 
+cudaError_t launch_select_layer(const LayerSelParams& p, size_t zero_bytes, void* zero_base, cudaStream_t st) {
+  const size_t n16 = zero_bytes / 16;
+  const int zb = (int)std::min<size_t>((n16 + 255) / 256, 1024);
+  cudaError_t e = launch_pdl(select_zero_kernel, dim3(zb > 0 ? zb : 1), dim3(256), 0, st,
+                             reinterpret_cast<uint4*>(zero_base), n16);
+  if (e != cudaSuccess) return e;
+  const dim3 grid(p.chunks, p.Hkv, p.B);
+  if ((e = launch_pdl(layer_hist1_kernel, grid, dim3(kSelThreads), 0, st, p)) != cudaSuccess) return e;
+  if ((e = launch_pdl(layer_hist2_kernel, grid, dim3(kSelThreads), 0, st, p)) != cudaSuccess) return e;
+  if ((e = launch_pdl(layer_hist3_kernel, grid, dim3(kSelThreads), 0, st, p)) != cudaSuccess) return e;
+  if ((e = launch_pdl(layer_count_kernel, grid, dim3(kSelThreads), 0, st, p)) != cudaSuccess) return e;
+  return launch_pdl(layer_write_kernel, grid, dim3(kSelThreads), 0, st, p);
+}
+
 cudaError_t launch_compact(const CompactParams& p, cudaStream_t st) {
   if (p.out_rows <= 0) return cudaSuccess;
-  dim3 grid((p.out_rows + kRowsPerBlock - 1) / kRowsPerBlock, p.B * p.Hkv);
+  // about four waves of 8 resident CTAs per SM over all heads, at most one
+  // CTA per kRowsPerBlock output rows
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return cudaErrorUnknown;
+  const int units = p.B * p.Hkv;
+  const int per_unit = std::max(1, 4 * 8 * sms / units);
+  dim3 grid(std::min((p.out_rows + kRowsPerBlock - 1) / kRowsPerBlock, per_unit), units);
   return launch_pdl(compact_kernel, grid, dim3(kCompactThreads), 0, st, p);
 }
 

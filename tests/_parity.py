@@ -77,3 +77,36 @@ def check_kept(kept_gpu: np.ndarray, len_gpu: np.ndarray, kept_ref: np.ndarray, 
                 b, h, diff[~band[diff]][:10])
             band_total += diff.size
     return band_total
+
+
+def check_kept_layer(kept_gpu, len_gpu, kept_ref, len_ref, final_ref, lengths, evict_total):
+    """Layer-wide selection: per sequence, the kept set (over all heads) must
+    match the oracle's except for slots whose oracle score lies within the
+    tolerance of the pool's evict_total-th smallest score; the total kept per
+    sequence must be exact.  kept_*: [B,H,n_max], len_*: [B,H]."""
+    B, H, _ = final_ref.shape
+    band_total = 0
+    for b in range(B):
+        nb, e = int(lengths[b]), int(evict_total[b])
+        assert int(len_gpu[b].sum()) == int(len_ref[b].sum()) == H * nb - e
+        got = np.zeros((H, nb), dtype=bool)
+        ref = np.zeros((H, nb), dtype=bool)
+        for h in range(H):
+            g = kept_gpu[b, h, :len_gpu[b, h]]
+            assert np.all(np.diff(g) > 0), "kept indices must be strictly ascending (b=%d h=%d)" % (b, h)
+            if g.size:
+                assert g.min() >= 0 and g.max() < nb
+            got[h, g] = True
+            ref[h, kept_ref[b, h, :len_ref[b, h]]] = True
+        if np.array_equal(got, ref):
+            continue
+        fin = final_ref[b, :, :nb]
+        assert e > 0, "nothing to evict but kept sets differ (b=%d)" % b
+        flat = fin.reshape(-1)
+        T = flat[np.lexsort((np.arange(flat.size), flat))[e - 1]]
+        tolT = RTOL * abs(T) + ATOL * float(np.max(flat[np.isfinite(flat)]))
+        band = np.abs(fin - T) <= tolT
+        diff = got != ref
+        assert np.all(band[diff]), "kept sets differ outside the tolerance band (b=%d)" % b
+        band_total += int(diff.sum())
+    return band_total
