@@ -89,8 +89,11 @@ def config_of(spec, lengths, score="dropkv", select="head"):
 
 
 def workload_bytes(spec, lengths, kept, score="dropkv", select="head"):
-    """Algorithmic bytes of the two-pass structure (byte model).
-    The SnapKV score reads only K in both passes."""
+    """Algorithmic bytes of one step: each attention pass reads K and V once
+    (the SnapKV score reads only K), pass 2 writes a raw score per head-token,
+    pooling reads and writes one score, the selection writes the kept indices
+    (plus its score re-reads where it has them), and compaction moves the kept
+    K and V rows and reads their indices."""
     U_tok = spec.Hkv * int(sum(lengths))                  # head-tokens
     kv = (4 if score == "dropkv" else 2) * spec.d         # K (+ V) bytes per head-token
     p1 = U_tok * kv
