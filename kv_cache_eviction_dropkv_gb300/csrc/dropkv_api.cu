@@ -121,6 +121,7 @@ WsPlan make_plan(const Geom& g) {
   w.ahl = take((size_t)g.U * 2 * kMaxR * kDPad * 2);
   w.part_o = take((size_t)g.U * g.splits1 * g.R * g.d * 4);
   w.part_ml = take((size_t)g.U * g.splits1 * g.R * 2 * 4);
+  w.tile_ctr = take((size_t)g.U * 4);
   w.raw = take((size_t)g.U * g.n_max * 4);
   w.sel_zero_begin = off;
   w.hist = take((size_t)g.U * kHistBins * 4);
@@ -204,6 +205,7 @@ dropkv_status score_impl(const dropkv_shape* shape, const void* q_window, const 
   p.ahl = reinterpret_cast<__nv_bfloat16*>(ws + w.ahl);
   p.part_o = reinterpret_cast<float*>(ws + w.part_o);
   p.part_ml = reinterpret_cast<float*>(ws + w.part_ml);
+  p.tile_ctr = reinterpret_cast<uint32_t*>(ws + w.tile_ctr);
   p.raw = raw_scores ? raw_scores : reinterpret_cast<float*>(ws + w.raw);
   p.status = status;
   p.kind = kind == DROPKV_SCORE_SNAPKV ? kKindSnapKV : kKindDropKV;

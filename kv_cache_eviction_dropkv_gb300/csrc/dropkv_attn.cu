@@ -190,6 +190,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_splits_kernel(const AttnP
   const int nb = p.lengths ? p.lengths[b] : p.n_max;   // a caller input: read before the wait
   grid_dep_wait();                                // the partials come from pass 1
   grid_dep_launch();
+  if (blockIdx.x == 0 && threadIdx.x == 0) p.tile_ctr[unit] = 0;   // pass 2 claims its tiles from 0
   if (nb < p.w || nb > p.n_max) return;          // flagged by pass 1
   const int S = p.splits, R = p.R, d = p.d, D4 = d >> 2;
   __nv_bfloat16* ahl = p.ahl + (size_t)unit * 2 * kMaxR * kDPad;
@@ -602,18 +603,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ============================================================== pass 2
-// SNAP: K only; the V ring's stages go to K (V keeps one unused stage).
+// SNAP: K only; the V ring's shared memory goes to K.  Its barriers and tile
+// indices stay (the workers learn each tile's index through the V slots), as
+// deep as the K ring but with no data behind them.
 template <int NR, bool SNAP = false>
 struct Pass2Cfg {
   static constexpr int HR = NR / 2;
   static constexpr int KS0 = 2;                     // K is released right after S = K Q^T
   static constexpr int VS0 = NR <= 32 ? 4 : 3;      // V is held until A.V^T and |v|^2 are done
-  static constexpr int KS = SNAP ? KS0 + VS0 - 1 : KS0;
-  static constexpr int VS = SNAP ? 1 : VS0;
+  static constexpr int KS = SNAP ? KS0 + VS0 : KS0;
+  static constexpr int VS = SNAP ? KS : VS0;        // V slots (tile indices; data only without SNAP)
+  static constexpr int kVStages = SNAP ? 0 : VS;    // V ring stages in shared memory
   static constexpr int kQBytes = NR * kDPad * 2;
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + KS * kTileBytes;
-  static constexpr int kOffQ = kOffV + VS * kTileBytes;
+  static constexpr int kOffQ = kOffV + kVStages * kTileBytes;
   static constexpr int kOffAhi = kOffQ + kQBytes;
   static constexpr int kOffAlo = kOffAhi + kQBytes;
   static constexpr int kOffSmall = kOffAlo + kQBytes;
@@ -623,6 +627,7 @@ struct Pass2Cfg {
 
 struct Pass2Small {
   uint64_t kfull[kMaxStages], kempty[kMaxStages], vfull[kMaxStages], vempty[kMaxStages];
+  int ktile[kMaxStages], vtile[kMaxStages];   // tile held by each ring slot (-1: no more tiles)
   uint64_t accfull[2], accempty[2], drain, aready;
   uint32_t tmem_base;
   int abort;
@@ -657,14 +662,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nb = p.lengths ? p.lengths[b] : p.n_max;
   if (nb < p.w || nb > p.n_max) return;      // flagged by pass 1
   const int R = p.R;
-  const int t0 = split * p.tpc;
-  const int t1 = min(t0 + p.tpc, ceil_div(nb, kTile));
-  const int T = t1 - t0;
-  if (T <= 0) return;
+  // The CTAs of a KV head claim its tiles one at a time from a counter (the
+  // merge kernel clears it), so they all finish within about a tile of each
+  // other whatever bandwidth each SM gets.  The producer claims a tile only
+  // once both of its ring slots are free, and passes its index (or -1: no
+  // more tiles) to the MMA warp through the K slot and to the workers
+  // through the V slot.
+  const int ntiles = ceil_div(nb, kTile);
+  (void)split;
 
   if (tid == 0) {
     for (int i = 0; i < C::KS; ++i) { mbar_init(&S.kfull[i], 1); mbar_init(&S.kempty[i], 1); }
-    for (int i = 0; i < C::VS; ++i) { mbar_init(&S.vfull[i], 1); mbar_init(&S.vempty[i], kWorkerWarps + 1); }
+    for (int i = 0; i < C::VS; ++i) { mbar_init(&S.vfull[i], 1); mbar_init(&S.vempty[i], kWorkerWarps + (SNAP ? 0 : 1)); }
     for (int i = 0; i < 2; ++i) { mbar_init(&S.accfull[i], 1); mbar_init(&S.accempty[i], kWorkerWarps); }
     mbar_init(&S.drain, 1);
     mbar_init(&S.aready, 1);
@@ -693,20 +702,57 @@ __global__ void __launch_bounds__(kThreads, 1)
   grid_dep_launch();
 
   if (warp == kProducerWarp) {
-    // TMA producer: lane 0 K, lane 1 V
-    grid_dep_wait();
-    if (lane == 0) stream_ring<C::KS>(sK, S.kfull, S.kempty, &tmk, t0, T, unit, &S.abort, p.status);
-    else if (lane == 1 && !SNAP) stream_ring<C::VS>(sV, S.vfull, S.vempty, &tmv, t0, T, unit, &S.abort, p.status);
+    // TMA producer (lane 0): claims a tile, then streams its K and V
+    grid_dep_wait();                              // the tile counter is cleared by the merge
+    if (lane == 0) {
+      int issued = 0;
+      bool ok = true;
+      for (int i = 0;; ++i) {
+        const int ks = i % C::KS, vs = i % C::VS;
+        if (i >= C::KS && !mbar_wait(&S.kempty[ks], ((i / C::KS) + 1) & 1, &S.abort)) { ok = false; break; }
+        if (i >= C::VS && !mbar_wait(&S.vempty[vs], ((i / C::VS) + 1) & 1, &S.abort)) { ok = false; break; }
+        const int tile = (int)atomicAdd(p.tile_ctr + unit, 1u);
+        if (tile >= ntiles) {
+          S.ktile[ks] = -1;
+          S.vtile[vs] = -1;
+          mbar_arrive(&S.kfull[ks]);
+          mbar_arrive(&S.vfull[vs]);
+          break;
+        }
+        S.ktile[ks] = tile;
+        S.vtile[vs] = tile;
+        mbar_arrive_expect_tx(&S.kfull[ks], kTileBytes);
+        tma_load_3d(sK + ks * kTileBytes, &tmk, &S.kfull[ks], 0, tile * kTile, unit);
+        tma_load_3d(sK + ks * kTileBytes + kHalfTile, &tmk, &S.kfull[ks], 64, tile * kTile, unit);
+        if (SNAP) {
+          mbar_arrive(&S.vfull[vs]);
+        } else {
+          mbar_arrive_expect_tx(&S.vfull[vs], kTileBytes);
+          tma_load_3d(sV + vs * kTileBytes, &tmv, &S.vfull[vs], 0, tile * kTile, unit);
+          tma_load_3d(sV + vs * kTileBytes + kHalfTile, &tmv, &S.vfull[vs], 64, tile * kTile, unit);
+        }
+        ++issued;
+      }
+      if (!ok) {
+        S.abort = 1;
+        atomicOr(p.status, DROPKV_FLAG_TIMEOUT);
+        // wait (bounded) for this CTA's copies still in flight
+        for (int i = max(0, issued - C::KS); i < issued; ++i) mbar_drain(&S.kfull[i % C::KS], (i / C::KS) & 1);
+        if (!SNAP)
+          for (int i = max(0, issued - C::VS); i < issued; ++i) mbar_drain(&S.vfull[i % C::VS], (i / C::VS) & 1);
+      }
+    }
     __syncwarp();
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
       const uint32_t idS = umma_idesc_bf16(128, NR, 0, 0);
       const uint32_t qaddr = smem_addr(sQ), ahi = smem_addr(sAhi), alo = smem_addr(sAlo);
       bool ok = true;
-      for (int i = 0; i < T; ++i) {
+      for (int i = 0;; ++i) {
         const int ks = i % C::KS, vs = i % C::VS, ab = i & 1;
         const uint32_t dS = tmem + ab * 2 * NR, dAV = dS + NR;
         if (!mbar_wait(&S.kfull[ks], (i / C::KS) & 1, &S.abort)) { ok = false; break; }
+        if (*reinterpret_cast<volatile int*>(&S.ktile[ks]) < 0) break;     // no more tiles
         if (i >= 2 && !mbar_wait(&S.accempty[ab], ((i >> 1) + 1) & 1, &S.abort)) { ok = false; break; }
         tc_fence_after();
         const uint32_t kb = smem_addr(sK + ks * kTileBytes);
@@ -775,13 +821,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       named_bar(kBarWork, kWorkers);
       if (tid == 0) mbar_arrive(&S.aready);
     }
-    for (int i = 0; i < T; ++i) {
-      const int tile0 = (t0 + i) * kTile, vs = i % C::VS, ab = i & 1;
+    for (int i = 0;; ++i) {
+      const int vs = i % C::VS, ab = i & 1;
+      // the V slot carries the tile index (and, in the SnapKV mode, nothing else)
+      bool ok = __all_sync(0xffffffffu, mbar_wait(&S.vfull[vs], (i / C::VS) & 1, &S.abort));
+      const int tile = ok ? *reinterpret_cast<volatile int*>(&S.vtile[vs]) : 0;
+      const bool stop = ok && tile < 0;             // no more tiles (the same slot for every worker)
+      const int tile0 = max(tile, 0) * kTile;
       const int j = tile0 + tok;
       const bool full = tile0 + kTile - 1 <= all_see;
-      bool ok = SNAP ? true : mbar_wait(&S.vfull[vs], (i / C::VS) & 1, &S.abort);
       float vvh = 0.f;
-      if (!SNAP && ok) {
+      if (!SNAP && ok && !stop) {
         // this half's 64 columns of the staged V row; chunks visited in a
         // per-thread rotated order so a warp's reads spread over all banks
         const uint8_t* vrow = sV + vs * kTileBytes + half * kHalfTile + tok * 128;
@@ -790,12 +840,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           vvh = sumsq_bf16x8(*reinterpret_cast<const uint4*>(vrow + ((c + tok) & 7) * 16), vvh);
       }
       __syncwarp();
-      if (!SNAP && lane == 0) mbar_arrive(&S.vempty[vs]);
-      if (ok) ok = mbar_wait(&S.accfull[ab], (i >> 1) & 1, &S.abort);
+      if (lane == 0 && !stop) mbar_arrive(&S.vempty[vs]);
+      if (ok && !stop) ok = mbar_wait(&S.accfull[ab], (i >> 1) & 1, &S.abort);
       ok = __all_sync(0xffffffffu, ok);
       float A = 0.f, W = 0.f;
       bool singular = false;
-      if (ok) {
+      if (ok && !stop) {
         tc_fence_after();
         float sv[HR], av[HR];
         tmem_ld_cols<HR>(tmem + lane_base + ab * 2 * NR + r0, sv);
@@ -834,9 +884,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&S.accempty[ab]);
+      if (lane == 0 && !stop) mbar_arrive(&S.accempty[ab]);
       if (half == 1) S.xch[ab][tok] = make_float4(A, W, vvh, singular ? 1.f : 0.f);
-      if (named_bar_or(kBarWork, kWorkers, !ok)) { failed = true; break; }
+      // one barrier per tile: it carries both "some wait failed" and "no more tiles"
+      if (named_bar_or(kBarWork, kWorkers, !ok || stop)) {
+        if (named_bar_or(kBarAux, kWorkers, !ok)) failed = true;
+        break;
+      }
       if (SNAP && half == 0 && j < nb) {
         float s = (A + S.xch[ab][tok].x) * inv_g;
         if (!isfinite(s)) flags |= DROPKV_FLAG_NONFINITE | DROPKV_FLAG_NONFINITE_SCORE;

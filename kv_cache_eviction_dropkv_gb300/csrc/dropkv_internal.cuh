@@ -38,6 +38,7 @@ struct WsPlan {
   size_t m2, aa;                 // max in log2 units, |a|^2
   size_t ahl;                    // bf16 [U][2][NR][128]: a split into hi + lo parts
   size_t part_o, part_ml;        // pass-1 partial states
+  size_t tile_ctr;               // u32 [U]: pass-2 tile claims (cleared by the merge kernel)
   size_t raw;                    // f32 [U][n_max] raw scores when the caller passes none
   // selection
   size_t hist;                   // u32 [U][kHistBins]
@@ -75,6 +76,7 @@ struct AttnParams {
   float *m, *l, *a, *m2, *aa;
   __nv_bfloat16* ahl;
   float *part_o, *part_ml;
+  uint32_t* tile_ctr;            // [U] next unclaimed pass-2 tile of each KV head
   float* raw;                    // raw score output [U][n_max]
   uint32_t* status;
   int kind;                      // kKindDropKV or kKindSnapKV

@@ -115,10 +115,12 @@ extern "C" dropkv_status dropkv_score_noalloc(const dropkv_shape* shape, const v
   p.ahl = reinterpret_cast<__nv_bfloat16*>(ws + w.ahl);
   p.part_o = reinterpret_cast<float*>(ws + w.part_o);
   p.part_ml = reinterpret_cast<float*>(ws + w.part_ml);
+  p.tile_ctr = reinterpret_cast<uint32_t*>(ws + w.tile_ctr);
   p.raw = raw_scores ? raw_scores : reinterpret_cast<float*>(ws + w.raw);
   p.status = status;
   // the array keeps the previous call's contents; scoring writes every scratch
-  // value before reading it, so nothing has to be cleared first
+  // value before reading it (the merge kernel resets pass 2's tile counters),
+  // so nothing has to be cleared first
   p.splits = g.splits1;
   p.tpc = g.tpc1;
   if (launch_window_attention(p, g.NR, tk, tv, g.splits1, stream) != cudaSuccess) return DROPKV_ERR_CUDA;
