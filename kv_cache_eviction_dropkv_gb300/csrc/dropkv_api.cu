@@ -101,6 +101,7 @@ bool make_geom(const dropkv_shape* s, int num_sms, Geom* g) {
   g->tpc2 = g->tpc1;
   g->splits2 = g->splits1;
   g->chunks = ceil_div_i(s->n_max, kSelChunk);
+  g->layer_chunks = ceil_div_i(s->n_max, kLayerChunk);
   return g->NR > 0;
 }
 
@@ -139,7 +140,7 @@ WsPlan make_plan(const Geom& g) {
   w.layer_h3 = take((size_t)g.B * 256 * 4);
   w.layer_zero_end = off;
   w.layer_state = take((size_t)g.B * 8 * 4);
-  w.layer_counts = take((size_t)g.U * g.chunks * 2 * 4);
+  w.layer_counts = take((size_t)g.U * g.layer_chunks * 2 * 4);
   w.total = off;
   return w;
 }
@@ -399,7 +400,7 @@ dropkv_status dropkv_select_layer(const dropkv_shape* shape, const float* scores
   p.evict_total = evict_total;
   p.kept_idx = kept_idx;
   p.kept_len = kept_len;
-  p.B = g.B; p.Hkv = g.Hkv; p.n_max = g.n_max; p.protect = protect; p.chunks = g.chunks;
+  p.B = g.B; p.Hkv = g.Hkv; p.n_max = g.n_max; p.protect = protect; p.chunks = g.layer_chunks;
   p.h1 = reinterpret_cast<uint32_t*>(ws + w.layer_h1);
   p.h2 = reinterpret_cast<uint32_t*>(ws + w.layer_h2);
   p.h3 = reinterpret_cast<uint32_t*>(ws + w.layer_h3);

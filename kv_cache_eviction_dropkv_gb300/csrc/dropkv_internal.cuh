@@ -17,6 +17,7 @@ constexpr int kDPad = 128;          // head dimension as staged in shared memory
 constexpr int kMaxR = 64;           // rows (g * w) per KV head supported
 constexpr int kMaxSplits = 160;    // split-K partial states per KV head (merge holds 5 per lane)
 constexpr int kSelChunk = 16384;    // tokens per block in the selection kernels
+constexpr int kLayerChunk = 4096;   // tokens per block in the layer-wide selection kernels
 constexpr int kHistBins = 4096;     // first-level radix histogram (top 12 key bits)
 constexpr int kCandCap = 8192;      // candidates resolved in shared memory
 constexpr int kMaxPool = 63;
@@ -30,6 +31,7 @@ struct Geom {
   int splits1, tpc1;     // pass-1 CTAs per unit and tiles per CTA
   int splits2, tpc2;     // pass-2 CTAs per unit and tiles per CTA
   int chunks;            // ceil(n_max / kSelChunk)
+  int layer_chunks;      // ceil(n_max / kLayerChunk)
 };
 
 // Byte offsets of the workspace regions (all 256-byte aligned).
@@ -127,6 +129,7 @@ struct LayerSelParams {
   uint32_t *h1, *h2, *h3;        // [B][4096], [B][4096], [B][256] (cleared before the first kernel)
   uint32_t* state;               // [B][8]
   uint32_t* counts;              // [B][Hkv][chunks][2]: slots above T, slots equal to T
+                                 // (chunks of kLayerChunk slots)
   uint32_t* status;
 };
 

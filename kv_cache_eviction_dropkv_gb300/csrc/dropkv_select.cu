@@ -854,14 +854,14 @@ __global__ void __launch_bounds__(kClThreads, 1) select_cluster_kernel(const Sel
 // and Appendix A.3), read as one pool per sequence: the scores of all its KV
 // heads compete, and the evict_total[b] smallest (score, head, position)
 // triples are evicted, so each head keeps its own number of slots.  Grid
-// (chunks, Hkv, B): one 16384-slot chunk of one head per CTA, 64 consecutive
-// slots per thread.  The k-th triple is found digit by digit (key bits
+// (chunks, Hkv, B): one 4096-slot chunk of one head per CTA (many CTAs: each
+// kernel is short and latency-bound), 16 consecutive slots per thread.  The k-th triple is found digit by digit (key bits
 // 31..20, 19..8, 7..0, then the tie rank among equal keys in head-major
 // order) over five kernels whose boundaries order the global histograms, so
 // nothing waits on another CTA; the last kernel turns per-chunk counts into
 // per-head output offsets.
 enum { kLsBin1 = 0, kLsRank1 = 1, kLsPre24 = 2, kLsRank2 = 3, kLsKey = 4, kLsRank3 = 5 };
-constexpr int kLsPer = kSelChunk / kSelThreads;   // 64 consecutive slots per thread
+constexpr int kLsPer = kLayerChunk / kSelThreads;   // 16 consecutive slots per thread
 
 struct LayerInfo {
   int nb, e;
@@ -878,7 +878,7 @@ __device__ __forceinline__ LayerInfo layer_info(const LayerSelParams& p, int b) 
   return u;
 }
 
-// Keys of this thread's slots j0 + 64 t + [0, 64) (slots >= nb are masked by nv).
+// Keys of this thread's slots j0 + 16 t + [0, 16) (slots >= nb are masked by nv).
 __device__ __forceinline__ int layer_keys(const LayerSelParams& p, int b, int h, int j0, int nb,
                                           uint32_t (&key)[kLsPer]) {
   const float* row = p.scores + ((size_t)b * p.Hkv + h) * p.n_max;
@@ -932,7 +932,7 @@ __global__ void __launch_bounds__(kSelThreads) layer_hist1_kernel(const LayerSel
     if (li.mode == kModeSkip) atomicOr(p.status, DROPKV_FLAG_BAD_LENGTH);
     else if (li.e < 0 || (long long)li.e > (long long)p.Hkv * (li.nb - p.protect)) atomicOr(p.status, DROPKV_FLAG_BAD_K);
   }
-  const int j0 = chunk * kSelChunk;
+  const int j0 = chunk * kLayerChunk;
   if (li.mode != kModeNormal || j0 >= li.nb) return;
   for (int i = threadIdx.x; i < kHistBins; i += kSelThreads) sh[i] = 0;
   __syncthreads();
@@ -950,7 +950,7 @@ __global__ void __launch_bounds__(kSelThreads) layer_hist2_kernel(const LayerSel
   grid_dep_launch();
   const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const LayerInfo li = layer_info(p, b);
-  const int j0 = chunk * kSelChunk;
+  const int j0 = chunk * kLayerChunk;
   if (li.mode != kModeNormal || j0 >= li.nb) return;
   uint32_t bin1, rank1, cnt1;
   find_bin(p.h1 + (size_t)b * kHistBins, (uint32_t)li.e, scratch, bin1, rank1, cnt1);
@@ -975,7 +975,7 @@ __global__ void __launch_bounds__(kSelThreads) layer_hist3_kernel(const LayerSel
   grid_dep_launch();
   const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const LayerInfo li = layer_info(p, b);
-  const int j0 = chunk * kSelChunk;
+  const int j0 = chunk * kLayerChunk;
   if (li.mode != kModeNormal || j0 >= li.nb) return;
   const uint32_t bin1 = __ldcg(&p.state[b * 8 + kLsBin1]), rank1 = __ldcg(&p.state[b * 8 + kLsRank1]);
   uint32_t bin2, rank2, cnt2;
@@ -1004,7 +1004,7 @@ __global__ void __launch_bounds__(kSelThreads) layer_count_kernel(const LayerSel
   const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const LayerInfo li = layer_info(p, b);
   if (li.mode != kModeNormal) return;
-  const int j0 = chunk * kSelChunk;
+  const int j0 = chunk * kLayerChunk;
   uint32_t* cnt_out = p.counts + (((size_t)b * p.Hkv + h) * p.chunks + chunk) * 2;
   if (j0 >= li.nb) {
     if (threadIdx.x == 0) { cnt_out[0] = 0; cnt_out[1] = 0; }
@@ -1033,7 +1033,7 @@ __global__ void __launch_bounds__(kSelThreads) layer_count_kernel(const LayerSel
     above += (u < nv && key[u] > T);
     ties += (u < nv && key[u] == T);
   }
-  uint32_t packed_total;   // (above << 16) | ties; a chunk holds at most 16384 slots
+  uint32_t packed_total;   // (above << 16) | ties; a chunk holds at most 4096 slots
   block_exclusive_scan<kSelThreads>((above << 16) | ties, scratch, &packed_total);
   if (threadIdx.x == 0) {
     cnt_out[0] = packed_total >> 16;
@@ -1044,12 +1044,12 @@ __global__ void __launch_bounds__(kSelThreads) layer_count_kernel(const LayerSel
 // Kept positions of every head, ascending, and the per-head kept counts.
 __global__ void __launch_bounds__(kSelThreads) layer_write_kernel(const LayerSelParams p) {
   __shared__ uint32_t scratch[32];
-  __shared__ uint32_t tie_off_s, head_off_s;
+  __shared__ uint32_t tie_off_s, head_off_s, kfirst_s, klast_s;
   grid_dep_wait();
   grid_dep_launch();
   const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const LayerInfo li = layer_info(p, b);
-  const int j0 = chunk * kSelChunk;
+  const int j0 = chunk * kLayerChunk;
   int32_t* out_row = p.kept_idx + ((size_t)b * p.Hkv + h) * p.n_max;
   int32_t* kept_len = p.kept_len + (size_t)b * p.Hkv + h;
   if (li.mode == kModeSkip) {
@@ -1058,33 +1058,40 @@ __global__ void __launch_bounds__(kSelThreads) layer_write_kernel(const LayerSel
   }
   if (li.mode == kModeKeepAll) {
     if (chunk == 0 && threadIdx.x == 0) *kept_len = li.nb;
-    for (int j = j0 + threadIdx.x; j < min(j0 + kSelChunk, li.nb); j += kSelThreads) out_row[j] = j;
+    for (int j = j0 + threadIdx.x; j < min(j0 + kLayerChunk, li.nb); j += kSelThreads) out_row[j] = j;
     return;
   }
   const uint32_t T = __ldcg(&p.state[b * 8 + kLsKey]), rank3 = __ldcg(&p.state[b * 8 + kLsRank3]);
-  if (threadIdx.x == 0) {
-    // walk the chunks in head-major order: tie offset of this chunk, kept
-    // slots of this head before it, and (chunk 0) the head's kept count
+  {
+    // per-chunk (above, tie) counts in head-major order, scanned 256 at a time:
+    // the tie offset of this chunk, the kept slots of this head before it, and
+    // (chunk 0) the head's kept count
     const uint32_t* cnt = p.counts + (size_t)b * p.Hkv * p.chunks * 2;
-    uint32_t tie_pre = 0, head_kept = 0, all_kept = 0, my_tie = 0, my_off = 0;
-    for (int hh = 0; hh < p.Hkv; ++hh) {
-      head_kept = 0;
-      for (int c = 0; c < p.chunks; ++c) {
-        const uint32_t a = __ldcg(&cnt[((size_t)hh * p.chunks + c) * 2]);
-        const uint32_t t = __ldcg(&cnt[((size_t)hh * p.chunks + c) * 2 + 1]);
-        if (hh == h && c == chunk) { my_tie = tie_pre; my_off = head_kept; }
-        const int past = (int)(tie_pre + t) - (int)rank3;   // ties of this chunk ranked after rank3
-        const uint32_t kept_c = a + (uint32_t)min(max(past, 0), (int)t);
-        tie_pre += t;
-        head_kept += kept_c;
-      }
-      if (hh == h && chunk == 0) *kept_len = (int32_t)head_kept;
-      all_kept += head_kept;
+    const int n = p.Hkv * p.chunks, mine = h * p.chunks + chunk;
+    const int head_first = h * p.chunks, head_last = head_first + p.chunks - 1;
+    uint32_t carry_t = 0, carry_k = 0;
+    for (int base = 0; base < n; base += kSelThreads) {
+      const int e = base + (int)threadIdx.x;
+      const uint32_t a = e < n ? __ldcg(&cnt[(size_t)e * 2]) : 0u;
+      const uint32_t t = e < n ? __ldcg(&cnt[(size_t)e * 2 + 1]) : 0u;
+      uint32_t tsum, ksum;
+      const uint32_t tie_pre = carry_t + block_exclusive_scan<kSelThreads>(t, scratch, &tsum);
+      const int past = (int)(tie_pre + t) - (int)rank3;   // ties of this chunk ranked after rank3
+      const uint32_t kept_e = a + (uint32_t)min(max(past, 0), (int)t);
+      const uint32_t kpre = carry_k + block_exclusive_scan<kSelThreads>(kept_e, scratch, &ksum);
+      if (e == mine) { tie_off_s = tie_pre; head_off_s = kpre; }
+      if (e == head_first) kfirst_s = kpre;
+      if (e == head_last) klast_s = kpre + kept_e;
+      carry_t += tsum;
+      carry_k += ksum;
     }
-    if (h == 0 && chunk == 0 && (long long)all_kept != (long long)p.Hkv * li.nb - li.e)
-      atomicOr(p.status, DROPKV_FLAG_INTERNAL);
-    tie_off_s = my_tie;
-    head_off_s = my_off;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      head_off_s -= kfirst_s;
+      if (chunk == 0) *kept_len = (int32_t)(klast_s - kfirst_s);
+      if (h == 0 && chunk == 0 && (long long)carry_k != (long long)p.Hkv * li.nb - li.e)
+        atomicOr(p.status, DROPKV_FLAG_INTERNAL);
+    }
   }
   __syncthreads();
   if (j0 >= li.nb) return;
