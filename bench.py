@@ -71,6 +71,30 @@ def dist_env():
     return rank, world, local
 
 
+def rank_seed(spec, rank):
+    """Each rank scores its own layer: the workload's seed offset by the rank
+    (weak scaling, no data exchanged between ranks)."""
+    return spec.seed + rank
+
+
+def reduce_max(x, world):
+    """Maximum of a per-rank value over all ranks (the slowest rank sets the
+    step time); the identity for one rank."""
+    if world == 1:
+        return float(x)
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank, world, step_ms):
+    """Whole-job units per second: every rank processed units_per_rank in the
+    (max-reduced) step time."""
+    return units_per_rank * world / (step_ms / 1e3)
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -260,7 +284,7 @@ def main():
     _build.build_library()
 
     # each rank scores its own layer (weak scaling, no data-path collective)
-    wl = synth.make_workload(args.workload, seed=spec.seed + rank)
+    wl = synth.make_workload(args.workload, seed=rank_seed(spec, rank))
     lengths_np = wl.lengths.numpy()
     kept_np = wl.kept_len()
     units = int(sum(lengths_np))
@@ -355,12 +379,8 @@ def main():
 
     phases = {"window_attention": ms(1, 2), "split_merge": ms(2, 3), "score": ms(3, 4), "pool_protect": ms(4, 5),
               "select": ms(5, 6), "compact": ms(6, 7)}
-    step_ms = sum(t_step) / K
-    if world > 1:
-        t = torch.tensor([step_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        step_ms = float(t.item())
-    value = units * world / (step_ms / 1e3)
+    step_ms = reduce_max(sum(t_step) / K, world)
+    value = job_throughput(units, world, step_ms)
 
     nbytes = workload_bytes(spec, lengths_np, kept_np, args.score, args.select)
     peak, peak_kind = measured_peaks()
@@ -459,15 +479,11 @@ def e2e_leg(op, wl, dev, stream, args, world):
         one(i)
     e1.record(s_down)
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / K
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = reduce_max(e0.elapsed_time(e1) / K, world)
     for o in ops:
         o.check(stream)
     units = int(wl.lengths.sum())
-    return {"value": units * world / (ms / 1e3), "unit": UNIT, "ms_per_step": ms, "steps": K,
+    return {"value": job_throughput(units, world, ms), "unit": UNIT, "ms_per_step": ms, "steps": K,
             "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
             "pipelined": "two buffer sets: upload of step s+1 and download of step s-1 overlap the scoring of step s"}
 
