@@ -200,3 +200,32 @@ def test_one_call_equals_three_calls(name, n_max, pool):
         outs.append([t.clone() for t in (op.scores, op.raw_scores, op.kept_idx, op.kept_len, op.k_out, op.v_out)])
     for a, b in zip(*outs):
         assert torch.equal(a.view(torch.int8), b.view(torch.int8))
+
+
+def _sweep_cases(count, seed):
+    """Seeded random shapes over the supported range: g, w with R = g w <= 64,
+    d a multiple of 8 up to 128, ragged lengths, any odd pooling kernel."""
+    rng = np.random.default_rng(seed)
+    cases = []
+    while len(cases) < count:
+        Hkv = int(rng.integers(1, 4))
+        g = int(rng.integers(1, 9))
+        w = int(rng.integers(1, 9))
+        if g * w > 64:
+            continue
+        d = int(rng.choice([8, 16, 24, 64, 96, 120, 128]))
+        B = int(rng.integers(1, 4))
+        n = int(rng.integers(w + 1, 3000))
+        lens = rng.integers(max(w, 1), n + 1, size=B)
+        protect = int(rng.integers(0, w + 1))
+        pool = int(rng.choice([1, 3, 5, 7, 9, 63]))
+        evict = [int(rng.integers(0, max(1, int(L) - protect) + 1)) for L in lens]
+        cases.append((B, g * Hkv, Hkv, d, n, w, pool, protect, lens.tolist(), evict))
+    return cases
+
+
+@pytest.mark.parametrize("case", _sweep_cases(12, 2026))
+def test_random_shape_sweep(case):
+    B, Hq, Hkv, d, n, w, pool, protect, lens, evict = case
+    q, k, v, lengths = _custom(B, Hq, Hkv, d, n, w, seed=sum(lens) + d, lengths=lens)
+    _run_custom(q, k, v, lengths, evict, pool, protect)
