@@ -59,8 +59,9 @@ typedef enum {
 #define DROPKV_FLAG_SINGULAR   0x01u
 #define DROPKV_FLAG_NONFINITE  0x02u
 #define DROPKV_FLAG_BAD_LENGTH 0x04u   /* lengths[b] outside [w, n_max] (or < protect) */
-#define DROPKV_FLAG_BAD_K      0x08u   /* evict_k[b] outside [0, n_b - protect] */
-#define DROPKV_FLAG_OVERFLOW   0x10u   /* kept_len[b] > out_rows in dropkv_compact */
+#define DROPKV_FLAG_BAD_K      0x08u   /* evict_k[b] outside [0, n_b - protect] (evict_total[b]
+                                          outside [0, Hkv (n_b - protect)] for the layer-wide call) */
+#define DROPKV_FLAG_OVERFLOW   0x10u   /* a kept count > out_rows in a compaction */
 #define DROPKV_FLAG_TIMEOUT    0x20u
 #define DROPKV_FLAG_INTERNAL   0x40u   /* a selection consistency check failed (kept count != n_b - k_b) */
 /* Detail bits that accompany DROPKV_FLAG_NONFINITE: where the value appeared. */
@@ -84,9 +85,10 @@ typedef struct {
   int32_t w;       /* observation window: tail queries per query head */
 } dropkv_shape;
 
-/* Bytes of device workspace the three calls need for `shape` on the current
- * device (0 if the shape is invalid or unsupported, or no device is present).
- * The same workspace may serve dropkv_score and dropkv_select.  After
+/* Bytes of device workspace the calls that take one need for `shape` on the
+ * current device (0 if the shape is invalid or unsupported, or no device is
+ * present).  One workspace serves every call on that shape (not two calls at
+ * once: calls that overlap on the GPU must use separate workspaces).  After
  * dropkv_score completes, the workspace starts with the window statistics of
  * step S1 (U = B * Hkv, R = g * w, row r = h_local * w + t of KV head (b, h),
  * logits x_j = q.k_j / sqrt(d) over the keys the row sees):
