@@ -73,9 +73,8 @@ __device__ __forceinline__ float warp_sum(float v) {
 // to drain work in flight before the CTA exits).
 __device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
   const uint64_t t0 = global_timer_ns();
-  while (!mbar_try_wait(bar, parity)) {
+  for (uint32_t it = 0; it < (1u << 26) && !mbar_try_wait(bar, parity); ++it)
     if (global_timer_ns() - t0 > kDrainNs) break;
-  }
 }
 
 // Stage `rows` x 128 bf16 of a row-major [rows_valid][ld] matrix into the

@@ -54,16 +54,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 
 // Wait until the phase with the given parity has completed.  Gives up after
 // kWaitLimitNs, or as soon as *abort is set by another role; returns false then.
+// (An iteration cap bounds the loop even if the global timer stood still.)
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
-  for (uint32_t it = 1;; ++it) {
+  for (uint32_t it = 1; it < (1u << 30); ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0) {
       if (*abort) return false;
       if (global_timer_ns() - t0 > kWaitLimitNs) return false;
     }
   }
+  return false;
 }
 
 // ---------------------------------------------------------------- programmatic dependent launch
