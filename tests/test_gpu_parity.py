@@ -9,7 +9,7 @@ import pytest
 import torch
 
 import oracle
-from kv_cache_eviction_dropkv_gb300 import DropKV, synth
+from kv_cache_eviction_dropkv_gb300 import DropKV, _binding as B, synth
 from tests._parity import check_kept, check_scores
 
 pytestmark = pytest.mark.gpu
@@ -229,3 +229,32 @@ def test_random_shape_sweep(case):
     B, Hq, Hkv, d, n, w, pool, protect, lens, evict = case
     q, k, v, lengths = _custom(B, Hq, Hkv, d, n, w, seed=sum(lens) + d, lengths=lens)
     _run_custom(q, k, v, lengths, evict, pool, protect)
+
+
+def test_short_sequences():
+    """Sequences of w + 1 and w + 2 tokens (the first window row sees two
+    keys, everything or all but one slot protected) next to a normal one."""
+    q, k, v, lens = _custom(3, 4, 2, 64, 300, 6, seed=17, lengths=[7, 300, 8])
+    _run_custom(q, k, v, lens, [1, 200, 0], 3, 6)
+
+
+def test_sequence_of_w_tokens_is_singular():
+    """With n_b = w the first window row sees a single key, so p = 1 and exact
+    removal is singular: the oracle rejects the input and the GPU reports
+    SINGULAR (the method's degenerate case, not patched)."""
+    q, k, v, lens = _custom(2, 4, 2, 64, 300, 6, seed=19, lengths=[6, 300])
+    with pytest.raises(oracle.SingularInput):
+        oracle.score(synth.bf16_round(q), synth.bf16_round(k), synth.bf16_round(v), lens, 3, 6)
+    op = DropKV(2, 4, 2, 64, 300, 6, 3, 6, device=DEV)
+    op.run(synth.bf16_round(q).to(DEV), synth.bf16_round(k).to(DEV), synth.bf16_round(v).to(DEV),
+           torch.from_numpy(lens).to(DEV), torch.tensor([0, 100], dtype=torch.int32, device=DEV))
+    code, flags = B.dropkv_read_status(op.status)
+    assert code == 3 and flags & B.FLAG_SINGULAR
+
+
+def test_one_million_tokens():
+    """n = 2^20 in one KV head (64 selection chunks: the multi-kernel radix
+    path; 8192 pass-1 tiles over every SM)."""
+    n = 1 << 20
+    q, k, v, lens = _custom(1, 1, 1, 128, n, 8, seed=23)
+    _run_custom(q, k, v, lens, [n * 9 // 10], 5, 8)
