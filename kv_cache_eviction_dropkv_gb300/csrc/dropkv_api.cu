@@ -93,10 +93,10 @@ bool make_geom(const dropkv_shape* s, int num_sms, Geom* g) {
   g->NR = nr_for(g->R);
   g->U = (int)U;
   g->tiles_max = ceil_div_i(s->n_max, kTile);
-  // One CTA per SM: spread the U * tiles_max tiles over about num_sms CTAs.
-  const long long total = (long long)g->U * g->tiles_max;
-  g->tpc1 = (int)std::max<long long>(1, (total + num_sms - 1) / num_sms);
-  g->tpc1 = std::max(g->tpc1, ceil_div_i(g->tiles_max, kMaxSplits));
+  // One CTA per SM, every CTA resident in a single wave: floor(SMs / U) splits
+  // per KV head (a CTA more per head would push some into a second wave).
+  const int per_unit = std::max(1, num_sms / g->U);
+  g->tpc1 = std::max(ceil_div_i(g->tiles_max, per_unit), ceil_div_i(g->tiles_max, kMaxSplits));
   g->splits1 = ceil_div_i(g->tiles_max, g->tpc1);
   g->tpc2 = g->tpc1;
   g->splits2 = g->splits1;
