@@ -163,7 +163,8 @@ struct Pass1Small {
   uint32_t tmem_base;
   int abort;
   int pos[kMaxR];          // last key visible to row r (tail-aligned causality)
-  float mref[kMaxR];       // exponent reference of row r at the end (log2 units)
+  float mref[kMaxR];       // exponent reference of row r (log2 units; live for NR = 64, else at the end)
+  float mnew[kMaxR];       // staging of a new reference (NR = 64)
   float red[4][kMaxR];     // per-lane-quarter reduction scratch
 };
 
@@ -429,9 +430,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int r = 0; r < HR; ++r) rowmask |= (uint32_t)(r0 + r < R) << r;
     const float scale = p.scale_log2;
     const int all_see = nb - p.w;            // keys j <= all_see are visible to every row
-    float lsum[HR], mr[HR];
+    // The exponent reference of a row is the same in every thread.  For
+    // NR <= 32 each thread keeps it in registers; for NR = 64 it stays in
+    // shared memory (S.mref), which keeps the 32-row arrays of a thread within
+    // the register budget of ten warps.
+    constexpr bool kRefSmem = NR > 32;
+    float lsum[HR], mr[kRefSmem ? 1 : HR];
 #pragma unroll
-    for (int r = 0; r < HR; ++r) { lsum[r] = 0.f; mr[r] = -INFINITY; }
+    for (int r = 0; r < HR; ++r) lsum[r] = 0.f;
+#pragma unroll
+    for (int r = 0; r < (kRefSmem ? 1 : HR); ++r) mr[r] = -INFINITY;
+    auto ref = [&](int r) -> float {
+      if constexpr (kRefSmem) return S.mref[r0 + r];
+      else return mr[r];
+    };
     for (int i = 0; i < T; ++i) {
       const int tile0 = (t0 + i) * kTile, sb = i & 1, vs = i % C::VS, pb = i % C::PB;
       const int j = tile0 + tok;
@@ -457,13 +469,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         vis &= v;
       }
-      float rel[HR];
       bool need = false;
 #pragma unroll
-      for (int r = 0; r < HR; ++r) {
-        rel[r] = fmaf(sraw[r], scale, -mr[r]);
-        need |= ((vis >> r) & 1u) && rel[r] > kRescaleLog2;
-      }
+      for (int r = 0; r < HR; ++r) need |= ((vis >> r) & 1u) && fmaf(sraw[r], scale, -ref(r)) > kRescaleLog2;
       // this tile's P buffer must be free (PV of tile i - PB done); the tail tile's V must have landed
       if (!STATS && ok && i >= C::PB) ok = mbar_wait(&S.pempty[pb], ((i / C::PB) + 1) & 1, &S.abort);
       if (!STATS && ok && tail) ok = mbar_wait(&S.vfull[vs], (i / C::VS) & 1, &S.abort);
@@ -484,11 +492,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int r = 0; r < HR; ++r) {
           const int rr = r0 + r;
-          const float nm = fmaxf(fmaxf(fmaxf(S.red[0][rr], S.red[1][rr]), fmaxf(S.red[2][rr], S.red[3][rr])), mr[r]);
-          factor[r] = (mr[r] == -INFINITY) ? 0.f : ex2_approx(mr[r] - nm);
+          const float old = ref(r);
+          const float nm = fmaxf(fmaxf(fmaxf(S.red[0][rr], S.red[1][rr]), fmaxf(S.red[2][rr], S.red[3][rr])), old);
+          factor[r] = (old == -INFINITY) ? 0.f : ex2_approx(old - nm);
           lsum[r] *= factor[r];
-          mr[r] = nm;
-          rel[r] = fmaf(sraw[r], scale, -nm);
+          if constexpr (kRefSmem) {
+            if (wq == 0 && lane == 0) S.mnew[rr] = nm;
+          } else {
+            mr[r] = nm;
+          }
+        }
+        if constexpr (kRefSmem) {
+          // every worker has read the old references: publish the new ones
+          named_bar(kBarAux, kWorkers);
+          if (wq == 0 && lane == 0)
+            for (int r = 0; r < HR; ++r) S.mref[r0 + r] = S.mnew[r0 + r];
+          named_bar(kBarAux, kWorkers);
         }
         if (!STATS && i > 0) {
           // rescale the accumulated O (lane = head dimension) once PV of tile i-1 is
@@ -512,7 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the normaliser only
 #pragma unroll
         for (int r = 0; r < HR; ++r)
-          if ((vis >> r) & 1u) lsum[r] += ex2_approx(rel[r]);
+          if ((vis >> r) & 1u) lsum[r] += ex2_approx(fmaf(sraw[r], scale, -ref(r)));
         continue;
       }
       // exponentials relative to the row reference, split into bf16 hi + lo
@@ -524,8 +543,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const int r = c8 * 8 + 2 * q;
-          const float e0 = ((vis >> r) & 1u) ? ex2_approx(rel[r]) : 0.f;
-          const float e1 = ((vis >> (r + 1)) & 1u) ? ex2_approx(rel[r + 1]) : 0.f;
+          const float e0 = ((vis >> r) & 1u) ? ex2_approx(fmaf(sraw[r], scale, -ref(r))) : 0.f;
+          const float e1 = ((vis >> (r + 1)) & 1u) ? ex2_approx(fmaf(sraw[r + 1], scale, -ref(r + 1))) : 0.f;
           lsum[r] += e0;
           lsum[r + 1] += e1;
           split_hi_lo(e0, e1, hp[q], lp[q]);
@@ -574,9 +593,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float v = warp_sum(lsum[r]);
       if (lane == 0) S.red[wq][r0 + r] = v;
     }
-    if (wq == 0 && lane == 0) {
+    if constexpr (!kRefSmem) {
+      if (wq == 0 && lane == 0) {
 #pragma unroll
-      for (int r = 0; r < HR; ++r) S.mref[r0 + r] = mr[r];
+        for (int r = 0; r < HR; ++r) S.mref[r0 + r] = mr[r];
+      }
     }
     named_bar(kBarAux, kWorkers);
     if (tid < R) {
