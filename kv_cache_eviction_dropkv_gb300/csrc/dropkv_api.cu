@@ -93,13 +93,20 @@ bool make_geom(const dropkv_shape* s, int num_sms, Geom* g) {
   g->NR = nr_for(g->R);
   g->U = (int)U;
   g->tiles_max = ceil_div_i(s->n_max, kTile);
-  // One CTA per SM, every CTA resident in a single wave: floor(SMs / U) splits
-  // per KV head (a CTA more per head would push some into a second wave).
-  const int per_unit = std::max(1, num_sms / g->U);
-  g->tpc1 = std::max(ceil_div_i(g->tiles_max, per_unit), ceil_div_i(g->tiles_max, kMaxSplits));
-  g->splits1 = ceil_div_i(g->tiles_max, g->tpc1);
-  g->tpc2 = g->tpc1;
-  g->splits2 = g->splits1;
+  // One CTA per SM, all resident in a single wave.  With one length for all
+  // units each KV head gets floor(SMs / U) CTAs (a CTA more per head would
+  // push some into a second wave).  With ragged lengths the kernels share a
+  // 1-D grid out over the heads in proportion to their sequences' lengths
+  // (read on the device): a head of a sequence twice the mean length can get
+  // up to twice its even share of pass-1 partial slots.  The kernels' share
+  // arithmetic stays in 32 bits with a grid below 256 CTAs whenever it has
+  // more CTAs than units.
+  g->ctas = (g->U >= std::min(num_sms, 256)) ? g->U : std::min(num_sms, 256);
+  const int per_unit = g->ctas / g->U;
+  g->tpc_even = std::max(ceil_div_i(g->tiles_max, per_unit), ceil_div_i(g->tiles_max, kMaxSplits));
+  g->even = ceil_div_i(g->tiles_max, g->tpc_even);
+  g->splits1 = (g->B == 1) ? g->even : std::max(g->even, std::min(std::min(kMaxSplits, g->tiles_max), 2 * per_unit));
+  g->splits2 = g->tiles_max;
   g->chunks = ceil_div_i(s->n_max, kSelChunk);
   g->layer_chunks = ceil_div_i(s->n_max, kLayerChunk);
   return g->NR > 0;
@@ -212,14 +219,15 @@ dropkv_status score_impl(const dropkv_shape* shape, const void* q_window, const 
   p.kind = kind == DROPKV_SCORE_SNAPKV ? kKindSnapKV : kKindDropKV;
 
   if (ev && cudaEventRecord(ev[0], stream) != cudaSuccess) return DROPKV_ERR_CUDA;
+  p.ctas = g.ctas;
+  p.even = (g.B == 1 || !lengths) ? g.even : 0;
+  p.tpc = g.tpc_even;
   p.splits = g.splits1;
-  p.tpc = g.tpc1;
   if (launch_window_attention(p, g.NR, tk, tv, g.splits1, stream) != cudaSuccess) return DROPKV_ERR_CUDA;
   if (ev && cudaEventRecord(ev[1], stream) != cudaSuccess) return DROPKV_ERR_CUDA;
   if (launch_merge(p, stream) != cudaSuccess) return DROPKV_ERR_CUDA;
   if (ev && cudaEventRecord(ev[2], stream) != cudaSuccess) return DROPKV_ERR_CUDA;
   p.splits = g.splits2;
-  p.tpc = g.tpc2;
   if (launch_score(p, g.NR, tk, tv, stream) != cudaSuccess) return DROPKV_ERR_CUDA;
   if (ev && cudaEventRecord(ev[3], stream) != cudaSuccess) return DROPKV_ERR_CUDA;
 

@@ -69,6 +69,81 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// ------------------------------------------------------------ grid sharing
+// A pass grid is shared out over the KV heads.  With one sequence (or no
+// lengths) every head gets p.even CTAs of a (p.even, U) grid, p.tpc tiles
+// each, known from the CTA index alone (the kernels' SHARE = false
+// instances).  Otherwise (SHARE = true) a 1-D grid of G = p.ctas CTAs, one
+// wave, follows the lengths: sequence b
+// has T_b = ceil(n_b / kTile) tiles in each of its heads, and each of those
+// heads gets
+//   s_b = min(p.splits, T_b, 1 + floor((G - U) T_b / (Hkv sum_b' T_b')))
+// CTAs: every head gets one, the rest go by length, and sum_u s_u <= G.  A
+// length outside [w, n_max] counts as one tile (the head's one CTA flags it).
+// Every lane of a warp computes the same result from the lengths alone, so
+// all CTAs of a pass and the merge kernel agree on it.  The products fit in
+// 32 bits: when G > U both G and U are below 256 (the host caps G there),
+// T_b <= 2^24, and split bounds are at most kMaxSplits 2^24.
+__device__ __forceinline__ int seq_len(const AttnParams& p, int b) { return p.lengths ? p.lengths[b] : p.n_max; }
+__device__ __forceinline__ int seq_tiles(const AttnParams& p, int nb) {
+  return (nb < p.w || nb > p.n_max) ? 1 : ceil_div(nb, kTile);
+}
+// Hkv times the sum over the sequences of T_b
+__device__ __forceinline__ uint32_t total_tiles(const AttnParams& p) {
+  uint32_t t = 0;
+  for (int b = threadIdx.x & 31; b < p.B; b += 32) t += (uint32_t)seq_tiles(p, seq_len(p, b));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+  return t * (uint32_t)p.Hkv;
+}
+__device__ __forceinline__ int seq_share(const AttnParams& p, int tiles, uint32_t tot) {
+  const uint32_t extra = (uint32_t)(p.ctas - p.U);
+  const int s = extra ? 1 + (int)(extra * (uint32_t)tiles / tot) : 1;
+  return min(min(p.splits, tiles), s);
+}
+
+struct CtaWork {
+  int unit;     // b * Hkv + h, or -1: a CTA left over, no work in this pass
+  int split;    // 0 .. nsplit-1
+  int nsplit;   // CTAs of this unit
+  int nb;       // length of the unit's sequence
+};
+
+// Work of CTA `cta`: the units are laid out sequence by sequence, head by
+// head, each with its s_b consecutive CTAs.  Warp-uniform.
+__device__ CtaWork cta_work(const AttnParams& p, int cta) {
+  CtaWork wk{-1, 0, 0, 0};
+  const int lane = threadIdx.x & 31;
+  const uint32_t tot = total_tiles(p);
+  int base = 0;
+  for (int b0 = 0; b0 < p.B; b0 += 32) {
+    const int b = b0 + lane;
+    const int nb = b < p.B ? seq_len(p, b) : 0;
+    const int s = b < p.B ? seq_share(p, seq_tiles(p, nb), tot) : 0;
+    int incl = s * p.Hkv;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    incl += base;
+    const unsigned hit = __ballot_sync(0xffffffffu, b < p.B && cta < incl);
+    if (hit) {
+      const int src = __ffs(hit) - 1;
+      const int sb = __shfl_sync(0xffffffffu, s, src);
+      const int start = __shfl_sync(0xffffffffu, incl, src) - sb * p.Hkv;
+      wk.nb = __shfl_sync(0xffffffffu, nb, src);
+      const int h = (cta - start) / sb;
+      wk.unit = (b0 + src) * p.Hkv + h;
+      wk.split = cta - start - h * sb;
+      wk.nsplit = sb;
+      break;
+    }
+    base = __shfl_sync(0xffffffffu, incl, 31);
+  }
+  return wk;
+}
+
 // Wait for a copy or MMA to land without honouring the abort flag (used only
 // to drain work in flight before the CTA exits).
 __device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
@@ -191,12 +266,14 @@ __global__ void __launch_bounds__(kMergeThreads) merge_splits_kernel(const AttnP
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int unit = blockIdx.y, r = blockIdx.x * kMergeRows + warp;
   const int b = unit / p.Hkv;
-  const int nb = p.lengths ? p.lengths[b] : p.n_max;   // a caller input: read before the wait
+  // caller inputs, read before the wait: the length and pass 1's split count
+  const int nb = seq_len(p, b);
+  const int S = p.even > 0 ? p.even : seq_share(p, seq_tiles(p, nb), total_tiles(p));
   grid_dep_wait();                                // the partials come from pass 1
   grid_dep_launch();
   if (blockIdx.x == 0 && threadIdx.x == 0) p.tile_ctr[unit] = 0;   // pass 2 claims its tiles from 0
   if (nb < p.w || nb > p.n_max) return;          // flagged by pass 1
-  const int S = p.splits, R = p.R, d = p.d, D4 = d >> 2;
+  const int R = p.R, d = p.d, D4 = d >> 2;
   __nv_bfloat16* ahl = p.ahl + (size_t)unit * 2 * kMaxR * kDPad;
   if (r >= R) {
     // padding rows of the MMA operand: zero (32 lanes x 4 columns = 128)
@@ -204,8 +281,8 @@ __global__ void __launch_bounds__(kMergeThreads) merge_splits_kernel(const AttnP
     reinterpret_cast<uint2*>(ahl + (size_t)(kMaxR + r) * kDPad)[lane] = make_uint2(0u, 0u);
     return;
   }
-  const float2* ml = reinterpret_cast<const float2*>(p.part_ml) + (size_t)unit * S * R;
-  const float4* po4 = reinterpret_cast<const float4*>(p.part_o + (size_t)unit * S * R * d);
+  const float2* ml = reinterpret_cast<const float2*>(p.part_ml) + (size_t)unit * p.splits * R;
+  const float4* po4 = reinterpret_cast<const float4*>(p.part_o + (size_t)unit * p.splits * R * d);
   const size_t split_stride = (size_t)R * D4;
   // one round trip: the (m, l) of every split and the O column of the first
   // 32 splits are all requested before any is used (the O partial of a split
@@ -297,7 +374,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_splits_kernel(const AttnP
 
 // STATS: the softmax statistics (m, l) only -- no V, no P V^T, no O partial
 // (the SnapKV score needs the normaliser of every window row, not a).
-template <int NR, bool STATS>
+template <int NR, bool STATS, bool SHARE>
 __global__ void __launch_bounds__(kThreads, 1)
     window_attention_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                             const AttnParams p) {
@@ -312,17 +389,31 @@ __global__ void __launch_bounds__(kThreads, 1)
   Pass1Small& S = *reinterpret_cast<Pass1Small*>(sm + C::kOffSmall);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int split = blockIdx.x, unit = blockIdx.y;
+  int split, unit, nb, t0, t1;
+  if constexpr (SHARE) {
+    const CtaWork wk = cta_work(p, blockIdx.x);
+    if (wk.unit < 0) return;                // left over: no work in this pass
+    split = wk.split;
+    unit = wk.unit;
+    nb = wk.nb;
+    // an even static split of the unit's tiles: floor or ceil of ntiles / nsplit each
+    const int ntiles = ceil_div(nb, kTile);
+    t0 = (int)((uint32_t)split * (uint32_t)ntiles / (uint32_t)wk.nsplit);
+    t1 = (int)((uint32_t)(split + 1) * (uint32_t)ntiles / (uint32_t)wk.nsplit);
+  } else {
+    split = blockIdx.x;
+    unit = blockIdx.y;
+    nb = seq_len(p, unit / p.Hkv);
+    t0 = split * p.tpc;
+    t1 = min(t0 + p.tpc, ceil_div(nb, kTile));
+  }
   const int b = unit / p.Hkv, h = unit - b * p.Hkv;
-  const int nb = p.lengths ? p.lengths[b] : p.n_max;
   if (nb < p.w || nb > p.n_max) {           // invalid length: the unit is skipped
     grid_dep_wait();
     if (tid == 0 && split == 0 && h == 0) atomicOr(p.status, DROPKV_FLAG_BAD_LENGTH);
     return;
   }
   const int R = p.R;
-  const int t0 = split * p.tpc;
-  const int t1 = min(t0 + p.tpc, ceil_div(nb, kTile));
   const int T = max(0, t1 - t0);
 
   if (tid == 0) {
@@ -665,7 +756,7 @@ constexpr int pass2_smem_bytes() {
 }
 
 // SNAP: the SnapKV score (1/g) sum_r p_r from K alone -- no V, no A V^T.
-template <int NR, bool SNAP>
+template <int NR, bool SNAP, bool SHARE>
 __global__ void __launch_bounds__(kThreads, 1)
     score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                  const AttnParams p) {
@@ -681,9 +772,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   Pass2Small& S = *reinterpret_cast<Pass2Small*>(sm + C::kOffSmall);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int split = blockIdx.x, unit = blockIdx.y;
+  int unit, nb;
+  if constexpr (SHARE) {
+    const CtaWork wk = cta_work(p, blockIdx.x);
+    if (wk.unit < 0) return;                 // left over: no work in this pass
+    unit = wk.unit;
+    nb = wk.nb;
+  } else {
+    unit = blockIdx.y;
+    nb = seq_len(p, unit / p.Hkv);
+  }
   const int b = unit / p.Hkv, h = unit - b * p.Hkv;
-  const int nb = p.lengths ? p.lengths[b] : p.n_max;
   if (nb < p.w || nb > p.n_max) return;      // flagged by pass 1
   const int R = p.R;
   // The CTAs of a KV head claim its tiles one at a time from a counter (the
@@ -693,7 +792,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   // more tiles) to the MMA warp through the K slot and to the workers
   // through the V slot.
   const int ntiles = ceil_div(nb, kTile);
-  (void)split;
 
   if (tid == 0) {
     for (int i = 0; i < C::KS; ++i) { mbar_init(&S.kfull[i], 1); mbar_init(&S.kempty[i], 1); }
@@ -948,19 +1046,23 @@ template <int NR, bool SNAP>
 cudaError_t launch_pass1_t(const AttnParams& p, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t st) {
   constexpr int smem = pass1_smem_bytes<NR, SNAP>();
   static_assert(smem <= 232448, "pass-1 shared memory exceeds the per-CTA limit");
-  cudaError_t e = cudaFuncSetAttribute(window_attention_kernel<NR, SNAP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       smem);
+  // (even, U) when every unit gets `even` CTAs, else the 1-D share grid
+  auto kern = p.even > 0 ? window_attention_kernel<NR, SNAP, false> : window_attention_kernel<NR, SNAP, true>;
+  const dim3 grid = p.even > 0 ? dim3(p.even, p.U) : dim3(p.ctas);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(window_attention_kernel<NR, SNAP>, dim3(p.splits, p.U), dim3(kThreads), smem, st, tk, tv, p);
+  return launch_pdl(kern, grid, dim3(kThreads), smem, st, tk, tv, p);
 }
 
 template <int NR, bool SNAP>
 cudaError_t launch_pass2_t(const AttnParams& p, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t st) {
   constexpr int smem = pass2_smem_bytes<NR, SNAP>();
   static_assert(smem <= 232448, "pass-2 shared memory exceeds the per-CTA limit");
-  cudaError_t e = cudaFuncSetAttribute(score_kernel<NR, SNAP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  auto kern = p.even > 0 ? score_kernel<NR, SNAP, false> : score_kernel<NR, SNAP, true>;
+  const dim3 grid = p.even > 0 ? dim3(p.even, p.U) : dim3(p.ctas);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(score_kernel<NR, SNAP>, dim3(p.splits, p.U), dim3(kThreads), smem, st, tk, tv, p);
+  return launch_pdl(kern, grid, dim3(kThreads), smem, st, tk, tv, p);
 }
 
 }  // namespace

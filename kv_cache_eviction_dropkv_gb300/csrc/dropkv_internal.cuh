@@ -28,8 +28,10 @@ struct Geom {
   int g, R, NR;          // NR: R rounded up to the MMA width instantiated (16, 32 or 64)
   int U;                 // B * Hkv units (KV heads)
   int tiles_max;         // ceil(n_max / kTile)
-  int splits1, tpc1;     // pass-1 CTAs per unit and tiles per CTA
-  int splits2, tpc2;     // pass-2 CTAs per unit and tiles per CTA
+  int ctas;              // CTAs of a pass grid: max(U, SMs), below 256 when above U
+  int even, tpc_even;    // CTAs per unit and tiles per CTA when all units have one length
+  int splits1;           // pass-1 partial slots per unit (most CTAs a unit can get)
+  int splits2;           // most pass-2 CTAs a unit can get
   int chunks;            // ceil(n_max / kSelChunk)
   int layer_chunks;      // ceil(n_max / kLayerChunk)
 };
@@ -72,7 +74,10 @@ struct AttnParams {
   const __nv_bfloat16* q;        // [B][Hq][w][d]
   const int32_t* lengths;        // [B] or null
   int B, Hq, Hkv, d, n_max, w, g, R, U;
-  int splits, tpc;
+  int splits;                    // most CTAs per unit (pass 1: its partial slots per unit)
+  int ctas;                      // CTAs of the pass grid (>= U)
+  int even;                      // > 0: every unit gets this many CTAs; 0: shares by length
+  int tpc;                       // tiles per CTA when even > 0
   float scale_log2;              // log2(e) / sqrt(d)
   // workspace
   float *m, *l, *a, *m2, *aa;

@@ -121,12 +121,13 @@ extern "C" dropkv_status dropkv_score_noalloc(const dropkv_shape* shape, const v
   // the array keeps the previous call's contents; scoring writes every scratch
   // value before reading it (the merge kernel resets pass 2's tile counters),
   // so nothing has to be cleared first
+  p.ctas = g.ctas;
+  p.even = (g.B == 1 || !lengths) ? g.even : 0;
+  p.tpc = g.tpc_even;
   p.splits = g.splits1;
-  p.tpc = g.tpc1;
   if (launch_window_attention(p, g.NR, tk, tv, g.splits1, stream) != cudaSuccess) return DROPKV_ERR_CUDA;
   if (launch_merge(p, stream) != cudaSuccess) return DROPKV_ERR_CUDA;
   p.splits = g.splits2;
-  p.tpc = g.tpc2;
   if (launch_score(p, g.NR, tk, tv, stream) != cudaSuccess) return DROPKV_ERR_CUDA;
   PoolParams pp{};
   pp.raw = p.raw;

@@ -258,3 +258,39 @@ def test_one_million_tokens():
     n = 1 << 20
     q, k, v, lens = _custom(1, 1, 1, 128, n, 8, seed=23)
     _run_custom(q, k, v, lens, [n * 9 // 10], 5, 8)
+
+
+# The passes share their one-wave grid out over the KV heads in proportion to
+# the sequence lengths (read on the device).  These batches put that mapping
+# far from the even split: one long sequence beside short ones, more than 32
+# sequences (several warp-wide chunks of the prefix scan), and more KV heads
+# than SMs (one CTA each).
+@pytest.mark.parametrize("case", [
+    # (B, Hq, Hkv, d, n, w, lengths or None for random, seed)
+    (5, 4, 2, 64, 20000, 4, [20000, 300, 129, 5000, 9], 31),
+    (37, 8, 4, 32, 700, 3, None, 32),
+    (40, 4, 4, 16, 400, 2, None, 33),
+])
+def test_grid_share_across_ragged_heads(case):
+    B, Hq, Hkv, d, n, w, lens, seed = case
+    if lens is None:
+        lens = np.random.default_rng(seed).integers(w + 1, n + 1, size=B).tolist()
+    q, k, v, lengths = _custom(B, Hq, Hkv, d, n, w, seed=seed, lengths=lens)
+    evict = [int(L) // 2 for L in lens]
+    _run_custom(q, k, v, lengths, evict, 3, w)
+
+
+def test_invalid_lengths_beside_valid_ones():
+    """Lengths below w or above n_max are flagged and their heads skipped; the
+    valid sequence between them is scored as if it were alone."""
+    Bn, Hq, Hkv, d, n, w = 3, 4, 2, 64, 3000, 4
+    q, k, v, _ = _custom(Bn, Hq, Hkv, d, n, w, seed=35)
+    qb, kb, vb = synth.bf16_round(q), synth.bf16_round(k), synth.bf16_round(v)
+    op = DropKV(Bn, Hq, Hkv, d, n, w, 3, w, device=DEV)
+    op.scores.fill_(SENTINEL)
+    lens = torch.tensor([3, 2500, 1 << 30], dtype=torch.int32, device=DEV)
+    op.score(qb.to(DEV), kb.to(DEV), vb.to(DEV), lens)
+    code, flags = B.dropkv_read_status(op.status)
+    assert code == 7 and flags & B.FLAG_BAD_LENGTH
+    ref = oracle.score(qb[1:2], kb[1:2], vb[1:2], np.array([2500], dtype=np.int32), 3, w)
+    check_scores(op.scores[1:2].cpu().numpy(), ref["final"], [2500])
