@@ -103,8 +103,7 @@ bool make_geom(const dropkv_shape* s, int num_sms, Geom* g) {
   // more CTAs than units.
   g->ctas = (g->U >= std::min(num_sms, 256)) ? g->U : std::min(num_sms, 256);
   const int per_unit = g->ctas / g->U;
-  g->tpc_even = std::max(ceil_div_i(g->tiles_max, per_unit), ceil_div_i(g->tiles_max, kMaxSplits));
-  g->even = ceil_div_i(g->tiles_max, g->tpc_even);
+  g->even = std::min(std::min(kMaxSplits, g->tiles_max), per_unit);
   g->splits1 = (g->B == 1) ? g->even : std::max(g->even, std::min(std::min(kMaxSplits, g->tiles_max), 2 * per_unit));
   g->splits2 = g->tiles_max;
   g->chunks = ceil_div_i(s->n_max, kSelChunk);
@@ -221,7 +220,6 @@ dropkv_status score_impl(const dropkv_shape* shape, const void* q_window, const 
   if (ev && cudaEventRecord(ev[0], stream) != cudaSuccess) return DROPKV_ERR_CUDA;
   p.ctas = g.ctas;
   p.even = (g.B == 1 || !lengths) ? g.even : 0;
-  p.tpc = g.tpc_even;
   p.splits = g.splits1;
   if (launch_window_attention(p, g.NR, tk, tv, g.splits1, stream) != cudaSuccess) return DROPKV_ERR_CUDA;
   if (ev && cudaEventRecord(ev[1], stream) != cudaSuccess) return DROPKV_ERR_CUDA;

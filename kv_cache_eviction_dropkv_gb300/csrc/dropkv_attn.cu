@@ -70,11 +70,9 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 // ------------------------------------------------------------ grid sharing
-// A pass grid is shared out over the KV heads.  With one sequence (or no
-// lengths) every head gets p.even CTAs of a (p.even, U) grid, p.tpc tiles
-// each, known from the CTA index alone (the kernels' SHARE = false
-// instances).  Otherwise (SHARE = true) a 1-D grid of G = p.ctas CTAs, one
-// wave, follows the lengths: sequence b
+// A pass grid of G = p.ctas CTAs (one wave) is shared out over the KV heads.
+// With one sequence (or no lengths) every head gets p.even CTAs, known from
+// the CTA index alone.  Otherwise the share follows the lengths: sequence b
 // has T_b = ceil(n_b / kTile) tiles in each of its heads, and each of those
 // heads gets
 //   s_b = min(p.splits, T_b, 1 + floor((G - U) T_b / (Hkv sum_b' T_b')))
@@ -113,6 +111,14 @@ struct CtaWork {
 // head, each with its s_b consecutive CTAs.  Warp-uniform.
 __device__ CtaWork cta_work(const AttnParams& p, int cta) {
   CtaWork wk{-1, 0, 0, 0};
+  if (p.even > 0) {
+    if (cta >= p.U * p.even) return wk;
+    wk.unit = cta / p.even;
+    wk.split = cta - wk.unit * p.even;
+    wk.nsplit = p.even;
+    wk.nb = seq_len(p, wk.unit / p.Hkv);
+    return wk;
+  }
   const int lane = threadIdx.x & 31;
   const uint32_t tot = total_tiles(p);
   int base = 0;
@@ -374,7 +380,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_splits_kernel(const AttnP
 
 // STATS: the softmax statistics (m, l) only -- no V, no P V^T, no O partial
 // (the SnapKV score needs the normaliser of every window row, not a).
-template <int NR, bool STATS, bool SHARE>
+template <int NR, bool STATS>
 __global__ void __launch_bounds__(kThreads, 1)
     window_attention_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                             const AttnParams p) {
@@ -389,24 +395,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   Pass1Small& S = *reinterpret_cast<Pass1Small*>(sm + C::kOffSmall);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  int split, unit, nb, t0, t1;
-  if constexpr (SHARE) {
-    const CtaWork wk = cta_work(p, blockIdx.x);
-    if (wk.unit < 0) return;                // left over: no work in this pass
-    split = wk.split;
-    unit = wk.unit;
-    nb = wk.nb;
-    // an even static split of the unit's tiles: floor or ceil of ntiles / nsplit each
-    const int ntiles = ceil_div(nb, kTile);
-    t0 = (int)((uint32_t)split * (uint32_t)ntiles / (uint32_t)wk.nsplit);
-    t1 = (int)((uint32_t)(split + 1) * (uint32_t)ntiles / (uint32_t)wk.nsplit);
-  } else {
-    split = blockIdx.x;
-    unit = blockIdx.y;
-    nb = seq_len(p, unit / p.Hkv);
-    t0 = split * p.tpc;
-    t1 = min(t0 + p.tpc, ceil_div(nb, kTile));
-  }
+  const CtaWork wk = cta_work(p, blockIdx.x);
+  if (wk.unit < 0) return;                  // left over: no work in this pass
+  const int split = wk.split, unit = wk.unit, nb = wk.nb;
+  // an even static split of the unit's tiles: floor or ceil of ntiles / nsplit each
+  const int ntiles = ceil_div(nb, kTile);
+  const int t0 = (int)((uint32_t)split * (uint32_t)ntiles / (uint32_t)wk.nsplit);
+  const int t1 = (int)((uint32_t)(split + 1) * (uint32_t)ntiles / (uint32_t)wk.nsplit);
   const int b = unit / p.Hkv, h = unit - b * p.Hkv;
   if (nb < p.w || nb > p.n_max) {           // invalid length: the unit is skipped
     grid_dep_wait();
@@ -756,7 +751,7 @@ constexpr int pass2_smem_bytes() {
 }
 
 // SNAP: the SnapKV score (1/g) sum_r p_r from K alone -- no V, no A V^T.
-template <int NR, bool SNAP, bool SHARE>
+template <int NR, bool SNAP>
 __global__ void __launch_bounds__(kThreads, 1)
     score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                  const AttnParams p) {
@@ -772,16 +767,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   Pass2Small& S = *reinterpret_cast<Pass2Small*>(sm + C::kOffSmall);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  int unit, nb;
-  if constexpr (SHARE) {
-    const CtaWork wk = cta_work(p, blockIdx.x);
-    if (wk.unit < 0) return;                 // left over: no work in this pass
-    unit = wk.unit;
-    nb = wk.nb;
-  } else {
-    unit = blockIdx.y;
-    nb = seq_len(p, unit / p.Hkv);
-  }
+  const CtaWork wk = cta_work(p, blockIdx.x);
+  if (wk.unit < 0) return;                   // left over: no work in this pass
+  const int unit = wk.unit, nb = wk.nb;
   const int b = unit / p.Hkv, h = unit - b * p.Hkv;
   if (nb < p.w || nb > p.n_max) return;      // flagged by pass 1
   const int R = p.R;
@@ -1046,23 +1034,20 @@ template <int NR, bool SNAP>
 cudaError_t launch_pass1_t(const AttnParams& p, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t st) {
   constexpr int smem = pass1_smem_bytes<NR, SNAP>();
   static_assert(smem <= 232448, "pass-1 shared memory exceeds the per-CTA limit");
-  // (even, U) when every unit gets `even` CTAs, else the 1-D share grid
-  auto kern = p.even > 0 ? window_attention_kernel<NR, SNAP, false> : window_attention_kernel<NR, SNAP, true>;
-  const dim3 grid = p.even > 0 ? dim3(p.even, p.U) : dim3(p.ctas);
+  auto kern = window_attention_kernel<NR, SNAP>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, grid, dim3(kThreads), smem, st, tk, tv, p);
+  return launch_pdl(kern, dim3(p.ctas), dim3(kThreads), smem, st, tk, tv, p);
 }
 
 template <int NR, bool SNAP>
 cudaError_t launch_pass2_t(const AttnParams& p, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t st) {
   constexpr int smem = pass2_smem_bytes<NR, SNAP>();
   static_assert(smem <= 232448, "pass-2 shared memory exceeds the per-CTA limit");
-  auto kern = p.even > 0 ? score_kernel<NR, SNAP, false> : score_kernel<NR, SNAP, true>;
-  const dim3 grid = p.even > 0 ? dim3(p.even, p.U) : dim3(p.ctas);
+  auto kern = score_kernel<NR, SNAP>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, grid, dim3(kThreads), smem, st, tk, tv, p);
+  return launch_pdl(kern, dim3(p.ctas), dim3(kThreads), smem, st, tk, tv, p);
 }
 
 }  // namespace

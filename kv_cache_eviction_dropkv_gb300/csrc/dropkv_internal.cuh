@@ -29,7 +29,7 @@ struct Geom {
   int U;                 // B * Hkv units (KV heads)
   int tiles_max;         // ceil(n_max / kTile)
   int ctas;              // CTAs of a pass grid: max(U, SMs), below 256 when above U
-  int even, tpc_even;    // CTAs per unit and tiles per CTA when all units have one length
+  int even;              // CTAs per unit when all units have one length
   int splits1;           // pass-1 partial slots per unit (most CTAs a unit can get)
   int splits2;           // most pass-2 CTAs a unit can get
   int chunks;            // ceil(n_max / kSelChunk)
@@ -77,7 +77,6 @@ struct AttnParams {
   int splits;                    // most CTAs per unit (pass 1: its partial slots per unit)
   int ctas;                      // CTAs of the pass grid (>= U)
   int even;                      // > 0: every unit gets this many CTAs; 0: shares by length
-  int tpc;                       // tiles per CTA when even > 0
   float scale_log2;              // log2(e) / sqrt(d)
   // workspace
   float *m, *l, *a, *m2, *aa;

@@ -123,7 +123,6 @@ extern "C" dropkv_status dropkv_score_noalloc(const dropkv_shape* shape, const v
   // so nothing has to be cleared first
   p.ctas = g.ctas;
   p.even = (g.B == 1 || !lengths) ? g.even : 0;
-  p.tpc = g.tpc_even;
   p.splits = g.splits1;
   if (launch_window_attention(p, g.NR, tk, tv, g.splits1, stream) != cudaSuccess) return DROPKV_ERR_CUDA;
   if (launch_merge(p, stream) != cudaSuccess) return DROPKV_ERR_CUDA;
