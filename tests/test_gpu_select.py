@@ -144,3 +144,19 @@ def test_multi_kernel_path(case):
     pos = rng.choice(n, n_tied, replace=False)
     s[0, :, pos] = np.float32(2.5)
     _check(s, [n], [int(np.sum(s[0, 0] < 2.5)) + n_tied // 3], 0)
+
+
+@pytest.mark.parametrize("n_members", [1, 200, 256, 257, 600])
+def test_prefix_members_across_cluster_ctas(n_members):
+    """Slots sharing the k-th item's 24-bit key prefix, spread over the CTAs
+    of a 5-chunk cluster, resolved by the last digit and the tie rank.  Their
+    scores differ only in the last 6 mantissa bits, with ties among them, and
+    the cut falls inside them."""
+    rng = np.random.default_rng(n_members + 40)
+    n = 80000
+    s = (rng.random((1, 2, n)) + 2.0).astype(np.float32)
+    pos = rng.choice(n, n_members, replace=False)
+    low = rng.integers(0, 40, size=n_members).astype(np.float32) * np.float32(2 ** -23)
+    s[0][:, pos] = np.float32(1.5) + low
+    below = int(np.sum(s[0, 0] < 1.5))
+    _check(s, [n], [below + (n_members + 1) // 2], 0)
