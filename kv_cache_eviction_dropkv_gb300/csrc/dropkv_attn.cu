@@ -11,10 +11,12 @@
 // warps own the 128 lanes twice over (warps w and w + 4 read lane quarter w)
 // and split the R window rows between them, so each worker thread owns one
 // token and half of the rows and needs no cross-thread reduction on the hot
-// path; a TMA warp and an MMA warp feed them through mbarrier rings.  Pass 1
-// splits each KV head's tiles statically over ~152/(B Hkv) CTAs (one partial
-// state each, merged by merge_splits_kernel); pass 2's CTAs claim the head's
-// tiles dynamically.  The SnapKV score kind runs the same kernels with K only
+// path; a TMA warp and an MMA warp feed them through mbarrier rings.  Each
+// pass runs one wave of CTAs shared out over the KV heads (floor(SMs / U) per
+// head for one sequence, in proportion to the lengths for a ragged batch).
+// Pass 1 splits a head's tiles statically over its CTAs (one partial state
+// each, merged by merge_splits_kernel); pass 2's CTAs claim the head's tiles
+// dynamically.  The SnapKV score kind runs the same kernels with K only
 // (pass 1 keeps the softmax statistics, pass 2 sums p over the window).
 //
 // Method: "DropKV: Exact single-entry output-perturbation scoring", Core
