@@ -278,7 +278,11 @@ __global__ void __launch_bounds__(kMergeThreads) merge_splits_kernel(const AttnP
   const int nb = seq_len(p, b);
   const int S = p.even > 0 ? p.even : seq_share(p, seq_tiles(p, nb), total_tiles(p));
   grid_dep_wait();                                // the partials come from pass 1
-  grid_dep_launch();
+  // Pass 2's CTAs may be scheduled now when this grid fits in one wave (their
+  // start-up then overlaps the merge); a larger merge grid triggers them only
+  // as its CTAs exit, so that they do not take the SM slots its later CTAs
+  // wait for.
+  if (gridDim.x * gridDim.y <= (unsigned)p.ctas) grid_dep_launch();
   if (blockIdx.x == 0 && threadIdx.x == 0) p.tile_ctr[unit] = 0;   // pass 2 claims its tiles from 0
   if (nb < p.w || nb > p.n_max) return;          // flagged by pass 1
   const int R = p.R, d = p.d, D4 = d >> 2;
