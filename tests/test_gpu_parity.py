@@ -294,3 +294,11 @@ def test_invalid_lengths_beside_valid_ones():
     assert code == 7 and flags & B.FLAG_BAD_LENGTH
     ref = oracle.score(qb[1:2], kb[1:2], vb[1:2], np.array([2500], dtype=np.int32), 3, w)
     check_scores(op.scores[1:2].cpu().numpy(), ref["final"], [2500])
+
+
+def test_single_sequence_far_shorter_than_the_cache():
+    """One sequence of 300 tokens in a 40000-slot cache: the one-sequence grid
+    gives the head floor(SMs / Hkv) CTAs from the capacity, most of which find
+    no tile of the sequence and publish an empty split state."""
+    q, k, v, lens = _custom(1, 8, 2, 64, 40000, 4, seed=41, lengths=[300])
+    _run_custom(q, k, v, lens, [150], 5, 4)
