@@ -115,8 +115,16 @@ __device__ CtaWork cta_work(const AttnParams& p, int cta) {
   CtaWork wk{-1, 0, 0, 0};
   if (p.even > 0) {
     if (cta >= p.U * p.even) return wk;
-    wk.unit = cta / p.even;
-    wk.split = cta - wk.unit * p.even;
+    if (p.even >= 8) {
+      // many CTAs per head: heads interleaved over the grid (CTA c serves
+      // head c mod U), so that each head's CTAs sit on SMs all over the chip
+      // and pass 2's heads, each claiming from its own counter, finish together
+      wk.split = cta / p.U;
+      wk.unit = cta - wk.split * p.U;
+    } else {
+      wk.unit = cta / p.even;
+      wk.split = cta - wk.unit * p.even;
+    }
     wk.nsplit = p.even;
     wk.nb = seq_len(p, wk.unit / p.Hkv);
     return wk;
