@@ -126,8 +126,13 @@ WsPlan make_plan(const Geom& g) {
   w.m2 = take(UR * 4);
   w.aa = take(UR * 4);
   w.ahl = take((size_t)g.U * 2 * kMaxR * kDPad * 2);
+  w.cvec = take((size_t)g.U * kDPad * 4);
+  w.cflag = take((size_t)g.U * 4);
+  w.dom_s = take(UR * 4);
+  w.dom_l = take(UR * 4);
+  w.dom_o = take(UR * g.d * 4);
   w.part_o = take((size_t)g.U * g.splits1 * g.R * g.d * 4);
-  w.part_ml = take((size_t)g.U * g.splits1 * g.R * 2 * 4);
+  w.part_ml = take((size_t)g.U * g.splits1 * g.R * 4 * 4);
   w.tile_ctr = take((size_t)g.U * 4);
   w.raw = take((size_t)g.U * g.n_max * 4);
   w.sel_zero_begin = off;
@@ -166,13 +171,13 @@ size_t dropkv_workspace_size(const dropkv_shape* shape) {
 
 }  // extern "C"
 
-namespace {
+namespace dropkv {
 
-dropkv_status score_impl(const dropkv_shape* shape, const void* q_window, const void* k, const void* v,
+dropkv_status score_core(const dropkv_shape* shape, const void* q_window, const void* k, const void* v,
                          const int32_t* lengths, int32_t pool_kernel, int32_t protect, float* scores,
                          float* raw_scores, void* workspace, size_t workspace_bytes, uint32_t* status,
-                         cudaStream_t stream, cudaEvent_t* ev, PoolParams* defer_pool = nullptr,
-                         int kind = DROPKV_SCORE_DROPKV) {
+                         cudaStream_t stream, cudaEvent_t* ev, PoolParams* defer_pool, int kind,
+                         bool scoring_regions_only) {
   const int sms = current_sms(nullptr);
   if (sms <= 0) return DROPKV_ERR_CUDA;
   if (!shape) return DROPKV_ERR_INVALID_ARG;
@@ -190,7 +195,9 @@ dropkv_status score_impl(const dropkv_shape* shape, const void* q_window, const 
     return DROPKV_ERR_INVALID_ARG;
   if (kind != DROPKV_SCORE_DROPKV && kind != DROPKV_SCORE_SNAPKV) return DROPKV_ERR_INVALID_ARG;
   const WsPlan w = make_plan(g);
-  if (!workspace || workspace_bytes < w.total || !aligned16(workspace)) return DROPKV_ERR_WORKSPACE;
+  // the scoring regions lie ahead of the selection regions
+  const size_t need = scoring_regions_only ? w.sel_zero_begin : w.total;
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return DROPKV_ERR_WORKSPACE;
   const size_t score_bytes = (size_t)g.U * g.n_max * 4;
   if (raw_scores && ranges_overlap(raw_scores, score_bytes, scores, score_bytes)) return DROPKV_ERR_INVALID_ARG;
 
@@ -200,9 +207,10 @@ dropkv_status score_impl(const dropkv_shape* shape, const void* q_window, const 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   AttnParams p{};
   p.q = static_cast<const __nv_bfloat16*>(q_window);
+  p.v = static_cast<const __nv_bfloat16*>(v);
   p.lengths = lengths;
   p.B = g.B; p.Hq = g.Hq; p.Hkv = g.Hkv; p.d = g.d; p.n_max = g.n_max; p.w = g.w;
-  p.g = g.g; p.R = g.R; p.U = g.U;
+  p.g = g.g; p.R = g.R; p.U = g.U; p.NR = g.NR;
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)g.d));
   p.m = reinterpret_cast<float*>(ws + w.m);
   p.l = reinterpret_cast<float*>(ws + w.l);
@@ -210,6 +218,11 @@ dropkv_status score_impl(const dropkv_shape* shape, const void* q_window, const 
   p.m2 = reinterpret_cast<float*>(ws + w.m2);
   p.aa = reinterpret_cast<float*>(ws + w.aa);
   p.ahl = reinterpret_cast<__nv_bfloat16*>(ws + w.ahl);
+  p.cvec = reinterpret_cast<float*>(ws + w.cvec);
+  p.cflag = reinterpret_cast<int*>(ws + w.cflag);
+  p.dom_s = reinterpret_cast<int*>(ws + w.dom_s);
+  p.dom_l = reinterpret_cast<float*>(ws + w.dom_l);
+  p.dom_o = reinterpret_cast<float*>(ws + w.dom_o);
   p.part_o = reinterpret_cast<float*>(ws + w.part_o);
   p.part_ml = reinterpret_cast<float*>(ws + w.part_ml);
   p.tile_ctr = reinterpret_cast<uint32_t*>(ws + w.tile_ctr);
@@ -221,6 +234,7 @@ dropkv_status score_impl(const dropkv_shape* shape, const void* q_window, const 
   p.ctas = g.ctas;
   p.even = (g.B == 1 || !lengths) ? g.even : 0;
   p.splits = g.splits1;
+  p.splits1 = g.splits1;
   if (launch_window_attention(p, g.NR, tk, tv, g.splits1, stream) != cudaSuccess) return DROPKV_ERR_CUDA;
   if (ev && cudaEventRecord(ev[1], stream) != cudaSuccess) return DROPKV_ERR_CUDA;
   if (launch_merge(p, stream) != cudaSuccess) return DROPKV_ERR_CUDA;
@@ -244,6 +258,19 @@ dropkv_status score_impl(const dropkv_shape* shape, const void* q_window, const 
   if (launch_pool_protect(pp, stream) != cudaSuccess) return DROPKV_ERR_CUDA;
   if (ev && cudaEventRecord(ev[4], stream) != cudaSuccess) return DROPKV_ERR_CUDA;
   return DROPKV_OK;
+}
+
+}  // namespace dropkv
+
+namespace {
+
+dropkv_status score_impl(const dropkv_shape* shape, const void* q_window, const void* k, const void* v,
+                         const int32_t* lengths, int32_t pool_kernel, int32_t protect, float* scores,
+                         float* raw_scores, void* workspace, size_t workspace_bytes, uint32_t* status,
+                         cudaStream_t stream, cudaEvent_t* ev, PoolParams* defer_pool = nullptr,
+                         int kind = DROPKV_SCORE_DROPKV) {
+  return score_core(shape, q_window, k, v, lengths, pool_kernel, protect, scores, raw_scores, workspace,
+                    workspace_bytes, status, stream, ev, defer_pool, kind, false);
 }
 
 dropkv_status select_impl(const dropkv_shape* shape, const float* scores, const int32_t* lengths,

@@ -189,6 +189,20 @@ __device__ __forceinline__ void split_hi_lo(float e0, float e1, uint32_t& hi, ui
   lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
+// Max of two pairs of non-negative bf16 values (their bit patterns order as
+// unsigned 16-bit integers).
+__device__ __forceinline__ uint32_t max_bf16x2(uint32_t a, uint32_t b) {
+  const __nv_bfloat162 m =
+      __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&a), *reinterpret_cast<const __nv_bfloat162*>(&b));
+  return *reinterpret_cast<const uint32_t*>(&m);
+}
+// A pair of bf16 values times (f0, f1), rounded back to bf16.
+__device__ __forceinline__ uint32_t scale_bf16x2(uint32_t a, float f0, float f1) {
+  const __nv_bfloat162 h =
+      __floats2bfloat162_rn(__uint_as_float(a << 16) * f0, __uint_as_float(a & 0xFFFF0000u) * f1);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
 // Sum of squares of 8 packed bf16 values.
 __device__ __forceinline__ float sumsq_bf16x8(const uint4 v, float acc) {
   const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
@@ -257,6 +271,7 @@ struct Pass1Small {
   float mref[kMaxR];       // exponent reference of row r (log2 units; live for NR = 64, else at the end)
   float mnew[kMaxR];       // staging of a new reference (NR = 64)
   float red[4][kMaxR];     // per-lane-quarter reduction scratch
+  uint32_t rmax[4][kMaxR]; // per lane quarter: largest e of row r (bf16 bits of a non-negative value)
 };
 
 template <int NR, bool STATS>
@@ -267,20 +282,39 @@ constexpr int pass1_smem_bytes() {
 // Merge of the split-K partial states (its own small kernel: it sits on the
 // critical path, so it is spread over many CTAs with all loads in flight).
 //   m = max_s m_s;  L = sum_s l_s 2^(m_s - m);  a = sum_s O_s 2^(m_s - m) / L.
-// CTA (row group, KV head): warp w takes row r = 4 * group + w.  Lane c holds
-// the (m, l) of splits c, c + 32, ... and float4 column c of every split's O,
-// all requested in one round trip.  Also writes |a|^2, the bf16 hi/lo split
-// of a (zero rows past R and zero columns past d) and the exported
-// log-sum-exp.
-constexpr int kMergeRows = 4;                 // rows per CTA (one warp each)
-constexpr int kMergeThreads = 32 * kMergeRows;
+// CTA (row group, KV head): warp w < 4 takes row r = 4 * group + w.  Lane c
+// holds the (m, l, largest e) of splits c, c + 32, ... and float4 column c of
+// every split's O, all requested in one round trip.  Writes a, m, L and the
+// exported log-sum-exp.
+//
+// Shift of the scoring basis: warp 4 of every CTA merges row 0 too; its
+// output rounded to bf16, c, is the head's shift when |c|^2 > 2 d (the values
+// share an offset large against their spread), else c = 0.  Each row is
+// written as a' = a - c, split into bf16 hi + lo parts (pass 2's A.V^T
+// operand; rows past R are zero), with K = |a'|^2 + 2 a'.c, so that pass 2
+// evaluates |a - v|^2 = K - 2 a'.v + |v - c|^2 without the cancellation of
+// |a|^2 - 2 a.v + |v|^2 when |v| is far above |a - v|.
+//
+// A row whose largest probability p* = e* / L reaches kDomP (e* = the largest
+// e of any split, weighted like its l) is dominated: the merge records the
+// split s* that holds that key (unique, since p* > 1/2) and the (O, L) of
+// every other split -- sums whose terms do not contain the dominant key, from
+// which pass 2 rebuilds the output without that key with no cancellation.
+// Each split's largest e comes from the bf16 hi parts of pass 1's P operand:
+// good to 2^-9, which only blurs the threshold; pass 2 uses the key's own e.
+constexpr int kMergeRows = 4;                       // rows per CTA (one warp each)
+constexpr int kMergeThreads = 32 * (kMergeRows + 1);  // + the warp that merges row 0 for the shift
 constexpr int kMergeSplitRegs = kMaxSplits / 32;
 static_assert(kMergeSplitRegs * 32 == kMaxSplits, "split states are held 32 per register slot");
 
 __global__ void __launch_bounds__(kMergeThreads) merge_splits_kernel(const AttnParams p) {
-  __shared__ float wts_s[kMergeRows][32];
+  __shared__ float wts_s[kMergeRows + 1][32];
+  __shared__ float wex_s[kMergeRows + 1][32];   // the same weights without split s* (dominated rows)
+  __shared__ __align__(16) float c_s[kDPad];    // the shift c (bf16 values; zero when not shifted)
+  __shared__ int shift_s;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int unit = blockIdx.y, r = blockIdx.x * kMergeRows + warp;
+  const bool shift_warp = warp == kMergeRows;
+  const int unit = blockIdx.y, r = shift_warp ? 0 : blockIdx.x * kMergeRows + warp;
   const int b = unit / p.Hkv;
   // caller inputs, read before the wait: the length and pass 1's split count
   const int nb = seq_len(p, b);
@@ -292,102 +326,166 @@ __global__ void __launch_bounds__(kMergeThreads) merge_splits_kernel(const AttnP
   // wait for.
   if (gridDim.x * gridDim.y <= (unsigned)p.ctas) grid_dep_launch();
   if (blockIdx.x == 0 && threadIdx.x == 0) p.tile_ctr[unit] = 0;   // pass 2 claims its tiles from 0
-  if (nb < p.w || nb > p.n_max) return;          // flagged by pass 1
+  if (nb < p.w || nb > p.n_max) return;          // flagged by pass 1 (the whole CTA leaves)
   const int R = p.R, d = p.d, D4 = d >> 2;
+  const bool stats_only = p.kind == kKindSnapKV;   // no O partials were written
+  const bool live = r < R;
+  const size_t ro = (size_t)unit * R + r;
+  float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+  float M = -INFINITY, L = 0.f, Lx = 0.f;
+  bool dom = false;
+  int sstar = -1;
+  if (live) {
+    const float4* ml = reinterpret_cast<const float4*>(p.part_ml) + (size_t)unit * p.splits * R;
+    const float4* po4 = reinterpret_cast<const float4*>(p.part_o + (size_t)unit * p.splits * R * d);
+    const size_t split_stride = (size_t)R * D4;
+    // one round trip: the (m, l, largest e) of every split and the O column
+    // of the first 32 splits are all requested before any is used (the O
+    // partial of a split without visible keys is never written; its weight is
+    // 0 and it is dropped by a select, not a multiply, so whatever it holds
+    // cannot leak in)
+    float4 v[kMergeSplitRegs];
+#pragma unroll
+    for (int q = 0; q < kMergeSplitRegs; ++q) {
+      const int s = q * 32 + lane;
+      v[q] = (s < S) ? __ldcg(ml + (size_t)s * R + r) : make_float4(-INFINITY, 0.f, 0.f, 0.f);
+    }
+    float4 o[32];
+#pragma unroll
+    for (int u = 0; u < 32; ++u)
+      o[u] = (!stats_only && lane < D4 && u < S) ? __ldcg(po4 + (size_t)u * split_stride + (size_t)r * D4 + lane)
+                                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int q = 0; q < kMergeSplitRegs; ++q)
+      if (v[q].y > 0.f) M = fmaxf(M, v[q].x);
+#pragma unroll
+    for (int o2 = 16; o2 > 0; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o2));
+    float wgt[kMergeSplitRegs];
+    float E = 0.f;                 // the largest e of any split, in the merged reference
+#pragma unroll
+    for (int q = 0; q < kMergeSplitRegs; ++q) {
+      wgt[q] = (v[q].y > 0.f) ? exp2f(v[q].x - M) : 0.f;
+      L = fmaf(v[q].y, wgt[q], L);
+      E = fmaxf(E, v[q].z * wgt[q]);
+    }
+    L = warp_sum(L);
+#pragma unroll
+    for (int o2 = 16; o2 > 0; o2 >>= 1) E = fmaxf(E, __shfl_xor_sync(0xffffffffu, E, o2));
+    dom = !stats_only && !shift_warp && E >= kDomP * L;   // the same in every lane
+    float wex[kMergeSplitRegs];
+    if (dom) {
+      int first = 0x7fffffff;
+#pragma unroll
+      for (int q = 0; q < kMergeSplitRegs; ++q)
+        if (v[q].y > 0.f && v[q].z * wgt[q] == E) first = min(first, q * 32 + lane);
+#pragma unroll
+      for (int o2 = 16; o2 > 0; o2 >>= 1) first = min(first, __shfl_xor_sync(0xffffffffu, first, o2));
+      sstar = first;
+#pragma unroll
+      for (int q = 0; q < kMergeSplitRegs; ++q) {
+        wex[q] = (q * 32 + lane == sstar) ? 0.f : wgt[q];
+        Lx = fmaf(v[q].y, wex[q], Lx);
+      }
+      Lx = warp_sum(Lx);
+    }
+    if (!stats_only) {
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f), acx = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int q = 0; q < kMergeSplitRegs; ++q) {
+        if (q * 32 >= S) break;
+        __syncwarp();
+        wts_s[warp][lane] = wgt[q];
+        if (dom) wex_s[warp][lane] = wex[q];
+        __syncwarp();
+        if (q > 0) {
+#pragma unroll
+          for (int u = 0; u < 32; ++u)
+            o[u] = (lane < D4 && q * 32 + u < S)
+                       ? __ldcg(po4 + (size_t)(q * 32 + u) * split_stride + (size_t)r * D4 + lane)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < 32; ++u) {
+          const float wu = wts_s[warp][u];
+          if (wu != 0.f) {
+            acc.x = fmaf(o[u].x, wu, acc.x);
+            acc.y = fmaf(o[u].y, wu, acc.y);
+            acc.z = fmaf(o[u].z, wu, acc.z);
+            acc.w = fmaf(o[u].w, wu, acc.w);
+          }
+        }
+        if (dom) {
+#pragma unroll
+          for (int u = 0; u < 32; ++u) {
+            const float wx = wex_s[warp][u];
+            if (wx != 0.f) {
+              acx.x = fmaf(o[u].x, wx, acx.x);
+              acx.y = fmaf(o[u].y, wx, acx.y);
+              acx.z = fmaf(o[u].z, wx, acx.z);
+              acx.w = fmaf(o[u].w, wx, acx.w);
+            }
+          }
+        }
+      }
+      const float inv = 1.0f / L;
+      a = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+      if (lane >= D4) a = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (!shift_warp && lane < D4) reinterpret_cast<float4*>(p.a + ro * d)[lane] = a;
+      if (dom && lane < D4) reinterpret_cast<float4*>(p.dom_o + ro * d)[lane] = acx;
+    }
+    if (!shift_warp && lane == 0) {
+      p.m2[ro] = M;
+      p.l[ro] = L;
+      // exported: log-sum-exp of the natural-unit logits, log(L) + m ln 2
+      p.m[ro] = (M + log2f(L)) * 0.69314718055994531f;
+      if (!stats_only) {
+        p.dom_s[ro] = sstar;
+        p.dom_l[ro] = Lx;
+      }
+    }
+  }
+  if (stats_only) {
+    if (live && !shift_warp && lane == 0 && (!(L > 0.f) || !isfinite(L)))
+      atomicOr(p.status, DROPKV_FLAG_NONFINITE | DROPKV_FLAG_NONFINITE_STATS);
+    return;
+  }
+  if (shift_warp) {
+    // c = bf16(a of row 0) when it is large (|c|^2 > 2 d), else 0
+    const __nv_bfloat162 c01 = __floats2bfloat162_rn(a.x, a.y), c23 = __floats2bfloat162_rn(a.z, a.w);
+    const float2 f01 = __bfloat1622float2(c01), f23 = __bfloat1622float2(c23);
+    const float cc = warp_sum(f01.x * f01.x + f01.y * f01.y + f23.x * f23.x + f23.y * f23.y);
+    const bool shift = cc > 2.0f * (float)d;
+    reinterpret_cast<float4*>(c_s)[lane] = shift ? make_float4(f01.x, f01.y, f23.x, f23.y) : make_float4(0.f, 0.f, 0.f, 0.f);
+    if (lane == 0) shift_s = shift ? 1 : 0;
+  }
+  __syncthreads();
+  if (shift_warp) {
+    if (blockIdx.x == 0) {
+      reinterpret_cast<float4*>(p.cvec + (size_t)unit * kDPad)[lane] = reinterpret_cast<const float4*>(c_s)[lane];
+      if (lane == 0) p.cflag[unit] = shift_s;
+    }
+    return;
+  }
   __nv_bfloat16* ahl = p.ahl + (size_t)unit * 2 * kMaxR * kDPad;
-  if (r >= R) {
+  if (!live) {
     // padding rows of the MMA operand: zero (32 lanes x 4 columns = 128)
     reinterpret_cast<uint2*>(ahl + (size_t)r * kDPad)[lane] = make_uint2(0u, 0u);
     reinterpret_cast<uint2*>(ahl + (size_t)(kMaxR + r) * kDPad)[lane] = make_uint2(0u, 0u);
     return;
   }
-  const float2* ml = reinterpret_cast<const float2*>(p.part_ml) + (size_t)unit * p.splits * R;
-  const float4* po4 = reinterpret_cast<const float4*>(p.part_o + (size_t)unit * p.splits * R * d);
-  const size_t split_stride = (size_t)R * D4;
-  // one round trip: the (m, l) of every split and the O column of the first
-  // 32 splits are all requested before any is used (the O partial of a split
-  // without visible keys is never written; its weight is 0 and it is dropped
-  // by a select, not a multiply, so whatever it holds cannot leak in)
-  float2 v[kMergeSplitRegs];
-#pragma unroll
-  for (int q = 0; q < kMergeSplitRegs; ++q) {
-    const int s = q * 32 + lane;
-    v[q] = (s < S) ? __ldcg(ml + (size_t)s * R + r) : make_float2(-INFINITY, 0.f);
-  }
-  const bool stats_only = p.kind == kKindSnapKV;   // no O partials were written
-  float4 o[32];
-#pragma unroll
-  for (int u = 0; u < 32; ++u)
-    o[u] = (!stats_only && lane < D4 && u < S) ? __ldcg(po4 + (size_t)u * split_stride + (size_t)r * D4 + lane)
-                                               : make_float4(0.f, 0.f, 0.f, 0.f);
-  float M = -INFINITY;
-#pragma unroll
-  for (int q = 0; q < kMergeSplitRegs; ++q)
-    if (v[q].y > 0.f) M = fmaxf(M, v[q].x);
-#pragma unroll
-  for (int o2 = 16; o2 > 0; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o2));
-  float wgt[kMergeSplitRegs];
-  float L = 0.f;
-#pragma unroll
-  for (int q = 0; q < kMergeSplitRegs; ++q) {
-    wgt[q] = (v[q].y > 0.f) ? exp2f(v[q].x - M) : 0.f;
-    L = fmaf(v[q].y, wgt[q], L);
-  }
-  L = warp_sum(L);
-  if (stats_only) {
-    if (lane == 0) {
-      const size_t o2 = (size_t)unit * R + r;
-      p.m2[o2] = M;
-      p.l[o2] = L;
-      p.m[o2] = (M + log2f(L)) * 0.69314718055994531f;
-      if (!(L > 0.f) || !isfinite(L)) atomicOr(p.status, DROPKV_FLAG_NONFINITE | DROPKV_FLAG_NONFINITE_STATS);
-    }
-    return;
-  }
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-  for (int q = 0; q < kMergeSplitRegs; ++q) {
-    if (q * 32 >= S) break;
-    __syncwarp();
-    wts_s[warp][lane] = wgt[q];
-    __syncwarp();
-    if (q > 0) {
-#pragma unroll
-      for (int u = 0; u < 32; ++u)
-        o[u] = (lane < D4 && q * 32 + u < S)
-                   ? __ldcg(po4 + (size_t)(q * 32 + u) * split_stride + (size_t)r * D4 + lane)
-                   : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-#pragma unroll
-    for (int u = 0; u < 32; ++u) {
-      const float wu = wts_s[warp][u];
-      if (wu != 0.f) {
-        acc.x = fmaf(o[u].x, wu, acc.x);
-        acc.y = fmaf(o[u].y, wu, acc.y);
-        acc.z = fmaf(o[u].z, wu, acc.z);
-        acc.w = fmaf(o[u].w, wu, acc.w);
-      }
-    }
-  }
-  const float inv = 1.0f / L;
-  const float4 a = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-  if (lane < D4) reinterpret_cast<float4*>(p.a + ((size_t)unit * R + r) * d)[lane] = a;
-  const float aa = warp_sum(lane < D4 ? a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w : 0.f);
-  // hi/lo bf16 split of the row (columns >= d are zero)
+  const float4 c = reinterpret_cast<const float4*>(c_s)[lane];   // zero past d
+  const float4 ap = make_float4(a.x - c.x, a.y - c.y, a.z - c.z, a.w - c.w);
+  // K = |a'|^2 + 2 a'.c
+  const float K = warp_sum(ap.x * (ap.x + 2.f * c.x) + ap.y * (ap.y + 2.f * c.y) + ap.z * (ap.z + 2.f * c.z) +
+                           ap.w * (ap.w + 2.f * c.w));
   uint32_t h01, l01, h23, l23;
-  split_hi_lo(a.x, a.y, h01, l01);
-  split_hi_lo(a.z, a.w, h23, l23);
-  if (lane >= D4) h01 = l01 = h23 = l23 = 0u;
+  split_hi_lo(ap.x, ap.y, h01, l01);
+  split_hi_lo(ap.z, ap.w, h23, l23);
   reinterpret_cast<uint2*>(ahl + (size_t)r * kDPad)[lane] = make_uint2(h01, h23);
   reinterpret_cast<uint2*>(ahl + (size_t)(kMaxR + r) * kDPad)[lane] = make_uint2(l01, l23);
   if (lane == 0) {
-    const size_t o = (size_t)unit * R + r;
-    p.aa[o] = aa;
-    p.m2[o] = M;
-    p.l[o] = L;
-    // exported: log-sum-exp of the natural-unit logits, log(L) + m ln 2
-    p.m[o] = (M + log2f(L)) * 0.69314718055994531f;
-    if (!(L > 0.f) || !isfinite(L) || !isfinite(aa))
+    p.aa[ro] = K;
+    if (!(L > 0.f) || !isfinite(L) || !isfinite(K))
       atomicOr(p.status, DROPKV_FLAG_NONFINITE | DROPKV_FLAG_NONFINITE_STATS);
   }
 }
@@ -536,6 +634,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the register budget of ten warps.
     constexpr bool kRefSmem = NR > 32;
     float lsum[HR], mr[kRefSmem ? 1 : HR];
+    // Largest e of each row pair (r0 + 2q, r0 + 2q + 1), kept as the bf16 hi
+    // parts the P operand is built from (one max per pair and token): the
+    // merge finds from it the split that holds a row's largest probability
+    // and whether that key dominates the row.
+    uint32_t emax2[STATS ? 1 : HR / 2];
+#pragma unroll
+    for (int q = 0; q < (STATS ? 1 : HR / 2); ++q) emax2[q] = 0u;
 #pragma unroll
     for (int r = 0; r < HR; ++r) lsum[r] = 0.f;
 #pragma unroll
@@ -596,6 +701,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float nm = fmaxf(fmaxf(fmaxf(S.red[0][rr], S.red[1][rr]), fmaxf(S.red[2][rr], S.red[3][rr])), old);
           factor[r] = (old == -INFINITY) ? 0.f : ex2_approx(old - nm);
           lsum[r] *= factor[r];
+          if (!STATS && (r & 1)) emax2[r >> 1] = scale_bf16x2(emax2[r >> 1], factor[r - 1], factor[r]);
           if constexpr (kRefSmem) {
             if (wq == 0 && lane == 0) S.mnew[rr] = nm;
           } else {
@@ -648,6 +754,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           lsum[r] += e0;
           lsum[r + 1] += e1;
           split_hi_lo(e0, e1, hp[q], lp[q]);
+          emax2[c8 * 4 + q] = max_bf16x2(emax2[c8 * 4 + q], hp[q]);
         }
         const uint32_t off = interleave_mn_offset(tok, r0 + c8 * 8, NR);
         *reinterpret_cast<uint4*>(phi + off) = make_uint4(hp[0], hp[1], hp[2], hp[3]);
@@ -693,6 +800,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float v = warp_sum(lsum[r]);
       if (lane == 0) S.red[wq][r0 + r] = v;
     }
+    if constexpr (!STATS) {
+#pragma unroll
+      for (int q = 0; q < HR / 2; ++q) {
+        const uint32_t lo = __reduce_max_sync(0xffffffffu, emax2[q] & 0xFFFFu);
+        const uint32_t hi = __reduce_max_sync(0xffffffffu, emax2[q] >> 16);
+        if (lane == 0) {
+          S.rmax[wq][r0 + 2 * q] = lo;
+          S.rmax[wq][r0 + 2 * q + 1] = hi;
+        }
+      }
+    }
     if constexpr (!kRefSmem) {
       if (wq == 0 && lane == 0) {
 #pragma unroll
@@ -701,9 +819,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     named_bar(kBarAux, kWorkers);
     if (tid < R) {
-      float* ml = p.part_ml + (part * R + tid) * 2;
-      ml[0] = S.mref[tid];
-      ml[1] = failed ? 0.f : (S.red[0][tid] + S.red[1][tid]) + (S.red[2][tid] + S.red[3][tid]);
+      // (reference, normaliser, largest e relative to the reference (bf16), unused)
+      const uint32_t mx = STATS ? 0u : max(max(S.rmax[0][tid], S.rmax[1][tid]), max(S.rmax[2][tid], S.rmax[3][tid]));
+      reinterpret_cast<float4*>(p.part_ml)[part * R + tid] =
+          make_float4(S.mref[tid], failed ? 0.f : (S.red[0][tid] + S.red[1][tid]) + (S.red[2][tid] + S.red[3][tid]),
+                      __uint_as_float(mx << 16), 0.f);
     }
   }
 
@@ -711,10 +831,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // empty split (past the end of a shorter sequence): publish an empty state
     grid_dep_wait();
     const size_t part = (size_t)unit * p.splits + split;
-    for (int idx = tid; idx < R; idx += kThreads) {
-      p.part_ml[(part * R + idx) * 2] = -INFINITY;
-      p.part_ml[(part * R + idx) * 2 + 1] = 0.f;
-    }
+    for (int idx = tid; idx < R; idx += kThreads)
+      reinterpret_cast<float4*>(p.part_ml)[part * R + idx] = make_float4(-INFINITY, 0.f, 0.f, 0.f);
   }
 
   tc_fence_before();
@@ -727,6 +845,32 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ============================================================== pass 2
+// Score of every token from the merged statistics of pass 1:
+//   s_j = (1/g) sum_r r_r^2 |a_r - v_j|^2,   r_r = e / (L_r - e) = p / (1 - p),
+// with |a_r - v_j|^2 evaluated in a basis shifted by c, the head's mean window
+// output rounded to bf16:  K_r - 2 a'_r.v_j + |v_j - c|^2,  a' = a - c,
+// K_r = |a'_r|^2 + 2 a'_r.c.  The products a'_r.v_j run on the tensor cores
+// (a' split into bf16 hi + lo), |v_j - c|^2 is summed directly from the staged
+// tile, and the shift keeps the expanded form accurate when the values share
+// a large common offset (|v|^2 far above |a - v|^2).
+//
+// Mode of a CTA (chosen by the producer once the merge is done):
+//  - dynamic: no row of the unit is dominated; the unit's CTAs claim its
+//    tiles one at a time from a counter (the merge clears it).
+//  - static: some row of the unit is dominated; every CTA of the unit takes
+//    the tiles pass 1's split of the same index read, so the key a dominated
+//    row hinges on is met by the CTA whose split the merge named.
+//  - dominant: that CTA.  It leaves the dominant (row, key) pairs out of the
+//    scores, accumulates O_rest^T += V^T P^T over its tiles with P = e of
+//    every other visible key (tensor cores, a third TMEM accumulator, P staged
+//    as in pass 1, one tile behind the scores), and at the end forms the window
+//    output without the dominant key, a_rest = (O_other + O_rest) / (L_other +
+//    L_rest), from sums that never contained that key, and adds the key's
+//    exact term p*^2 |a_rest - v*|^2 (Delta = p / (1 - p) (a - v*) equals
+//    p (a_rest - v*)) to its score.  When L_rest <= 2^-53 e*, p* rounds to 1
+//    in double precision: the input is singular and the slot gets +inf.
+enum : int { kModeDynamic = 0, kModeStatic = 1, kModeDominant = 2 };
+
 // SNAP: K only; the V ring's shared memory goes to K.  Its barriers and tile
 // indices stay (the workers learn each tile's index through the V slots), as
 // deep as the K ring but with no data behind them.
@@ -734,34 +878,513 @@ template <int NR, bool SNAP = false>
 struct Pass2Cfg {
   static constexpr int HR = NR / 2;
   static constexpr int KS0 = 2;                     // K is released right after S = K Q^T
-  static constexpr int VS0 = NR <= 32 ? 4 : 3;      // V is held until A.V^T and |v|^2 are done
+  static constexpr int VS0 = NR <= 32 ? 4 : 3;      // V is held until A.V^T and |v - c|^2 are done
   static constexpr int KS = SNAP ? KS0 + VS0 : KS0;
   static constexpr int VS = SNAP ? KS : VS0;        // V slots (tile indices; data only without SNAP)
   static constexpr int kVStages = SNAP ? 0 : VS;    // V ring stages in shared memory
   static constexpr int kQBytes = NR * kDPad * 2;
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + KS * kTileBytes;
-  static constexpr int kOffQ = kOffV + kVStages * kTileBytes;
+  static constexpr int kOffQ = kOffV + kVStages * kTileBytes;   // end of the ring region
   static constexpr int kOffAhi = kOffQ + kQBytes;
   static constexpr int kOffAlo = kOffAhi + kQBytes;
   static constexpr int kOffSmall = kOffAlo + kQBytes;
-  static constexpr uint32_t kTmemCols = (4 * NR <= 64) ? 64u : (4 * NR <= 128 ? 128u : 256u);
+  // S and A.V^T double-buffered, then O_rest (dominant mode)
+  static constexpr uint32_t kCols = SNAP ? 4 * NR : 5 * NR;
+  static constexpr uint32_t kTmemCols = kCols <= 64 ? 64u : kCols <= 128 ? 128u : kCols <= 256 ? 256u : 512u;
   static_assert(KS <= kMaxStages && VS <= kMaxStages, "ring depth");
+};
+
+// Ring of the dominant mode, carved from the same region: fewer stages and
+// one P buffer (bf16 hi, then lo) for O_rest.
+template <int NR>
+struct Pass2Dom {
+  static constexpr int KS = NR <= 32 ? 2 : 1;
+  static constexpr int VS = 3;
+  static constexpr int kPBytes = kTile * NR * 2;
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = KS * kTileBytes;
+  static constexpr int kOffP = kOffV + VS * kTileBytes;
+  static_assert(kOffP + 2 * kPBytes <= Pass2Cfg<NR, false>::kOffQ, "dominant ring exceeds the ring region");
 };
 
 struct Pass2Small {
   uint64_t kfull[kMaxStages], kempty[kMaxStages], vfull[kMaxStages], vempty[kMaxStages];
   int ktile[kMaxStages], vtile[kMaxStages];   // tile held by each ring slot (-1: no more tiles)
-  uint64_t accfull[2], accempty[2], drain, aready;
+  uint64_t accfull[2], accempty[2], drain, aready, pfull, pempty;
   uint32_t tmem_base;
   int abort;
-  float4 rowc[kMaxR];        // per row: (max in log2 units, normaliser L, |a|^2, last visible key as int bits)
-  float4 xch[2][kTile];      // upper-half partials per token (sum r^2 (|a|^2 - 2 a.v), sum r^2, |v|^2 part, singular)
+  int mode;                  // kMode*: written by the producer before it fills the first slot
+  float4 pml[kMaxR / 2];     // per row pair (r, r + 1), r even: (-m_r, -m_r+1, L_r, L_r+1), m in log2 units
+  float2 pk[kMaxR / 2];      // (K_r, K_r+1), K = |a'|^2 + 2 a'.c
+  int pos[kMaxR];            // last key row r sees (tail-aligned causality); -1 for padding rows
+  float4 xch[2][kTile];      // upper-half partials per token (sum r^2 (K - 2 a'.v), sum r^2, |v - c|^2 part, singular)
+  int domf[kMaxR];           // 1: the row's dominant key lies in this CTA's split (dominant mode)
+  int domj[kMaxR];           // position of that key (found while scoring; -1 before)
+  float dome[kMaxR];         // its e
+  alignas(16) float cf[kDPad];   // the shift c (bf16 values) as f32
+  int shift;                 // 1: |v - c|^2 with this c; 0: c = 0 and |v|^2
+  float red[4][kMaxR];       // per-lane-quarter sums (dominant mode)
+  float red2[4][kMaxR];
+  float ltot[kMaxR];
 };
 
 template <int NR, bool SNAP>
 constexpr int pass2_smem_bytes() {
   return Pass2Cfg<NR, SNAP>::kOffSmall + (int)sizeof(Pass2Small) + 1024;
+}
+
+// Splits pass 1 gave a unit of a sequence of length nb (as its grid share
+// computed them).  Warp-collective.
+__device__ __forceinline__ int pass1_splits(const AttnParams& p, int nb) {
+  if (p.even > 0) return p.even;
+  const int tiles = seq_tiles(p, nb);
+  const uint32_t tot = total_tiles(p);
+  const uint32_t extra = (uint32_t)(p.ctas - p.U);
+  const int s = extra ? 1 + (int)(extra * (uint32_t)tiles / tot) : 1;
+  return min(min(p.splits1, tiles), s);
+}
+
+// acc + (v0^2, v1^2) for the bf16 pair w = (v0, v1) (packed f32x2)
+__device__ __forceinline__ uint64_t sq_bf16x2(uint32_t w, uint64_t acc) {
+  const uint64_t v = f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+  return f2_fma(v, v, acc);
+}
+// acc + ((v0 - c0)^2, (v1 - c1)^2) for the bf16 pair w = (v0, v1) (packed
+// f32x2; the differences of bf16 values are exact in fp32)
+__device__ __forceinline__ uint64_t sqdiff_bf16x2(uint32_t w, float c0, float c1, uint64_t acc) {
+  const uint64_t dv = f2_sub(f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u)), f2_pack(c0, c1));
+  return f2_fma(dv, dv, acc);
+}
+
+// TMA producer (one lane): fills the K ring (and the V ring when HAS_V) tile
+// by tile; each slot also carries its tile index, -1 ending the stream.
+// dynamic: tiles claimed from the unit's counter (the first claim is passed
+// in); otherwise the range [t0, t1).  Returns false after a timeout.
+template <int KS, int VS, bool HAS_V>
+__device__ bool p2_produce(uint8_t* sK, uint8_t* sV, Pass2Small& S, const CUtensorMap* tmk, const CUtensorMap* tmv,
+                           uint32_t* ctr, int unit, int ntiles, bool dynamic, int first, int t0, int t1,
+                           uint32_t* status) {
+  int issued = 0;
+  bool ok = true;
+  for (int i = 0;; ++i) {
+    const int ks = i % KS, vs = i % VS;
+    if (i >= KS && !mbar_wait(&S.kempty[ks], ((i / KS) + 1) & 1, &S.abort)) { ok = false; break; }
+    if (i >= VS && !mbar_wait(&S.vempty[vs], ((i / VS) + 1) & 1, &S.abort)) { ok = false; break; }
+    const int tile = dynamic ? (i == 0 ? first : (int)atomicAdd(ctr, 1u)) : (t0 + i < t1 ? t0 + i : ntiles);
+    if (tile >= ntiles) {
+      S.ktile[ks] = -1;
+      S.vtile[vs] = -1;
+      mbar_arrive(&S.kfull[ks]);
+      mbar_arrive(&S.vfull[vs]);
+      break;
+    }
+    S.ktile[ks] = tile;
+    S.vtile[vs] = tile;
+    mbar_arrive_expect_tx(&S.kfull[ks], kTileBytes);
+    tma_load_3d(sK + ks * kTileBytes, tmk, &S.kfull[ks], 0, tile * kTile, unit);
+    tma_load_3d(sK + ks * kTileBytes + kHalfTile, tmk, &S.kfull[ks], 64, tile * kTile, unit);
+    if (!HAS_V) {
+      mbar_arrive(&S.vfull[vs]);
+    } else {
+      mbar_arrive_expect_tx(&S.vfull[vs], kTileBytes);
+      tma_load_3d(sV + vs * kTileBytes, tmv, &S.vfull[vs], 0, tile * kTile, unit);
+      tma_load_3d(sV + vs * kTileBytes + kHalfTile, tmv, &S.vfull[vs], 64, tile * kTile, unit);
+    }
+    ++issued;
+  }
+  if (!ok) {
+    S.abort = 1;
+    atomicOr(status, DROPKV_FLAG_TIMEOUT);
+    // wait (bounded) for this CTA's copies still in flight
+    for (int i = max(0, issued - KS); i < issued; ++i) mbar_drain(&S.kfull[i % KS], (i / KS) & 1);
+    if (HAS_V)
+      for (int i = max(0, issued - VS); i < issued; ++i) mbar_drain(&S.vfull[i % VS], (i / VS) & 1);
+  }
+  return ok;
+}
+
+// MMA issuer (one lane): S^T = K Q^T into one of two accumulator pairs and
+// A.V^T = V a'_hi^T + V a'_lo^T beside it (not for the SnapKV kind); in the
+// dominant mode also O_rest^T += V^T P^T, one tile behind (the workers write
+// P from the tile's S).  A V stage is released after its last MMA.  Returns
+// false after a timeout.
+template <int NR, int KS, int VS, bool SNAP, bool DOM>
+__device__ bool p2_mma(const uint8_t* sK, const uint8_t* sV, const uint8_t* sP, Pass2Small& S, uint32_t tmem,
+                       uint32_t qaddr, uint32_t ahi, uint32_t alo) {
+  const uint32_t idS = umma_idesc_bf16(128, NR, 0, 0);
+  const uint32_t idO = umma_idesc_bf16(128, NR, 1, 1);
+  const uint32_t tO = tmem + 4 * NR;
+  auto pv = [&](int t) -> bool {
+    if (!mbar_wait(&S.pfull, t & 1, &S.abort)) return false;
+    tc_fence_after();
+    const uint32_t vb = smem_addr(sV + (t % VS) * kTileBytes);
+    const uint32_t phi = smem_addr(sP), plo = smem_addr(sP + kTile * NR * 2);
+#pragma unroll
+    for (int s = 0; s < 8; ++s)
+      umma_bf16(tO, desc_mnmajor_sw128(vb, kTile, s), desc_mnmajor_interleave(phi, NR, s), idO, (t > 0 || s > 0));
+#pragma unroll
+    for (int s = 0; s < 8; ++s)
+      umma_bf16(tO, desc_mnmajor_sw128(vb, kTile, s), desc_mnmajor_interleave(plo, NR, s), idO, 1);
+    umma_commit(&S.pempty);
+    umma_commit(&S.vempty[t % VS]);
+    return true;
+  };
+  int i = 0;
+  for (;; ++i) {
+    const int ks = i % KS, vs = i % VS, ab = i & 1;
+    const uint32_t dS = tmem + ab * 2 * NR, dAV = dS + NR;
+    if (!mbar_wait(&S.kfull[ks], (i / KS) & 1, &S.abort)) return false;
+    if (*reinterpret_cast<volatile int*>(&S.ktile[ks]) < 0) break;     // no more tiles
+    if (i >= 2 && !mbar_wait(&S.accempty[ab], ((i >> 1) + 1) & 1, &S.abort)) return false;
+    tc_fence_after();
+    const uint32_t kb = smem_addr(sK + ks * kTileBytes);
+#pragma unroll
+    for (int s = 0; s < 8; ++s)
+      umma_bf16(dS, desc_kmajor_sw128(kb, kTile, s), desc_kmajor_sw128(qaddr, NR, s), idS, s > 0);
+    umma_commit(&S.kempty[ks]);
+    if (SNAP) {
+      umma_commit(&S.accfull[ab]);
+      continue;
+    }
+    if (i == 0 && !mbar_wait(&S.aready, 0, &S.abort)) return false;
+    if (!mbar_wait(&S.vfull[vs], (i / VS) & 1, &S.abort)) return false;
+    tc_fence_after();
+    const uint32_t vb = smem_addr(sV + vs * kTileBytes);
+#pragma unroll
+    for (int s = 0; s < 8; ++s)
+      umma_bf16(dAV, desc_kmajor_sw128(vb, kTile, s), desc_kmajor_sw128(ahi, NR, s), idS, s > 0);
+#pragma unroll
+    for (int s = 0; s < 8; ++s)
+      umma_bf16(dAV, desc_kmajor_sw128(vb, kTile, s), desc_kmajor_sw128(alo, NR, s), idS, 1);
+    if (!DOM) umma_commit(&S.vempty[vs]);
+    umma_commit(&S.accfull[ab]);
+    if (DOM && i > 0 && !pv(i - 1)) return false;
+  }
+  if (DOM && i > 0 && !pv(i - 1)) return false;
+  return true;
+}
+
+// Worker prologue (after the merge): the merged a' = a - c (bf16 hi + lo,
+// the A.V^T operand), the per-row constants, the head's shift c and the
+// dominated rows whose key lies in this CTA's split.
+template <int NR, bool SNAP>
+__device__ void p2_prologue(uint8_t* sAhi, uint8_t* sAlo, Pass2Small& S, const AttnParams& p, int unit, int split,
+                            int nb, int tid) {
+  const int R = p.R;
+  const size_t rowbase = (size_t)unit * R;
+  if (!SNAP) {
+    const __nv_bfloat16* ahl = p.ahl + (size_t)unit * 2 * kMaxR * kDPad;
+    stage_rows_sw128(sAhi, ahl, NR, NR, kDPad, kDPad, tid, kWorkers);
+    stage_rows_sw128(sAlo, ahl + kMaxR * kDPad, NR, NR, kDPad, kDPad, tid, kWorkers);
+    if (tid < kDPad) S.cf[tid] = p.cvec[(size_t)unit * kDPad + tid];
+    if (tid == 0) S.shift = p.cflag[unit];
+    fence_proxy_async_smem();
+  }
+  if (tid < kMaxR) {
+    const bool real = tid < R;
+    const size_t o = rowbase + tid;
+    float* pm = reinterpret_cast<float*>(&S.pml[tid >> 1]);
+    pm[tid & 1] = real ? -p.m2[o] : 0.f;
+    pm[2 + (tid & 1)] = real ? p.l[o] : 1.f;
+    reinterpret_cast<float*>(&S.pk[tid >> 1])[tid & 1] = (!SNAP && real) ? p.aa[o] : 0.f;
+    S.pos[tid] = real ? nb - p.w + (tid % p.w) : -1;
+    S.domf[tid] = (!SNAP && real && p.dom_s[o] == split) ? 1 : 0;
+    S.domj[tid] = -1;
+  }
+}
+
+// Score workers: thread (quarter wq, half) owns token wq*32 + lane of each
+// tile, rows [r0, r0 + HR) and columns [64 half, 64 half + 64) of |v - c|^2;
+// the upper half hands its partial sums to the lower half, which writes the
+// score.  DOM: the dominant mode (P for O_rest, the dominant keys' terms at the
+// end).  Returns true when a wait gave up.
+template <int NR, int VS, bool SNAP, bool DOM>
+__device__ bool p2_work(uint8_t* sV, uint8_t* sP, Pass2Small& S, const AttnParams& p, uint32_t tmem, int unit,
+                        int nb, int tid, uint32_t& flags) {
+  constexpr int HR = NR / 2;
+  constexpr int kPBytes = kTile * NR * 2;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int wq = warp & 3, half = warp >> 2;
+  const int tok = wq * 32 + lane;
+  const int r0 = half * HR;
+  const int R = p.R;
+  const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+  uint32_t rowmask = 0, dommask = 0;
+#pragma unroll
+  for (int r = 0; r < HR; ++r) rowmask |= (uint32_t)(r0 + r < R) << r;
+  if (DOM) {
+#pragma unroll
+    for (int r = 0; r < HR; ++r) dommask |= (uint32_t)S.domf[r0 + r] << r;
+  }
+  float lrest[DOM ? HR : 1];
+#pragma unroll
+  for (int r = 0; r < (DOM ? HR : 1); ++r) lrest[r] = 0.f;
+  const float scale = p.scale_log2;
+  const float inv_g = 1.0f / (float)p.g;
+  const int all_see = nb - p.w;
+  const bool shifted = !SNAP && S.shift != 0;
+  float* raw = p.raw + (size_t)unit * p.n_max;
+  bool failed = false;
+  for (int i = 0;; ++i) {
+    const int vs = i % VS, ab = i & 1;
+    // the V slot carries the tile index (and, in the SnapKV mode, nothing else)
+    bool ok = __all_sync(0xffffffffu, mbar_wait(&S.vfull[vs], (i / VS) & 1, &S.abort));
+    const int tile = ok ? *reinterpret_cast<volatile int*>(&S.vtile[vs]) : 0;
+    const bool stop = ok && tile < 0;             // no more tiles (the same slot for every worker)
+    const int tile0 = max(tile, 0) * kTile;
+    const int j = tile0 + tok;
+    const bool full = tile0 + kTile - 1 <= all_see;
+    uint8_t* vrow = sV + vs * kTileBytes + half * kHalfTile + tok * 128;
+    float vvh = 0.f;
+    if (!SNAP && ok && !stop) {
+      // |v - c|^2 (or |v|^2 when the head is not shifted) over this half's 64
+      // columns, two columns per packed instruction; the chunks are visited in
+      // a per-thread rotated order so a warp's reads spread over all banks
+      // (physical chunk pc of swizzled row tok holds columns 8 (pc ^ (tok & 7)) .. + 7)
+      uint64_t acc = 0;
+      if (shifted) {
+        const float* cfh = S.cf + half * 64;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const int pc = (c + tok) & 7, lc = pc ^ (tok & 7);
+          const uint4 w = *reinterpret_cast<const uint4*>(vrow + pc * 16);
+          const float4 c0 = *reinterpret_cast<const float4*>(cfh + lc * 8);
+          const float4 c1 = *reinterpret_cast<const float4*>(cfh + lc * 8 + 4);
+          acc = sqdiff_bf16x2(w.x, c0.x, c0.y, acc);
+          acc = sqdiff_bf16x2(w.y, c0.z, c0.w, acc);
+          acc = sqdiff_bf16x2(w.z, c1.x, c1.y, acc);
+          acc = sqdiff_bf16x2(w.w, c1.z, c1.w, acc);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 w = *reinterpret_cast<const uint4*>(vrow + ((c + tok) & 7) * 16);
+          acc = sq_bf16x2(w.x, acc);
+          acc = sq_bf16x2(w.y, acc);
+          acc = sq_bf16x2(w.z, acc);
+          acc = sq_bf16x2(w.w, acc);
+        }
+      }
+      vvh = f2_lo(acc) + f2_hi(acc);
+    }
+    __syncwarp();
+    if (lane == 0 && !stop) mbar_arrive(&S.vempty[vs]);
+    if (ok && !stop) ok = mbar_wait(&S.accfull[ab], (i >> 1) & 1, &S.abort);
+    ok = __all_sync(0xffffffffu, ok);
+    // dominant mode: the P buffer is free once the previous tile's PV is done
+    if (DOM && ok && !stop && i > 0) ok = __all_sync(0xffffffffu, mbar_wait(&S.pempty, (i - 1) & 1, &S.abort));
+    float A = 0.f, W = 0.f;
+    bool singular = false;
+    if (ok && !stop) {
+      tc_fence_after();
+      const uint32_t tS = tmem + lane_base + ab * 2 * NR + r0, tAV = tS + NR;
+      uint32_t vis = rowmask;
+      if (!full) {
+        uint32_t v = 0;
+        if (j < nb) {
+#pragma unroll
+          for (int r = 0; r < HR; ++r) v |= (uint32_t)(j <= S.pos[r0 + r]) << r;
+        }
+        vis &= v;
+      }
+      if (SNAP) {
+        // SnapKV: A accumulates p_j = e / L over the visible rows
+        float sv[HR];
+        tmem_ld_cols<HR>(tS, sv);
+        tmem_wait_ld();
+#pragma unroll
+        for (int r = 0; r < HR; ++r)
+          if ((vis >> r) & 1u) {
+            const float4 c = S.pml[(r0 + r) >> 1];
+            A = fmaf(ex2_approx(fmaf(sv[r], scale, (r & 1) ? c.y : c.x)), rcp_approx((r & 1) ? c.w : c.z), A);
+          }
+      } else if (!DOM) {
+        // two rows per packed instruction, in groups of 16 rows (fewer live
+        // registers); rows the token is invisible to get e = 0 (their terms
+        // vanish; slots past the sequence are never written)
+        constexpr int CH = HR < 16 ? HR : 16;
+        uint64_t A2 = 0, W2 = 0;
+        const uint64_t scale2 = f2_pack(scale, scale), neg2 = f2_pack(-2.f, -2.f);
+#pragma unroll
+        for (int c0 = 0; c0 < HR; c0 += CH) {
+          float sv[CH], av[CH];
+          tmem_ld_cols<CH>(tS + c0, sv);
+          tmem_ld_cols<CH>(tAV + c0, av);
+          tmem_wait_ld();
+#pragma unroll
+          for (int rr = 0; rr < CH; rr += 2) {
+            const int r = c0 + rr;
+            const float4 ml = S.pml[(r0 + r) >> 1];
+            const float2 kk = S.pk[(r0 + r) >> 1];
+            const uint64_t y = f2_fma(f2_pack(sv[rr], sv[rr + 1]), scale2, f2_pack(ml.x, ml.y));
+            const float e0 = ((vis >> r) & 1u) ? ex2_approx(f2_lo(y)) : 0.f;
+            const float e1 = ((vis >> (r + 1)) & 1u) ? ex2_approx(f2_hi(y)) : 0.f;
+            const uint64_t e2 = f2_pack(e0, e1);
+            const uint64_t den = f2_sub(f2_pack(ml.z, ml.w), e2);         // L (1 - p_j)
+            const float d0 = f2_lo(den), d1 = f2_hi(den);
+            singular |= !(d0 > 0.f) || !(d1 > 0.f);
+            const uint64_t ratio = f2_mul(e2, f2_pack(rcp_approx(d0), rcp_approx(d1)));   // p_j / (1 - p_j)
+            const uint64_t q = f2_mul(ratio, ratio);
+            A2 = f2_fma(q, f2_fma(f2_pack(av[rr], av[rr + 1]), neg2, f2_pack(kk.x, kk.y)), A2);
+            W2 = f2_add(W2, q);
+          }
+        }
+        A = f2_lo(A2) + f2_hi(A2);
+        W = f2_lo(W2) + f2_hi(W2);
+      } else {
+        // dominant mode, in groups of 16 rows like the packed path
+        constexpr int CH = HR < 16 ? HR : 16;
+#pragma unroll
+        for (int c0 = 0; c0 < HR; c0 += CH) {
+        float sv[CH], av[CH];
+        tmem_ld_cols<CH>(tS + c0, sv);
+        tmem_ld_cols<CH>(tAV + c0, av);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c8 = c0 / 8; c8 < (c0 + CH) / 8; ++c8) {
+          uint32_t hp[4], lp[4];
+#pragma unroll
+          for (int q2 = 0; q2 < 4; ++q2) {
+            float pe[2];
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+              const int r = c8 * 8 + 2 * q2 + h2;
+              const bool vr = (vis >> r) & 1u;
+              const float4 ml = S.pml[(r0 + r) >> 1];
+              const float2 kk = S.pk[(r0 + r) >> 1];
+              const float negm = h2 ? ml.y : ml.x, L = h2 ? ml.w : ml.z, K = h2 ? kk.y : kk.x;
+              const float e = vr ? ex2_approx(fmaf(sv[r - c0], scale, negm)) : 0.f;
+              // the dominant key of a row this CTA answers for (p > 1/2: unique)
+              const bool dp = DOM && vr && ((dommask >> r) & 1u) && e > 0.5f * L;
+              if (DOM && dp) {
+                S.domj[r0 + r] = j;
+                S.dome[r0 + r] = e;
+              }
+              pe[h2] = dp ? 0.f : e;
+              if (DOM) lrest[r] += pe[h2];
+              if (vr && !dp) {
+                const float den = L - e;                   // L (1 - p_j)
+                singular |= !(den > 0.f);
+                const float ratio = e * rcp_approx(den);   // p_j / (1 - p_j)
+                const float q = ratio * ratio;
+                A = fmaf(q, fmaf(-2.f, av[r - c0], K), A);
+                W += q;
+              }
+            }
+            if (DOM) split_hi_lo(pe[0], pe[1], hp[q2], lp[q2]);
+          }
+          if (DOM) {
+            const uint32_t off = interleave_mn_offset(tok, r0 + c8 * 8, NR);
+            *reinterpret_cast<uint4*>(sP + off) = make_uint4(hp[0], hp[1], hp[2], hp[3]);
+            *reinterpret_cast<uint4*>(sP + kPBytes + off) = make_uint4(lp[0], lp[1], lp[2], lp[3]);
+          }
+        }
+        }
+        if (DOM && j >= nb) {
+          // slots past the sequence may hold anything (NaN): zero this half of
+          // their V rows so that 0 * NaN never reaches the O_rest accumulator
+          // (the tile's A.V^T has completed and this thread's |v - c|^2 is done)
+#pragma unroll
+          for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(vrow + c * 16) = make_uint4(0, 0, 0, 0);
+        }
+      }
+      tc_fence_before();
+    }
+    if (DOM && ok && !stop) {
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.pfull);
+    }
+    __syncwarp();
+    if (lane == 0 && !stop) mbar_arrive(&S.accempty[ab]);
+    if (half == 1) S.xch[ab][tok] = make_float4(A, W, vvh, singular ? 1.f : 0.f);
+    // one barrier per tile: it carries both "some wait failed" and "no more tiles"
+    if (named_bar_or(kBarWork, kWorkers, !ok || stop)) {
+      if (named_bar_or(kBarAux, kWorkers, !ok)) failed = true;
+      break;
+    }
+    if (SNAP && half == 0 && j < nb) {
+      float s = (A + S.xch[ab][tok].x) * inv_g;
+      if (!isfinite(s)) flags |= DROPKV_FLAG_NONFINITE | DROPKV_FLAG_NONFINITE_SCORE;
+      raw[j] = s;
+    } else if (!SNAP && half == 0 && j < nb) {
+      const float4 o = S.xch[ab][tok];
+      float s = fmaf(vvh + o.z, W + o.y, A + o.x);
+      if (singular || o.w != 0.f) {
+        s = INFINITY;
+        flags |= DROPKV_FLAG_SINGULAR;
+      } else if (!isfinite(s)) {
+        flags |= DROPKV_FLAG_NONFINITE | DROPKV_FLAG_NONFINITE_SCORE;
+      } else {
+        s = fmaxf(s, 0.f) * inv_g;   // the exact value is >= 0; rounding may not make it negative
+      }
+      raw[j] = s;
+    }
+  }
+  if constexpr (DOM) {
+    // The dominant keys' terms.  The MMA warp commits `drain` after its last
+    // MMA (the final PV): a single-phase wait.
+    bool okw = true;
+    if (!failed) okw = __all_sync(0xffffffffu, mbar_wait(&S.drain, 0, &S.abort));
+    if (named_bar_or(kBarWork, kWorkers, failed || !okw)) return true;
+    tc_fence_after();
+    float o[HR];   // O_rest^T: lane = head dimension tok, columns = rows
+    tmem_ld_cols<HR>(tmem + 4 * NR + lane_base + r0, o);
+    tmem_wait_ld();
+    tc_fence_before();
+#pragma unroll
+    for (int r = 0; r < HR; ++r) {
+      const float v = warp_sum(lrest[r]);
+      if (lane == 0) S.red[wq][r0 + r] = v;
+    }
+    named_bar(kBarAux, kWorkers);
+    const size_t rowbase = (size_t)unit * R;
+#pragma unroll
+    for (int r = 0; r < HR; ++r) {
+      if (!((dommask >> r) & 1u)) continue;       // the same in the whole warp
+      const int rr = r0 + r;
+      const float lt = p.dom_l[rowbase + rr] + ((S.red[0][rr] + S.red[1][rr]) + (S.red[2][rr] + S.red[3][rr]));
+      const int jst = S.domj[rr];
+      float sq = 0.f;
+      if (jst >= 0 && tok < p.d) {
+        const float ar = (p.dom_o[(rowbase + rr) * p.d + tok] + o[r]) / lt;
+        const float vst = __bfloat162float(p.v[((size_t)unit * p.n_max + jst) * p.d + tok]);
+        const float df = ar - vst;
+        sq = df * df;
+      }
+      sq = warp_sum(sq);
+      if (lane == 0) {
+        S.red2[wq][rr] = sq;
+        if (wq == 0) S.ltot[rr] = lt;
+      }
+    }
+    named_bar(kBarAux, kWorkers);
+    if (tid == 0) {
+      // rows in order, one thread: several rows may share a dominant key
+      for (int rr = 0; rr < R; ++rr) {
+        if (!S.domf[rr]) continue;
+        // no key above half the mass: the row is not dominated after all (the
+        // merge's threshold is only good to bf16) and was scored as usual
+        const int jst = S.domj[rr];
+        if (jst < 0) continue;
+        const float es = S.dome[rr];
+        const float lt = S.ltot[rr];
+        if (!(lt > es * 0x1p-53f)) {     // p* = e* / (e* + L_rest) rounds to 1 in double precision
+          raw[jst] = INFINITY;
+          flags |= DROPKV_FLAG_SINGULAR;
+          continue;
+        }
+        const float pr = es / (es + lt);
+        const float dist = (S.red2[0][rr] + S.red2[1][rr]) + (S.red2[2][rr] + S.red2[3][rr]);
+        const float cur = raw[jst];
+        const float nv = cur + pr * pr * dist * inv_g;
+        if (!isfinite(nv) && !isinf(cur)) flags |= DROPKV_FLAG_NONFINITE | DROPKV_FLAG_NONFINITE_SCORE;
+        raw[jst] = nv;
+      }
+    }
+  }
+  return failed;
 }
 
 // SNAP: the SnapKV score (1/g) sum_r p_r from K alone -- no V, no A V^T.
@@ -770,11 +1393,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     score_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                  const AttnParams p) {
   using C = Pass2Cfg<NR, SNAP>;
-  constexpr int HR = C::HR;
+  using D = Pass2Dom<NR>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = align1024(smem_raw);
-  uint8_t* sK = sm + C::kOffK;
-  uint8_t* sV = sm + C::kOffV;
   uint8_t* sQ = sm + C::kOffQ;
   uint8_t* sAhi = sm + C::kOffAhi;
   uint8_t* sAlo = sm + C::kOffAlo;
@@ -787,21 +1408,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int b = unit / p.Hkv, h = unit - b * p.Hkv;
   if (nb < p.w || nb > p.n_max) return;      // flagged by pass 1
   const int R = p.R;
-  // The CTAs of a KV head claim its tiles one at a time from a counter (the
-  // merge kernel clears it), so they all finish within about a tile of each
-  // other whatever bandwidth each SM gets.  The producer claims a tile only
-  // once both of its ring slots are free, and passes its index (or -1: no
-  // more tiles) to the MMA warp through the K slot and to the workers
-  // through the V slot.
   const int ntiles = ceil_div(nb, kTile);
 
   if (tid == 0) {
-    for (int i = 0; i < C::KS; ++i) { mbar_init(&S.kfull[i], 1); mbar_init(&S.kempty[i], 1); }
-    for (int i = 0; i < C::VS; ++i) { mbar_init(&S.vfull[i], 1); mbar_init(&S.vempty[i], kWorkerWarps + (SNAP ? 0 : 1)); }
+    for (int i = 0; i < kMaxStages; ++i) {
+      mbar_init(&S.kfull[i], 1);
+      mbar_init(&S.kempty[i], 1);
+      mbar_init(&S.vfull[i], 1);
+      mbar_init(&S.vempty[i], kWorkerWarps + (SNAP ? 0 : 1));
+    }
     for (int i = 0; i < 2; ++i) { mbar_init(&S.accfull[i], 1); mbar_init(&S.accempty[i], kWorkerWarps); }
     mbar_init(&S.drain, 1);
     mbar_init(&S.aready, 1);
+    mbar_init(&S.pfull, kWorkerWarps);
+    mbar_init(&S.pempty, 1);
     S.abort = 0;
+    S.mode = kModeDynamic;
     fence_mbar_init();
   }
   if (warp == kMmaWarp) tmem_alloc(&S.tmem_base, C::kTmemCols);
@@ -826,80 +1448,45 @@ __global__ void __launch_bounds__(kThreads, 1)
   grid_dep_launch();
 
   if (warp == kProducerWarp) {
-    // TMA producer (lane 0): claims a tile, then streams its K and V
-    grid_dep_wait();                              // the tile counter is cleared by the merge
+    grid_dep_wait();                              // the merge's outputs and the cleared tile counter
+    int mode = kModeDynamic, first = 0, t0 = 0, t1 = 0;
+    if (lane == 0) first = (int)atomicAdd(p.tile_ctr + unit, 1u);   // in flight with the loads below
+    if constexpr (!SNAP) {
+      const int* ds = p.dom_s + (size_t)unit * R;
+      const int s0 = lane < R ? ds[lane] : -1;
+      const int s1 = lane + 32 < R ? ds[lane + 32] : -1;
+      if (__any_sync(0xffffffffu, s0 >= 0 || s1 >= 0)) {
+        const int ns1 = pass1_splits(p, nb);
+        mode = __any_sync(0xffffffffu, s0 == wk.split || s1 == wk.split) ? kModeDominant : kModeStatic;
+        if (wk.split < ns1) {
+          t0 = (int)((uint32_t)wk.split * (uint32_t)ntiles / (uint32_t)ns1);
+          t1 = (int)((uint32_t)(wk.split + 1) * (uint32_t)ntiles / (uint32_t)ns1);
+        }
+      }
+    }
     if (lane == 0) {
-      int issued = 0;
-      bool ok = true;
-      for (int i = 0;; ++i) {
-        const int ks = i % C::KS, vs = i % C::VS;
-        if (i >= C::KS && !mbar_wait(&S.kempty[ks], ((i / C::KS) + 1) & 1, &S.abort)) { ok = false; break; }
-        if (i >= C::VS && !mbar_wait(&S.vempty[vs], ((i / C::VS) + 1) & 1, &S.abort)) { ok = false; break; }
-        const int tile = (int)atomicAdd(p.tile_ctr + unit, 1u);
-        if (tile >= ntiles) {
-          S.ktile[ks] = -1;
-          S.vtile[vs] = -1;
-          mbar_arrive(&S.kfull[ks]);
-          mbar_arrive(&S.vfull[vs]);
-          break;
-        }
-        S.ktile[ks] = tile;
-        S.vtile[vs] = tile;
-        mbar_arrive_expect_tx(&S.kfull[ks], kTileBytes);
-        tma_load_3d(sK + ks * kTileBytes, &tmk, &S.kfull[ks], 0, tile * kTile, unit);
-        tma_load_3d(sK + ks * kTileBytes + kHalfTile, &tmk, &S.kfull[ks], 64, tile * kTile, unit);
-        if (SNAP) {
-          mbar_arrive(&S.vfull[vs]);
-        } else {
-          mbar_arrive_expect_tx(&S.vfull[vs], kTileBytes);
-          tma_load_3d(sV + vs * kTileBytes, &tmv, &S.vfull[vs], 0, tile * kTile, unit);
-          tma_load_3d(sV + vs * kTileBytes + kHalfTile, &tmv, &S.vfull[vs], 64, tile * kTile, unit);
-        }
-        ++issued;
-      }
-      if (!ok) {
-        S.abort = 1;
-        atomicOr(p.status, DROPKV_FLAG_TIMEOUT);
-        // wait (bounded) for this CTA's copies still in flight
-        for (int i = max(0, issued - C::KS); i < issued; ++i) mbar_drain(&S.kfull[i % C::KS], (i / C::KS) & 1);
-        if (!SNAP)
-          for (int i = max(0, issued - C::VS); i < issued; ++i) mbar_drain(&S.vfull[i % C::VS], (i / C::VS) & 1);
-      }
+      S.mode = mode;                              // published by the first slot's arrival
+      if (!SNAP && mode == kModeDominant)
+        p2_produce<D::KS, D::VS, true>(sm + D::kOffK, sm + D::kOffV, S, &tmk, &tmv, p.tile_ctr + unit, unit,
+                                       ntiles, false, 0, t0, t1, p.status);
+      else
+        p2_produce<C::KS, C::VS, !SNAP>(sm + C::kOffK, sm + C::kOffV, S, &tmk, &tmv, p.tile_ctr + unit, unit,
+                                        ntiles, mode == kModeDynamic, first, t0, t1, p.status);
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
-      const uint32_t idS = umma_idesc_bf16(128, NR, 0, 0);
       const uint32_t qaddr = smem_addr(sQ), ahi = smem_addr(sAhi), alo = smem_addr(sAlo);
-      bool ok = true;
-      for (int i = 0;; ++i) {
-        const int ks = i % C::KS, vs = i % C::VS, ab = i & 1;
-        const uint32_t dS = tmem + ab * 2 * NR, dAV = dS + NR;
-        if (!mbar_wait(&S.kfull[ks], (i / C::KS) & 1, &S.abort)) { ok = false; break; }
-        if (*reinterpret_cast<volatile int*>(&S.ktile[ks]) < 0) break;     // no more tiles
-        if (i >= 2 && !mbar_wait(&S.accempty[ab], ((i >> 1) + 1) & 1, &S.abort)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t kb = smem_addr(sK + ks * kTileBytes);
-#pragma unroll
-        for (int s = 0; s < 8; ++s)
-          umma_bf16(dS, desc_kmajor_sw128(kb, kTile, s), desc_kmajor_sw128(qaddr, NR, s), idS, s > 0);
-        umma_commit(&S.kempty[ks]);
-        if (SNAP) {
-          umma_commit(&S.accfull[ab]);
-          continue;
-        }
-        if (i == 0 && !mbar_wait(&S.aready, 0, &S.abort)) { ok = false; break; }
-        if (!mbar_wait(&S.vfull[vs], (i / C::VS) & 1, &S.abort)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t vb = smem_addr(sV + vs * kTileBytes);
-#pragma unroll
-        for (int s = 0; s < 8; ++s)
-          umma_bf16(dAV, desc_kmajor_sw128(vb, kTile, s), desc_kmajor_sw128(ahi, NR, s), idS, s > 0);
-#pragma unroll
-        for (int s = 0; s < 8; ++s)
-          umma_bf16(dAV, desc_kmajor_sw128(vb, kTile, s), desc_kmajor_sw128(alo, NR, s), idS, 1);
-        umma_commit(&S.vempty[vs]);
-        umma_commit(&S.accfull[ab]);
+      // the first slot (stage 0 in every layout) brings the mode
+      bool ok = mbar_wait(&S.kfull[0], 0, &S.abort);
+      if (ok) {
+        const int mode = *reinterpret_cast<volatile int*>(&S.mode);
+        if (!SNAP && mode == kModeDominant)
+          ok = p2_mma<NR, D::KS, D::VS, false, true>(sm + D::kOffK, sm + D::kOffV, sm + D::kOffP, S, tmem, qaddr,
+                                                     ahi, alo);
+        else
+          ok = p2_mma<NR, C::KS, C::VS, SNAP, false>(sm + C::kOffK, sm + C::kOffV, nullptr, S, tmem, qaddr, ahi,
+                                                     alo);
       }
       if (!ok) {
         failed = true;
@@ -911,127 +1498,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else if (warp < kWorkerWarps) {
-    // ---------------------------------------------------- score workers
-    // Thread (quarter wq, half) owns token wq*32 + lane, rows [r0, r0 + HR)
-    // and columns [64 half, 64 half + 64) of |v|^2; the upper half hands its
-    // partial sums to the lower half, which writes the score.
-    //   s = (1/g) sum_r r_r^2 (|a_r|^2 - 2 a_r.v + |v|^2),  r_r = e / (L_r - e) = p/(1-p)
-    const int wq = warp & 3, half = warp >> 2;
-    const int tok = wq * 32 + lane;
-    const int r0 = half * HR;
-    const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
-    uint32_t rowmask = 0;
-#pragma unroll
-    for (int r = 0; r < HR; ++r) rowmask |= (uint32_t)(r0 + r < R) << r;
-    const float scale = p.scale_log2;
-    const float inv_g = 1.0f / (float)p.g;
-    const int all_see = nb - p.w;
-    float* raw = p.raw + (size_t)unit * p.n_max;
     uint32_t flags = 0;
-    grid_dep_wait();                              // a, |a|^2, m and L come from the merge
-    {
-      if (!SNAP) {
-        const __nv_bfloat16* ahl = p.ahl + (size_t)unit * 2 * kMaxR * kDPad;
-        stage_rows_sw128(sAhi, ahl, NR, NR, kDPad, kDPad, tid, kWorkers);
-        stage_rows_sw128(sAlo, ahl + kMaxR * kDPad, NR, NR, kDPad, kDPad, tid, kWorkers);
-        fence_proxy_async_smem();
-      }
-      if (tid < kMaxR) {
-        const bool real = tid < R;
-        const size_t o = (size_t)unit * R + tid;
-        S.rowc[tid] = make_float4(real ? p.m2[o] : 0.f, real ? p.l[o] : 1.f, (real && !SNAP) ? p.aa[o] : 0.f,
-                                  __int_as_float(real ? nb - p.w + (tid % p.w) : -1));
-      }
-      named_bar(kBarWork, kWorkers);
-      if (tid == 0) mbar_arrive(&S.aready);
-    }
-    for (int i = 0;; ++i) {
-      const int vs = i % C::VS, ab = i & 1;
-      // the V slot carries the tile index (and, in the SnapKV mode, nothing else)
-      bool ok = __all_sync(0xffffffffu, mbar_wait(&S.vfull[vs], (i / C::VS) & 1, &S.abort));
-      const int tile = ok ? *reinterpret_cast<volatile int*>(&S.vtile[vs]) : 0;
-      const bool stop = ok && tile < 0;             // no more tiles (the same slot for every worker)
-      const int tile0 = max(tile, 0) * kTile;
-      const int j = tile0 + tok;
-      const bool full = tile0 + kTile - 1 <= all_see;
-      float vvh = 0.f;
-      if (!SNAP && ok && !stop) {
-        // this half's 64 columns of the staged V row; chunks visited in a
-        // per-thread rotated order so a warp's reads spread over all banks
-        const uint8_t* vrow = sV + vs * kTileBytes + half * kHalfTile + tok * 128;
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          vvh = sumsq_bf16x8(*reinterpret_cast<const uint4*>(vrow + ((c + tok) & 7) * 16), vvh);
-      }
-      __syncwarp();
-      if (lane == 0 && !stop) mbar_arrive(&S.vempty[vs]);
-      if (ok && !stop) ok = mbar_wait(&S.accfull[ab], (i >> 1) & 1, &S.abort);
-      ok = __all_sync(0xffffffffu, ok);
-      float A = 0.f, W = 0.f;
-      bool singular = false;
-      if (ok && !stop) {
-        tc_fence_after();
-        float sv[HR], av[HR];
-        tmem_ld_cols<HR>(tmem + lane_base + ab * 2 * NR + r0, sv);
-        if (!SNAP) tmem_ld_cols<HR>(tmem + lane_base + ab * 2 * NR + NR + r0, av);
-        tmem_wait_ld();
-        tc_fence_before();
-        uint32_t vis = rowmask;
-        if (!full) {
-          uint32_t v = 0;
-          if (j < nb) {
-#pragma unroll
-            for (int r = 0; r < HR; ++r) v |= (uint32_t)(j <= __float_as_int(S.rowc[r0 + r].w)) << r;
-          }
-          vis &= v;
-        }
-#pragma unroll
-        for (int r = 0; r < HR; ++r) {
-          if (SNAP) {
-            // SnapKV: A accumulates p_j = e / L over the visible rows
-            if ((vis >> r) & 1u) {
-              const float4 c = S.rowc[r0 + r];
-              A = fmaf(ex2_approx(fmaf(sv[r], scale, -c.x)), rcp_approx(c.y), A);
-            }
-            continue;
-          }
-          if ((vis >> r) & 1u) {
-            const float4 c = S.rowc[r0 + r];
-            const float e = ex2_approx(fmaf(sv[r], scale, -c.x));
-            const float den = c.y - e;                 // L (1 - p_j)
-            singular |= !(den > 0.f);
-            const float ratio = e * rcp_approx(den);   // p_j / (1 - p_j)
-            const float q = ratio * ratio;
-            A = fmaf(q, fmaf(-2.f, av[r], c.z), A);
-            W += q;
-          }
-        }
-      }
-      __syncwarp();
-      if (lane == 0 && !stop) mbar_arrive(&S.accempty[ab]);
-      if (half == 1) S.xch[ab][tok] = make_float4(A, W, vvh, singular ? 1.f : 0.f);
-      // one barrier per tile: it carries both "some wait failed" and "no more tiles"
-      if (named_bar_or(kBarWork, kWorkers, !ok || stop)) {
-        if (named_bar_or(kBarAux, kWorkers, !ok)) failed = true;
-        break;
-      }
-      if (SNAP && half == 0 && j < nb) {
-        float s = (A + S.xch[ab][tok].x) * inv_g;
-        if (!isfinite(s)) flags |= DROPKV_FLAG_NONFINITE | DROPKV_FLAG_NONFINITE_SCORE;
-        raw[j] = s;
-      } else if (half == 0 && j < nb) {
-        const float4 o = S.xch[ab][tok];
-        float s = fmaf(vvh + o.z, W + o.y, A + o.x);
-        if (singular || o.w != 0.f) {
-          s = INFINITY;
-          flags |= DROPKV_FLAG_SINGULAR;
-        } else if (!isfinite(s)) {
-          flags |= DROPKV_FLAG_NONFINITE | DROPKV_FLAG_NONFINITE_SCORE;
-        } else {
-          s = fmaxf(s, 0.f) * inv_g;   // the exact value is >= 0; rounding may not make it negative
-        }
-        raw[j] = s;
-      }
+    grid_dep_wait();                              // a, m, L and the dominated rows come from the merge
+    p2_prologue<NR, SNAP>(sAhi, sAlo, S, p, unit, wk.split, nb, tid);
+    named_bar(kBarWork, kWorkers);
+    if (tid == 0) mbar_arrive(&S.aready);
+    // the first slot (stage 0 in every layout) brings the mode; every worker
+    // takes the same branch
+    const bool ok0 = mbar_wait(&S.vfull[0], 0, &S.abort);
+    if (named_bar_or(kBarAux, kWorkers, !ok0)) {
+      failed = true;
+    } else {
+      const int mode = *reinterpret_cast<volatile int*>(&S.mode);
+      if (!SNAP && mode == kModeDominant)
+        failed = p2_work<NR, D::VS, false, true>(sm + D::kOffV, sm + D::kOffP, S, p, tmem, unit, nb, tid, flags);
+      else
+        failed = p2_work<NR, C::VS, SNAP, false>(sm + C::kOffV, nullptr, S, p, tmem, unit, nb, tid, flags);
     }
     if (flags) atomicOr(p.status, flags);
   }
@@ -1078,7 +1560,8 @@ cudaError_t launch_window_attention(const AttnParams& p, int NR, const CUtensorM
 }
 
 cudaError_t launch_merge(const AttnParams& p, cudaStream_t st) {
-  return launch_pdl(merge_splits_kernel, dim3(kMaxR / kMergeRows, p.U), dim3(kMergeThreads), 0, st, p);
+  // row groups covering the NR rows of the A.V^T operand (rows past R get zeros)
+  return launch_pdl(merge_splits_kernel, dim3(p.NR / kMergeRows, p.U), dim3(kMergeThreads), 0, st, p);
 }
 
 cudaError_t launch_score(const AttnParams& p, int NR, const CUtensorMap& tk, const CUtensorMap& tv,

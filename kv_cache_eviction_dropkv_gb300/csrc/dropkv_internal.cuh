@@ -39,9 +39,13 @@ struct Geom {
 // Byte offsets of the workspace regions (all 256-byte aligned).
 struct WsPlan {
   size_t m, l, a;                // exported statistics (see dropkv.h)
-  size_t m2, aa;                 // max in log2 units, |a|^2
-  size_t ahl;                    // bf16 [U][2][NR][128]: a split into hi + lo parts
-  size_t part_o, part_ml;        // pass-1 partial states
+  size_t m2;                     // max in log2 units
+  size_t aa;                     // K = |a'|^2 + 2 a'.c per row
+  size_t ahl;                    // bf16 [U][2][64][128]: a' = a - c split into hi + lo parts
+  size_t cvec, cflag;            // f32 [U][128] shift c of each head, i32 [U] 1 when shifted
+  size_t dom_s, dom_l;           // dominated rows: pass-1 split of the dominant key, L of the other splits
+  size_t dom_o;                  // dominated rows: f32 [U][R][d] sum of the other splits' O
+  size_t part_o, part_ml;        // pass-1 partial states (part_ml: m, l, largest logit, unused)
   size_t tile_ctr;               // u32 [U]: pass-2 tile claims (cleared by the merge kernel)
   size_t raw;                    // f32 [U][n_max] raw scores when the caller passes none
   // selection
@@ -70,17 +74,32 @@ WsPlan make_plan(const Geom& g);
 constexpr int kKindDropKV = 0;   // exact single-token output perturbation
 constexpr int kKindSnapKV = 1;   // window sum of attention probabilities
 
+// A window row is "dominated" when its largest attention probability reaches
+// kDomP: then 1 - p of that key and |a - v| are tiny differences of large
+// quantities, and pass 2 takes that key's score from the attention output
+// recomputed without it (see the pass-2 kernel).
+constexpr float kDomP = 0.8f;
+
 struct AttnParams {
   const __nv_bfloat16* q;        // [B][Hq][w][d]
+  const __nv_bfloat16* v;        // [B][Hkv][n_max][d] (pass 2 reads the rows of dominant keys)
   const int32_t* lengths;        // [B] or null
   int B, Hq, Hkv, d, n_max, w, g, R, U;
+  int NR;                        // R rounded up to the MMA width (16, 32 or 64)
   int splits;                    // most CTAs per unit (pass 1: its partial slots per unit)
+  int splits1;                   // pass-1 partial slots per unit (both passes)
   int ctas;                      // CTAs of the pass grid (>= U)
   int even;                      // > 0: every unit gets this many CTAs; 0: shares by length
   float scale_log2;              // log2(e) / sqrt(d)
   // workspace
-  float *m, *l, *a, *m2, *aa;
-  __nv_bfloat16* ahl;
+  float *m, *l, *a, *m2;
+  float* aa;                     // [U][R] K = |a'|^2 + 2 a'.c
+  __nv_bfloat16* ahl;            // [U][2][64][128] a' split into bf16 hi, then lo (rows past R zero)
+  float* cvec;                   // [U][128] shift c (bf16 values; zero when not shifted)
+  int* cflag;                    // [U] 1: the head's scores use the shift
+  int* dom_s;                    // [U][R] pass-1 split holding a dominated row's largest probability, else -1
+  float* dom_l;                  // [U][R] normaliser of the other splits (dominated rows)
+  float* dom_o;                  // [U][R][d] unnormalised output of the other splits (dominated rows)
   float *part_o, *part_ml;
   uint32_t* tile_ctr;            // [U] next unclaimed pass-2 tile of each KV head
   float* raw;                    // raw score output [U][n_max]
@@ -156,6 +175,15 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
+
+// Steps S1-S4 on the caller's workspace (the body of dropkv_score and its
+// variants).  scoring_regions_only: the workspace need only hold the regions
+// scoring uses (the ones ahead of the selection's).
+dropkv_status score_core(const dropkv_shape* shape, const void* q_window, const void* k, const void* v,
+                         const int32_t* lengths, int32_t pool_kernel, int32_t protect, float* scores,
+                         float* raw_scores, void* workspace, size_t workspace_bytes, uint32_t* status,
+                         cudaStream_t stream, cudaEvent_t* ev, PoolParams* defer_pool, int kind,
+                         bool scoring_regions_only);
 
 cudaError_t launch_window_attention(const AttnParams& p, int NR, const CUtensorMap& tk, const CUtensorMap& tv,
                                     int num_ctas_x, cudaStream_t st);

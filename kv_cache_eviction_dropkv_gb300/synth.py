@@ -28,6 +28,14 @@ Recipe (numpy PCG64, one generator per workload, fixed draw order):
   [1, n_b - w), each aligned with one window query q_r of the group (r drawn
   uniformly): key j becomes |k_j| (0.8 q_r/|q_r| + 0.6 w_j), w_j a random unit
   vector orthogonal to q_r (cosine 0.8 with that query).
+* Sink mass (optional, `sink_margin` nats): the sink's target logit is raised
+  by the margin, so each row puts roughly p0 = 1 / (1 + exp(-margin)) of its
+  mass on the sink (margin = ln(p0 / (1 - p0))); 0 keeps the half-mass sink.
+* Value offset (optional, `v_offset` = sigma): after the needles, every KV
+  head draws a per-channel mean mu_c ~ N(0, sigma^2) plus 4 value outlier
+  channels with mu_c = +-4 sigma, added to all of its values (V = mu + N(0, 1)),
+  the common offset real value caches carry; |v|^2 is then far above
+  |a - v|^2.
 * Everything is rounded to bf16 (round to nearest even) once; the GPU and the
   oracle see exactly those bf16 values.  The tiny workload also keeps its
   float32 draws for the oracle's own self-checks.
@@ -141,10 +149,12 @@ def _unit(x: np.ndarray) -> np.ndarray:
 
 
 def make_workload(name: str, seed: Optional[int] = None, n_max: Optional[int] = None,
-                  keep_fp32: Optional[bool] = None) -> Workload:
+                  keep_fp32: Optional[bool] = None, sink_margin: float = 0.0, v_offset: float = 0.0) -> Workload:
     """Build a named workload.  `seed` overrides the workload's seed; `n_max`
     shrinks the sequence (tests use it for reduced sizes; ragged ranges are
-    scaled with it)."""
+    scaled with it).  `sink_margin` raises the sink's logits by that many nats
+    (workloads with a sink); `v_offset` adds a per-head value offset of that
+    per-channel spread (module docstring)."""
     spec = WORKLOADS[name]
     if n_max is not None and n_max != spec.n_max:
         rag = spec.ragged
@@ -182,7 +192,7 @@ def make_workload(name: str, seed: Optional[int] = None, n_max: Optional[int] = 
             for h in range(Hkv):
                 qg = q[b, h * g:(h + 1) * g].reshape(g * w, d).astype(np.float64)
                 sigma2 = ((qg ** 2) * chan_scale[b, h]).sum(axis=1) / d
-                target = math.sqrt(d) * (_lse_estimate(nb, sigma2) + SINK_MARGIN)
+                target = math.sqrt(d) * (_lse_estimate(nb, sigma2) + SINK_MARGIN + sink_margin)
                 # minimum-norm key whose dot product with every window row equals its target
                 k0 = qg.T @ np.linalg.solve(qg @ qg.T, target)
                 k[b, h, 0] = k0.astype(np.float32)
@@ -200,6 +210,14 @@ def make_workload(name: str, seed: Optional[int] = None, n_max: Optional[int] = 
                         wv = _unit(wv)
                         nk = float(np.linalg.norm(k[b, h, j].astype(np.float64)))
                         k[b, h, j] = (nk * (0.8 * u + 0.6 * wv)).astype(np.float32)
+
+    if v_offset:
+        for b in range(B):
+            for h in range(Hkv):
+                mu = rng.normal(0.0, v_offset, d)
+                ch = rng.choice(d, N_OUTLIER_CHANNELS, replace=False)
+                mu[ch] = 4.0 * v_offset * rng.choice([-1.0, 1.0], N_OUTLIER_CHANNELS)
+                v[b, h] += mu.astype(np.float32)
 
     if spec.evict is not None:
         evict = np.full(B, spec.evict, dtype=np.int32)

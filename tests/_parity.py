@@ -11,6 +11,8 @@ within the score tolerance of the oracle's k-th smallest score (the band where
 the k-th and (k+1)-th scores are indistinguishable), and the number kept must
 be exact.
 """
+import math
+
 import numpy as np
 
 RTOL = 2e-3
@@ -110,3 +112,39 @@ def check_kept_layer(kept_gpu, len_gpu, kept_ref, len_ref, final_ref, lengths, e
         assert np.all(band[diff]), "kept sets differ outside the tolerance band (b=%d)" % b
         band_total += int(diff.sum())
     return band_total
+
+
+def deletion_score(q, k, v, lengths, j=0):
+    """Raw score of key j by deletion, in fp64 (the pages' definition of the
+    perturbation: Delta_j = a_{-j} - a = p_j (a_{-j} - v_j), "DropKV: Exact
+    single-entry output-perturbation scoring", Core equation): a_{-j} is the
+    softmax output over the other keys and 1 - p_j their mass, both summed
+    directly, so nothing cancels however close p_j is to 1.  q, k, v are float64
+    arrays [B,Hq,w,d] / [B,Hkv,n,d]; returns [B,Hkv]."""
+    B, Hq, w, d = q.shape
+    Hkv = k.shape[1]
+    g = Hq // Hkv
+    out = np.zeros((B, Hkv))
+    for b in range(B):
+        nb = int(lengths[b])
+        for h in range(Hkv):
+            acc = 0.0
+            for hl in range(g):
+                for t in range(w):
+                    pos = nb - w + t
+                    if j > pos:
+                        continue
+                    qq = q[b, h * g + hl, t]
+                    x = k[b, h, :pos + 1] @ qq / math.sqrt(d)
+                    others = np.arange(pos + 1) != j
+                    xr = x[others]
+                    if xr.size == 0:
+                        return None                        # a single visible key: removal is singular
+                    mr = xr.max()
+                    er = np.exp(xr - mr)
+                    a_rest = er @ v[b, h, :pos + 1][others] / er.sum()
+                    rest = np.exp(mr - x[j]) * er.sum()     # (1 - p_j) / p_j
+                    pj = 1.0 / (1.0 + rest)
+                    acc += pj * pj * float(((a_rest - v[b, h, j]) ** 2).sum())
+            out[b, h] = acc / g
+    return out

@@ -17,6 +17,7 @@ import torch.nn.functional as F
 
 import oracle
 from kv_cache_eviction_dropkv_gb300 import synth
+from tests._parity import deletion_score
 
 GOLDEN = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "pages_values.json")))
 SEEDS = GOLDEN["synthetic_case_seeds"]["value"]
@@ -216,6 +217,26 @@ def test_singular_input_rejected():
     k[0, 0, 5, 0] = 0.5          # moderate peak: finite scores, no rejection
     res = oracle.score(q, k, v, np.array([32], dtype=np.int32))
     assert np.all(np.isfinite(res["raw"]))
+
+
+@pytest.mark.parametrize("margin", [6.9, 13.8, 20.7])
+def test_sink_score_equals_deletion_near_one(margin):
+    """A sink carrying p = 1 - 1e-3, 1 - 1e-6 and 1 - 1e-9 of every row's mass:
+    the oracle's closed form (1 - p as (l - e) / l, |a - v| directly) against
+    deletion evaluated without cancellation (the other keys' output and mass
+    summed on their own).  fp64 keeps the closed form exact to about 1e-7
+    down to 1 - p = 1e-9; below about 1e-12 its sum l drops the other keys'
+    mass and deletion is the reference (the GPU tests do that)."""
+    wl = synth.make_workload("llama8b_gqa_d128_n32k", n_max=1500, sink_margin=margin)
+    s = wl.spec
+    res = oracle.score(wl.q, wl.k, wl.v, wl.lengths.numpy(), 1, 0)
+    dl = deletion_score(*(t.double().numpy() for t in (wl.q, wl.k, wl.v)), wl.lengths.numpy(), j=0)
+    np.testing.assert_allclose(res["raw"][:, :, 0], dl, rtol=2e-6)
+    # and the rows really are in that regime
+    q, k = wl.q.double().numpy(), wl.k.double().numpy()
+    x0 = np.einsum("htd,hd->ht", q[0], np.repeat(k[0, :, 0], s.g, axis=0)) / math.sqrt(s.d)
+    p0 = np.exp(x0 - res["m"][0]) / res["l"][0]
+    assert np.median(1 - p0) < 20 * math.exp(-margin)
 
 
 def test_invalid_arguments_rejected():
