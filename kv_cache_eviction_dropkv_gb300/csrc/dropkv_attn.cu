@@ -287,10 +287,11 @@ constexpr int pass1_smem_bytes() {
 // every split's O, all requested in one round trip.  Writes a, m, L and the
 // exported log-sum-exp.
 //
-// Shift of the scoring basis: warp 4 of every CTA merges row 0 too; its
-// output rounded to bf16, c, is the head's shift when |c|^2 > 2 d (the values
-// share an offset large against their spread), else c = 0.  Each row is
-// written as a' = a - c, split into bf16 hi + lo parts (pass 2's A.V^T
+// Shift of the scoring basis: the partial output of row 0 over the split that
+// holds tile 0 (a weighted average of values, read in the same round trip by
+// every warp), rounded to bf16, is the head's shift c when |c|^2 > 2 d (the
+// values share an offset large against their spread), else c = 0.  Each row
+// is written as a' = a - c, split into bf16 hi + lo parts (pass 2's A.V^T
 // operand; rows past R are zero), with K = |a'|^2 + 2 a'.c, so that pass 2
 // evaluates |a - v|^2 = K - 2 a'.v + |v - c|^2 without the cancellation of
 // |a|^2 - 2 a.v + |v|^2 when |v| is far above |a - v|.
@@ -302,19 +303,14 @@ constexpr int pass1_smem_bytes() {
 // which pass 2 rebuilds the output without that key with no cancellation.
 // Each split's largest e comes from the bf16 hi parts of pass 1's P operand:
 // good to 2^-9, which only blurs the threshold; pass 2 uses the key's own e.
-constexpr int kMergeRows = 4;                       // rows per CTA (one warp each)
-constexpr int kMergeThreads = 32 * (kMergeRows + 1);  // + the warp that merges row 0 for the shift
+constexpr int kMergeRows = 4;                 // rows per CTA (one warp each)
+constexpr int kMergeThreads = 32 * kMergeRows;
 constexpr int kMergeSplitRegs = kMaxSplits / 32;
 static_assert(kMergeSplitRegs * 32 == kMaxSplits, "split states are held 32 per register slot");
 
 __global__ void __launch_bounds__(kMergeThreads) merge_splits_kernel(const AttnParams p) {
-  __shared__ float wts_s[kMergeRows + 1][32];
-  __shared__ float wex_s[kMergeRows + 1][32];   // the same weights without split s* (dominated rows)
-  __shared__ __align__(16) float c_s[kDPad];    // the shift c (bf16 values; zero when not shifted)
-  __shared__ int shift_s;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const bool shift_warp = warp == kMergeRows;
-  const int unit = blockIdx.y, r = shift_warp ? 0 : blockIdx.x * kMergeRows + warp;
+  const int unit = blockIdx.y, r = blockIdx.x * kMergeRows + warp;
   const int b = unit / p.Hkv;
   // caller inputs, read before the wait: the length and pass 1's split count
   const int nb = seq_len(p, b);
@@ -335,6 +331,16 @@ __global__ void __launch_bounds__(kMergeThreads) merge_splits_kernel(const AttnP
   float M = -INFINITY, L = 0.f, Lx = 0.f;
   bool dom = false;
   int sstar = -1;
+  // the shift's source: row 0 of the split that holds tile 0 (split
+  // ceil(S / T) - 1 when a head has fewer tiles T than splits S)
+  float4 c0 = make_float4(0.f, 0.f, 0.f, 0.f);
+  float c0l = 0.f;
+  if (!stats_only) {
+    const int T = ceil_div(nb, kTile);
+    const int s0 = T >= S ? 0 : ceil_div(S, T) - 1;
+    c0l = __ldcg(p.part_ml + ((size_t)unit * p.splits + s0) * R * 4 + 1);
+    if (lane < D4) c0 = __ldcg(reinterpret_cast<const float4*>(p.part_o + ((size_t)unit * p.splits + s0) * R * d) + lane);
+  }
   if (live) {
     const float4* ml = reinterpret_cast<const float4*>(p.part_ml) + (size_t)unit * p.splits * R;
     const float4* po4 = reinterpret_cast<const float4*>(p.part_o + (size_t)unit * p.splits * R * d);
@@ -371,7 +377,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_splits_kernel(const AttnP
     L = warp_sum(L);
 #pragma unroll
     for (int o2 = 16; o2 > 0; o2 >>= 1) E = fmaxf(E, __shfl_xor_sync(0xffffffffu, E, o2));
-    dom = !stats_only && !shift_warp && E >= kDomP * L;   // the same in every lane
+    dom = !stats_only && E >= kDomP * L;        // the same in every lane
     float wex[kMergeSplitRegs];
     if (dom) {
       int first = 0x7fffffff;
@@ -393,10 +399,6 @@ __global__ void __launch_bounds__(kMergeThreads) merge_splits_kernel(const AttnP
 #pragma unroll
       for (int q = 0; q < kMergeSplitRegs; ++q) {
         if (q * 32 >= S) break;
-        __syncwarp();
-        wts_s[warp][lane] = wgt[q];
-        if (dom) wex_s[warp][lane] = wex[q];
-        __syncwarp();
         if (q > 0) {
 #pragma unroll
           for (int u = 0; u < 32; ++u)
@@ -404,9 +406,11 @@ __global__ void __launch_bounds__(kMergeThreads) merge_splits_kernel(const AttnP
                        ? __ldcg(po4 + (size_t)(q * 32 + u) * split_stride + (size_t)r * D4 + lane)
                        : make_float4(0.f, 0.f, 0.f, 0.f);
         }
+        // split q * 32 + u's weight from lane u (no shared memory: the
+        // kernel then fits beside an early pass-2 CTA on an SM)
 #pragma unroll
         for (int u = 0; u < 32; ++u) {
-          const float wu = wts_s[warp][u];
+          const float wu = __shfl_sync(0xffffffffu, wgt[q], u);
           if (wu != 0.f) {
             acc.x = fmaf(o[u].x, wu, acc.x);
             acc.y = fmaf(o[u].y, wu, acc.y);
@@ -417,7 +421,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_splits_kernel(const AttnP
         if (dom) {
 #pragma unroll
           for (int u = 0; u < 32; ++u) {
-            const float wx = wex_s[warp][u];
+            const float wx = __shfl_sync(0xffffffffu, wex[q], u);
             if (wx != 0.f) {
               acx.x = fmaf(o[u].x, wx, acx.x);
               acx.y = fmaf(o[u].y, wx, acx.y);
@@ -430,10 +434,10 @@ __global__ void __launch_bounds__(kMergeThreads) merge_splits_kernel(const AttnP
       const float inv = 1.0f / L;
       a = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
       if (lane >= D4) a = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (!shift_warp && lane < D4) reinterpret_cast<float4*>(p.a + ro * d)[lane] = a;
+      if (lane < D4) reinterpret_cast<float4*>(p.a + ro * d)[lane] = a;
       if (dom && lane < D4) reinterpret_cast<float4*>(p.dom_o + ro * d)[lane] = acx;
     }
-    if (!shift_warp && lane == 0) {
+    if (lane == 0) {
       p.m2[ro] = M;
       p.l[ro] = L;
       // exported: log-sum-exp of the natural-unit logits, log(L) + m ln 2
@@ -445,26 +449,25 @@ __global__ void __launch_bounds__(kMergeThreads) merge_splits_kernel(const AttnP
     }
   }
   if (stats_only) {
-    if (live && !shift_warp && lane == 0 && (!(L > 0.f) || !isfinite(L)))
+    if (live && lane == 0 && (!(L > 0.f) || !isfinite(L)))
       atomicOr(p.status, DROPKV_FLAG_NONFINITE | DROPKV_FLAG_NONFINITE_STATS);
     return;
   }
-  if (shift_warp) {
-    // c = bf16(a of row 0) when it is large (|c|^2 > 2 d), else 0
-    const __nv_bfloat162 c01 = __floats2bfloat162_rn(a.x, a.y), c23 = __floats2bfloat162_rn(a.z, a.w);
+  // c = bf16(the source's output) when it is large (|c|^2 > 2 d), else 0; the
+  // same in every warp of the head
+  float4 c;
+  {
+    const float inv0 = c0l > 0.f ? 1.0f / c0l : 0.f;
+    const __nv_bfloat162 c01 = __floats2bfloat162_rn(c0.x * inv0, c0.y * inv0);
+    const __nv_bfloat162 c23 = __floats2bfloat162_rn(c0.z * inv0, c0.w * inv0);
     const float2 f01 = __bfloat1622float2(c01), f23 = __bfloat1622float2(c23);
     const float cc = warp_sum(f01.x * f01.x + f01.y * f01.y + f23.x * f23.x + f23.y * f23.y);
-    const bool shift = cc > 2.0f * (float)d;
-    reinterpret_cast<float4*>(c_s)[lane] = shift ? make_float4(f01.x, f01.y, f23.x, f23.y) : make_float4(0.f, 0.f, 0.f, 0.f);
-    if (lane == 0) shift_s = shift ? 1 : 0;
-  }
-  __syncthreads();
-  if (shift_warp) {
-    if (blockIdx.x == 0) {
-      reinterpret_cast<float4*>(p.cvec + (size_t)unit * kDPad)[lane] = reinterpret_cast<const float4*>(c_s)[lane];
-      if (lane == 0) p.cflag[unit] = shift_s;
+    const bool shift = cc > 2.0f * (float)d;      // also false for a non-finite source
+    c = shift ? make_float4(f01.x, f01.y, f23.x, f23.y) : make_float4(0.f, 0.f, 0.f, 0.f);
+    if (blockIdx.x == 0 && warp == 0) {
+      reinterpret_cast<float4*>(p.cvec + (size_t)unit * kDPad)[lane] = c;
+      if (lane == 0) p.cflag[unit] = shift ? 1 : 0;
     }
-    return;
   }
   __nv_bfloat16* ahl = p.ahl + (size_t)unit * 2 * kMaxR * kDPad;
   if (!live) {
@@ -473,7 +476,6 @@ __global__ void __launch_bounds__(kMergeThreads) merge_splits_kernel(const AttnP
     reinterpret_cast<uint2*>(ahl + (size_t)(kMaxR + r) * kDPad)[lane] = make_uint2(0u, 0u);
     return;
   }
-  const float4 c = reinterpret_cast<const float4*>(c_s)[lane];   // zero past d
   const float4 ap = make_float4(a.x - c.x, a.y - c.y, a.z - c.z, a.w - c.w);
   // K = |a'|^2 + 2 a'.c
   const float K = warp_sum(ap.x * (ap.x + 2.f * c.x) + ap.y * (ap.y + 2.f * c.y) + ap.z * (ap.z + 2.f * c.z) +
@@ -895,16 +897,15 @@ struct Pass2Cfg {
   static_assert(KS <= kMaxStages && VS <= kMaxStages, "ring depth");
 };
 
-// Ring of the dominant mode, carved from the same region: fewer stages and
-// one P buffer (bf16 hi, then lo) for O_rest.
+// Ring of the dominant mode: the same K ring and V stage addresses, a
+// shallower V ring, and one P buffer (bf16 hi, then lo) for O_rest after it.
+// (One copy of the producer and MMA code serves both modes.)
 template <int NR>
 struct Pass2Dom {
-  static constexpr int KS = NR <= 32 ? 2 : 1;
-  static constexpr int VS = 3;
+  static constexpr int VS = NR <= 32 ? 3 : 2;
   static constexpr int kPBytes = kTile * NR * 2;
-  static constexpr int kOffK = 0;
-  static constexpr int kOffV = KS * kTileBytes;
-  static constexpr int kOffP = kOffV + VS * kTileBytes;
+  static constexpr int kOffP = Pass2Cfg<NR, false>::kOffV + VS * kTileBytes;
+  static_assert(Pass2Cfg<NR, false>::KS == 2, "both modes share the K ring");
   static_assert(kOffP + 2 * kPBytes <= Pass2Cfg<NR, false>::kOffQ, "dominant ring exceeds the ring region");
 };
 
@@ -918,15 +919,17 @@ struct Pass2Small {
   float4 pml[kMaxR / 2];     // per row pair (r, r + 1), r even: (-m_r, -m_r+1, L_r, L_r+1), m in log2 units
   float2 pk[kMaxR / 2];      // (K_r, K_r+1), K = |a'|^2 + 2 a'.c
   int pos[kMaxR];            // last key row r sees (tail-aligned causality); -1 for padding rows
-  float4 xch[2][kTile];      // upper-half partials per token (sum r^2 (K - 2 a'.v), sum r^2, |v - c|^2 part, singular)
-  int domf[kMaxR];           // 1: the row's dominant key lies in this CTA's split (dominant mode)
+  union {
+    float4 xch[2][kTile];    // upper-half partials per token (sum r^2 (K - 2 a'.v), sum r^2, |v - c|^2 part, singular)
+    struct {                 // after the last tile (dominant mode): per-lane-quarter sums
+      float red[4][kMaxR], red2[4][kMaxR], ltot[kMaxR];
+    } fx;
+  };
+  unsigned long long domf;   // bit r: row r's dominant key lies in this CTA's split (dominant mode)
   int domj[kMaxR];           // position of that key (found while scoring; -1 before)
   float dome[kMaxR];         // its e
   alignas(16) float cf[kDPad];   // the shift c (bf16 values) as f32
   int shift;                 // 1: |v - c|^2 with this c; 0: c = 0 and |v|^2
-  float red[4][kMaxR];       // per-lane-quarter sums (dominant mode)
-  float red2[4][kMaxR];
-  float ltot[kMaxR];
 };
 
 template <int NR, bool SNAP>
@@ -961,16 +964,18 @@ __device__ __forceinline__ uint64_t sqdiff_bf16x2(uint32_t w, float c0, float c1
 // by tile; each slot also carries its tile index, -1 ending the stream.
 // dynamic: tiles claimed from the unit's counter (the first claim is passed
 // in); otherwise the range [t0, t1).  Returns false after a timeout.
-template <int KS, int VS, bool HAS_V>
-__device__ bool p2_produce(uint8_t* sK, uint8_t* sV, Pass2Small& S, const CUtensorMap* tmk, const CUtensorMap* tmv,
-                           uint32_t* ctr, int unit, int ntiles, bool dynamic, int first, int t0, int t1,
-                           uint32_t* status) {
+template <int KS, bool HAS_V>
+__device__ __forceinline__ bool p2_produce(uint8_t* sK, uint8_t* sV, Pass2Small& S, const CUtensorMap* tmk,
+                                           const CUtensorMap* tmv, uint32_t* ctr, int unit, int ntiles, int VS,
+                                           bool dynamic, int first, int t0, int t1, uint32_t* status) {
   int issued = 0;
   bool ok = true;
+  int vs = 0;            // V slot of tile i (VS is set at run time) and the ring's wraps so far
+  uint32_t vwrap = 0;
   for (int i = 0;; ++i) {
-    const int ks = i % KS, vs = i % VS;
+    const int ks = i % KS;
     if (i >= KS && !mbar_wait(&S.kempty[ks], ((i / KS) + 1) & 1, &S.abort)) { ok = false; break; }
-    if (i >= VS && !mbar_wait(&S.vempty[vs], ((i / VS) + 1) & 1, &S.abort)) { ok = false; break; }
+    if (i >= VS && !mbar_wait(&S.vempty[vs], (vwrap + 1) & 1, &S.abort)) { ok = false; break; }
     const int tile = dynamic ? (i == 0 ? first : (int)atomicAdd(ctr, 1u)) : (t0 + i < t1 ? t0 + i : ntiles);
     if (tile >= ntiles) {
       S.ktile[ks] = -1;
@@ -992,6 +997,10 @@ __device__ bool p2_produce(uint8_t* sK, uint8_t* sV, Pass2Small& S, const CUtens
       tma_load_3d(sV + vs * kTileBytes + kHalfTile, tmv, &S.vfull[vs], 64, tile * kTile, unit);
     }
     ++issued;
+    if (++vs == VS) {
+      vs = 0;
+      ++vwrap;
+    }
   }
   if (!ok) {
     S.abort = 1;
@@ -1009,16 +1018,17 @@ __device__ bool p2_produce(uint8_t* sK, uint8_t* sV, Pass2Small& S, const CUtens
 // dominant mode also O_rest^T += V^T P^T, one tile behind (the workers write
 // P from the tile's S).  A V stage is released after its last MMA.  Returns
 // false after a timeout.
-template <int NR, int KS, int VS, bool SNAP, bool DOM>
-__device__ bool p2_mma(const uint8_t* sK, const uint8_t* sV, const uint8_t* sP, Pass2Small& S, uint32_t tmem,
-                       uint32_t qaddr, uint32_t ahi, uint32_t alo) {
+template <int NR, int KS, bool SNAP>
+__device__ __forceinline__ bool p2_mma(const uint8_t* sK, const uint8_t* sV, const uint8_t* sP, Pass2Small& S,
+                                       uint32_t tmem, uint32_t qaddr, uint32_t ahi, uint32_t alo, int VS, bool dom) {
   const uint32_t idS = umma_idesc_bf16(128, NR, 0, 0);
   const uint32_t idO = umma_idesc_bf16(128, NR, 1, 1);
   const uint32_t tO = tmem + 4 * NR;
-  auto pv = [&](int t) -> bool {
+  // O_rest^T += V_t^T P_t^T for tile t held in V slot `slot`
+  auto pv = [&](int t, int slot) -> bool {
     if (!mbar_wait(&S.pfull, t & 1, &S.abort)) return false;
     tc_fence_after();
-    const uint32_t vb = smem_addr(sV + (t % VS) * kTileBytes);
+    const uint32_t vb = smem_addr(sV + slot * kTileBytes);
     const uint32_t phi = smem_addr(sP), plo = smem_addr(sP + kTile * NR * 2);
 #pragma unroll
     for (int s = 0; s < 8; ++s)
@@ -1027,12 +1037,14 @@ __device__ bool p2_mma(const uint8_t* sK, const uint8_t* sV, const uint8_t* sP, 
     for (int s = 0; s < 8; ++s)
       umma_bf16(tO, desc_mnmajor_sw128(vb, kTile, s), desc_mnmajor_interleave(plo, NR, s), idO, 1);
     umma_commit(&S.pempty);
-    umma_commit(&S.vempty[t % VS]);
+    umma_commit(&S.vempty[slot]);
     return true;
   };
+  int vs = 0, pvs = 0;     // V slots of tiles i and i - 1 (VS is set at run time)
+  uint32_t vwrap = 0;
   int i = 0;
   for (;; ++i) {
-    const int ks = i % KS, vs = i % VS, ab = i & 1;
+    const int ks = i % KS, ab = i & 1;
     const uint32_t dS = tmem + ab * 2 * NR, dAV = dS + NR;
     if (!mbar_wait(&S.kfull[ks], (i / KS) & 1, &S.abort)) return false;
     if (*reinterpret_cast<volatile int*>(&S.ktile[ks]) < 0) break;     // no more tiles
@@ -1048,7 +1060,7 @@ __device__ bool p2_mma(const uint8_t* sK, const uint8_t* sV, const uint8_t* sP, 
       continue;
     }
     if (i == 0 && !mbar_wait(&S.aready, 0, &S.abort)) return false;
-    if (!mbar_wait(&S.vfull[vs], (i / VS) & 1, &S.abort)) return false;
+    if (!mbar_wait(&S.vfull[vs], vwrap & 1, &S.abort)) return false;
     tc_fence_after();
     const uint32_t vb = smem_addr(sV + vs * kTileBytes);
 #pragma unroll
@@ -1057,11 +1069,16 @@ __device__ bool p2_mma(const uint8_t* sK, const uint8_t* sV, const uint8_t* sP, 
 #pragma unroll
     for (int s = 0; s < 8; ++s)
       umma_bf16(dAV, desc_kmajor_sw128(vb, kTile, s), desc_kmajor_sw128(alo, NR, s), idS, 1);
-    if (!DOM) umma_commit(&S.vempty[vs]);
+    if (!dom) umma_commit(&S.vempty[vs]);
     umma_commit(&S.accfull[ab]);
-    if (DOM && i > 0 && !pv(i - 1)) return false;
+    if (dom && i > 0 && !pv(i - 1, pvs)) return false;
+    pvs = vs;
+    if (++vs == VS) {
+      vs = 0;
+      ++vwrap;
+    }
   }
-  if (DOM && i > 0 && !pv(i - 1)) return false;
+  if (dom && i > 0 && !pv(i - 1, pvs)) return false;
   return true;
 }
 
@@ -1069,7 +1086,7 @@ __device__ bool p2_mma(const uint8_t* sK, const uint8_t* sV, const uint8_t* sP, 
 // the A.V^T operand), the per-row constants, the head's shift c and the
 // dominated rows whose key lies in this CTA's split.
 template <int NR, bool SNAP>
-__device__ void p2_prologue(uint8_t* sAhi, uint8_t* sAlo, Pass2Small& S, const AttnParams& p, int unit, int split,
+__device__ __forceinline__ void p2_prologue(uint8_t* sAhi, uint8_t* sAlo, Pass2Small& S, const AttnParams& p, int unit, int split,
                             int nb, int tid) {
   const int R = p.R;
   const size_t rowbase = (size_t)unit * R;
@@ -1089,7 +1106,10 @@ __device__ void p2_prologue(uint8_t* sAhi, uint8_t* sAlo, Pass2Small& S, const A
     pm[2 + (tid & 1)] = real ? p.l[o] : 1.f;
     reinterpret_cast<float*>(&S.pk[tid >> 1])[tid & 1] = (!SNAP && real) ? p.aa[o] : 0.f;
     S.pos[tid] = real ? nb - p.w + (tid % p.w) : -1;
-    S.domf[tid] = (!SNAP && real && p.dom_s[o] == split) ? 1 : 0;
+    const bool mine = !SNAP && real && p.dom_s[o] == split;
+    const unsigned ballot_lo = __ballot_sync(0xffffffffu, mine);   // tid < 64: warps 0 and 1, whole warps
+    if (tid == 0) reinterpret_cast<unsigned*>(&S.domf)[0] = ballot_lo;
+    if (tid == 32) reinterpret_cast<unsigned*>(&S.domf)[1] = ballot_lo;
     S.domj[tid] = -1;
   }
 }
@@ -1098,9 +1118,11 @@ __device__ void p2_prologue(uint8_t* sAhi, uint8_t* sAlo, Pass2Small& S, const A
 // tile, rows [r0, r0 + HR) and columns [64 half, 64 half + 64) of |v - c|^2;
 // the upper half hands its partial sums to the lower half, which writes the
 // score.  DOM: the dominant mode (P for O_rest, the dominant keys' terms at the
-// end).  Returns true when a wait gave up.
-template <int NR, int VS, bool SNAP, bool DOM>
-__device__ bool p2_work(uint8_t* sV, uint8_t* sP, Pass2Small& S, const AttnParams& p, uint32_t tmem, int unit,
+// end).  SHIFT: 0 |v|^2 (the head is not shifted), 1 |v - c|^2, 2 either, as
+// the head says (the dominant mode); a CTA's hot loop holds one variant only.
+// Returns true when a wait gave up.
+template <int NR, int VS, bool SNAP, bool DOM, int SHIFT>
+__device__ __forceinline__ bool p2_work(uint8_t* sV, uint8_t* sP, Pass2Small& S, const AttnParams& p, uint32_t tmem, int unit,
                         int nb, int tid, uint32_t& flags) {
   constexpr int HR = NR / 2;
   constexpr int kPBytes = kTile * NR * 2;
@@ -1115,7 +1137,7 @@ __device__ bool p2_work(uint8_t* sV, uint8_t* sP, Pass2Small& S, const AttnParam
   for (int r = 0; r < HR; ++r) rowmask |= (uint32_t)(r0 + r < R) << r;
   if (DOM) {
 #pragma unroll
-    for (int r = 0; r < HR; ++r) dommask |= (uint32_t)S.domf[r0 + r] << r;
+    for (int r = 0; r < HR; ++r) dommask |= (uint32_t)((S.domf >> (r0 + r)) & 1ull) << r;
   }
   float lrest[DOM ? HR : 1];
 #pragma unroll
@@ -1123,7 +1145,7 @@ __device__ bool p2_work(uint8_t* sV, uint8_t* sP, Pass2Small& S, const AttnParam
   const float scale = p.scale_log2;
   const float inv_g = 1.0f / (float)p.g;
   const int all_see = nb - p.w;
-  const bool shifted = !SNAP && S.shift != 0;
+  const bool shifted = SHIFT == 1 || (SHIFT == 2 && S.shift != 0);
   float* raw = p.raw + (size_t)unit * p.n_max;
   bool failed = false;
   for (int i = 0;; ++i) {
@@ -1143,7 +1165,7 @@ __device__ bool p2_work(uint8_t* sV, uint8_t* sP, Pass2Small& S, const AttnParam
       // a per-thread rotated order so a warp's reads spread over all banks
       // (physical chunk pc of swizzled row tok holds columns 8 (pc ^ (tok & 7)) .. + 7)
       uint64_t acc = 0;
-      if (shifted) {
+      if (SHIFT != 0 && (SHIFT == 1 || shifted)) {
         const float* cfh = S.cf + half * 64;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
@@ -1156,7 +1178,7 @@ __device__ bool p2_work(uint8_t* sV, uint8_t* sP, Pass2Small& S, const AttnParam
           acc = sqdiff_bf16x2(w.z, c1.x, c1.y, acc);
           acc = sqdiff_bf16x2(w.w, c1.z, c1.w, acc);
         }
-      } else {
+      } else if (SHIFT != 1) {
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           const uint4 w = *reinterpret_cast<const uint4*>(vrow + ((c + tok) & 7) * 16);
@@ -1336,7 +1358,7 @@ __device__ bool p2_work(uint8_t* sV, uint8_t* sP, Pass2Small& S, const AttnParam
 #pragma unroll
     for (int r = 0; r < HR; ++r) {
       const float v = warp_sum(lrest[r]);
-      if (lane == 0) S.red[wq][r0 + r] = v;
+      if (lane == 0) S.fx.red[wq][r0 + r] = v;
     }
     named_bar(kBarAux, kWorkers);
     const size_t rowbase = (size_t)unit * R;
@@ -1344,7 +1366,8 @@ __device__ bool p2_work(uint8_t* sV, uint8_t* sP, Pass2Small& S, const AttnParam
     for (int r = 0; r < HR; ++r) {
       if (!((dommask >> r) & 1u)) continue;       // the same in the whole warp
       const int rr = r0 + r;
-      const float lt = p.dom_l[rowbase + rr] + ((S.red[0][rr] + S.red[1][rr]) + (S.red[2][rr] + S.red[3][rr]));
+      const float lt =
+          p.dom_l[rowbase + rr] + ((S.fx.red[0][rr] + S.fx.red[1][rr]) + (S.fx.red[2][rr] + S.fx.red[3][rr]));
       const int jst = S.domj[rr];
       float sq = 0.f;
       if (jst >= 0 && tok < p.d) {
@@ -1355,28 +1378,28 @@ __device__ bool p2_work(uint8_t* sV, uint8_t* sP, Pass2Small& S, const AttnParam
       }
       sq = warp_sum(sq);
       if (lane == 0) {
-        S.red2[wq][rr] = sq;
-        if (wq == 0) S.ltot[rr] = lt;
+        S.fx.red2[wq][rr] = sq;
+        if (wq == 0) S.fx.ltot[rr] = lt;
       }
     }
     named_bar(kBarAux, kWorkers);
     if (tid == 0) {
       // rows in order, one thread: several rows may share a dominant key
       for (int rr = 0; rr < R; ++rr) {
-        if (!S.domf[rr]) continue;
+        if (!((S.domf >> rr) & 1ull)) continue;
         // no key above half the mass: the row is not dominated after all (the
         // merge's threshold is only good to bf16) and was scored as usual
         const int jst = S.domj[rr];
         if (jst < 0) continue;
         const float es = S.dome[rr];
-        const float lt = S.ltot[rr];
+        const float lt = S.fx.ltot[rr];
         if (!(lt > es * 0x1p-53f)) {     // p* = e* / (e* + L_rest) rounds to 1 in double precision
           raw[jst] = INFINITY;
           flags |= DROPKV_FLAG_SINGULAR;
           continue;
         }
         const float pr = es / (es + lt);
-        const float dist = (S.red2[0][rr] + S.red2[1][rr]) + (S.red2[2][rr] + S.red2[3][rr]);
+        const float dist = (S.fx.red2[0][rr] + S.fx.red2[1][rr]) + (S.fx.red2[2][rr] + S.fx.red2[3][rr]);
         const float cur = raw[jst];
         const float nv = cur + pr * pr * dist * inv_g;
         if (!isfinite(nv) && !isinf(cur)) flags |= DROPKV_FLAG_NONFINITE | DROPKV_FLAG_NONFINITE_SCORE;
@@ -1385,6 +1408,21 @@ __device__ bool p2_work(uint8_t* sV, uint8_t* sP, Pass2Small& S, const AttnParam
     }
   }
   return failed;
+}
+
+// The workers of a CTA in the dominant mode, as a function of their own: the
+// kernel's main body keeps only the common path's code, next to the prologue
+// (instruction fetch of a cold kernel is on pass 2's critical path).
+template <int NR>
+__device__ __noinline__ bool p2_work_dominant(uint8_t* sV, uint8_t* sP, Pass2Small* S, const AttnParams* p,
+                                              uint32_t tmem, int unit, int nb, int tid, uint32_t* flags) {
+  return p2_work<NR, Pass2Dom<NR>::VS, false, true, 2>(sV, sP, *S, *p, tmem, unit, nb, tid, *flags);
+}
+// The same for a head whose scores use the shift (|v - c|^2).
+template <int NR>
+__device__ __noinline__ bool p2_work_shifted(uint8_t* sV, Pass2Small* S, const AttnParams* p, uint32_t tmem,
+                                             int unit, int nb, int tid, uint32_t* flags) {
+  return p2_work<NR, Pass2Cfg<NR, false>::VS, false, false, 1>(sV, nullptr, *S, *p, tmem, unit, nb, tid, *flags);
 }
 
 // SNAP: the SnapKV score (1/g) sum_r p_r from K alone -- no V, no A V^T.
@@ -1466,12 +1504,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (lane == 0) {
       S.mode = mode;                              // published by the first slot's arrival
-      if (!SNAP && mode == kModeDominant)
-        p2_produce<D::KS, D::VS, true>(sm + D::kOffK, sm + D::kOffV, S, &tmk, &tmv, p.tile_ctr + unit, unit,
-                                       ntiles, false, 0, t0, t1, p.status);
-      else
-        p2_produce<C::KS, C::VS, !SNAP>(sm + C::kOffK, sm + C::kOffV, S, &tmk, &tmv, p.tile_ctr + unit, unit,
-                                        ntiles, mode == kModeDynamic, first, t0, t1, p.status);
+      p2_produce<C::KS, !SNAP>(sm + C::kOffK, sm + C::kOffV, S, &tmk, &tmv, p.tile_ctr + unit, unit, ntiles,
+                               (!SNAP && mode == kModeDominant) ? D::VS : C::VS, mode == kModeDynamic, first, t0, t1,
+                               p.status);
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
@@ -1481,12 +1516,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = mbar_wait(&S.kfull[0], 0, &S.abort);
       if (ok) {
         const int mode = *reinterpret_cast<volatile int*>(&S.mode);
-        if (!SNAP && mode == kModeDominant)
-          ok = p2_mma<NR, D::KS, D::VS, false, true>(sm + D::kOffK, sm + D::kOffV, sm + D::kOffP, S, tmem, qaddr,
-                                                     ahi, alo);
-        else
-          ok = p2_mma<NR, C::KS, C::VS, SNAP, false>(sm + C::kOffK, sm + C::kOffV, nullptr, S, tmem, qaddr, ahi,
-                                                     alo);
+        const bool dom = !SNAP && mode == kModeDominant;
+        ok = p2_mma<NR, C::KS, SNAP>(sm + C::kOffK, sm + C::kOffV, sm + D::kOffP, S, tmem, qaddr, ahi, alo,
+                                     dom ? D::VS : C::VS, dom);
       }
       if (!ok) {
         failed = true;
@@ -1511,9 +1543,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
       const int mode = *reinterpret_cast<volatile int*>(&S.mode);
       if (!SNAP && mode == kModeDominant)
-        failed = p2_work<NR, D::VS, false, true>(sm + D::kOffV, sm + D::kOffP, S, p, tmem, unit, nb, tid, flags);
+        failed = p2_work_dominant<NR>(sm + C::kOffV, sm + D::kOffP, &S, &p, tmem, unit, nb, tid, &flags);
+      else if (!SNAP && S.shift)
+        failed = p2_work_shifted<NR>(sm + C::kOffV, &S, &p, tmem, unit, nb, tid, &flags);
       else
-        failed = p2_work<NR, C::VS, SNAP, false>(sm + C::kOffV, nullptr, S, p, tmem, unit, nb, tid, flags);
+        failed = p2_work<NR, C::VS, SNAP, false, 0>(sm + C::kOffV, nullptr, S, p, tmem, unit, nb, tid, flags);
     }
     if (flags) atomicOr(p.status, flags);
   }
