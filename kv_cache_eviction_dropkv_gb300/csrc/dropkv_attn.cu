@@ -309,6 +309,8 @@ constexpr int kMergeSplitRegs = kMaxSplits / 32;
 static_assert(kMergeSplitRegs * 32 == kMaxSplits, "split states are held 32 per register slot");
 
 __global__ void __launch_bounds__(kMergeThreads) merge_splits_kernel(const AttnParams p) {
+  __shared__ float wts_s[kMergeRows][32];
+  __shared__ float wex_s[kMergeRows][32];       // the same weights without split s* (dominated rows)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int unit = blockIdx.y, r = blockIdx.x * kMergeRows + warp;
   const int b = unit / p.Hkv;
@@ -333,7 +335,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_splits_kernel(const AttnP
   int sstar = -1;
   // the shift's source: row 0 of the split that holds tile 0 (split
   // ceil(S / T) - 1 when a head has fewer tiles T than splits S)
-  float4 c0 = make_float4(0.f, 0.f, 0.f, 0.f);
+  float4 c0 = make_float4(0.f, 0.f, 0.f, 0.f), c = c0;
   float c0l = 0.f;
   if (!stats_only) {
     const int T = ceil_div(nb, kTile);
@@ -377,6 +379,21 @@ __global__ void __launch_bounds__(kMergeThreads) merge_splits_kernel(const AttnP
     L = warp_sum(L);
 #pragma unroll
     for (int o2 = 16; o2 > 0; o2 >>= 1) E = fmaxf(E, __shfl_xor_sync(0xffffffffu, E, o2));
+    if (!stats_only) {
+      // c = bf16(the source's output) when it is large (|c|^2 > 2 d), else 0;
+      // the same in every warp of the head (its loads were issued first)
+      const float inv0 = c0l > 0.f ? 1.0f / c0l : 0.f;
+      const __nv_bfloat162 c01 = __floats2bfloat162_rn(c0.x * inv0, c0.y * inv0);
+      const __nv_bfloat162 c23 = __floats2bfloat162_rn(c0.z * inv0, c0.w * inv0);
+      const float2 f01 = __bfloat1622float2(c01), f23 = __bfloat1622float2(c23);
+      const float cc = warp_sum(f01.x * f01.x + f01.y * f01.y + f23.x * f23.x + f23.y * f23.y);
+      const bool shift = cc > 2.0f * (float)d;    // also false for a non-finite source
+      c = shift ? make_float4(f01.x, f01.y, f23.x, f23.y) : make_float4(0.f, 0.f, 0.f, 0.f);
+      if (blockIdx.x == 0 && warp == 0) {
+        reinterpret_cast<float4*>(p.cvec + (size_t)unit * kDPad)[lane] = c;
+        if (lane == 0) p.cflag[unit] = shift ? 1 : 0;
+      }
+    }
     dom = !stats_only && E >= kDomP * L;        // the same in every lane
     float wex[kMergeSplitRegs];
     if (dom) {
@@ -399,6 +416,10 @@ __global__ void __launch_bounds__(kMergeThreads) merge_splits_kernel(const AttnP
 #pragma unroll
       for (int q = 0; q < kMergeSplitRegs; ++q) {
         if (q * 32 >= S) break;
+        __syncwarp();
+        wts_s[warp][lane] = wgt[q];
+        if (dom) wex_s[warp][lane] = wex[q];
+        __syncwarp();
         if (q > 0) {
 #pragma unroll
           for (int u = 0; u < 32; ++u)
@@ -406,11 +427,9 @@ __global__ void __launch_bounds__(kMergeThreads) merge_splits_kernel(const AttnP
                        ? __ldcg(po4 + (size_t)(q * 32 + u) * split_stride + (size_t)r * D4 + lane)
                        : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        // split q * 32 + u's weight from lane u (no shared memory: the
-        // kernel then fits beside an early pass-2 CTA on an SM)
 #pragma unroll
         for (int u = 0; u < 32; ++u) {
-          const float wu = __shfl_sync(0xffffffffu, wgt[q], u);
+          const float wu = wts_s[warp][u];
           if (wu != 0.f) {
             acc.x = fmaf(o[u].x, wu, acc.x);
             acc.y = fmaf(o[u].y, wu, acc.y);
@@ -421,7 +440,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_splits_kernel(const AttnP
         if (dom) {
 #pragma unroll
           for (int u = 0; u < 32; ++u) {
-            const float wx = __shfl_sync(0xffffffffu, wex[q], u);
+            const float wx = wex_s[warp][u];
             if (wx != 0.f) {
               acx.x = fmaf(o[u].x, wx, acx.x);
               acx.y = fmaf(o[u].y, wx, acx.y);
@@ -452,22 +471,6 @@ __global__ void __launch_bounds__(kMergeThreads) merge_splits_kernel(const AttnP
     if (live && lane == 0 && (!(L > 0.f) || !isfinite(L)))
       atomicOr(p.status, DROPKV_FLAG_NONFINITE | DROPKV_FLAG_NONFINITE_STATS);
     return;
-  }
-  // c = bf16(the source's output) when it is large (|c|^2 > 2 d), else 0; the
-  // same in every warp of the head
-  float4 c;
-  {
-    const float inv0 = c0l > 0.f ? 1.0f / c0l : 0.f;
-    const __nv_bfloat162 c01 = __floats2bfloat162_rn(c0.x * inv0, c0.y * inv0);
-    const __nv_bfloat162 c23 = __floats2bfloat162_rn(c0.z * inv0, c0.w * inv0);
-    const float2 f01 = __bfloat1622float2(c01), f23 = __bfloat1622float2(c23);
-    const float cc = warp_sum(f01.x * f01.x + f01.y * f01.y + f23.x * f23.x + f23.y * f23.y);
-    const bool shift = cc > 2.0f * (float)d;      // also false for a non-finite source
-    c = shift ? make_float4(f01.x, f01.y, f23.x, f23.y) : make_float4(0.f, 0.f, 0.f, 0.f);
-    if (blockIdx.x == 0 && warp == 0) {
-      reinterpret_cast<float4*>(p.cvec + (size_t)unit * kDPad)[lane] = c;
-      if (lane == 0) p.cflag[unit] = shift ? 1 : 0;
-    }
   }
   __nv_bfloat16* ahl = p.ahl + (size_t)unit * 2 * kMaxR * kDPad;
   if (!live) {
@@ -1164,7 +1167,7 @@ __device__ __forceinline__ bool p2_work(uint8_t* sV, uint8_t* sP, Pass2Small& S,
       // columns, two columns per packed instruction; the chunks are visited in
       // a per-thread rotated order so a warp's reads spread over all banks
       // (physical chunk pc of swizzled row tok holds columns 8 (pc ^ (tok & 7)) .. + 7)
-      uint64_t acc = 0;
+      uint64_t acc = 0, accb = 0;    // two accumulators: shorter dependency chains
       if (SHIFT != 0 && (SHIFT == 1 || shifted)) {
         const float* cfh = S.cf + half * 64;
 #pragma unroll
@@ -1174,20 +1177,21 @@ __device__ __forceinline__ bool p2_work(uint8_t* sV, uint8_t* sP, Pass2Small& S,
           const float4 c0 = *reinterpret_cast<const float4*>(cfh + lc * 8);
           const float4 c1 = *reinterpret_cast<const float4*>(cfh + lc * 8 + 4);
           acc = sqdiff_bf16x2(w.x, c0.x, c0.y, acc);
-          acc = sqdiff_bf16x2(w.y, c0.z, c0.w, acc);
+          accb = sqdiff_bf16x2(w.y, c0.z, c0.w, accb);
           acc = sqdiff_bf16x2(w.z, c1.x, c1.y, acc);
-          acc = sqdiff_bf16x2(w.w, c1.z, c1.w, acc);
+          accb = sqdiff_bf16x2(w.w, c1.z, c1.w, accb);
         }
       } else if (SHIFT != 1) {
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           const uint4 w = *reinterpret_cast<const uint4*>(vrow + ((c + tok) & 7) * 16);
           acc = sq_bf16x2(w.x, acc);
-          acc = sq_bf16x2(w.y, acc);
+          accb = sq_bf16x2(w.y, accb);
           acc = sq_bf16x2(w.z, acc);
-          acc = sq_bf16x2(w.w, acc);
+          accb = sq_bf16x2(w.w, accb);
         }
       }
+      acc = f2_add(acc, accb);
       vvh = f2_lo(acc) + f2_hi(acc);
     }
     __syncwarp();
@@ -1226,7 +1230,7 @@ __device__ __forceinline__ bool p2_work(uint8_t* sV, uint8_t* sP, Pass2Small& S,
         // registers); rows the token is invisible to get e = 0 (their terms
         // vanish; slots past the sequence are never written)
         constexpr int CH = HR < 16 ? HR : 16;
-        uint64_t A2 = 0, W2 = 0;
+        uint64_t A2 = 0, W2 = 0, A2b = 0, W2b = 0;    // alternate pairs: shorter chains
         const uint64_t scale2 = f2_pack(scale, scale), neg2 = f2_pack(-2.f, -2.f);
 #pragma unroll
         for (int c0 = 0; c0 < HR; c0 += CH) {
@@ -1248,10 +1252,17 @@ __device__ __forceinline__ bool p2_work(uint8_t* sV, uint8_t* sP, Pass2Small& S,
             singular |= !(d0 > 0.f) || !(d1 > 0.f);
             const uint64_t ratio = f2_mul(e2, f2_pack(rcp_approx(d0), rcp_approx(d1)));   // p_j / (1 - p_j)
             const uint64_t q = f2_mul(ratio, ratio);
-            A2 = f2_fma(q, f2_fma(f2_pack(av[rr], av[rr + 1]), neg2, f2_pack(kk.x, kk.y)), A2);
-            W2 = f2_add(W2, q);
+            if ((rr & 2) == 0) {
+              A2 = f2_fma(q, f2_fma(f2_pack(av[rr], av[rr + 1]), neg2, f2_pack(kk.x, kk.y)), A2);
+              W2 = f2_add(W2, q);
+            } else {
+              A2b = f2_fma(q, f2_fma(f2_pack(av[rr], av[rr + 1]), neg2, f2_pack(kk.x, kk.y)), A2b);
+              W2b = f2_add(W2b, q);
+            }
           }
         }
+        A2 = f2_add(A2, A2b);
+        W2 = f2_add(W2, W2b);
         A = f2_lo(A2) + f2_hi(A2);
         W = f2_lo(W2) + f2_hi(W2);
       } else {
