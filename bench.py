@@ -210,23 +210,17 @@ class ClockSampler:
 
 def run_reference(args, spec, wl):
     """Reference arm: the fp64 CPU oracle on the host cores, same workload,
-    metric and unit.  Each step is a bounded sample of the layer: one query
-    head of one KV head over all of its sequence's tokens (the oracle's unit of
-    independent work), cycling through the layer's (sequence, KV head, query
-    head) triples; it counts n_b / Hq scored tokens, the share of the layer's
-    tokens that one query head's scoring represents."""
+    metric and unit.  Each step scores the whole layer with one thread per
+    host core (the oracle spreads (sequence, KV head, query head) items over
+    them) and counts the layer's tokens."""
     import oracle
     lengths = wl.lengths.numpy()
-    g = spec.Hq // spec.Hkv
-    triples = [(b, h, hl) for b in range(spec.B) for h in range(spec.Hkv) for hl in range(g)]
+    nproc = os.cpu_count() or 1
 
     def step(i):
-        b, h, hl = triples[i % len(triples)]
-        hq = h * g + hl
-        oracle.run_path(wl.q[b:b + 1, hq:hq + 1], wl.k[b:b + 1, h:h + 1], wl.v[b:b + 1, h:h + 1],
-                        wl.lengths[b:b + 1], wl.evict_k[b:b + 1], spec.pool_kernel, spec.protect, nthreads=1,
+        oracle.run_path(wl.q, wl.k, wl.v, wl.lengths, wl.evict_k, spec.pool_kernel, spec.protect, nthreads=nproc,
                         kind=args.score)
-        return int(lengths[b]) / spec.Hq
+        return int(lengths.sum())
 
     for i in range(args.warmup):
         step(i)
@@ -237,29 +231,42 @@ def run_reference(args, spec, wl):
         times.append(time.perf_counter() - t0)
     total = sum(times)
     value = units / total
-    sample = ("per step one query head of one KV head over all n_b tokens (1/%d of the layer's scoring work), "
-              "fp64, 1 thread" % spec.Hq)
+    sample = "per step the whole layer (%d KV heads x %d query heads, %d tokens), fp64, %d threads" % (
+        spec.B * spec.Hkv, spec.Hq // spec.Hkv, int(lengths.sum()), nproc)
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded generator; stands in for RULER/LongBench layers)",
             "config": config_of(spec, lengths, args.score),
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": nproc, "nproc": nproc, "kind": "oracle",
+                             "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
 
 
 def cpu_baseline(spec, wl, score="dropkv"):
+    """The fp64 oracle on the host: the whole layer with one thread per core,
+    and a bounded sample on one thread (one query head of one KV head over all
+    of its sequence's tokens, 1/Hq of the layer's scoring work, scaled to the
+    tokens it represents)."""
     import oracle
-    cores = min(spec.B * spec.Hkv, os.cpu_count() or 1)
+    nproc = os.cpu_count() or 1
     units = int(wl.lengths.sum())
     t0 = time.perf_counter()
-    oracle.run_path(wl.q, wl.k, wl.v, wl.lengths, wl.evict_k, spec.pool_kernel, spec.protect, nthreads=cores,
+    oracle.run_path(wl.q, wl.k, wl.v, wl.lengths, wl.evict_k, spec.pool_kernel, spec.protect, nthreads=nproc,
                     kind=score)
-    dt = time.perf_counter() - t0
-    return {"value": units / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": "one full layer (%d KV heads, %d tokens), fp64, %.1f s on %d threads" % (
-                spec.B * spec.Hkv, units, dt, cores)}
+    dt_all = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    oracle.run_path(wl.q[:1, :1], wl.k[:1, :1], wl.v[:1, :1], wl.lengths[:1], wl.evict_k[:1], spec.pool_kernel,
+                    spec.protect, nthreads=1, kind=score)
+    dt_one = time.perf_counter() - t0
+    one_units = int(wl.lengths[0]) / spec.Hq
+    return {"value": units / dt_all, "unit": UNIT, "cores": nproc, "nproc": nproc, "kind": "oracle",
+            "threads": nproc, "seconds": dt_all,
+            "one_thread": {"value": one_units / dt_one, "threads": 1, "seconds": dt_one,
+                           "sample": "one query head of one KV head (1/%d of the layer)" % spec.Hq},
+            "sample": "one full layer (%d KV heads, %d tokens), fp64, %.2f s on %d threads (nproc %d)" % (
+                spec.B * spec.Hkv, units, dt_all, nproc, nproc)}
 
 
 def main():
@@ -409,8 +416,7 @@ def main():
             "ms_per_step": step_ms, "ms_per_step_median": reduce_max(float(sorted(t_step)[K // 2]), world),
             "head_tokens_per_s": value * spec.Hkv, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f32", "data": "synthetic (seeded generator; stands in for RULER/LongBench layers)",
-            "config": dict(config_of(spec, lengths_np, args.score, args.select),
-                           parallelism="one independent layer per GPU"),
+            "config": config_of(spec, lengths_np, args.score, args.select),
             "roofline": roofline,
             "path_roofline": {"achieved": path_gbs, "peak": peak, "unit": "GB/s", "frac": path_gbs / peak,
                               "algorithmic_bytes_per_step": nbytes["path"]},

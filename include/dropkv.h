@@ -85,7 +85,9 @@ typedef struct {
   int32_t w;       /* observation window: tail queries per query head */
 } dropkv_shape;
 
-/* Bytes of device workspace the calls that take one need for `shape` on the
+/* Infrastructure (no passage of the pages): the workspace sizing of this
+ * library's own scratch layout.
+ * Bytes of device workspace the calls that take one need for `shape` on the
  * current device (0 if the shape is invalid or unsupported, or no device is
  * present).  One workspace serves every call on that shape (not two calls at
  * once: calls that overlap on the GPU must use separate workspaces).  After
@@ -118,7 +120,8 @@ DROPKV_API dropkv_status dropkv_score(const dropkv_shape* shape, const void* q_w
                            float* raw_scores, void* workspace, size_t workspace_bytes, uint32_t* status,
                            cudaStream_t stream);
 
-/* dropkv_score_ex that also records phase_events[0..4] on `stream`: before
+/* Infrastructure (no passage of the pages): per-kernel timing.
+ * dropkv_score_ex that also records phase_events[0..4] on `stream`: before
  * pass 1 (window attention), between pass 1 and the split-K merge, between the
  * merge and pass 2 (scoring), between pass 2 and pooling, and after pooling --
  * for per-kernel timing with CUDA events.  The events are created by the
@@ -234,7 +237,8 @@ DROPKV_API dropkv_status dropkv_evict_ex(const dropkv_shape* shape, int32_t scor
                                          void* v_out, void* workspace, size_t workspace_bytes, uint32_t* status,
                                          cudaStream_t stream);
 
-/* Synchronise `stream`, read the device status word and map it to a status
+/* Infrastructure (no passage of the pages): error reporting.
+ * Synchronise `stream`, read the device status word and map it to a status
  * (the first of SINGULAR, NONFINITE, DEVICE_ARG, TIMEOUT that is set, else OK;
  * FLAG_INTERNAL maps to DROPKV_ERR_CUDA).
  * *flags_out (if not NULL) receives the raw word. */

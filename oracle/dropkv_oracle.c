@@ -77,16 +77,18 @@ typedef struct {
     const int32_t* lengths;
     int pool_kernel, protect, kind;
     double *m_out, *l_out, *a_out, *raw_out, *final_out;
-    /* work distribution */
-    int next_unit;
+    double* s_heads;         /* [B * Hkv][g][n_max]: per query head sums of S3 */
+    /* work distribution: items are (unit, query head) in phase 1, units in phase 2 */
+    int next_item;
+    int phase;
     pthread_mutex_t lock;
     int status;              /* ORACLE_OK or first error */
     int singular_unit;
 } score_job;
 
-static int take_unit(score_job* job) {
+static int take_item(score_job* job) {
     pthread_mutex_lock(&job->lock);
-    int u = job->next_unit++;
+    int u = job->next_item++;
     pthread_mutex_unlock(&job->lock);
     return u;
 }
@@ -100,78 +102,90 @@ static void set_status(score_job* job, int st, int unit) {
     pthread_mutex_unlock(&job->lock);
 }
 
-/* One (b, KV head) unit: steps S1-S5. */
-static int score_unit(score_job* job, int unit, double* x, double* e, double* qrow,
-                      double* a, double* s_head, double* s_sum) {
+/* One query head hl of one (b, KV head) unit: steps S1-S3 for its w window
+ * rows, summed over the rows into s_head[0, n_b). */
+static int score_head(score_job* job, int unit, int hl, double* x, double* e, double* qrow, double* a,
+                      double* s_head) {
     const oracle_shape* s = job->s;
     const int b = unit / s->Hkv, h = unit % s->Hkv;
     const int g = s->Hq / s->Hkv, d = s->d, w = s->w;
     const int nb = job->lengths[b];
-    const size_t n_max = (size_t)s->n_max;
     const double inv_sqrt_d = 1.0 / sqrt((double)d);
-    const size_t kv_base = ((size_t)b * s->Hkv + h) * n_max * d;
+    const size_t kv_base = ((size_t)b * s->Hkv + h) * (size_t)s->n_max * d;
+    const int hq = h * g + hl;
 
-    for (int j = 0; j < nb; ++j) s_sum[j] = 0.0;
+    for (int j = 0; j < nb; ++j) s_head[j] = 0.0;
+    for (int t = 0; t < w; ++t) {
+        const int pos = nb - w + t;            /* last visible key of this query */
+        const size_t row = ((size_t)b * s->Hq + hq) * w + t;
+        for (int c = 0; c < d; ++c) qrow[c] = load_elem(job->q, job->dtype, row * d + c);
 
-    for (int hl = 0; hl < g; ++hl) {
-        const int hq = h * g + hl;
-        for (int j = 0; j < nb; ++j) s_head[j] = 0.0;
-        for (int t = 0; t < w; ++t) {
-            const int pos = nb - w + t;            /* last visible key of this query */
-            const size_t row = ((size_t)b * s->Hq + hq) * w + t;
-            for (int c = 0; c < d; ++c) qrow[c] = load_elem(job->q, job->dtype, row * d + c);
-
-            /* S1: logits, max, exponentials, normaliser */
-            double m = -INFINITY;
-            for (int j = 0; j <= pos; ++j) {
-                double acc = 0.0;
-                for (int c = 0; c < d; ++c)
-                    acc += qrow[c] * load_elem(job->k, job->dtype, kv_base + (size_t)j * d + c);
-                x[j] = acc * inv_sqrt_d;
-                if (x[j] > m) m = x[j];
-            }
-            double l = 0.0;
-            for (int j = 0; j <= pos; ++j) {
-                e[j] = exp(x[j] - m);
-                l += e[j];
-            }
-            /* a = sum_j p_j v_j */
-            for (int c = 0; c < d; ++c) a[c] = 0.0;
-            for (int j = 0; j <= pos; ++j) {
-                const double p = e[j] / l;
-                /* S2: a probability rounded to 1 is rejected */
-                if (p == 1.0 && job->kind == ORACLE_KIND_DROPKV) return ORACLE_SINGULAR;
-                for (int c = 0; c < d; ++c)
-                    a[c] += p * load_elem(job->v, job->dtype, kv_base + (size_t)j * d + c);
-            }
-            if (job->m_out) job->m_out[row] = m;
-            if (job->l_out) job->l_out[row] = l;
-            if (job->a_out)
-                for (int c = 0; c < d; ++c) job->a_out[row * d + c] = a[c];
-
-            if (job->kind == ORACLE_KIND_SNAPKV) {
-                /* SnapKV: the attention probability of every visible key */
-                for (int j = 0; j <= pos; ++j) s_head[j] += e[j] / l;
-                continue;
-            }
-            /* S3: ||p_j / (1 - p_j) (a - v_j)||^2 for every visible key */
-            for (int j = 0; j <= pos; ++j) {
-                const double p = e[j] / l;
-                const double one_minus_p = (l - e[j]) / l;
-                const double ratio = p / one_minus_p;
-                double dist = 0.0;
-                for (int c = 0; c < d; ++c) {
-                    const double diff = a[c] - load_elem(job->v, job->dtype, kv_base + (size_t)j * d + c);
-                    dist += diff * diff;
-                }
-                s_head[j] += ratio * ratio * dist;
-            }
+        /* S1: logits, max, exponentials, normaliser */
+        double m = -INFINITY;
+        for (int j = 0; j <= pos; ++j) {
+            double acc = 0.0;
+            for (int c = 0; c < d; ++c)
+                acc += qrow[c] * load_elem(job->k, job->dtype, kv_base + (size_t)j * d + c);
+            x[j] = acc * inv_sqrt_d;
+            if (x[j] > m) m = x[j];
         }
-        for (int j = 0; j < nb; ++j) s_sum[j] += s_head[j];
+        double l = 0.0;
+        for (int j = 0; j <= pos; ++j) {
+            e[j] = exp(x[j] - m);
+            l += e[j];
+        }
+        /* a = sum_j p_j v_j */
+        for (int c = 0; c < d; ++c) a[c] = 0.0;
+        for (int j = 0; j <= pos; ++j) {
+            const double p = e[j] / l;
+            /* S2: a probability rounded to 1 is rejected */
+            if (p == 1.0 && job->kind == ORACLE_KIND_DROPKV) return ORACLE_SINGULAR;
+            for (int c = 0; c < d; ++c)
+                a[c] += p * load_elem(job->v, job->dtype, kv_base + (size_t)j * d + c);
+        }
+        if (job->m_out) job->m_out[row] = m;
+        if (job->l_out) job->l_out[row] = l;
+        if (job->a_out)
+            for (int c = 0; c < d; ++c) job->a_out[row * d + c] = a[c];
+
+        if (job->kind == ORACLE_KIND_SNAPKV) {
+            /* SnapKV: the attention probability of every visible key */
+            for (int j = 0; j <= pos; ++j) s_head[j] += e[j] / l;
+            continue;
+        }
+        /* S3: ||p_j / (1 - p_j) (a - v_j)||^2 for every visible key */
+        for (int j = 0; j <= pos; ++j) {
+            const double p = e[j] / l;
+            const double one_minus_p = (l - e[j]) / l;
+            const double ratio = p / one_minus_p;
+            double dist = 0.0;
+            for (int c = 0; c < d; ++c) {
+                const double diff = a[c] - load_elem(job->v, job->dtype, kv_base + (size_t)j * d + c);
+                dist += diff * diff;
+            }
+            s_head[j] += ratio * ratio * dist;
+        }
     }
+    return ORACLE_OK;
+}
+
+/* Steps S4-S5 of one unit: the mean over its g query heads (summed in query
+ * head order), MaxPool1D and protection. */
+static void finish_unit(score_job* job, int unit) {
+    const oracle_shape* s = job->s;
+    const int b = unit / s->Hkv;
+    const int g = s->Hq / s->Hkv;
+    const int nb = job->lengths[b];
+    const size_t n_max = (size_t)s->n_max;
+    const double* heads = job->s_heads + (size_t)unit * g * n_max;
+
     /* S4: mean over the g query heads of the group */
     double* raw = job->raw_out + (size_t)unit * n_max;
-    for (int j = 0; j < nb; ++j) raw[j] = s_sum[j] / (double)g;
+    for (int j = 0; j < nb; ++j) {
+        double sum = 0.0;
+        for (int hl = 0; hl < g; ++hl) sum += heads[(size_t)hl * n_max + j];
+        raw[j] = sum / (double)g;
+    }
     for (size_t j = (size_t)nb; j < n_max; ++j) raw[j] = NAN;
 
     /* S5: MaxPool1D (window clipped to the sequence), then protection */
@@ -189,31 +203,51 @@ static int score_unit(score_job* job, int unit, double* x, double* e, double* qr
     for (int j = nb - job->protect; j < nb; ++j)
         if (j >= 0) fin[j] = INFINITY;
     for (size_t j = (size_t)nb; j < n_max; ++j) fin[j] = NAN;
-    return ORACLE_OK;
 }
 
 static void* score_worker(void* arg) {
     score_job* job = (score_job*)arg;
     const oracle_shape* s = job->s;
+    const int g = s->Hq / s->Hkv, units = s->B * s->Hkv;
     const size_t n = (size_t)s->n_max;
+    if (job->phase == 2) {
+        for (;;) {
+            const int u = take_item(job);
+            if (u >= units) break;
+            finish_unit(job, u);
+        }
+        return NULL;
+    }
     double* x = (double*)malloc(n * sizeof(double));
     double* e = (double*)malloc(n * sizeof(double));
-    double* s_head = (double*)malloc(n * sizeof(double));
-    double* s_sum = (double*)malloc(n * sizeof(double));
     double* qrow = (double*)malloc((size_t)s->d * sizeof(double));
     double* a = (double*)malloc((size_t)s->d * sizeof(double));
-    if (!x || !e || !s_head || !s_sum || !qrow || !a) {
+    if (!x || !e || !qrow || !a) {
         set_status(job, ORACLE_NOMEM, -1);
     } else {
         for (;;) {
-            const int u = take_unit(job);
-            if (u >= s->B * s->Hkv) break;
-            const int st = score_unit(job, u, x, e, qrow, a, s_head, s_sum);
+            const int it = take_item(job);
+            if (it >= units * g) break;
+            const int u = it / g, hl = it % g;
+            const int st = score_head(job, u, hl, x, e, qrow, a, job->s_heads + ((size_t)u * g + hl) * n);
             if (st != ORACLE_OK) set_status(job, st, u);
         }
     }
-    free(x); free(e); free(s_head); free(s_sum); free(qrow); free(a);
+    free(x); free(e); free(qrow); free(a);
     return NULL;
+}
+
+/* Run score_worker on nthreads threads (the calling thread included). */
+static void run_phase(score_job* job, int phase, int nthreads) {
+    job->phase = phase;
+    job->next_item = 0;
+    pthread_t* th = (pthread_t*)malloc((size_t)nthreads * sizeof(pthread_t));
+    int started = 0;
+    for (int i = 1; i < nthreads && th; ++i)
+        if (pthread_create(&th[i], NULL, score_worker, job) == 0) started = i; else break;
+    score_worker(job);
+    for (int i = 1; i <= started; ++i) pthread_join(th[i], NULL);
+    free(th);
 }
 
 static int check_shape(const oracle_shape* s) {
@@ -241,18 +275,16 @@ int oracle_score_kind(const oracle_shape* s, int kind, int dtype, const void* q,
     job.m_out = m_out; job.l_out = l_out; job.a_out = a_out;
     job.raw_out = raw_out; job.final_out = final_out;
     job.status = ORACLE_OK; job.singular_unit = -1;
+    const int units = s->B * s->Hkv, g = s->Hq / s->Hkv;
+    job.s_heads = (double*)malloc((size_t)units * g * (size_t)s->n_max * sizeof(double));
+    if (!job.s_heads) return ORACLE_NOMEM;
     pthread_mutex_init(&job.lock, NULL);
 
-    int units = s->B * s->Hkv;
     if (nthreads < 1) nthreads = 1;
-    if (nthreads > units) nthreads = units;
-    pthread_t* th = (pthread_t*)malloc((size_t)nthreads * sizeof(pthread_t));
-    int started = 0;
-    for (int i = 1; i < nthreads; ++i)
-        if (pthread_create(&th[i], NULL, score_worker, &job) == 0) started = i; else break;
-    score_worker(&job);
-    for (int i = 1; i <= started; ++i) pthread_join(th[i], NULL);
-    free(th);
+    /* phase 1: S1-S3 per (unit, query head); phase 2: S4-S5 per unit */
+    run_phase(&job, 1, nthreads > units * g ? units * g : nthreads);
+    if (job.status == ORACLE_OK) run_phase(&job, 2, nthreads > units ? units : nthreads);
+    free(job.s_heads);
     pthread_mutex_destroy(&job.lock);
     if (singular_unit) *singular_unit = job.singular_unit;
     return job.status;

@@ -15,7 +15,8 @@ MUTATIONS = {
     "causal_diagonal_dropped": ("const int pos = nb - w + t;", "const int pos = nb - w + t - 1;"),
     "ratio_without_one_minus_p": ("const double ratio = p / one_minus_p;", "const double ratio = p;"),
     "residual_sign": ("const double diff = a[c] - load_elem", "const double diff = a[c] + load_elem"),
-    "gqa_sum_not_mean": ("raw[j] = s_sum[j] / (double)g;", "raw[j] = s_sum[j];"),
+    "gqa_sum_not_mean": ("raw[j] = sum / (double)g;", "raw[j] = sum;"),
+    "gqa_last_head_dropped": ("for (int hl = 0; hl < g; ++hl) sum += heads", "for (int hl = 0; hl + 1 < g; ++hl) sum += heads"),
     "gqa_interleaved_heads": ("const int hq = h * g + hl;", "const int hq = hl * s->Hkv + h;"),
     "scale_1_over_d": ("1.0 / sqrt((double)d)", "1.0 / (double)d"),
     "unnormalised_output": ("a[c] += p * load_elem", "a[c] += e[j] * load_elem"),
