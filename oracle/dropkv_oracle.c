@@ -105,7 +105,7 @@ static void set_status(score_job* job, int st, int unit) {
 /* One query head hl of one (b, KV head) unit: steps S1-S3 for its w window
  * rows, summed over the rows into s_head[0, n_b). */
 static int score_head(score_job* job, int unit, int hl, double* x, double* e, double* qrow, double* a,
-                      double* s_head) {
+                      double* ar, double* s_head) {
     const oracle_shape* s = job->s;
     const int b = unit / s->Hkv, h = unit % s->Hkv;
     const int g = s->Hq / s->Hkv, d = s->d, w = s->w;
@@ -153,8 +153,34 @@ static int score_head(score_job* job, int unit, int hl, double* x, double* e, do
             for (int j = 0; j <= pos; ++j) s_head[j] += e[j] / l;
             continue;
         }
-        /* S3: ||p_j / (1 - p_j) (a - v_j)||^2 for every visible key */
+        /* S3: ||p_j / (1 - p_j) (a - v_j)||^2 for every visible key.  That
+         * vector is the change of the output when key j is deleted,
+         * a_{-j} - a, which also equals p_j (a_{-j} - v_j) (a = p_j v_j +
+         * (1 - p_j) a_{-j}).  For the one key that may hold more than half of
+         * the row's mass, a - v_j and l - e_j cancel as p_j nears 1 (at
+         * 1 - p_j = 1e-14 the closed form keeps one digit), so its term is
+         * taken in the second form, with the other keys' mass and output
+         * summed on their own. */
         for (int j = 0; j <= pos; ++j) {
+            if (e[j] > 0.5 * l) {
+                double l_rest = 0.0;
+                for (int c = 0; c < d; ++c) ar[c] = 0.0;
+                for (int i = 0; i <= pos; ++i) {
+                    if (i == j) continue;
+                    l_rest += e[i];
+                    for (int c = 0; c < d; ++c)
+                        ar[c] += e[i] * load_elem(job->v, job->dtype, kv_base + (size_t)i * d + c);
+                }
+                /* l_rest > 0 here: otherwise p_j == 1.0 was rejected above */
+                const double p_dom = e[j] / (e[j] + l_rest);
+                double dist_rest = 0.0;
+                for (int c = 0; c < d; ++c) {
+                    const double diff = ar[c] / l_rest - load_elem(job->v, job->dtype, kv_base + (size_t)j * d + c);
+                    dist_rest += diff * diff;
+                }
+                s_head[j] += p_dom * p_dom * dist_rest;
+                continue;
+            }
             const double p = e[j] / l;
             const double one_minus_p = (l - e[j]) / l;
             const double ratio = p / one_minus_p;
@@ -222,18 +248,19 @@ static void* score_worker(void* arg) {
     double* e = (double*)malloc(n * sizeof(double));
     double* qrow = (double*)malloc((size_t)s->d * sizeof(double));
     double* a = (double*)malloc((size_t)s->d * sizeof(double));
-    if (!x || !e || !qrow || !a) {
+    double* ar = (double*)malloc((size_t)s->d * sizeof(double));
+    if (!x || !e || !qrow || !a || !ar) {
         set_status(job, ORACLE_NOMEM, -1);
     } else {
         for (;;) {
             const int it = take_item(job);
             if (it >= units * g) break;
             const int u = it / g, hl = it % g;
-            const int st = score_head(job, u, hl, x, e, qrow, a, job->s_heads + ((size_t)u * g + hl) * n);
+            const int st = score_head(job, u, hl, x, e, qrow, a, ar, job->s_heads + ((size_t)u * g + hl) * n);
             if (st != ORACLE_OK) set_status(job, st, u);
         }
     }
-    free(x); free(e); free(qrow); free(a);
+    free(x); free(e); free(qrow); free(a); free(ar);
     return NULL;
 }
 

@@ -20,7 +20,7 @@ import torch
 import oracle
 from kv_cache_eviction_dropkv_gb300 import DropKV, _binding as B, synth
 from tests._gpu import DEV, _compare, _custom, _run, _run_custom
-from tests._parity import check_scores, deletion_score
+from tests._parity import deletion_score
 
 pytestmark = pytest.mark.gpu
 
@@ -133,20 +133,20 @@ def test_sink_at_one_minus_1e9():
     _compare(wl, op, k, v, ref, "sink 20.7 nats")
 
 
-def test_sink_just_short_of_double_precision_matches_deletion():
+def test_sink_just_short_of_double_precision():
     """About 30 nats (1 - p near 1e-13): p does not round to 1 in double
-    precision, so the input is scored.  Here the fp64 closed form of the oracle
-    loses its digits (each other key's e is below half an ulp of the sink's,
-    so its sum l drops them), and the sink's score is checked against fp64
-    deletion instead; every other key's score against the oracle."""
+    precision, so the input is scored.  The closed form would keep three
+    digits here; the oracle takes the sink in the deletion form and so does
+    the GPU's dominant-key path.  Every output against the oracle, and the
+    sink's score also against fp64 deletion from the logits."""
     wl = synth.make_workload("llama8b_gqa_d128_n32k", n_max=6000, sink_margin=30.0)
     s = wl.spec
-    ref = oracle.score(wl.q, wl.k, wl.v, wl.lengths.numpy(), s.pool_kernel, s.protect)
-    op, _, _, flags = _run(wl)
+    ref = oracle.run_path(wl.q, wl.k, wl.v, wl.lengths, wl.evict_k, s.pool_kernel, s.protect)
+    op, k, v, flags = _run(wl)
+    _compare(wl, op, k, v, ref, "sink 30 nats")
     raw = op.raw_scores.cpu().numpy()
     dl = deletion_score(*(t.double().numpy() for t in (wl.q, wl.k, wl.v)), wl.lengths.numpy(), j=0)
     np.testing.assert_allclose(raw[:, :, 0], dl, rtol=2e-3)
-    check_scores(raw[:, :, 1:], ref["raw"][:, :, 1:], wl.lengths.numpy() - 1, "sink 30 nats raw, keys > 0")
 
 
 def _run_nocheck(wl):

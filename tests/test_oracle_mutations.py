@@ -26,6 +26,10 @@ MUTATIONS = {
     "tie_break_reversed": ("return (a->idx > b->idx) - (a->idx < b->idx);",
                            "return (a->idx < b->idx) - (a->idx > b->idx);"),
     "square_not_taken": ("s_head[j] += ratio * ratio * dist;", "s_head[j] += ratio * dist;"),
+    "dominant_key_in_its_own_rest": ("if (i == j) continue;", "if (i == j && i < 0) continue;"),
+    "dominant_square_not_taken": ("s_head[j] += p_dom * p_dom * dist_rest;", "s_head[j] += p_dom * dist_rest;"),
+    "dominant_rest_unnormalised": ("const double diff = ar[c] / l_rest - load_elem",
+                                   "const double diff = ar[c] - load_elem"),
     "snapkv_unnormalised": ("for (int j = 0; j <= pos; ++j) s_head[j] += e[j] / l;",
                             "for (int j = 0; j <= pos; ++j) s_head[j] += e[j];"),
     "snapkv_singular_rule": ("if (p == 1.0 && job->kind == ORACLE_KIND_DROPKV) return ORACLE_SINGULAR;",
@@ -47,6 +51,7 @@ def _run_pins():
     pins.test_snapkv_raw_vs_torch_softmax(42)
     pins.test_snapkv_has_no_singular_rule()
     pins.test_select_layer_vs_stable_sort(0)
+    pins.test_sink_score_equals_deletion_near_one(13.8)
 
 
 def test_unmodified_source_passes(tmp_path):

@@ -219,19 +219,19 @@ def test_singular_input_rejected():
     assert np.all(np.isfinite(res["raw"]))
 
 
-@pytest.mark.parametrize("margin", [6.9, 13.8, 20.7])
+@pytest.mark.parametrize("margin", [6.9, 13.8, 20.7, 27.6, 31.0])
 def test_sink_score_equals_deletion_near_one(margin):
-    """A sink carrying p = 1 - 1e-3, 1 - 1e-6 and 1 - 1e-9 of every row's mass:
-    the oracle's closed form (1 - p as (l - e) / l, |a - v| directly) against
-    deletion evaluated without cancellation (the other keys' output and mass
-    summed on their own).  fp64 keeps the closed form exact to about 1e-7
-    down to 1 - p = 1e-9; below about 1e-12 its sum l drops the other keys'
-    mass and deletion is the reference (the GPU tests do that)."""
+    """A sink carrying p = 1 - 1e-3 ... 1 - 3e-14 of every row's mass: the
+    oracle's score of the sink against deletion evaluated from the logits
+    (softmax over the other keys, their output and mass summed on their own),
+    to 1e-9.  The closed form p/(1 - p) (a - v) would keep one digit at
+    1 - p = 1e-14; the oracle takes the key above half the mass in the equal
+    deletion form, so nothing cancels."""
     wl = synth.make_workload("llama8b_gqa_d128_n32k", n_max=1500, sink_margin=margin)
     s = wl.spec
     res = oracle.score(wl.q, wl.k, wl.v, wl.lengths.numpy(), 1, 0)
     dl = deletion_score(*(t.double().numpy() for t in (wl.q, wl.k, wl.v)), wl.lengths.numpy(), j=0)
-    np.testing.assert_allclose(res["raw"][:, :, 0], dl, rtol=2e-6)
+    np.testing.assert_allclose(res["raw"][:, :, 0], dl, rtol=1e-9)
     # and the rows really are in that regime
     q, k = wl.q.double().numpy(), wl.k.double().numpy()
     x0 = np.einsum("htd,hd->ht", q[0], np.repeat(k[0, :, 0], s.g, axis=0)) / math.sqrt(s.d)
