@@ -36,51 +36,84 @@ class dropkv_shape(ctypes.Structure):
 
 _lock = threading.Lock()
 _lib = None
+_active = None          # a library loaded by use_library(), else None
 
 
 def library_path() -> str:
     return _build.LIB_PATH
 
 
+def _load(path):
+    if not os.path.exists(path):
+        raise RuntimeError("%s is not built; run __graft_entry__.build()" % path)
+    L = ctypes.CDLL(path)
+    P, I32, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+    SH = ctypes.POINTER(dropkv_shape)
+    L.dropkv_workspace_size.argtypes = [SH]
+    L.dropkv_workspace_size.restype = SZ
+    L.dropkv_score.argtypes = [SH, P, P, P, P, I32, I32, P, P, P, SZ, P, P]
+    L.dropkv_score.restype = ctypes.c_int
+    L.dropkv_score_timed.argtypes = [SH, I32, P, P, P, P, I32, I32, P, P, P, SZ, P, P, P]
+    L.dropkv_score_timed.restype = ctypes.c_int
+    L.dropkv_score_noalloc.argtypes = [SH, P, P, P, P, I32, I32, P, P, P, P]
+    L.dropkv_score_noalloc.restype = ctypes.c_int
+    L.dropkv_select.argtypes = [SH, P, P, P, I32, P, P, P, SZ, P, P]
+    L.dropkv_select.restype = ctypes.c_int
+    L.dropkv_compact.argtypes = [SH, P, P, P, P, I32, P, P, P, P]
+    L.dropkv_compact.restype = ctypes.c_int
+    L.dropkv_evict.argtypes = [SH, P, P, P, P, P, I32, I32, P, P, P, P, I32, P, P, P, SZ, P, P]
+    L.dropkv_evict.restype = ctypes.c_int
+    L.dropkv_evict_ex.argtypes = [SH, I32, P, P, P, P, P, I32, I32, P, P, P, P, I32, P, P, P, SZ, P, P]
+    L.dropkv_evict_ex.restype = ctypes.c_int
+    L.dropkv_score_ex.argtypes = [SH, I32, P, P, P, P, I32, I32, P, P, P, SZ, P, P]
+    L.dropkv_score_ex.restype = ctypes.c_int
+    L.dropkv_select_layer.argtypes = [SH, P, P, P, I32, P, P, P, SZ, P, P]
+    L.dropkv_select_layer.restype = ctypes.c_int
+    L.dropkv_compact_heads.argtypes = [SH, P, P, P, P, I32, P, P, P, P]
+    L.dropkv_compact_heads.restype = ctypes.c_int
+    L.dropkv_read_status.argtypes = [P, P, ctypes.POINTER(ctypes.c_uint32)]
+    L.dropkv_read_status.restype = ctypes.c_int
+    L.dropkv_version.argtypes = []
+    L.dropkv_version.restype = ctypes.c_char_p
+    if hasattr(L, "dropkv_test_skip_pass2_k"):
+        L.dropkv_test_skip_pass2_k.argtypes = [I32, I32]
+        L.dropkv_test_skip_pass2_k.restype = ctypes.c_int
+    return L
+
+
 def lib():
-    """Load libdropkv.so (raises if it was not built)."""
+    """The library the calls go to: libdropkv.so (raises if it was not
+    built), or the one a use_library() block selected."""
     global _lib
+    if _active is not None:
+        return _active
     with _lock:
         if _lib is None:
-            path = _build.LIB_PATH
-            if not os.path.exists(path):
-                raise RuntimeError("libdropkv.so is not built (%s); run __graft_entry__.build()" % path)
-            L = ctypes.CDLL(path)
-            P, I32, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
-            SH = ctypes.POINTER(dropkv_shape)
-            L.dropkv_workspace_size.argtypes = [SH]
-            L.dropkv_workspace_size.restype = SZ
-            L.dropkv_score.argtypes = [SH, P, P, P, P, I32, I32, P, P, P, SZ, P, P]
-            L.dropkv_score.restype = ctypes.c_int
-            L.dropkv_score_timed.argtypes = [SH, I32, P, P, P, P, I32, I32, P, P, P, SZ, P, P, P]
-            L.dropkv_score_timed.restype = ctypes.c_int
-            L.dropkv_score_noalloc.argtypes = [SH, P, P, P, P, I32, I32, P, P, P, P]
-            L.dropkv_score_noalloc.restype = ctypes.c_int
-            L.dropkv_select.argtypes = [SH, P, P, P, I32, P, P, P, SZ, P, P]
-            L.dropkv_select.restype = ctypes.c_int
-            L.dropkv_compact.argtypes = [SH, P, P, P, P, I32, P, P, P, P]
-            L.dropkv_compact.restype = ctypes.c_int
-            L.dropkv_evict.argtypes = [SH, P, P, P, P, P, I32, I32, P, P, P, P, I32, P, P, P, SZ, P, P]
-            L.dropkv_evict.restype = ctypes.c_int
-            L.dropkv_evict_ex.argtypes = [SH, I32, P, P, P, P, P, I32, I32, P, P, P, P, I32, P, P, P, SZ, P, P]
-            L.dropkv_evict_ex.restype = ctypes.c_int
-            L.dropkv_score_ex.argtypes = [SH, I32, P, P, P, P, I32, I32, P, P, P, SZ, P, P]
-            L.dropkv_score_ex.restype = ctypes.c_int
-            L.dropkv_select_layer.argtypes = [SH, P, P, P, I32, P, P, P, SZ, P, P]
-            L.dropkv_select_layer.restype = ctypes.c_int
-            L.dropkv_compact_heads.argtypes = [SH, P, P, P, P, I32, P, P, P, P]
-            L.dropkv_compact_heads.restype = ctypes.c_int
-            L.dropkv_read_status.argtypes = [P, P, ctypes.POINTER(ctypes.c_uint32)]
-            L.dropkv_read_status.restype = ctypes.c_int
-            L.dropkv_version.argtypes = []
-            L.dropkv_version.restype = ctypes.c_char_p
-            _lib = L
+            _lib = _load(_build.LIB_PATH)
     return _lib
+
+
+class use_library:
+    """Route this module's calls to another build of the library (the test
+    build of include/dropkv_test_hooks.h) inside a with-block."""
+
+    _cache = {}
+
+    def __init__(self, path):
+        with _lock:
+            if path not in self._cache:
+                self._cache[path] = _load(path)
+        self.L = self._cache[path]
+
+    def __enter__(self):
+        global _active
+        self.prev, _active = _active, self.L
+        return self.L
+
+    def __exit__(self, *exc):
+        global _active
+        _active = self.prev
+        return False
 
 
 def declared_functions(header: str = None):
@@ -88,7 +121,7 @@ def declared_functions(header: str = None):
     header = header or os.path.join(_build.INCLUDE, "dropkv.h")
     text = open(header).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(dropkv_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(dropkv_[a-z0-9_]+)\s*\(", text)))
 
 
 def _ptr(t):

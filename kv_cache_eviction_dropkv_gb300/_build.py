@@ -3,6 +3,10 @@
 Compiles csrc/*.cu in parallel and links kv_cache_eviction_dropkv_gb300/_lib/libdropkv.so.
 The library links the shared CUDA runtime (libcudart.so.13), so in a process
 that imported torch first it shares torch's runtime and streams.
+
+The "test_hooks" variant (libdropkv_test_hooks.so, -DDROPKV_TEST_HOOKS) is the
+same source with the hooks of include/dropkv_test_hooks.h and a 10 ms pipeline
+wait limit; only the tests build and load it.
 """
 from __future__ import annotations
 
@@ -15,6 +19,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_lib")
 LIB_PATH = os.path.join(OUT_DIR, "libdropkv.so")
+VARIANTS = {"": [], "test_hooks": ["-DDROPKV_TEST_HOOKS"]}
 ROOT = os.path.dirname(HERE)
 INCLUDE = os.path.join(ROOT, "include")
 
@@ -38,22 +43,29 @@ def _deps():
     return _sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(INCLUDE, "*.h")) + [__file__]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB_PATH):
+def lib_path(variant: str = "") -> str:
+    return LIB_PATH if not variant else os.path.join(OUT_DIR, "libdropkv_%s.so" % variant)
+
+
+def up_to_date(variant: str = "") -> bool:
+    path = lib_path(variant)
+    if not os.path.exists(path):
         return False
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(path)
     return all(os.path.getmtime(f) <= t for f in _deps())
 
 
-def build_library(force: bool = False, verbose: bool = False) -> str:
-    if not force and up_to_date():
-        return LIB_PATH
-    os.makedirs(OUT_DIR, exist_ok=True)
+def build_library(force: bool = False, verbose: bool = False, variant: str = "") -> str:
+    path = lib_path(variant)
+    if not force and up_to_date(variant):
+        return path
+    obj_dir = OUT_DIR if not variant else os.path.join(OUT_DIR, variant)
+    os.makedirs(obj_dir, exist_ok=True)
     nvcc = _nvcc()
     objs, procs = [], []
     for src in _sources():
-        obj = os.path.join(OUT_DIR, os.path.basename(src)[:-3] + ".o")
-        cmd = [nvcc, *ARCH, *NVCC_FLAGS, "-I", INCLUDE, "-c", src, "-o", obj]
+        obj = os.path.join(obj_dir, os.path.basename(src)[:-3] + ".o")
+        cmd = [nvcc, *ARCH, *NVCC_FLAGS, *VARIANTS[variant], "-I", INCLUDE, "-c", src, "-o", obj]
         if verbose:
             print(" ".join(cmd))
         procs.append((src, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)))
@@ -67,9 +79,9 @@ def build_library(force: bool = False, verbose: bool = False) -> str:
             print(out.decode(errors="replace"))
     if failed:
         raise RuntimeError("nvcc failed:\n" + "\n".join("%s\n%s" % f for f in failed))
-    tmp = LIB_PATH + ".tmp%d" % os.getpid()
+    tmp = path + ".tmp%d" % os.getpid()
     cmd = [nvcc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
            "-Xlinker", "-rpath,/usr/local/cuda/lib64"]
     subprocess.run(cmd, check=True)
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, path)
+    return path

@@ -963,6 +963,13 @@ __device__ __forceinline__ uint64_t sqdiff_bf16x2(uint32_t w, float c0, float c1
   return f2_fma(dv, dv, acc);
 }
 
+#ifdef DROPKV_TEST_HOOKS
+// Test build only: the (unit, tile) whose K copy the scoring pass leaves out,
+// so that the MMA issuer's bounded wait for it runs out and the pipeline takes
+// its timeout exit.  {-1, -1}: none.
+__device__ int g_test_skip_k[2] = {-1, -1};
+#endif
+
 // TMA producer (one lane): fills the K ring (and the V ring when HAS_V) tile
 // by tile; each slot also carries its tile index, -1 ending the stream.
 // dynamic: tiles claimed from the unit's counter (the first claim is passed
@@ -989,9 +996,14 @@ __device__ __forceinline__ bool p2_produce(uint8_t* sK, uint8_t* sV, Pass2Small&
     }
     S.ktile[ks] = tile;
     S.vtile[vs] = tile;
-    mbar_arrive_expect_tx(&S.kfull[ks], kTileBytes);
-    tma_load_3d(sK + ks * kTileBytes, tmk, &S.kfull[ks], 0, tile * kTile, unit);
-    tma_load_3d(sK + ks * kTileBytes + kHalfTile, tmk, &S.kfull[ks], 64, tile * kTile, unit);
+#ifdef DROPKV_TEST_HOOKS
+    if (unit != g_test_skip_k[0] || tile != g_test_skip_k[1])   // the test build may leave one K copy out
+#endif
+    {
+      mbar_arrive_expect_tx(&S.kfull[ks], kTileBytes);
+      tma_load_3d(sK + ks * kTileBytes, tmk, &S.kfull[ks], 0, tile * kTile, unit);
+      tma_load_3d(sK + ks * kTileBytes + kHalfTile, tmk, &S.kfull[ks], 64, tile * kTile, unit);
+    }
     if (!HAS_V) {
       mbar_arrive(&S.vfull[vs]);
     } else {
@@ -1621,3 +1633,11 @@ cudaError_t launch_score(const AttnParams& p, int NR, const CUtensorMap& tk, con
 }
 
 }  // namespace dropkv
+
+#ifdef DROPKV_TEST_HOOKS
+#include "dropkv_test_hooks.h"
+extern "C" dropkv_status dropkv_test_skip_pass2_k(int32_t unit, int32_t tile) {
+  const int v[2] = {unit, tile};
+  return cudaMemcpyToSymbol(dropkv::g_test_skip_k, v, sizeof v) == cudaSuccess ? DROPKV_OK : DROPKV_ERR_CUDA;
+}
+#endif

@@ -9,7 +9,11 @@
 namespace dropkv {
 
 // Longest any pipeline wait may spin before it gives up and flags a timeout.
+#ifdef DROPKV_TEST_HOOKS
+constexpr uint64_t kWaitLimitNs = 10000000ull;     // 10 ms in the test build (pipeline timeout tests)
+#else
 constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s
+#endif
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

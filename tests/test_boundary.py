@@ -2,6 +2,7 @@
 declares (CPU), host-side validation rejects bad calls without launching, and
 device-side checks report through the status word (GPU)."""
 import ctypes
+import os
 import subprocess
 
 import numpy as np
@@ -27,6 +28,16 @@ def test_library_exports_every_declared_symbol():
     assert exported == declared, (exported, declared)
     lib.dropkv_version.restype = ctypes.c_char_p
     assert b"sm_103a" in lib.dropkv_version()
+
+
+def test_product_library_exports_no_test_hook():
+    """include/dropkv_test_hooks.h is served only by the test build."""
+    path = _build.build_library()
+    hooks = B.declared_functions(os.path.join(_build.INCLUDE, "dropkv_test_hooks.h"))
+    assert hooks == ["dropkv_test_skip_pass2_k"]
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True, check=True).stdout
+    assert not any(h in out for h in hooks)
+    assert "DROPKV_TEST_HOOKS" not in " ".join(_build.NVCC_FLAGS)
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):

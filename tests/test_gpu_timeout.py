@@ -6,6 +6,14 @@ to DROPKV_ERR_TIMEOUT, and the context stays usable for the next call.
 The probe kernel is compiled here from the library's own wait primitive
 (csrc/sm103_ptx.cuh: mbar_wait): one thread waits on an mbarrier that no one
 arrives at; another case sets the abort flag that every pipeline role polls.
+
+The pipeline cases run the real scoring call from the test build of the
+library (libdropkv_test_hooks.so: 10 ms wait limit, include/dropkv_test_hooks.h),
+told to leave out one K tile copy of one head: that CTA's MMA issuer gives up,
+every role of the CTA leaves its loop, copies and MMAs in flight are waited
+for, the tensor memory is released, the status reads DROPKV_ERR_TIMEOUT, the
+other heads are scored as usual, and the next call on the same context is
+clean.
 """
 import ctypes
 import os
@@ -16,7 +24,10 @@ import numpy as np
 import pytest
 import torch
 
-from kv_cache_eviction_dropkv_gb300 import DropKV, _binding as B, synth
+import time
+
+from kv_cache_eviction_dropkv_gb300 import DropKV, _binding as B, _build, synth
+from tests._parity import check_scores
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda", 0) if torch.cuda.is_available() else None
@@ -107,3 +118,51 @@ def test_wait_returns_when_another_role_aborts(probe):
     assert flags & B.FLAG_TIMEOUT and code == 8
     assert 0.04 < secs < 0.5, secs
     _context_still_works()
+
+
+@pytest.fixture(scope="module")
+def hooks_lib():
+    return _build.build_library(variant="test_hooks")
+
+
+@pytest.mark.parametrize("case", ["dynamic_split", "dominant_split"])
+def test_scoring_pipeline_times_out_and_recovers(hooks_lib, case):
+    if case == "dynamic_split":
+        wl = synth.make_workload("llama8b_gqa_d128_n32k", n_max=16384)
+        unit, tile = 3, 40
+    else:   # a sink of p ~ 0.999: unit 0's first split runs in the dominant mode
+        wl = synth.make_workload("llama8b_gqa_d128_n32k", n_max=16384, sink_margin=float(np.log(999.0)))
+        unit, tile = 0, 5
+    s = wl.spec
+    q, k, v, lengths = wl.q.to(DEV), wl.k.to(DEV), wl.v.to(DEV), wl.lengths.to(DEV)
+    ref = DropKV(s.B, s.Hq, s.Hkv, s.d, s.n_max, s.w, s.pool_kernel, s.protect, device=DEV)
+    ref.score(q, k, v, lengths)
+    assert ref.check() == 0
+    want = ref.raw_scores.cpu().numpy()
+    others = [h for h in range(s.Hkv) if h != unit]
+    with B.use_library(hooks_lib) as L:
+        assert hasattr(L, "dropkv_test_skip_pass2_k")
+        op = DropKV(s.B, s.Hq, s.Hkv, s.d, s.n_max, s.w, s.pool_kernel, s.protect, device=DEV)
+        assert L.dropkv_test_skip_pass2_k(unit, tile) == 0
+        try:
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            op.score(q, k, v, lengths)
+            code, flags = B.dropkv_read_status(op.status)
+            secs = time.perf_counter() - t0
+        finally:
+            assert L.dropkv_test_skip_pass2_k(-1, -1) == 0
+        assert code == 8 and flags & B.FLAG_TIMEOUT, (code, flags)      # DROPKV_ERR_TIMEOUT
+        assert secs < 0.5, secs                                        # 10 ms waits, not the 1 s of the product
+        got = op.raw_scores.cpu().numpy()
+        check_scores(got[:, others], want[:, others], wl.lengths.numpy(), "heads the hook left alone")
+        # the same context, the hook off: a clean call, twice
+        for _ in range(2):
+            op.reset_status()
+            op.score(q, k, v, lengths)
+            assert op.check() == 0
+            check_scores(op.raw_scores.cpu().numpy(), want, wl.lengths.numpy(), "call after the timeout")
+    # and the product library on the same context
+    ref.reset_status()
+    ref.score(q, k, v, lengths)
+    assert ref.check() == 0
