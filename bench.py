@@ -61,6 +61,9 @@ def parse_args():
                     help="score kind: the DropKV perturbation score (default) or the SnapKV baseline")
     ap.add_argument("--select", choices=["head", "layer"], default="head",
                     help="bottom-k per KV head (default) or one pool per sequence over its KV heads (AdaDropKV)")
+    ap.add_argument("--decode", type=int, default=0, metavar="M",
+                    help="decode-time re-scoring: evict the workload once, append M decode tokens to the "
+                         "compacted cache, and time score -> select -> compact of M rows on that grown cache")
     return ap.parse_args()
 
 
@@ -108,8 +111,12 @@ def config_of(spec, lengths, score="dropkv", select="head"):
     return {"workload": spec.name, "score": score, "select": select, "B": spec.B, "Hq": spec.Hq, "Hkv": spec.Hkv, "d": spec.d, "n_max": spec.n_max,
             "n_tokens": int(sum(lengths)), "w": spec.w, "pool_kernel": spec.pool_kernel, "protect": spec.protect,
             "budget_pct_kept": spec.budget_pct, "inputs": "bf16",
-            "l2": "inputs larger than L2 (K+V %.0f MB); between steps a 256 MB write flushes L2 and a 256 MB read cleans it" % (
-                2 * spec.B * spec.Hkv * spec.n_max * spec.d * 2 / 1e6)}
+            "l2": "inputs %s than L2 (K+V %.0f MB); between steps a 256 MB write flushes L2 and a 256 MB read cleans it" % (
+                "larger" if kv_bytes(spec) > 129e6 else "smaller", kv_bytes(spec) / 1e6)}
+
+
+def kv_bytes(spec):
+    return 2 * spec.B * spec.Hkv * spec.n_max * spec.d * 2
 
 
 def workload_bytes(spec, lengths, kept, score="dropkv", select="head"):
@@ -244,6 +251,52 @@ def run_reference(args, spec, wl):
     print(json.dumps(line))
 
 
+def oracle_decode_workload(wl, m, seed):
+    """The decode-time workload of the reference arm: the oracle's prefill
+    kept set, gathered on the host, grown by the same m seeded tokens."""
+    import oracle
+    from kv_cache_eviction_dropkv_gb300.decode import append_decode_tokens
+    s = wl.spec
+    ref = oracle.run_path(wl.q, wl.k, wl.v, wl.lengths, wl.evict_k, s.pool_kernel, s.protect,
+                          nthreads=os.cpu_count() or 1)
+    idx = torch.from_numpy(ref["kept_idx"]).long().clamp(min=0)[..., None].expand(-1, -1, -1, s.d)
+    return append_decode_tokens(wl, torch.gather(wl.k, 2, idx), torch.gather(wl.v, 2, idx), m, seed)
+
+
+def window_rows_probe(spec, wl, dev, stream, m, reps):
+    """Upper bound on what an incremental re-score could save: a re-score has
+    to stream K and V through both passes for any new window row, so reusing
+    the w - m surviving rows' statistics would at most shrink window attention
+    to m rows per query head.  Times window attention on the same cache with
+    all w rows and with min(m, w) rows."""
+    from kv_cache_eviction_dropkv_gb300 import DropKV, _binding as B
+    out = {}
+    lengths = wl.lengths.to(dev)
+    k, v = wl.k.to(dev), wl.v.to(dev)
+    for rows in sorted({spec.w, min(m, spec.w)}):
+        op = DropKV(spec.B, spec.Hq, spec.Hkv, spec.d, spec.n_max, rows, spec.pool_kernel, spec.protect,
+                    out_rows=spec.n_max, device=dev)
+        q = wl.q[:, :, spec.w - rows:].contiguous().to(dev)
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(reps)]
+        for row in evs:
+            for e in row:
+                e.record(stream)
+        for i in range(reps):
+            B.dropkv_score_timed(op.shape, q, k, v, lengths, op.pool_kernel, op.protect, op.scores, None,
+                                 op.workspace, op.status, evs[i][1:6], stream)
+        torch.cuda.synchronize()
+        op.check(stream)
+        t = sorted(evs[i][1].elapsed_time(evs[i][2]) for i in range(reps))
+        t2 = sorted(evs[i][1].elapsed_time(evs[i][5]) for i in range(reps))
+        out["w%d" % rows] = {"window_attention_ms": t[reps // 2], "score_call_ms": t2[reps // 2]}
+    full, part = out["w%d" % spec.w], out["w%d" % min(m, spec.w)]
+    out["max_saving_ms"] = full["window_attention_ms"] - part["window_attention_ms"]
+    out["note"] = ("an incremental re-score still reads K and V in both passes (the new rows need their own "
+                   "window attention, and every surviving row's p and a change when rows are evicted); at most "
+                   "it runs window attention on min(m, w) instead of w rows per query head (medians of %d)" % reps)
+    return out
+
+
 def cpu_baseline(spec, wl, score="dropkv"):
     """The fp64 oracle on the host: the whole layer with one thread per core,
     and a bounded sample on one thread (one query head of one KV head over all
@@ -278,6 +331,9 @@ def main():
         if rank != 0:
             return
         wl = synth.make_workload(args.workload)
+        if args.decode:
+            wl = oracle_decode_workload(wl, args.decode, spec.seed + 1000)
+            spec = wl.spec
         run_reference(args, spec, wl)
         return
 
@@ -292,6 +348,10 @@ def main():
 
     # each rank scores its own layer (weak scaling, no data-path collective)
     wl = synth.make_workload(args.workload, seed=rank_seed(spec, rank))
+    if args.decode:
+        from kv_cache_eviction_dropkv_gb300.decode import grow_after_eviction
+        wl = grow_after_eviction(wl, args.decode, seed=rank_seed(spec, rank) + 1000, device=dev)
+        spec = wl.spec
     lengths_np = wl.lengths.numpy()
     kept_np = wl.kept_len()
     units = int(sum(lengths_np))
@@ -426,6 +486,11 @@ def main():
             "wall_s_timed": wall, "gpu_launches": kernels_per_step(spec.n_max, args.select) * K,
             "clocks": clocks}
 
+    if args.decode:
+        line["decode"] = {"m": args.decode, "cache_rows": int(spec.n_max),
+                          "reading": "prefill eviction, then m decode tokens appended to the compacted cache, "
+                                     "window moved to the newest w positions, m rows evicted again",
+                          "incremental": window_rows_probe(spec, wl, dev, stream, args.decode, 20)}
     if not args.no_e2e:
         line["e2e"] = e2e_leg(op, wl, dev, stream, args, world)
 
