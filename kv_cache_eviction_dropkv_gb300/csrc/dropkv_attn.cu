@@ -218,12 +218,14 @@ __device__ __forceinline__ float sumsq_bf16x8(const uint4 v, float acc) {
 // TMA producer of one ring: streams the tiles [t0, t0 + T) of one tensor into
 // a ring of DEPTH 32 KB stages.  K and V rings are driven by different lanes
 // of the producer warp, so each can run ahead of the consumers by its own depth.
+// The first `start` tiles were issued already (during the CTA's set-up).
 template <int DEPTH>
 __device__ __forceinline__ void stream_ring(uint8_t* ring, uint64_t* full, uint64_t* empty, const CUtensorMap* map,
-                                            int t0, int T, int unit, volatile int* abort, uint32_t* status) {
-  int issued = 0;
+                                            int t0, int T, int unit, int start, volatile int* abort,
+                                            uint32_t* status) {
+  int issued = start;
   bool ok = true;
-  for (int i = 0; i < T; ++i) {
+  for (int i = start; i < T; ++i) {
     const int s = i % DEPTH;
     if (i >= DEPTH && !mbar_wait(&empty[s], ((i / DEPTH) + 1) & 1, abort)) { ok = false; break; }
     mbar_arrive_expect_tx(&full[s], kTileBytes);
@@ -250,7 +252,10 @@ struct Pass1Cfg {
   static constexpr int VS0 = 3;                     // V ring depth (V is held until PV completes)
   static constexpr int KS = STATS ? KS0 + VS0 - 1 : KS0;
   static constexpr int VS = STATS ? 1 : VS0;
-  static constexpr int PB = NR <= 32 ? 2 : 1;       // P buffers
+  // One P buffer: the workers write P(i) once PV(i-1) is done.  Measured on
+  // GB300 at n = 128K, a second buffer made the pass slower (1.50 against
+  // 1.42 us per tile per CTA), and deeper K or V rings gained nothing.
+  static constexpr int PB = 1;
   static constexpr int kQBytes = NR * kDPad * 2;
   static constexpr int kPBytes = kTile * NR * 2;    // one of (hi, lo) of one P buffer
   static constexpr int kOffK = 0;
@@ -511,6 +516,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sP = sm + C::kOffP;
   Pass1Small& S = *reinterpret_cast<Pass1Small*>(sm + C::kOffSmall);
 
+  // The lengths, Q, K and V are the caller's, and the kernel before this one
+  // (a previous call's compaction, for one) may still be writing them.
+  grid_dep_wait();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const CtaWork wk = cta_work(p, blockIdx.x);
   if (wk.unit < 0) return;                  // left over: no work in this pass
@@ -521,21 +529,45 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int t1 = (int)((uint32_t)(split + 1) * (uint32_t)ntiles / (uint32_t)wk.nsplit);
   const int b = unit / p.Hkv, h = unit - b * p.Hkv;
   if (nb < p.w || nb > p.n_max) {           // invalid length: the unit is skipped
-    grid_dep_wait();
     if (tid == 0 && split == 0 && h == 0) atomicOr(p.status, DROPKV_FLAG_BAD_LENGTH);
     return;
   }
   const int R = p.R;
   const int T = max(0, t1 - t0);
 
-  if (tid == 0) {
+  // Set-up.  The producer lane sets up the rings' barriers itself and issues
+  // the first stages of both rings at once, so the first tiles are in flight
+  // while the other warps set up.
+  int k_issued = 0, v_issued = 0;
+  if (warp == kProducerWarp && lane == 0) {
     for (int i = 0; i < C::KS; ++i) { mbar_init(&S.kfull[i], 1); mbar_init(&S.kempty[i], 1); }
     for (int i = 0; i < C::VS; ++i) { mbar_init(&S.vfull[i], 1); mbar_init(&S.vempty[i], 1); }
+    S.abort = 0;
+    fence_mbar_init();
+    if (T > 0) {
+      tma_prefetch_desc(&tmk);
+      if (!STATS) tma_prefetch_desc(&tmv);
+      k_issued = min(T, C::KS);
+      for (int i = 0; i < k_issued; ++i) {
+        mbar_arrive_expect_tx(&S.kfull[i], kTileBytes);
+        tma_load_3d(sK + i * kTileBytes, &tmk, &S.kfull[i], 0, (t0 + i) * kTile, unit);
+        tma_load_3d(sK + i * kTileBytes + kHalfTile, &tmk, &S.kfull[i], 64, (t0 + i) * kTile, unit);
+      }
+      if (!STATS) {
+        v_issued = min(T, C::VS);
+        for (int i = 0; i < v_issued; ++i) {
+          mbar_arrive_expect_tx(&S.vfull[i], kTileBytes);
+          tma_load_3d(sV + i * kTileBytes, &tmv, &S.vfull[i], 0, (t0 + i) * kTile, unit);
+          tma_load_3d(sV + i * kTileBytes + kHalfTile, &tmv, &S.vfull[i], 64, (t0 + i) * kTile, unit);
+        }
+      }
+    }
+  }
+  if (tid == 0) {
     for (int i = 0; i < 2; ++i) { mbar_init(&S.sfull[i], 1); mbar_init(&S.sempty[i], kWorkerWarps); }
     for (int i = 0; i < C::PB; ++i) { mbar_init(&S.pfull[i], kWorkerWarps); mbar_init(&S.pempty[i], 1); }
     mbar_init(&S.ofull, 1);
     mbar_init(&S.drain, 1);
-    S.abort = 0;
     fence_mbar_init();
   }
   if (tid < kMaxR) {
@@ -548,10 +580,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const __nv_bfloat16* qsrc = p.q + ((size_t)b * p.Hq + (size_t)h * p.g) * p.w * p.d;
       stage_rows_sw128(sQ, qsrc, NR, R, p.d, p.d, tid, kWorkers);
       fence_proxy_async_smem();
-    }
-    if (warp == kProducerWarp && lane == 0) {
-      tma_prefetch_desc(&tmk);
-      if (!STATS) tma_prefetch_desc(&tmv);
     }
   }
   tc_fence_before();
@@ -566,8 +594,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (T > 0 && warp == kProducerWarp) {
     // ---------------------------------------------------- TMA producer: lane 0 K, lane 1 V
-    if (lane == 0) stream_ring<C::KS>(sK, S.kfull, S.kempty, &tmk, t0, T, unit, &S.abort, p.status);
-    else if (lane == 1 && !STATS) stream_ring<C::VS>(sV, S.vfull, S.vempty, &tmv, t0, T, unit, &S.abort, p.status);
+    // lane 0 issued the first stages of both rings during the set-up
+    const int kis = __shfl_sync(0xffffffffu, k_issued, 0), vis = __shfl_sync(0xffffffffu, v_issued, 0);
+    if (lane == 0) stream_ring<C::KS>(sK, S.kfull, S.kempty, &tmk, t0, T, unit, kis, &S.abort, p.status);
+    else if (lane == 1 && !STATS) stream_ring<C::VS>(sV, S.vfull, S.vempty, &tmv, t0, T, unit, vis, &S.abort, p.status);
     __syncwarp();
   } else if (T > 0 && warp == kMmaWarp) {
     // ---------------------------------------------------- MMA issuer
@@ -783,7 +813,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The MMA warp commits `drain` once, after its last MMA: a single-phase
     // wait.  (A parity wait on the per-tile `ofull` barrier would be ambiguous
     // here, since up to two PV commits may still be outstanding.)
-    grid_dep_wait();                              // earlier kernels are done before we write
     bool okw = true;
     if (!failed) okw = mbar_wait(&S.drain, 0, &S.abort);
     okw = __all_sync(0xffffffffu, okw);
@@ -834,7 +863,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (T == 0) {
     // empty split (past the end of a shorter sequence): publish an empty state
-    grid_dep_wait();
     const size_t part = (size_t)unit * p.splits + split;
     for (int idx = tid; idx < R; idx += kThreads)
       reinterpret_cast<float4*>(p.part_ml)[part * R + idx] = make_float4(-INFINITY, 0.f, 0.f, 0.f);
