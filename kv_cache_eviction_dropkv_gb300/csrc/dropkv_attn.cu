@@ -1411,50 +1411,125 @@ __device__ __forceinline__ bool p2_work(uint8_t* sV, uint8_t* sP, Pass2Small& S,
       const float v = warp_sum(lrest[r]);
       if (lane == 0) S.fx.red[wq][r0 + r] = v;
     }
-    named_bar(kBarAux, kWorkers);
+    // Stage, with independent loads (one round trip), the merge's O and L of
+    // the other splits for every dominated row and its dominant key's V row,
+    // in the V ring, idle now that the last MMA is done: [kMaxR][kDPad] f32
+    // O, [kMaxR][kDPad] bf16 V, [kMaxR] f32 L.
+    float* so = reinterpret_cast<float*>(sV);
+    __nv_bfloat16* svs = reinterpret_cast<__nv_bfloat16*>(sV + kMaxR * kDPad * 4);
+    float* sdl = reinterpret_cast<float*>(sV + kMaxR * kDPad * 6);
     const size_t rowbase = (size_t)unit * R;
+    const int d4 = p.d >> 2;
+    for (int idx = tid; idx < R * d4; idx += kWorkers) {
+      const int rr = idx / d4, c4 = idx - rr * d4;
+      const int jst = S.domj[rr];
+      if (((S.domf >> rr) & 1ull) && jst >= 0) {
+        reinterpret_cast<float4*>(so + rr * kDPad)[c4] =
+            reinterpret_cast<const float4*>(p.dom_o + (rowbase + rr) * p.d)[c4];
+        reinterpret_cast<uint2*>(svs + rr * kDPad)[c4] =
+            reinterpret_cast<const uint2*>(p.v + ((size_t)unit * p.n_max + jst) * p.d)[c4];
+        if (c4 == 0) sdl[rr] = p.dom_l[rowbase + rr];
+      }
+    }
+    named_bar(kBarAux, kWorkers);
+    // (a) every thread: the squared differences of its token for the
+    // dominated rows of its half, into [kMaxR][kDPad] f32 (also in the ring)
+    float* ssq = reinterpret_cast<float*>(sV + kMaxR * kDPad * 6 + kMaxR * 4);
 #pragma unroll
     for (int r = 0; r < HR; ++r) {
       if (!((dommask >> r) & 1u)) continue;       // the same in the whole warp
       const int rr = r0 + r;
-      const float lt =
-          p.dom_l[rowbase + rr] + ((S.fx.red[0][rr] + S.fx.red[1][rr]) + (S.fx.red[2][rr] + S.fx.red[3][rr]));
-      const int jst = S.domj[rr];
+      if (S.domj[rr] < 0) continue;               // the same in the whole warp
+      const float lt = sdl[rr] + ((S.fx.red[0][rr] + S.fx.red[1][rr]) + (S.fx.red[2][rr] + S.fx.red[3][rr]));
       float sq = 0.f;
-      if (jst >= 0 && tok < p.d) {
-        const float ar = (p.dom_o[(rowbase + rr) * p.d + tok] + o[r]) / lt;
-        const float vst = __bfloat162float(p.v[((size_t)unit * p.n_max + jst) * p.d + tok]);
-        const float df = ar - vst;
+      if (tok < p.d) {
+        const float ar = (so[rr * kDPad + tok] + o[r]) / lt;
+        const float df = ar - __bfloat162float(svs[rr * kDPad + tok]);
         sq = df * df;
       }
-      sq = warp_sum(sq);
-      if (lane == 0) {
-        S.fx.red2[wq][rr] = sq;
-        if (wq == 0) S.fx.ltot[rr] = lt;
+      ssq[rr * kDPad + tok] = sq;
+      if (tok == 0) S.fx.ltot[rr] = lt;
+    }
+    named_bar(kBarAux, kWorkers);
+    // (b) |a_rest - v*|^2 of each dominated row: 8 threads per row, 16
+    // tokens each in order, then a fixed butterfly over the 8
+    {
+      const int rr = tid >> 3, part = tid & 7;
+      const bool act = rr < R && ((S.domf >> rr) & 1ull) && S.domj[rr] >= 0;
+      float sum = 0.f;
+      if (act)
+        for (int c = part * 16; c < part * 16 + 16 && c < p.d; ++c) sum += ssq[rr * kDPad + c];
+      sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+      sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+      sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+      if (act && part == 0) S.fx.red2[0][rr] = sum;
+      if (R > 32) {   // rows 32 .. 63: a second pass
+        const int r2 = rr + 32;
+        const bool act2 = r2 < R && ((S.domf >> r2) & 1ull) && S.domj[r2] >= 0;
+        float sum2 = 0.f;
+        if (act2)
+          for (int c = part * 16; c < part * 16 + 16 && c < p.d; ++c) sum2 += ssq[r2 * kDPad + c];
+        sum2 += __shfl_xor_sync(0xffffffffu, sum2, 1);
+        sum2 += __shfl_xor_sync(0xffffffffu, sum2, 2);
+        sum2 += __shfl_xor_sync(0xffffffffu, sum2, 4);
+        if (act2 && part == 0) S.fx.red2[0][r2] = sum2;
       }
     }
     named_bar(kBarAux, kWorkers);
-    if (tid == 0) {
-      // rows in order, one thread: several rows may share a dominant key
-      for (int rr = 0; rr < R; ++rr) {
-        if (!((S.domf >> rr) & 1ull)) continue;
-        // no key above half the mass: the row is not dominated after all (the
-        // merge's threshold is only good to bf16) and was scored as usual
-        const int jst = S.domj[rr];
-        if (jst < 0) continue;
-        const float es = S.dome[rr];
-        const float lt = S.fx.ltot[rr];
-        if (!(lt > es * 0x1p-53f)) {     // p* = e* / (e* + L_rest) rounds to 1 in double precision
-          raw[jst] = INFINITY;
-          flags |= DROPKV_FLAG_SINGULAR;
-          continue;
+    if (tid < 32) {
+      // (c) one lane per row (two passes for rows 32 .. 63): the row's term;
+      // the terms of the rows that share a dominant key are summed in row
+      // order by the first of them, which adds them to the key's score with
+      // one read-modify-write (several rows may share a key)
+      float term[2];
+      int key[2];
+      bool sing[2];
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        const int rr = lane + 32 * h2;
+        key[h2] = (rr < R && ((S.domf >> rr) & 1ull)) ? S.domj[rr] : -1;
+        term[h2] = 0.f;
+        sing[h2] = false;
+        if (key[h2] >= 0) {
+          const float es = S.dome[rr], lt = S.fx.ltot[rr];
+          if (!(lt > es * 0x1p-53f)) {   // p* = e* / (e* + L_rest) rounds to 1 in double precision
+            sing[h2] = true;
+          } else {
+            const float pr = es / (es + lt);
+            term[h2] = pr * pr * S.fx.red2[0][rr];
+          }
         }
-        const float pr = es / (es + lt);
-        const float dist = (S.fx.red2[0][rr] + S.fx.red2[1][rr]) + (S.fx.red2[2][rr] + S.fx.red2[3][rr]);
-        const float cur = raw[jst];
-        const float nv = cur + pr * pr * dist * inv_g;
-        if (!isfinite(nv) && !isinf(cur)) flags |= DROPKV_FLAG_NONFINITE | DROPKV_FLAG_NONFINITE_SCORE;
-        raw[jst] = nv;
+      }
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        if (32 * h2 >= R) break;
+        const int kk = key[h2];
+        const int rr = lane + 32 * h2;
+        float add = 0.f;
+        bool sg = false, first = kk >= 0;
+        // rows in order: q < rr with the same key makes this row not the first
+        for (int q = 0; q < R; ++q) {
+          const int qh = q >> 5, ql = q & 31;
+          const int kq = __shfl_sync(0xffffffffu, qh ? key[1] : key[0], ql);
+          const float tq = __shfl_sync(0xffffffffu, qh ? term[1] : term[0], ql);
+          const bool sq2 = __shfl_sync(0xffffffffu, (int)(qh ? sing[1] : sing[0]), ql) != 0;
+          if (kk >= 0 && kq == kk) {
+            if (q < rr) first = false;
+            add += tq;
+            sg |= sq2;
+          }
+        }
+        if (first) {
+          const float cur = raw[kk];
+          if (sg) {
+            raw[kk] = INFINITY;
+            flags |= DROPKV_FLAG_SINGULAR;
+          } else {
+            const float nv = cur + add * inv_g;
+            if (!isfinite(nv) && !isinf(cur)) flags |= DROPKV_FLAG_NONFINITE | DROPKV_FLAG_NONFINITE_SCORE;
+            raw[kk] = nv;
+          }
+        }
       }
     }
   }

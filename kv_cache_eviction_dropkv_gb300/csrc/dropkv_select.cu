@@ -537,7 +537,11 @@ __global__ void __launch_bounds__(kSelThreads) select_write_kernel(const SelPara
 // the merged histogram in every CTA and the k-th item's bin is found from
 // local shared memory.  No global scratch and a single launch.
 constexpr int kClThreads = 1024;
-constexpr int kClPer = kSelChunk / kClThreads;   // 16 consecutive slots per thread
+// Slots per thread (PER) of the cluster selection: 4, 8 or 16 consecutive
+// slots, a chunk of PER * 1024 slots per CTA.  The launch takes the smallest
+// PER whose chunks cover the head with at most kClMax CTAs, so shorter heads
+// are spread over more SMs (at n = 32K, 8 CTAs of 4096 slots instead of 2 of
+// 16384).
 constexpr int kClMax = 8;                        // portable cluster size
 
 struct ClusterSmem {
@@ -554,8 +558,10 @@ struct ClusterSmem {
 // so the chunk itself is 16-byte aligned for vector copies).
 constexpr int kClHalo = 32;
 static_assert(kClHalo >= kMaxPool / 2 && kClHalo % 4 == 0, "pooling halo");
-constexpr int kClPoolFloats = kSelChunk + 2 * kClHalo;
 constexpr size_t kClPoolOff = (sizeof(ClusterSmem) + 15) & ~size_t(15);   // 16-byte aligned for float4 reads
+constexpr size_t cl_smem_bytes(int per, bool pool) {
+  return pool ? kClPoolOff + (size_t)(per * kClThreads + 2 * kClHalo) * sizeof(float) : sizeof(ClusterSmem);
+}
 
 // Cluster barrier halves (every thread of every CTA of the cluster arrives;
 // release / acquire order the shared-memory accesses around it).
@@ -628,12 +634,12 @@ __device__ __forceinline__ void cluster_find_bin(const uint32_t* merged, uint32_
 
 // Run-aggregated shared-memory histogram of this thread's slots: slot u adds
 // to bin `digit(key)` when u < nv and `member(key)`.
-template <typename Member, typename Digit>
-__device__ __forceinline__ void cluster_hist_add(uint32_t* hist, const uint32_t (&key)[kClPer], int nv, Member member,
+template <int PER, typename Member, typename Digit>
+__device__ __forceinline__ void cluster_hist_add(uint32_t* hist, const uint32_t (&key)[PER], int nv, Member member,
                                                  Digit digit) {
   uint32_t cur = kNoBin, cnt = 0;
 #pragma unroll
-  for (int u = 0; u < kClPer; ++u) {
+  for (int u = 0; u < PER; ++u) {
     const uint32_t bn = (u < nv && member(key[u])) ? digit(key[u]) : kNoBin;
     if (bn == cur) {
       ++cnt;
@@ -646,7 +652,9 @@ __device__ __forceinline__ void cluster_hist_add(uint32_t* hist, const uint32_t 
   if (cur != kNoBin) atomicAdd(&hist[cur], cnt);
 }
 
+template <int PER>
 __global__ void __launch_bounds__(kClThreads, 1) select_cluster_kernel(const SelParams p) {
+  constexpr int kClPer = PER, kChunk = PER * kClThreads;
   extern __shared__ __align__(16) uint8_t cl_smem_raw[];
   ClusterSmem& S = *reinterpret_cast<ClusterSmem*>(cl_smem_raw);
   // the cluster spans blockIdx.x (its dimension is gridDim.x), so the rank
@@ -671,7 +679,7 @@ __global__ void __launch_bounds__(kClThreads, 1) select_cluster_kernel(const Sel
     p.kept_len[b] = (ui.mode == kModeSkip) ? 0 : ui.nb - (normal ? ui.kb : 0);
   }
   const int nb = (ui.mode == kModeSkip) ? 0 : ui.nb;
-  const int jt = r * kSelChunk + (int)threadIdx.x * kClPer;
+  const int jt = r * kChunk + (int)threadIdx.x * kClPer;
   const int nv = min(max(nb - jt, 0), kClPer);
   int32_t* out_row = p.kept_idx + (size_t)unit * p.n_max;
   const bool vec = (p.n_max & 3) == 0;
@@ -685,7 +693,7 @@ __global__ void __launch_bounds__(kClThreads, 1) select_cluster_kernel(const Sel
     if (pnb >= p.pool.w && pnb <= p.n_max) {
       // buf[i] = raw[j0 - kClHalo + i]; -inf outside [0, n_b)
       float* buf = reinterpret_cast<float*>(cl_smem_raw + kClPoolOff);
-      const int half = p.pool.half, j0 = r * kSelChunk;
+      const int half = p.pool.half, j0 = r * kChunk;
       const float* raw = p.pool.raw + (size_t)unit * p.n_max;
       float4 x[kClPer / 4];
 #pragma unroll
@@ -701,7 +709,7 @@ __global__ void __launch_bounds__(kClThreads, 1) select_cluster_kernel(const Sel
         }
       }
       if (threadIdx.x < 2 * kClHalo) {
-        const int i = threadIdx.x < kClHalo ? (int)threadIdx.x : kSelChunk + (int)threadIdx.x;
+        const int i = threadIdx.x < kClHalo ? (int)threadIdx.x : kChunk + (int)threadIdx.x;
         const int jj = j0 - kClHalo + i;
         buf[i] = (jj >= 0 && jj < pnb) ? __ldg(raw + jj) : -INFINITY;
       }
@@ -1175,24 +1183,25 @@ cudaError_t launch_select(const SelParams& p, size_t zero_bytes, void* zero_base
   dim3 grid(p.chunks, p.B * p.Hkv);
   if (p.chunks <= kClMax) {
     // one cluster per KV head: no global counters to clear
+    const int per = p.n_max <= kClMax * 4 * kClThreads ? 4 : (p.n_max <= kClMax * 8 * kClThreads ? 8 : 16);
+    const int C = (p.n_max + per * kClThreads - 1) / (per * kClThreads);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
+    cfg.gridDim = dim3(C, p.B * p.Hkv);
     cfg.blockDim = dim3(kClThreads);
     cfg.stream = st;
-    const size_t smem = p.pool.raw ? kClPoolOff + kClPoolFloats * sizeof(float) : sizeof(ClusterSmem);
-    cfg.dynamicSmemBytes = smem;
+    cfg.dynamicSmemBytes = cl_smem_bytes(per, p.pool.raw != nullptr);
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)p.chunks;
+    attr[0].val.clusterDim.x = (unsigned)C;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    cudaError_t e = cudaFuncSetAttribute(select_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)(kClPoolOff + kClPoolFloats * sizeof(float)));
-    if (e == cudaSuccess) e = cudaLaunchKernelEx(&cfg, select_cluster_kernel, p);
+    auto kern = per == 4 ? select_cluster_kernel<4> : (per == 8 ? select_cluster_kernel<8> : select_cluster_kernel<16>);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cl_smem_bytes(per, true));
+    if (e == cudaSuccess) e = cudaLaunchKernelEx(&cfg, kern, p);
     if (e == cudaSuccess) return e;
     (void)cudaGetLastError();   // clusters refused on this device: take the multi-kernel path
   }
