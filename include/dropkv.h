@@ -113,6 +113,19 @@ DROPKV_API size_t dropkv_workspace_size(const dropkv_shape* shape);
  *             before pooling
  *   workspace / workspace_bytes  device scratch of dropkv_workspace_size() bytes
  *   status    device uint32 status word
+ * Numerics (fp32 with bf16 tensor-core operands):
+ *  - A key with p_j <= 1/2 is scored as e/(L - e) (a - v).  A row whose
+ *    largest key holds about 0.8 of its mass or more (judged by the merge
+ *    from bf16 maxima) is "dominated": that key's term is taken in the equal
+ *    form p*^2 |a_rest - v*|^2, with the other keys' mass L_rest and output
+ *    summed on their own (no cancellation as p* -> 1), by the CTA that holds
+ *    the key.  The key is rejected as singular (DROPKV_FLAG_SINGULAR, score
+ *    +inf) when L_rest <= 2^-53 e*, i.e. when p* rounds to 1 in double
+ *    precision, the oracle's rule.
+ *  - |a - v_j|^2 is expanded around c: K - 2 a'.v_j + |v_j - c|^2 with
+ *    a' = a - c and K = |a'|^2 + 2 a'.c.  c is window row 0's output over the
+ *    keys of the first pass-1 split, rounded to bf16, when |c|^2 > 2d (values
+ *    sharing a large offset), else 0.
  * Sources: "... output-perturbation scoring", Core equation, Algorithm 1
  * summary, Code mapping (tail-aligned causality, GQA). */
 DROPKV_API dropkv_status dropkv_score(const dropkv_shape* shape, const void* q_window, const void* k, const void* v,
