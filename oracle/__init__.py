@@ -78,6 +78,9 @@ def _load():
             lib.oracle_compact_heads.argtypes = [ctypes.POINTER(_Shape), ctypes.c_int, P, P, P, P,
                                                  ctypes.c_int, P, P]
             lib.oracle_compact_heads.restype = ctypes.c_int
+            lib.oracle_prefill_attention.argtypes = [ctypes.POINTER(_Shape), ctypes.c_int, P, P, P, P, P,
+                                                     ctypes.c_int]
+            lib.oracle_prefill_attention.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -187,6 +190,27 @@ def score(q, k, v, lengths=None, pool_kernel: int = 1, protect: int = 0,
     if st != OK:
         raise OracleError("oracle_score failed with status %d" % st)
     return {"m": m, "l": l, "a": a, "raw": raw, "final": fin}
+
+
+def prefill_attention(q, k, v, lengths=None, nthreads: Optional[int] = None) -> np.ndarray:
+    """Causal prefill attention of every query row: q [B,Hq,n_max,d], k, v
+    [B,Hkv,n_max,d] -> out [B,Hq,n_max,d] float64 (NaN for rows >= n_b)."""
+    qa, dt_q = _as_input(q)
+    ka, dt_k = _as_input(k)
+    va, dt_v = _as_input(v)
+    if not (dt_q == dt_k == dt_v):
+        raise OracleError("q, k, v must share one element type")
+    B, Hq, n_max, d = qa.shape
+    Hkv = ka.shape[1]
+    lens = (np.full(B, n_max, dtype=np.int32) if lengths is None
+            else np.ascontiguousarray(np.asarray(lengths), dtype=np.int32))
+    out = np.empty((B, Hq, n_max, d))
+    shape = _Shape(B, Hq, Hkv, d, n_max, 1)
+    st = _load().oracle_prefill_attention(ctypes.byref(shape), dt_q, _ptr(qa), _ptr(ka), _ptr(va), _ptr(lens),
+                                          _ptr(out), nthreads if nthreads is not None else default_threads())
+    if st != OK:
+        raise OracleError("oracle_prefill_attention failed with status %d" % st)
+    return out
 
 
 def select(final, lengths, evict_k, protect: int = 0):

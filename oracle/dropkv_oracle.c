@@ -25,7 +25,10 @@
  *       s_j = sum_t ||Delta_j^(t)||^2 (same page, Core equation; "DropKV:
  *       Decoupling ...", sections 3.1 and 3.3).  1 - p_j is evaluated as
  *       (l - e_j) / l and ||a - v_j||^2 as the direct sum of squared
- *       differences.  Keys a query cannot see contribute nothing for it.
+ *       differences; for the one key a row may give more than half its mass,
+ *       Delta_j is taken in the equal deletion form p_j (a_{-j} - v_j), with
+ *       the other keys' mass and output summed on their own (no cancellation
+ *       as p_j -> 1).  Keys a query cannot see contribute nothing for it.
  *  [S4] local GQA averaging: the scores of the query heads that share a KV
  *       head are averaged (same page, Algorithm 1 summary).
  *  [S5] MaxPool1D along the sequence (kernel kappa, stride 1, window clipped to
@@ -43,6 +46,12 @@
  * the scores of all its KV heads form one pool; the evict_total[b] smallest
  * (score, head, position) triples are evicted, so each head keeps its own
  * number of slots.  Each head's kept positions are listed ascending.
+ *
+ * Prefill attention (the model's own causal attention over the prompt,
+ * "DropKV: Decoupling ...", section 2.1, whose last-w rows give the window
+ * statistics of S1 for free when the scorer is fused into it): every query
+ * row i < n_b of every query head sees the keys j <= i of its KV head;
+ * out_i = sum_j p_j v_j with p = softmax(x), x_j = q_i.k_j / sqrt(d).
  *
  * Score kind SnapKV (the attention-only baseline of "DropKV: Decoupling ...",
  * Appendix B, Table 14: MaxPool1d over the window sum of p_j): step S3 becomes
@@ -457,4 +466,92 @@ int oracle_compact(const oracle_shape* s, int elem_bytes, const void* k, const v
         }
     }
     return ORACLE_OK;
+}
+
+/* Causal prefill attention over every query row (definition in the header
+ * comment).  Items are (sequence, query head) pairs spread over the threads. */
+typedef struct {
+    const oracle_shape* s;
+    int dtype;
+    const void *q, *k, *v;
+    const int32_t* lengths;
+    double* out;
+    int next_item;
+    int status;
+    pthread_mutex_t mu;
+} prefill_job;
+
+static void* prefill_worker(void* arg) {
+    prefill_job* job = (prefill_job*)arg;
+    const oracle_shape* s = job->s;
+    const int g = s->Hq / s->Hkv, d = s->d;
+    const size_t n = (size_t)s->n_max;
+    double* x = (double*)malloc(n * sizeof(double));
+    double* qrow = (double*)malloc((size_t)d * sizeof(double));
+    double* acc = (double*)malloc((size_t)d * sizeof(double));
+    if (!x || !qrow || !acc) {
+        pthread_mutex_lock(&job->mu);
+        job->status = ORACLE_NOMEM;
+        pthread_mutex_unlock(&job->mu);
+        free(x); free(qrow); free(acc);
+        return NULL;
+    }
+    const double inv_sqrt_d = 1.0 / sqrt((double)d);
+    for (;;) {
+        pthread_mutex_lock(&job->mu);
+        const int it = job->next_item++;
+        pthread_mutex_unlock(&job->mu);
+        if (it >= s->B * s->Hq) break;
+        const int b = it / s->Hq, hq = it % s->Hq, h = hq / g;
+        const int nb = job->lengths[b];
+        const size_t kv_base = ((size_t)b * s->Hkv + h) * n * d;
+        const size_t q_base = ((size_t)b * s->Hq + hq) * n * d;
+        for (int i = 0; i < nb; ++i) {
+            for (int c = 0; c < d; ++c) qrow[c] = load_elem(job->q, job->dtype, q_base + (size_t)i * d + c);
+            double m = -INFINITY;
+            for (int j = 0; j <= i; ++j) {
+                double dot = 0.0;
+                for (int c = 0; c < d; ++c) dot += qrow[c] * load_elem(job->k, job->dtype, kv_base + (size_t)j * d + c);
+                x[j] = dot * inv_sqrt_d;
+                if (x[j] > m) m = x[j];
+            }
+            double l = 0.0;
+            for (int j = 0; j <= i; ++j) {
+                x[j] = exp(x[j] - m);
+                l += x[j];
+            }
+            for (int c = 0; c < d; ++c) acc[c] = 0.0;
+            for (int j = 0; j <= i; ++j) {
+                const double p = x[j] / l;
+                for (int c = 0; c < d; ++c) acc[c] += p * load_elem(job->v, job->dtype, kv_base + (size_t)j * d + c);
+            }
+            for (int c = 0; c < d; ++c) job->out[q_base + (size_t)i * d + c] = acc[c];
+        }
+        for (size_t i = (size_t)nb; i < n; ++i)
+            for (int c = 0; c < d; ++c) job->out[q_base + i * d + c] = NAN;
+    }
+    free(x); free(qrow); free(acc);
+    return NULL;
+}
+
+int oracle_prefill_attention(const oracle_shape* s, int dtype, const void* q, const void* k, const void* v,
+                             const int32_t* lengths, double* out, int nthreads) {
+    if (!s || !q || !k || !v || !lengths || !out) return ORACLE_INVALID;
+    if (s->B < 1 || s->Hq < 1 || s->Hkv < 1 || s->Hq % s->Hkv != 0 || s->d < 1 || s->n_max < 1) return ORACLE_INVALID;
+    for (int b = 0; b < s->B; ++b)
+        if (lengths[b] < 1 || lengths[b] > s->n_max) return ORACLE_INVALID;
+    prefill_job job;
+    job.s = s; job.dtype = dtype; job.q = q; job.k = k; job.v = v; job.lengths = lengths; job.out = out;
+    job.next_item = 0; job.status = ORACLE_OK;
+    pthread_mutex_init(&job.mu, NULL);
+    if (nthreads < 1) nthreads = 1;
+    pthread_t* th = (pthread_t*)malloc((size_t)nthreads * sizeof(pthread_t));
+    int started = 0;
+    for (int i = 1; i < nthreads && th; ++i)
+        if (pthread_create(&th[i], NULL, prefill_worker, &job) == 0) started = i; else break;
+    prefill_worker(&job);
+    for (int i = 1; i <= started; ++i) pthread_join(th[i], NULL);
+    free(th);
+    pthread_mutex_destroy(&job.mu);
+    return job.status;
 }

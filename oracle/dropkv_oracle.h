@@ -48,4 +48,9 @@ int oracle_compact_heads(const oracle_shape* s, int elem_bytes, const void* k, c
 int oracle_compact(const oracle_shape* s, int elem_bytes, const void* k, const void* v,
                    const int32_t* kept_idx, const int32_t* kept_len, int out_rows,
                    void* k_out, void* v_out);
+/* Causal prefill attention: out[b][hq][i] = sum_{j <= i} p_j v_j for every
+ * row i < n_b (rows >= n_b set to NaN).  q [B,Hq,n_max,d], k/v [B,Hkv,n_max,d],
+ * out [B,Hq,n_max,d]; s->w is not used. */
+int oracle_prefill_attention(const oracle_shape* s, int dtype, const void* q, const void* k, const void* v,
+                             const int32_t* lengths, double* out, int nthreads);
 #endif

@@ -18,7 +18,10 @@ MUTATIONS = {
     "gqa_sum_not_mean": ("raw[j] = sum / (double)g;", "raw[j] = sum;"),
     "gqa_last_head_dropped": ("for (int hl = 0; hl < g; ++hl) sum += heads", "for (int hl = 0; hl + 1 < g; ++hl) sum += heads"),
     "gqa_interleaved_heads": ("const int hq = h * g + hl;", "const int hq = hl * s->Hkv + h;"),
-    "scale_1_over_d": ("1.0 / sqrt((double)d)", "1.0 / (double)d"),
+    "scale_1_over_d": ("const double inv_sqrt_d = 1.0 / sqrt((double)d);\n    const size_t kv_base",
+                       "const double inv_sqrt_d = 1.0 / (double)d;\n    const size_t kv_base"),
+    "prefill_scale_1_over_d": ("const double inv_sqrt_d = 1.0 / sqrt((double)d);\n    for (;;) {",
+                               "const double inv_sqrt_d = 1.0 / (double)d;\n    for (;;) {"),
     "unnormalised_output": ("a[c] += p * load_elem", "a[c] += e[j] * load_elem"),
     "pool_window_short": ("int lo = j - half, hi = j + half;", "int lo = j - half, hi = j + half - 1;"),
     "protect_one_short": ("for (int j = nb - job->protect; j < nb; ++j)",
@@ -36,6 +39,10 @@ MUTATIONS = {
                              "if (p == 1.0) return ORACLE_SINGULAR;"),
     "layer_evicts_one_more": ("for (size_t i = (size_t)evict_total[b]; i < m; ++i) keep[tmp[i].idx] = 1;",
                               "for (size_t i = (size_t)evict_total[b] + 1; i < m; ++i) keep[tmp[i].idx] = 1;"),
+    "prefill_diagonal_dropped": ("for (int j = 0; j <= i; ++j) {\n                double dot = 0.0;",
+                                 "for (int j = 0; j < i; ++j) {\n                double dot = 0.0;"),
+    "prefill_unnormalised": ("const double p = x[j] / l;\n                for (int c = 0; c < d; ++c) acc[c]",
+                             "const double p = x[j];\n                for (int c = 0; c < d; ++c) acc[c]"),
     "layer_ties_by_position_first": ("tmp[m].idx = (int32_t)((size_t)h * n_max + (size_t)j);",
                                      "tmp[m].idx = (int32_t)((size_t)j * s->Hkv + (size_t)h);"),
 }
@@ -52,6 +59,7 @@ def _run_pins():
     pins.test_snapkv_has_no_singular_rule()
     pins.test_select_layer_vs_stable_sort(0)
     pins.test_sink_score_equals_deletion_near_one(13.8)
+    pins.test_prefill_attention_vs_sdpa(0)
 
 
 def test_unmodified_source_passes(tmp_path):

@@ -624,3 +624,43 @@ def test_cone_condition_decision_and_prevalence():
     frac = pos_count / total
     assert frac >= 0.98, frac
     print("c* > 0 on %d / %d triples (%.4f; Wendel %.4f)" % (pos_count, total, frac, wendel))
+
+
+# ------------------------------------------------------------ prefill attention (the fused path)
+@pytest.mark.parametrize("seed", [0, 1])
+def test_prefill_attention_vs_sdpa(seed):
+    """The oracle's causal prefill attention ("DropKV: Decoupling ...", section
+    2.1: the model's own attention over the prompt) against torch's fp64
+    scaled_dot_product_attention with an explicit causal + length mask, GQA
+    group 3, ragged lengths."""
+    rng = np.random.default_rng(seed)
+    B, Hq, Hkv, n, d = 2, 6, 2, 70, 16
+    q = rng.standard_normal((B, Hq, n, d))
+    k = rng.standard_normal((B, Hkv, n, d))
+    v = rng.standard_normal((B, Hkv, n, d))
+    lengths = np.array([n, 41], dtype=np.int32)
+    out = oracle.prefill_attention(q, k, v, lengths)
+    g = Hq // Hkv
+    for b in range(B):
+        nb = int(lengths[b])
+        qq = torch.from_numpy(q[b:b + 1, :, :nb])
+        kk = torch.from_numpy(np.repeat(k[b:b + 1, :, :nb], g, axis=1))
+        vv = torch.from_numpy(np.repeat(v[b:b + 1, :, :nb], g, axis=1))
+        mask = torch.ones(nb, nb, dtype=torch.bool).tril()
+        ref = torch.nn.functional.scaled_dot_product_attention(qq, kk, vv, attn_mask=mask).numpy()[0]
+        np.testing.assert_allclose(out[b, :, :nb], ref, rtol=1e-12, atol=1e-13)
+        assert np.all(np.isnan(out[b, :, nb:]))
+
+
+def test_prefill_last_rows_are_the_window_statistics():
+    """The last w rows of the prefill attention are the window rows of step S1:
+    the same outputs a, through the oracle's other code path (S1's window
+    attention), bf16 inputs."""
+    wl = synth.make_workload("llama8b_gqa_d128_n32k", n_max=300)
+    s = wl.spec
+    rng = np.random.default_rng(5)
+    q_full = synth.bf16_round(rng.standard_normal((s.B, s.Hq, s.n_max, s.d)).astype(np.float32))
+    q_full[:, :, -s.w:] = wl.q
+    out = oracle.prefill_attention(q_full, wl.k, wl.v)
+    res = oracle.score(wl.q, wl.k, wl.v, wl.lengths.numpy(), 1, 0)
+    np.testing.assert_allclose(out[:, :, -s.w:], res["a"], rtol=1e-12, atol=1e-14)
