@@ -133,6 +133,31 @@ DROPKV_API dropkv_status dropkv_score(const dropkv_shape* shape, const void* q_w
                            float* raw_scores, void* workspace, size_t workspace_bytes, uint32_t* status,
                            cudaStream_t stream);
 
+/* Steps S1-S6 fused into the model's prefill attention: a causal attention
+ * over every query row of the prompt ("DropKV: Decoupling ...", section 2.1;
+ * the scorer fused into prefill, sections 1 and 5.4) writes the attention
+ * output and, as a by-product of its last w rows, the window statistics that
+ * step S1 would compute; the eviction then runs without pass 1's read of K
+ * and V: merge, scoring, pooling, selection and compaction as dropkv_evict_ex.
+ *   q         device bf16 [B][Hq][n_max][d]: every query row of the prompt (row
+ *             i of head hq attends to keys j <= i of KV head hq / g)
+ *   attn_out  device bf16 [B][Hq][n_max][d]: softmax(q k^T / sqrt(d)) v per row;
+ *             rows >= n_b are not written; must not overlap q, k or v
+ *   every other argument as dropkv_evict_ex (the window of the scores is the
+ *   last w rows of q).  Window rows use P in bf16 hi + lo on the tensor cores
+ *   (their statistics match pass 1's precision); the other rows use bf16 P.
+ *   The window states come as one partial per row, so a KV head with a
+ *   dominated row is scored by one CTA in the dominant mode (exact, slower).
+ * Sources: "DropKV: Decoupling ...", sections 1, 2.1 and 5.4 (fusion into
+ * prefill); "... output-perturbation scoring", Core equation. */
+DROPKV_API dropkv_status dropkv_evict_prefill(const dropkv_shape* shape, int32_t score_kind, const void* q,
+                                              const void* k, const void* v, const int32_t* lengths,
+                                              const int32_t* evict_k, int32_t pool_kernel, int32_t protect,
+                                              void* attn_out, float* scores, float* raw_scores, int32_t* kept_idx,
+                                              int32_t* kept_len, int32_t out_rows, void* k_out, void* v_out,
+                                              void* workspace, size_t workspace_bytes, uint32_t* status,
+                                              cudaStream_t stream);
+
 /* Infrastructure (no passage of the pages): per-kernel timing.
  * dropkv_score_ex that also records phase_events[0..4] on `stream`: before
  * pass 1 (window attention), between pass 1 and the split-K merge, between the

@@ -65,6 +65,8 @@ def _load(path):
     L.dropkv_evict.restype = ctypes.c_int
     L.dropkv_evict_ex.argtypes = [SH, I32, P, P, P, P, P, I32, I32, P, P, P, P, I32, P, P, P, SZ, P, P]
     L.dropkv_evict_ex.restype = ctypes.c_int
+    L.dropkv_evict_prefill.argtypes = [SH, I32, P, P, P, P, P, I32, I32, P, P, P, P, P, I32, P, P, P, SZ, P, P]
+    L.dropkv_evict_prefill.restype = ctypes.c_int
     L.dropkv_score_ex.argtypes = [SH, I32, P, P, P, P, I32, I32, P, P, P, SZ, P, P]
     L.dropkv_score_ex.restype = ctypes.c_int
     L.dropkv_select_layer.argtypes = [SH, P, P, P, I32, P, P, P, SZ, P, P]
@@ -227,6 +229,15 @@ def dropkv_evict_ex(shape, kind, q_window, k, v, lengths, evict_k, pool_kernel, 
                                  _ptr(v_out), _ptr(workspace), workspace.numel() * workspace.element_size(),
                                  _ptr(status), _stream(stream))
     return _check(code, "dropkv_evict_ex")
+
+
+def dropkv_evict_prefill(shape, kind, q, k, v, lengths, evict_k, pool_kernel, protect, attn_out, scores, raw_scores,
+                         kept_idx, kept_len, out_rows, k_out, v_out, workspace, status, stream=None):
+    _check(lib().dropkv_evict_prefill(ctypes.byref(shape), SCORE_KINDS[kind], _ptr(q), _ptr(k), _ptr(v), _ptr(lengths),
+                                      _ptr(evict_k), int(pool_kernel), int(protect), _ptr(attn_out), _ptr(scores),
+                                      _ptr(raw_scores), _ptr(kept_idx), _ptr(kept_len), int(out_rows), _ptr(k_out),
+                                      _ptr(v_out), _ptr(workspace), workspace.numel(), _ptr(status),
+                                      _stream(stream)), "dropkv_evict_prefill")
 
 
 def dropkv_select_layer(shape, scores, lengths, evict_total, protect, kept_idx, kept_len, workspace, status,

@@ -73,6 +73,15 @@ class DropKV:
                           self.scores, self.raw_scores if keep_raw else None, self.kept_idx, self.kept_len,
                           self.out_rows, self.k_out, self.v_out, self.workspace, self.status, stream)
 
+    def run_prefill(self, q, k, v, lengths, evict_k, attn_out, stream=None, keep_raw=True):
+        """The prompt's causal attention over every query row q [B,Hq,n_max,d]
+        (output into attn_out, same shape and dtype) with the eviction fused in:
+        the window statistics come from its last w rows (dropkv_evict_prefill)."""
+        B.dropkv_evict_prefill(self.shape, self.kind, q, k, v, lengths, evict_k, self.pool_kernel, self.protect,
+                               attn_out, self.scores, self.raw_scores if keep_raw else None, self.kept_idx,
+                               self.kept_len, self.out_rows, self.k_out, self.v_out, self.workspace, self.status,
+                               stream)
+
     def run_separate(self, q, k, v, lengths, evict_k, stream=None, keep_raw=True):
         """The same step as three library calls (score, select, compact)."""
         self.score(q, k, v, lengths, stream, keep_raw)

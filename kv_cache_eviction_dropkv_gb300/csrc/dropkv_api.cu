@@ -57,10 +57,12 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
 
 // K or V viewed as a 3-D tensor (d, n_max, B*Hkv) of bf16, loaded as boxes of
 // 64 columns x 128 rows with 128-byte swizzle; reads past d or n_max fill zero.
-bool encode_kv_map(CUtensorMap* map, const void* base, const Geom& g) {
+// A [depth][n_max][d] bf16 tensor (K or V: depth = B * Hkv; every query row:
+// depth = B * Hq) as boxes of 64 columns x 128 rows, 128-byte swizzled.
+bool encode_rows_map(CUtensorMap* map, const void* base, const Geom& g, int depth) {
   auto enc = encoder();
   if (!enc) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)g.d, (cuuint64_t)g.n_max, (cuuint64_t)g.U};
+  cuuint64_t dims[3] = {(cuuint64_t)g.d, (cuuint64_t)g.n_max, (cuuint64_t)depth};
   cuuint64_t strides[2] = {(cuuint64_t)g.d * 2, (cuuint64_t)g.d * 2 * (cuuint64_t)g.n_max};
   cuuint32_t box[3] = {64, (cuuint32_t)kTile, 1};
   cuuint32_t es[3] = {1, 1, 1};
@@ -69,6 +71,8 @@ bool encode_kv_map(CUtensorMap* map, const void* base, const Geom& g) {
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
+
+bool encode_kv_map(CUtensorMap* map, const void* base, const Geom& g) { return encode_rows_map(map, base, g, g.U); }
 
 bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb) {
   const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
@@ -134,6 +138,7 @@ WsPlan make_plan(const Geom& g) {
   w.part_o = take((size_t)g.U * g.splits1 * g.R * g.d * 4);
   w.part_ml = take((size_t)g.U * g.splits1 * g.R * 4 * 4);
   w.tile_ctr = take((size_t)g.U * 4);
+  w.qwin = take((size_t)g.B * g.Hq * g.w * g.d * 2);
   w.raw = take((size_t)g.U * g.n_max * 4);
   w.sel_zero_begin = off;
   w.hist = take((size_t)g.U * kHistBins * 4);
@@ -177,7 +182,7 @@ dropkv_status score_core(const dropkv_shape* shape, const void* q_window, const 
                          const int32_t* lengths, int32_t pool_kernel, int32_t protect, float* scores,
                          float* raw_scores, void* workspace, size_t workspace_bytes, uint32_t* status,
                          cudaStream_t stream, cudaEvent_t* ev, PoolParams* defer_pool, int kind,
-                         bool scoring_regions_only) {
+                         bool scoring_regions_only, const PrefillIn* pre) {
   const int sms = current_sms(nullptr);
   if (sms <= 0) return DROPKV_ERR_CUDA;
   if (!shape) return DROPKV_ERR_INVALID_ARG;
@@ -200,6 +205,16 @@ dropkv_status score_core(const dropkv_shape* shape, const void* q_window, const 
   if (!workspace || workspace_bytes < need || !aligned16(workspace)) return DROPKV_ERR_WORKSPACE;
   const size_t score_bytes = (size_t)g.U * g.n_max * 4;
   if (raw_scores && ranges_overlap(raw_scores, score_bytes, scores, score_bytes)) return DROPKV_ERR_INVALID_ARG;
+
+  if (pre) {
+    // every query row in, the attention output out: [B][Hq][n_max][d] bf16 each
+    const size_t rows_bytes = (size_t)g.B * g.Hq * g.n_max * g.d * 2;
+    if (!pre->q || !pre->out || !aligned16(pre->q) || !aligned16(pre->out)) return DROPKV_ERR_INVALID_ARG;
+    if (ranges_overlap(pre->out, rows_bytes, pre->q, rows_bytes) ||
+        ranges_overlap(pre->out, rows_bytes, k, (size_t)g.U * g.n_max * g.d * 2) ||
+        ranges_overlap(pre->out, rows_bytes, v, (size_t)g.U * g.n_max * g.d * 2))
+      return DROPKV_ERR_INVALID_ARG;
+  }
 
   CUtensorMap tk, tv;
   if (!encode_kv_map(&tk, k, g) || !encode_kv_map(&tv, v, g)) return DROPKV_ERR_CUDA;
@@ -235,7 +250,27 @@ dropkv_status score_core(const dropkv_shape* shape, const void* q_window, const 
   p.even = (g.B == 1 || !lengths) ? g.even : 0;
   p.splits = g.splits1;
   p.splits1 = g.splits1;
-  if (launch_window_attention(p, g.NR, tk, tv, g.splits1, stream) != cudaSuccess) return DROPKV_ERR_CUDA;
+  if (pre) {
+    // the prefill attention takes pass 1's place: one partial state per window row
+    CUtensorMap tq;
+    if (!encode_rows_map(&tq, pre->q, g, g.B * g.Hq)) return DROPKV_ERR_CUDA;
+    PrefillParams pf{};
+    pf.q = static_cast<const __nv_bfloat16*>(pre->q);
+    pf.out = static_cast<__nv_bfloat16*>(pre->out);
+    pf.q_win = reinterpret_cast<__nv_bfloat16*>(ws + w.qwin);
+    pf.lengths = lengths;
+    pf.part_o = p.part_o;
+    pf.part_ml = p.part_ml;
+    pf.B = g.B; pf.Hq = g.Hq; pf.Hkv = g.Hkv; pf.g = g.g; pf.d = g.d; pf.n_max = g.n_max; pf.w = g.w;
+    pf.R = g.R; pf.splits = g.splits1;
+    pf.scale_log2 = p.scale_log2;
+    pf.status = status;
+    if (launch_prefill(pf, tq, tk, tv, stream) != cudaSuccess) return DROPKV_ERR_CUDA;
+    p.q = pf.q_win;
+    p.part_splits = 1;
+  } else if (launch_window_attention(p, g.NR, tk, tv, g.splits1, stream) != cudaSuccess) {
+    return DROPKV_ERR_CUDA;
+  }
   if (ev && cudaEventRecord(ev[1], stream) != cudaSuccess) return DROPKV_ERR_CUDA;
   if (launch_merge(p, stream) != cudaSuccess) return DROPKV_ERR_CUDA;
   if (ev && cudaEventRecord(ev[2], stream) != cudaSuccess) return DROPKV_ERR_CUDA;
@@ -268,9 +303,9 @@ dropkv_status score_impl(const dropkv_shape* shape, const void* q_window, const 
                          const int32_t* lengths, int32_t pool_kernel, int32_t protect, float* scores,
                          float* raw_scores, void* workspace, size_t workspace_bytes, uint32_t* status,
                          cudaStream_t stream, cudaEvent_t* ev, PoolParams* defer_pool = nullptr,
-                         int kind = DROPKV_SCORE_DROPKV) {
+                         int kind = DROPKV_SCORE_DROPKV, const PrefillIn* pre = nullptr) {
   return score_core(shape, q_window, k, v, lengths, pool_kernel, protect, scores, raw_scores, workspace,
-                    workspace_bytes, status, stream, ev, defer_pool, kind, false);
+                    workspace_bytes, status, stream, ev, defer_pool, kind, false, pre);
 }
 
 dropkv_status select_impl(const dropkv_shape* shape, const float* scores, const int32_t* lengths,
@@ -372,11 +407,17 @@ dropkv_status dropkv_compact(const dropkv_shape* shape, const void* k, const voi
   return compact_impl(shape, k, v, kept_idx, kept_len, out_rows, k_out, v_out, status, stream, false);
 }
 
-dropkv_status dropkv_evict_ex(const dropkv_shape* shape, int32_t score_kind, const void* q_window, const void* k,
-                              const void* v, const int32_t* lengths, const int32_t* evict_k, int32_t pool_kernel,
-                              int32_t protect, float* scores, float* raw_scores, int32_t* kept_idx,
-                              int32_t* kept_len, int32_t out_rows, void* k_out, void* v_out, void* workspace,
-                              size_t workspace_bytes, uint32_t* status, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Score, select and compact in one call (dropkv_evict_ex, and with `pre` the
+// prefilled variant).
+dropkv_status evict_core(const dropkv_shape* shape, int32_t score_kind, const void* q_window, const void* k,
+                         const void* v, const int32_t* lengths, const int32_t* evict_k, int32_t pool_kernel,
+                         int32_t protect, float* scores, float* raw_scores, int32_t* kept_idx, int32_t* kept_len,
+                         int32_t out_rows, void* k_out, void* v_out, void* workspace, size_t workspace_bytes,
+                         uint32_t* status, cudaStream_t stream, const PrefillIn* pre) {
   // every argument is checked before anything is launched
   dropkv_status st = select_impl(shape, scores, lengths, evict_k, protect, kept_idx, kept_len, workspace,
                                  workspace_bytes, status, stream, nullptr, /*check_only=*/true);
@@ -388,12 +429,38 @@ dropkv_status dropkv_evict_ex(const dropkv_shape* shape, int32_t score_kind, con
   }
   PoolParams pool{};
   st = score_impl(shape, q_window, k, v, lengths, pool_kernel, protect, scores, raw_scores, workspace,
-                  workspace_bytes, status, stream, nullptr, &pool, score_kind);
+                  workspace_bytes, status, stream, nullptr, &pool, score_kind, pre);
   if (st != DROPKV_OK) return st;
   st = select_impl(shape, scores, lengths, evict_k, protect, kept_idx, kept_len, workspace, workspace_bytes, status,
                    stream, &pool);
   if (st != DROPKV_OK || !k_out) return st;
   return compact_impl(shape, k, v, kept_idx, kept_len, out_rows, k_out, v_out, status, stream, false);
+}
+
+}  // namespace
+
+extern "C" {
+
+dropkv_status dropkv_evict_ex(const dropkv_shape* shape, int32_t score_kind, const void* q_window, const void* k,
+                              const void* v, const int32_t* lengths, const int32_t* evict_k, int32_t pool_kernel,
+                              int32_t protect, float* scores, float* raw_scores, int32_t* kept_idx,
+                              int32_t* kept_len, int32_t out_rows, void* k_out, void* v_out, void* workspace,
+                              size_t workspace_bytes, uint32_t* status, cudaStream_t stream) {
+  return evict_core(shape, score_kind, q_window, k, v, lengths, evict_k, pool_kernel, protect, scores, raw_scores,
+                    kept_idx, kept_len, out_rows, k_out, v_out, workspace, workspace_bytes, status, stream, nullptr);
+}
+
+dropkv_status dropkv_evict_prefill(const dropkv_shape* shape, int32_t score_kind, const void* q, const void* k,
+                                   const void* v, const int32_t* lengths, const int32_t* evict_k,
+                                   int32_t pool_kernel, int32_t protect, void* attn_out, float* scores,
+                                   float* raw_scores, int32_t* kept_idx, int32_t* kept_len, int32_t out_rows,
+                                   void* k_out, void* v_out, void* workspace, size_t workspace_bytes,
+                                   uint32_t* status, cudaStream_t stream) {
+  const PrefillIn pre{q, attn_out};
+  // q stands in for the window argument in the argument checks; pass 2 reads
+  // the window rows the prefill kernel copies into the workspace
+  return evict_core(shape, score_kind, q, k, v, lengths, evict_k, pool_kernel, protect, scores, raw_scores, kept_idx,
+                    kept_len, out_rows, k_out, v_out, workspace, workspace_bytes, status, stream, &pre);
 }
 
 dropkv_status dropkv_evict(const dropkv_shape* shape, const void* q_window, const void* k, const void* v,

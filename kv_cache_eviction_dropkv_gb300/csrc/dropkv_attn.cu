@@ -321,7 +321,8 @@ __global__ void __launch_bounds__(kMergeThreads) merge_splits_kernel(const AttnP
   const int b = unit / p.Hkv;
   // caller inputs, read before the wait: the length and pass 1's split count
   const int nb = seq_len(p, b);
-  const int S = p.even > 0 ? p.even : seq_share(p, seq_tiles(p, nb), total_tiles(p));
+  const int S = p.part_splits > 0 ? p.part_splits
+                : (p.even > 0 ? p.even : seq_share(p, seq_tiles(p, nb), total_tiles(p)));
   grid_dep_wait();                                // the partials come from pass 1
   // Pass 2's CTAs may be scheduled now when this grid fits in one wave (their
   // start-up then overlaps the merge); a larger merge grid triggers them only
@@ -971,6 +972,7 @@ constexpr int pass2_smem_bytes() {
 // Splits pass 1 gave a unit of a sequence of length nb (as its grid share
 // computed them).  Warp-collective.
 __device__ __forceinline__ int pass1_splits(const AttnParams& p, int nb) {
+  if (p.part_splits > 0) return p.part_splits;   // the window states came from elsewhere (prefill)
   if (p.even > 0) return p.even;
   const int tiles = seq_tiles(p, nb);
   const uint32_t tot = total_tiles(p);
@@ -1706,6 +1708,321 @@ cudaError_t launch_pass2_t(const AttnParams& p, const CUtensorMap& tk, const CUt
   return launch_pdl(kern, dim3(p.ctas), dim3(kThreads), smem, st, tk, tv, p);
 }
 
+
+// ============================================================== prefill attention
+// Causal attention of every query row of a prompt ("DropKV: Decoupling ...",
+// section 2.1): the kernel a scorer fused into prefill lives in.  Its last w
+// rows are step S1's window rows, so pass 1 and its read of K and V drop out
+// of the eviction.  One CTA per (128-row query tile, query head, sequence),
+// the latest (heaviest) tiles first.  Thread t of the four worker warps owns
+// TMEM lane t = query row qt * 128 + t, so a row's softmax needs no
+// cross-thread reduction:
+//   S = Q K^T on tcgen05 (M = 128 rows, N = 128 keys) into one of two TMEM
+//   buffers;  P = 2^(x - ref) with a lazily moved reference as in pass 1,
+//   written as a K-major SW128 bf16 operand (hi, and lo in the tiles that
+//   hold window rows, so their output keeps pass 1's precision);
+//   O += P V (N = the 128 head dimensions, V read MN-major) in TMEM.
+// Window rows also write their state in pass 1's partial layout (one partial
+// per row) and their query row, for the merge and pass 2.
+constexpr int kPfWarps = 4;                       // softmax warps: warp w reads TMEM lanes 32w .. 32w + 31
+constexpr int kPfProducerWarp = 4, kPfMmaWarp = 5, kPfThreads = 192;
+constexpr int kPfOffQ = 0, kPfOffK = kTileBytes, kPfOffV = 3 * kTileBytes, kPfOffP = 5 * kTileBytes;
+constexpr int kPfOffSmall = 7 * kTileBytes;       // after Q, two K and two V stages, P hi and lo
+constexpr uint32_t kPfTmemCols = 512;             // S at [0, 256), O at [256, 384), O2 at [384, 512)
+// Every kPfFold key tiles the accumulator O is folded into O2 with fp32
+// register adds and restarted, so no tensor-core accumulation chain runs over
+// more than kPfFold tiles (at n = 32K one chain of 256 tiles left the window
+// output 1.7e-4 off in relative terms; pass 1's splits chain about 54).
+constexpr int kPfFold = 16;
+
+struct PrefillSmem {
+  uint64_t qbar, kfull[2], kempty[2], vfull[2], vempty[2], sfull[2], sempty[2], pfull, pempty, ofull, drain;
+  uint32_t tmem_base;
+  int abort;
+};
+constexpr int kPfSmem = kPfOffSmall + (int)sizeof(PrefillSmem) + 1024;
+static_assert(kPfSmem <= 232448, "prefill shared memory exceeds the per-CTA limit");
+
+__global__ void __launch_bounds__(kPfThreads, 1)
+    prefill_attention_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                             const __grid_constant__ CUtensorMap tmv, const PrefillParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = align1024(smem_raw);
+  PrefillSmem& S = *reinterpret_cast<PrefillSmem*>(sm + kPfOffSmall);
+  grid_dep_wait();                          // the inputs may come from the kernel before
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int b = blockIdx.z, hq = blockIdx.y;
+  const int nb = p.lengths ? p.lengths[b] : p.n_max;
+  const int qt = (int)gridDim.x - 1 - (int)blockIdx.x;
+  if (nb < p.w || nb > p.n_max) {
+    if (tid == 0 && blockIdx.x == 0 && hq == 0) atomicOr(p.status, DROPKV_FLAG_BAD_LENGTH);
+    return;
+  }
+  if (qt * kTile >= nb) return;             // past the sequence
+  const int h = hq / p.g, unit = b * p.Hkv + h;
+  const int nk = qt + 1;                    // key tiles 0 .. qt (causal)
+  const bool precise = qt * kTile + kTile > nb - p.w;
+
+  if (tid == 0) {
+    mbar_init(&S.qbar, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&S.kfull[i], 1); mbar_init(&S.kempty[i], 1);
+      mbar_init(&S.vfull[i], 1); mbar_init(&S.vempty[i], 1);
+      mbar_init(&S.sfull[i], 1); mbar_init(&S.sempty[i], kPfWarps);
+    }
+    mbar_init(&S.pfull, kPfWarps);
+    mbar_init(&S.pempty, 1);
+    mbar_init(&S.ofull, 1);
+    mbar_init(&S.drain, 1);
+    S.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == kPfMmaWarp) tmem_alloc(&S.tmem_base, kPfTmemCols);
+  if (warp == kPfProducerWarp && lane == 0) {
+    tma_prefetch_desc(&tmq);
+    tma_prefetch_desc(&tmk);
+    tma_prefetch_desc(&tmv);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = S.tmem_base;
+  const uint32_t tO = tmem + 256;
+  bool failed = false;
+  grid_dep_launch();
+
+  if (warp == kPfProducerWarp) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&S.qbar, kTileBytes);
+      tma_load_3d(sm + kPfOffQ, &tmq, &S.qbar, 0, qt * kTile, b * p.Hq + hq);
+      tma_load_3d(sm + kPfOffQ + kHalfTile, &tmq, &S.qbar, 64, qt * kTile, b * p.Hq + hq);
+      stream_ring<2>(sm + kPfOffK, S.kfull, S.kempty, &tmk, 0, nk, unit, 0, &S.abort, p.status);
+      mbar_drain(&S.qbar, 0);               // the Q copy has landed before the CTA can leave
+    } else if (lane == 1) {
+      stream_ring<2>(sm + kPfOffV, S.vfull, S.vempty, &tmv, 0, nk, unit, 0, &S.abort, p.status);
+    }
+    __syncwarp();
+  } else if (warp == kPfMmaWarp) {
+    if (lane == 0) {
+      const uint32_t idS = umma_idesc_bf16(128, 128, 0, 0);
+      const uint32_t idO = umma_idesc_bf16(128, 128, 0, 1);
+      const uint32_t qaddr = smem_addr(sm + kPfOffQ);
+      const uint32_t phi = smem_addr(sm + kPfOffP), plo = phi + kTileBytes;
+      auto issue_S = [&](int i) -> bool {
+        const int slot = i & 1;
+        if (!mbar_wait(&S.kfull[slot], (i >> 1) & 1, &S.abort)) return false;
+        if (i >= 2 && !mbar_wait(&S.sempty[slot], ((i >> 1) + 1) & 1, &S.abort)) return false;
+        tc_fence_after();
+        const uint32_t kb = smem_addr(sm + kPfOffK + slot * kTileBytes);
+#pragma unroll
+        for (int s = 0; s < 8; ++s)
+          umma_bf16(tmem + slot * 128, desc_kmajor_sw128(qaddr, kTile, s), desc_kmajor_sw128(kb, kTile, s), idS,
+                    s > 0);
+        umma_commit(&S.sfull[slot]);
+        umma_commit(&S.kempty[slot]);
+        return true;
+      };
+      bool ok = mbar_wait(&S.qbar, 0, &S.abort);
+      if (ok) ok = issue_S(0);
+      for (int i = 0; ok && i < nk; ++i) {
+        if (i + 1 < nk && !(ok = issue_S(i + 1))) break;
+        const int vs = i & 1;
+        if (!mbar_wait(&S.pfull, i & 1, &S.abort)) { ok = false; break; }
+        if (!mbar_wait(&S.vfull[vs], (i >> 1) & 1, &S.abort)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t vb = smem_addr(sm + kPfOffV + vs * kTileBytes);
+#pragma unroll
+        for (int s = 0; s < 8; ++s)
+          umma_bf16(tO, desc_kmajor_sw128(phi, kTile, s), desc_mnmajor_sw128(vb, kTile, s), idO,
+                    (i % kPfFold != 0 || s > 0));
+        if (precise) {
+#pragma unroll
+          for (int s = 0; s < 8; ++s)
+            umma_bf16(tO, desc_kmajor_sw128(plo, kTile, s), desc_mnmajor_sw128(vb, kTile, s), idO, 1);
+        }
+        umma_commit(&S.vempty[vs]);
+        umma_commit(&S.pempty);
+        umma_commit(&S.ofull);
+      }
+      if (!ok) {
+        failed = true;
+        S.abort = 1;
+        atomicOr(p.status, DROPKV_FLAG_TIMEOUT);
+      }
+      // make sure no MMA is still writing TMEM before it is released
+      umma_commit(&S.drain);
+      mbar_drain(&S.drain, 0);
+    }
+    __syncwarp();
+  } else {
+    // ---------------------------------------------------- softmax: one row per thread
+    const int pos = qt * kTile + tid;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const float scale = p.scale_log2;
+    uint8_t* phi_s = sm + kPfOffP;
+    uint8_t* plo_s = phi_s + kTileBytes;
+    float ref = -INFINITY, l = 0.f, emax = 0.f;
+    for (int i = 0; i < nk; ++i) {
+      const int sb = i & 1, vs = i & 1;
+      bool ok = __all_sync(0xffffffffu, mbar_wait(&S.sfull[sb], (i >> 1) & 1, &S.abort));
+      float x[kTile];
+      if (ok) {
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < kTile / 16; ++c) tmem_ld16(tmem + lane_base + sb * 128 + 16 * c, x + 16 * c);
+        tmem_wait_ld();
+        tc_fence_before();
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.sempty[sb]);
+      if (!ok) { failed = true; break; }
+      // keys past the row (or the sequence) only in the diagonal tile
+      const bool diag = i == qt;
+      float mt = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < kTile; ++c) {
+        const int j = i * kTile + c;
+        x[c] = (!diag || (j <= pos && j < nb)) ? x[c] * scale : -INFINITY;
+        mt = fmaxf(mt, x[c]);
+      }
+      const bool need = mt > ref + kRescaleLog2;
+      float factor = 1.f;
+      if (need) {
+        factor = (ref == -INFINITY) ? 0.f : ex2_approx(ref - mt);
+        ref = mt;
+        l *= factor;
+        emax *= factor;
+      }
+      if (i == 0) {
+        // O2 starts at zero (TMEM holds anything after allocation)
+        float z[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) z[u] = 0.f;
+#pragma unroll
+        for (int c = 0; c < kDPad / 16; ++c) tmem_st16(tO + kDPad + lane_base + 16 * c, z);
+        tmem_wait_st();
+      }
+      const bool fold = i > 0 && i % kPfFold == 0;   // the same in every thread
+      if (fold || __any_sync(0xffffffffu, need && i > 0)) {
+        // once PV(i - 1) is done (PV(i - 2) is: pempty was waited for at tile
+        // i - 1, so ofull is at most one phase behind): at a fold
+        // O2 = (O2 + O) * factor and PV(i) restarts O; else O *= factor and
+        // O2 *= factor
+        bool okw = __all_sync(0xffffffffu, mbar_wait(&S.ofull, (i - 1) & 1, &S.abort));
+        if (!okw) { failed = true; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < kDPad / 16; ++c) {
+          float o[16], o2[16];
+          tmem_ld16(tO + lane_base + 16 * c, o);
+          tmem_ld16(tO + kDPad + lane_base + 16 * c, o2);
+          tmem_wait_ld();
+#pragma unroll
+          for (int u = 0; u < 16; ++u) {
+            o2[u] = (fold ? o2[u] + o[u] : o2[u]) * factor;
+            o[u] *= factor;
+          }
+          if (!fold) tmem_st16(tO + lane_base + 16 * c, o);
+          tmem_st16(tO + kDPad + lane_base + 16 * c, o2);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+      }
+      // the P buffer is free once PV(i - 1) is done
+      if (i >= 1) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&S.pempty, (i - 1) & 1, &S.abort));
+        if (!ok) { failed = true; break; }
+      }
+      if ((i + 1) * kTile > nb) {
+        // slots past the sequence may hold anything (NaN): zero their V rows
+        // so that 0 * NaN never reaches the PV accumulator
+        ok = __all_sync(0xffffffffu, mbar_wait(&S.vfull[vs], (i >> 1) & 1, &S.abort));
+        if (!ok) { failed = true; break; }
+        if (i * kTile + tid >= nb) {
+          uint8_t* vrow = sm + kPfOffV + vs * kTileBytes + tid * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            *reinterpret_cast<uint4*>(vrow + c * 16) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(vrow + kHalfTile + c * 16) = make_uint4(0, 0, 0, 0);
+          }
+        }
+      }
+      float lsum = 0.f;
+#pragma unroll
+      for (int c8 = 0; c8 < kTile / 8; ++c8) {
+        uint32_t hp[4], lp[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float e0 = ex2_approx(x[8 * c8 + 2 * q] - ref);
+          const float e1 = ex2_approx(x[8 * c8 + 2 * q + 1] - ref);
+          lsum += e0 + e1;
+          emax = fmaxf(emax, fmaxf(e0, e1));
+          split_hi_lo(e0, e1, hp[q], lp[q]);
+        }
+        const uint32_t off = sw128_offset((uint32_t)tid, (uint32_t)(8 * c8), kTile);
+        *reinterpret_cast<uint4*>(phi_s + off) = make_uint4(hp[0], hp[1], hp[2], hp[3]);
+        if (precise) *reinterpret_cast<uint4*>(plo_s + off) = make_uint4(lp[0], lp[1], lp[2], lp[3]);
+      }
+      l += lsum;
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.pfull);
+    }
+    // ---------------------------------------------------- epilogue
+    // The MMA warp commits `drain` once, after its last MMA.
+    bool okw = false;
+    if (!failed) okw = mbar_wait(&S.drain, 0, &S.abort);
+    okw = __all_sync(0xffffffffu, okw);
+    if (okw) {
+      tc_fence_after();
+      const bool row_ok = pos < nb;
+      const bool win = row_ok && pos >= nb - p.w;
+      const int tw = pos - (nb - p.w);
+      const int r = (hq - h * p.g) * p.w + tw;
+      const size_t part = (size_t)unit * p.splits;          // the single partial of the row
+      const float inv_l = 1.0f / l;
+      __nv_bfloat16* orow = p.out + (((size_t)b * p.Hq + hq) * p.n_max + pos) * p.d;
+#pragma unroll
+      for (int c = 0; c < kDPad / 16; ++c) {
+        float o[16], o2[16];
+        tmem_ld16(tO + lane_base + 16 * c, o);
+        tmem_ld16(tO + kDPad + lane_base + 16 * c, o2);
+        tmem_wait_ld();
+#pragma unroll
+        for (int u = 0; u < 16; ++u) o[u] += o2[u];
+        if (row_ok && 16 * c < p.d) {
+          uint32_t w8[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const __nv_bfloat162 h2 = __floats2bfloat162_rn(o[2 * u] * inv_l, o[2 * u + 1] * inv_l);
+            w8[u] = *reinterpret_cast<const uint32_t*>(&h2);
+          }
+          *reinterpret_cast<uint4*>(orow + 16 * c) = make_uint4(w8[0], w8[1], w8[2], w8[3]);
+          if (16 * c + 8 < p.d) *reinterpret_cast<uint4*>(orow + 16 * c + 8) = make_uint4(w8[4], w8[5], w8[6], w8[7]);
+          if (win) {
+            float* po = p.part_o + (part * p.R + r) * p.d + 16 * c;
+#pragma unroll
+            for (int u = 0; u < 16; u += 4)
+              if (16 * c + u < p.d) *reinterpret_cast<float4*>(po + u) = make_float4(o[u], o[u + 1], o[u + 2], o[u + 3]);
+          }
+        }
+      }
+      tc_fence_before();
+      if (win) {
+        reinterpret_cast<float4*>(p.part_ml)[part * p.R + r] = make_float4(ref, l, emax, 0.f);
+        const uint4* qs = reinterpret_cast<const uint4*>(p.q + (((size_t)b * p.Hq + hq) * p.n_max + pos) * p.d);
+        uint4* qd = reinterpret_cast<uint4*>(p.q_win + (((size_t)b * p.Hq + hq) * p.w + tw) * p.d);
+        for (int c = 0; c < p.d / 8; ++c) qd[c] = qs[c];
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kPfMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kPfTmemCols);
+  }
+}
 }  // namespace
 
 cudaError_t launch_window_attention(const AttnParams& p, int NR, const CUtensorMap& tk, const CUtensorMap& tv,
@@ -1722,6 +2039,14 @@ cudaError_t launch_window_attention(const AttnParams& p, int NR, const CUtensorM
 cudaError_t launch_merge(const AttnParams& p, cudaStream_t st) {
   // row groups covering the NR rows of the A.V^T operand (rows past R get zeros)
   return launch_pdl(merge_splits_kernel, dim3(p.NR / kMergeRows, p.U), dim3(kMergeThreads), 0, st, p);
+}
+
+cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                           const CUtensorMap& tv, cudaStream_t st) {
+  cudaError_t e = cudaFuncSetAttribute(prefill_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmem);
+  if (e != cudaSuccess) return e;
+  const dim3 grid((p.n_max + kTile - 1) / kTile, p.Hq, p.B);
+  return launch_pdl(prefill_attention_kernel, grid, dim3(kPfThreads), kPfSmem, st, tq, tk, tv, p);
 }
 
 cudaError_t launch_score(const AttnParams& p, int NR, const CUtensorMap& tk, const CUtensorMap& tv,

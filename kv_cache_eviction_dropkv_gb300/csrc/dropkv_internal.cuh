@@ -47,6 +47,7 @@ struct WsPlan {
   size_t dom_o;                  // dominated rows: f32 [U][R][d] sum of the other splits' O
   size_t part_o, part_ml;        // pass-1 partial states (part_ml: m, l, largest logit, unused)
   size_t tile_ctr;               // u32 [U]: pass-2 tile claims (cleared by the merge kernel)
+  size_t qwin;                   // bf16 [B][Hq][w][d]: the window query rows (prefilled path)
   size_t raw;                    // f32 [U][n_max] raw scores when the caller passes none
   // selection
   size_t hist;                   // u32 [U][kHistBins]
@@ -105,6 +106,20 @@ struct AttnParams {
   float* raw;                    // raw score output [U][n_max]
   uint32_t* status;
   int kind;                      // kKindDropKV or kKindSnapKV
+  int part_splits;               // > 0: partial states per unit when they come from the prefill kernel (1)
+};
+
+// The prefill kernel (a causal attention over every query row, the window
+// states a by-product) in pass 1's place.
+struct PrefillParams {
+  const __nv_bfloat16* q;        // [B][Hq][n_max][d] every query row
+  __nv_bfloat16* out;            // [B][Hq][n_max][d] attention output (rows < n_b written)
+  __nv_bfloat16* q_win;          // [B][Hq][w][d] the window rows of q (pass 2's q)
+  const int32_t* lengths;        // [B] or null
+  float *part_o, *part_ml;       // window rows' states in pass 1's layout (one partial per row)
+  int B, Hq, Hkv, g, d, n_max, w, R, splits;
+  float scale_log2;
+  uint32_t* status;
 };
 
 struct PoolParams {
@@ -179,15 +194,23 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 // Steps S1-S4 on the caller's workspace (the body of dropkv_score and its
 // variants).  scoring_regions_only: the workspace need only hold the regions
 // scoring uses (the ones ahead of the selection's).
+// Inputs of the prefilled path: every query row and the attention output.
+struct PrefillIn {
+  const void* q;                 // bf16 [B][Hq][n_max][d]
+  void* out;                     // bf16 [B][Hq][n_max][d]
+};
+
 dropkv_status score_core(const dropkv_shape* shape, const void* q_window, const void* k, const void* v,
                          const int32_t* lengths, int32_t pool_kernel, int32_t protect, float* scores,
                          float* raw_scores, void* workspace, size_t workspace_bytes, uint32_t* status,
                          cudaStream_t stream, cudaEvent_t* ev, PoolParams* defer_pool, int kind,
-                         bool scoring_regions_only);
+                         bool scoring_regions_only, const PrefillIn* pre = nullptr);
 
 cudaError_t launch_window_attention(const AttnParams& p, int NR, const CUtensorMap& tk, const CUtensorMap& tv,
                                     int num_ctas_x, cudaStream_t st);
 cudaError_t launch_merge(const AttnParams& p, cudaStream_t st);
+cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                           const CUtensorMap& tv, cudaStream_t st);
 cudaError_t launch_score(const AttnParams& p, int NR, const CUtensorMap& tk, const CUtensorMap& tv,
                          cudaStream_t st);
 cudaError_t launch_pool_protect(const PoolParams& p, cudaStream_t st);
