@@ -61,6 +61,9 @@ def parse_args():
                     help="score kind: the DropKV perturbation score (default) or the SnapKV baseline")
     ap.add_argument("--select", choices=["head", "layer"], default="head",
                     help="bottom-k per KV head (default) or one pool per sequence over its KV heads (AdaDropKV)")
+    ap.add_argument("--prefill", action="store_true",
+                    help="the eviction fused into the prompt's causal attention over every query row "
+                         "(dropkv_evict_prefill), against that attention followed by dropkv_evict")
     ap.add_argument("--decode", type=int, default=0, metavar="M",
                     help="decode-time re-scoring: evict the workload once, append M decode tokens to the "
                          "compacted cache, and time score -> select -> compact of M rows on that grown cache")
@@ -251,6 +254,100 @@ def run_reference(args, spec, wl):
     print(json.dumps(line))
 
 
+def prefill_flops(spec, lengths):
+    """Algorithmic FLOPs of the causal attention over every query row: per
+    query head, row i multiplies its query with i + 1 keys (q.k, 2d FLOPs each)
+    and sums i + 1 value rows (2d each): 2 d n_b (n_b + 1) per head."""
+    return sum(spec.Hq * 2 * spec.d * int(nb) * (int(nb) + 1) for nb in lengths)
+
+
+def prefill_leg(args, spec, wl, op, dev, stream, flush, clean, world, rank):
+    """--prefill: one step = dropkv_evict_prefill (the causal attention over
+    every query row of the layer, with the eviction fused in), beside the
+    unfused pair (dropkv_prefill_attention, then dropkv_evict over the window
+    rows: pass 1 reads K and V once more) and the attention alone.  Query rows
+    are seeded N(0, 1) bf16, the workload's window rows at the tail."""
+    from kv_cache_eviction_dropkv_gb300 import _binding as B
+    rng = np.random.default_rng(spec.seed + 77)
+    lengths_np = wl.lengths.numpy()
+    q_full = synth.bf16_round(rng.standard_normal((spec.B, spec.Hq, spec.n_max, spec.d)).astype(np.float32))
+    for b in range(spec.B):
+        nb = int(lengths_np[b])
+        q_full[b, :, nb - spec.w:nb] = wl.q[b]
+    qwin = torch.stack([q_full[b, :, int(lengths_np[b]) - spec.w:int(lengths_np[b])] for b in range(spec.B)])
+    q, qw = q_full.to(dev), qwin.contiguous().to(dev)
+    k, v = wl.k.to(dev), wl.v.to(dev)
+    lengths, ev = wl.lengths.to(dev), wl.evict_k.to(dev)
+    out = torch.empty_like(q)
+
+    def fused():
+        op.run_prefill(q, k, v, lengths, ev, out, stream=stream, keep_raw=False)
+
+    def unfused():
+        op.prefill_attention(q, k, v, lengths, out, stream=stream)
+        op.run(qw, k, v, lengths, ev, stream=stream, keep_raw=False)
+
+    def attention():
+        op.prefill_attention(q, k, v, lengths, out, stream=stream)
+
+    def timed(fn, K):
+        ts = []
+        for i in range(K):
+            flush.fill_(float(i))
+            clean.sum()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            ts.append((e0, e1))
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b_) for a, b_ in ts]
+
+    for fn in (fused, unfused, attention):
+        for i in range(max(3, args.warmup)):
+            fn()
+    op.check(stream)
+    K = args.steps
+    sampler = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", "0").split(",")[0])
+                           if os.environ.get("CUDA_VISIBLE_DEVICES") else 0)
+    sampler.start()
+    if world > 1:
+        torch.distributed.barrier()
+    t_fused = timed(fused, K)
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    t_unfused = timed(unfused, K)
+    t_att = timed(attention, K)
+    op.check(stream)
+    med = lambda xs: float(sorted(xs)[len(xs) // 2])
+    step_ms = reduce_max(sum(t_fused) / K, world)
+    units = int(lengths_np.sum())
+    flops = prefill_flops(spec, lengths_np)
+    att_ms = med(t_att)
+    peaks_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    peaks = {}
+    if os.path.exists(peaks_path):
+        with open(peaks_path) as f:
+            peaks = json.load(f)
+    peak = float(peaks.get("bf16_tflops", 1900.0))
+    achieved = flops / (att_ms / 1e3) / 1e12
+    return {"metric": METRIC, "value": job_throughput(units, world, step_ms), "unit": UNIT, "n_gpus": world,
+            "steps": K, "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded generator; stands in for RULER/LongBench layers)",
+            "config": dict(config_of(spec, lengths_np), mode="prefill-fused"),
+            "roofline": {"bound": "tensor", "kernel": "prefill_attention", "achieved": achieved, "peak": peak,
+                         "unit": "TFLOP/s", "frac": achieved / peak,
+                         "peak_source": "measured (bf16 burst)" if "bf16_tflops" in peaks else "fallback",
+                         "traffic": None, "algorithmic_flops_per_launch": flops},
+            "prefill": {"fused_ms": med(t_fused), "unfused_ms": med(t_unfused), "attention_ms": att_ms,
+                        "saved_ms": med(t_unfused) - med(t_fused),
+                        "note": "fused = dropkv_evict_prefill; unfused = dropkv_prefill_attention then "
+                                "dropkv_evict on the window rows (pass 1 reads K and V again); medians"},
+            "gpu_launches": 5 * K, "clocks": clocks}
+
+
 def oracle_decode_workload(wl, m, seed):
     """The decode-time workload of the reference arm: the oracle's prefill
     kept set, gathered on the host, grown by the same m seeded tokens."""
@@ -366,6 +463,13 @@ def main():
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     clean = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
+    if args.prefill:
+        line = prefill_leg(args, spec, wl, op, dev, stream, flush, clean, world, rank)
+        if rank == 0:
+            print(json.dumps(line))
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
 
     def flush_l2(i):
         # write a buffer larger than L2 (evicts the previous step's data), then

@@ -133,6 +133,18 @@ DROPKV_API dropkv_status dropkv_score(const dropkv_shape* shape, const void* q_w
                            float* raw_scores, void* workspace, size_t workspace_bytes, uint32_t* status,
                            cudaStream_t stream);
 
+/* The prompt's causal attention alone (the kernel of dropkv_evict_prefill
+ * without the eviction): attn_out[b][hq][i] = softmax over keys j <= i of
+ * q_i k_j / sqrt(d), times v, for every row i < n_b ("DropKV: Decoupling ...",
+ * section 2.1).  q, k, v, attn_out as in dropkv_evict_prefill; the workspace
+ * (dropkv_workspace_size bytes) receives the window states as a by-product.
+ * For comparison with the fused call: this followed by dropkv_evict reads K
+ * and V once more in pass 1. */
+DROPKV_API dropkv_status dropkv_prefill_attention(const dropkv_shape* shape, const void* q, const void* k,
+                                                  const void* v, const int32_t* lengths, void* attn_out,
+                                                  void* workspace, size_t workspace_bytes, uint32_t* status,
+                                                  cudaStream_t stream);
+
 /* Steps S1-S6 fused into the model's prefill attention: a causal attention
  * over every query row of the prompt ("DropKV: Decoupling ...", section 2.1;
  * the scorer fused into prefill, sections 1 and 5.4) writes the attention

@@ -67,6 +67,8 @@ def _load(path):
     L.dropkv_evict_ex.restype = ctypes.c_int
     L.dropkv_evict_prefill.argtypes = [SH, I32, P, P, P, P, P, I32, I32, P, P, P, P, P, I32, P, P, P, SZ, P, P]
     L.dropkv_evict_prefill.restype = ctypes.c_int
+    L.dropkv_prefill_attention.argtypes = [SH, P, P, P, P, P, P, SZ, P, P]
+    L.dropkv_prefill_attention.restype = ctypes.c_int
     L.dropkv_score_ex.argtypes = [SH, I32, P, P, P, P, I32, I32, P, P, P, SZ, P, P]
     L.dropkv_score_ex.restype = ctypes.c_int
     L.dropkv_select_layer.argtypes = [SH, P, P, P, I32, P, P, P, SZ, P, P]
@@ -238,6 +240,12 @@ def dropkv_evict_prefill(shape, kind, q, k, v, lengths, evict_k, pool_kernel, pr
                                       _ptr(raw_scores), _ptr(kept_idx), _ptr(kept_len), int(out_rows), _ptr(k_out),
                                       _ptr(v_out), _ptr(workspace), workspace.numel(), _ptr(status),
                                       _stream(stream)), "dropkv_evict_prefill")
+
+
+def dropkv_prefill_attention(shape, q, k, v, lengths, attn_out, workspace, status, stream=None):
+    _check(lib().dropkv_prefill_attention(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(lengths),
+                                          _ptr(attn_out), _ptr(workspace), workspace.numel(), _ptr(status),
+                                          _stream(stream)), "dropkv_prefill_attention")
 
 
 def dropkv_select_layer(shape, scores, lengths, evict_total, protect, kept_idx, kept_len, workspace, status,

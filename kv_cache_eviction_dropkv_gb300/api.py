@@ -82,6 +82,10 @@ class DropKV:
                                self.kept_len, self.out_rows, self.k_out, self.v_out, self.workspace, self.status,
                                stream)
 
+    def prefill_attention(self, q, k, v, lengths, attn_out, stream=None):
+        """The prompt's causal attention alone (dropkv_prefill_attention)."""
+        B.dropkv_prefill_attention(self.shape, q, k, v, lengths, attn_out, self.workspace, self.status, stream)
+
     def run_separate(self, q, k, v, lengths, evict_k, stream=None, keep_raw=True):
         """The same step as three library calls (score, select, compact)."""
         self.score(q, k, v, lengths, stream, keep_raw)

@@ -450,6 +450,42 @@ dropkv_status dropkv_evict_ex(const dropkv_shape* shape, int32_t score_kind, con
                     kept_idx, kept_len, out_rows, k_out, v_out, workspace, workspace_bytes, status, stream, nullptr);
 }
 
+dropkv_status dropkv_prefill_attention(const dropkv_shape* shape, const void* q, const void* k, const void* v,
+                                       const int32_t* lengths, void* attn_out, void* workspace,
+                                       size_t workspace_bytes, uint32_t* status, cudaStream_t stream) {
+  const int sms = current_sms(nullptr);
+  if (sms <= 0) return DROPKV_ERR_CUDA;
+  Geom g;
+  if (!shape || !make_geom(shape, sms, &g)) return DROPKV_ERR_INVALID_ARG;
+  if (!q || !k || !v || !attn_out || !status) return DROPKV_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(attn_out) ||
+      (reinterpret_cast<uintptr_t>(status) & 3u))
+    return DROPKV_ERR_INVALID_ARG;
+  const size_t rows_bytes = (size_t)g.B * g.Hq * g.n_max * g.d * 2;
+  const size_t kv_bytes = (size_t)g.U * g.n_max * g.d * 2;
+  if (ranges_overlap(attn_out, rows_bytes, q, rows_bytes) || ranges_overlap(attn_out, rows_bytes, k, kv_bytes) ||
+      ranges_overlap(attn_out, rows_bytes, v, kv_bytes))
+    return DROPKV_ERR_INVALID_ARG;
+  const WsPlan w = make_plan(g);
+  if (!workspace || workspace_bytes < w.sel_zero_begin || !aligned16(workspace)) return DROPKV_ERR_WORKSPACE;
+  CUtensorMap tq, tk, tv;
+  if (!encode_rows_map(&tq, q, g, g.B * g.Hq) || !encode_kv_map(&tk, k, g) || !encode_kv_map(&tv, v, g))
+    return DROPKV_ERR_CUDA;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  PrefillParams pf{};
+  pf.q = static_cast<const __nv_bfloat16*>(q);
+  pf.out = static_cast<__nv_bfloat16*>(attn_out);
+  pf.q_win = reinterpret_cast<__nv_bfloat16*>(ws + w.qwin);
+  pf.lengths = lengths;
+  pf.part_o = reinterpret_cast<float*>(ws + w.part_o);
+  pf.part_ml = reinterpret_cast<float*>(ws + w.part_ml);
+  pf.B = g.B; pf.Hq = g.Hq; pf.Hkv = g.Hkv; pf.g = g.g; pf.d = g.d; pf.n_max = g.n_max; pf.w = g.w;
+  pf.R = g.R; pf.splits = g.splits1;
+  pf.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)g.d));
+  pf.status = status;
+  return launch_prefill(pf, tq, tk, tv, stream) == cudaSuccess ? DROPKV_OK : DROPKV_ERR_CUDA;
+}
+
 dropkv_status dropkv_evict_prefill(const dropkv_shape* shape, int32_t score_kind, const void* q, const void* k,
                                    const void* v, const int32_t* lengths, const int32_t* evict_k,
                                    int32_t pool_kernel, int32_t protect, void* attn_out, float* scores,

@@ -1724,10 +1724,14 @@ cudaError_t launch_pass2_t(const AttnParams& p, const CUtensorMap& tk, const CUt
 //   O += P V (N = the 128 head dimensions, V read MN-major) in TMEM.
 // Window rows also write their state in pass 1's partial layout (one partial
 // per row) and their query row, for the merge and pass 2.
-constexpr int kPfWarps = 4;                       // softmax warps: warp w reads TMEM lanes 32w .. 32w + 31
-constexpr int kPfProducerWarp = 4, kPfMmaWarp = 5, kPfThreads = 192;
+// Softmax warps: warp w reads TMEM lane quarter w & 3 (rows 32 (w & 3) ..
+// + 31) and takes key columns 32 (w >> 2) .. + 31 of each tile, so four warps
+// share a row and one scheduler runs four softmax warps.
+constexpr int kPfWarps = 16, kPfWorkers = 32 * kPfWarps;
+constexpr int kPfProducerWarp = 16, kPfMmaWarp = 17, kPfThreads = 32 * 18;
+constexpr uint32_t kPfBar = 1;                     // named barrier of the softmax warps
 constexpr int kPfOffQ = 0, kPfOffK = kTileBytes, kPfOffV = 3 * kTileBytes, kPfOffP = 5 * kTileBytes;
-constexpr int kPfOffSmall = 7 * kTileBytes;       // after Q, two K and two V stages, P hi and lo
+constexpr int kPfOffSmall = 6 * kTileBytes;       // after Q, two K and two V stages and P
 constexpr uint32_t kPfTmemCols = 512;             // S at [0, 256), O at [256, 384), O2 at [384, 512)
 // Every kPfFold key tiles the accumulator O is folded into O2 with fp32
 // register adds and restarted, so no tensor-core accumulation chain runs over
@@ -1739,6 +1743,8 @@ struct PrefillSmem {
   uint64_t qbar, kfull[2], kempty[2], vfull[2], vempty[2], sfull[2], sempty[2], pfull, pempty, ofull, drain;
   uint32_t tmem_base;
   int abort;
+  float red[2][4][kTile];       // per tile parity: each column group's largest x of row r
+  float red2[2][4][kTile];      // at the end: each column group's sum and largest e of row r
 };
 constexpr int kPfSmem = kPfOffSmall + (int)sizeof(PrefillSmem) + 1024;
 static_assert(kPfSmem <= 232448, "prefill shared memory exceeds the per-CTA limit");
@@ -1761,7 +1767,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   if (qt * kTile >= nb) return;             // past the sequence
   const int h = hq / p.g, unit = b * p.Hkv + h;
   const int nk = qt + 1;                    // key tiles 0 .. qt (causal)
+  // the tile holding window rows runs P V twice per key tile: P in bf16 hi,
+  // then its rounding remainder (lo) in the same buffer
   const bool precise = qt * kTile + kTile > nb - p.w;
+  const int pps = precise ? 2 : 1;          // pfull / pempty phases per key tile
 
   if (tid == 0) {
     mbar_init(&S.qbar, 1);
@@ -1807,7 +1816,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       const uint32_t idS = umma_idesc_bf16(128, 128, 0, 0);
       const uint32_t idO = umma_idesc_bf16(128, 128, 0, 1);
       const uint32_t qaddr = smem_addr(sm + kPfOffQ);
-      const uint32_t phi = smem_addr(sm + kPfOffP), plo = phi + kTileBytes;
+      const uint32_t paddr = smem_addr(sm + kPfOffP);
       auto issue_S = [&](int i) -> bool {
         const int slot = i & 1;
         if (!mbar_wait(&S.kfull[slot], (i >> 1) & 1, &S.abort)) return false;
@@ -1827,21 +1836,20 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       for (int i = 0; ok && i < nk; ++i) {
         if (i + 1 < nk && !(ok = issue_S(i + 1))) break;
         const int vs = i & 1;
-        if (!mbar_wait(&S.pfull, i & 1, &S.abort)) { ok = false; break; }
         if (!mbar_wait(&S.vfull[vs], (i >> 1) & 1, &S.abort)) { ok = false; break; }
-        tc_fence_after();
         const uint32_t vb = smem_addr(sm + kPfOffV + vs * kTileBytes);
-#pragma unroll
-        for (int s = 0; s < 8; ++s)
-          umma_bf16(tO, desc_kmajor_sw128(phi, kTile, s), desc_mnmajor_sw128(vb, kTile, s), idO,
-                    (i % kPfFold != 0 || s > 0));
-        if (precise) {
+        for (int part = 0; part < pps; ++part) {
+          const int ph = i * pps + part;
+          if (!mbar_wait(&S.pfull, ph & 1, &S.abort)) { ok = false; break; }
+          tc_fence_after();
 #pragma unroll
           for (int s = 0; s < 8; ++s)
-            umma_bf16(tO, desc_kmajor_sw128(plo, kTile, s), desc_mnmajor_sw128(vb, kTile, s), idO, 1);
+            umma_bf16(tO, desc_kmajor_sw128(paddr, kTile, s), desc_mnmajor_sw128(vb, kTile, s), idO,
+                      (part > 0 || i % kPfFold != 0 || s > 0));
+          umma_commit(&S.pempty);
         }
+        if (!ok) break;
         umma_commit(&S.vempty[vs]);
-        umma_commit(&S.pempty);
         umma_commit(&S.ofull);
       }
       if (!ok) {
@@ -1855,37 +1863,47 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     }
     __syncwarp();
   } else {
-    // ---------------------------------------------------- softmax: one row per thread
-    const int pos = qt * kTile + tid;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    // ---------------------------------------------------- softmax
+    const int quarter = warp & 3, cg = warp >> 2;
+    const int row = quarter * 32 + lane, col0 = cg * 32;
+    const int pos = qt * kTile + row;
+    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
     const float scale = p.scale_log2;
-    uint8_t* phi_s = sm + kPfOffP;
-    uint8_t* plo_s = phi_s + kTileBytes;
+    uint8_t* ps = sm + kPfOffP;
     float ref = -INFINITY, l = 0.f, emax = 0.f;
+    // A wait this warp gave up on sets `bad`: the warp skips the work that
+    // depended on it, and the OR barrier of the next tile (or of the
+    // epilogue) makes every softmax warp leave together, so none is left at
+    // a named barrier the others never reach.
+    bool bad = false;
     for (int i = 0; i < nk; ++i) {
-      const int sb = i & 1, vs = i & 1;
+      const int sb = i & 1, vs = i & 1, par = i & 1;
       bool ok = __all_sync(0xffffffffu, mbar_wait(&S.sfull[sb], (i >> 1) & 1, &S.abort));
-      float x[kTile];
+      float x[32];
       if (ok) {
         tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < kTile / 16; ++c) tmem_ld16(tmem + lane_base + sb * 128 + 16 * c, x + 16 * c);
+        tmem_ld16(tmem + lane_base + sb * 128 + col0, x);
+        tmem_ld16(tmem + lane_base + sb * 128 + col0 + 16, x + 16);
         tmem_wait_ld();
         tc_fence_before();
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.sempty[sb]);
-      if (!ok) { failed = true; break; }
       // keys past the row (or the sequence) only in the diagonal tile
       const bool diag = i == qt;
-      float mt = -INFINITY;
+      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int c = 0; c < kTile; ++c) {
-        const int j = i * kTile + c;
+      for (int c = 0; c < 32; ++c) {
+        const int j = i * kTile + col0 + c;
         x[c] = (!diag || (j <= pos && j < nb)) ? x[c] * scale : -INFINITY;
-        mt = fmaxf(mt, x[c]);
+        m4[c & 3] = fmaxf(m4[c & 3], x[c]);
       }
-      const bool need = mt > ref + kRescaleLog2;
+      S.red[par][cg][row] = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+      // one barrier per tile: the row's four partial maxima, and "some wait failed"
+      if (named_bar_or(kPfBar, kPfWorkers, bad || !ok)) { failed = true; break; }
+      const float mt = fmaxf(fmaxf(S.red[par][0][row], S.red[par][1][row]),
+                             fmaxf(S.red[par][2][row], S.red[par][3][row]));
+      const bool need = mt > ref + kRescaleLog2;   // the same in the row's four threads
       float factor = 1.f;
       if (need) {
         factor = (ref == -INFINITY) ? 0.f : ex2_approx(ref - mt);
@@ -1898,118 +1916,135 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         float z[16];
 #pragma unroll
         for (int u = 0; u < 16; ++u) z[u] = 0.f;
-#pragma unroll
-        for (int c = 0; c < kDPad / 16; ++c) tmem_st16(tO + kDPad + lane_base + 16 * c, z);
+        tmem_st16(tO + kDPad + lane_base + col0, z);
+        tmem_st16(tO + kDPad + lane_base + col0 + 16, z);
         tmem_wait_st();
       }
       const bool fold = i > 0 && i % kPfFold == 0;   // the same in every thread
       if (fold || __any_sync(0xffffffffu, need && i > 0)) {
         // once PV(i - 1) is done (PV(i - 2) is: pempty was waited for at tile
-        // i - 1, so ofull is at most one phase behind): at a fold
-        // O2 = (O2 + O) * factor and PV(i) restarts O; else O *= factor and
-        // O2 *= factor
-        bool okw = __all_sync(0xffffffffu, mbar_wait(&S.ofull, (i - 1) & 1, &S.abort));
-        if (!okw) { failed = true; break; }
+        // i - 1, so ofull is at most one phase behind), on this thread's 32
+        // columns of O: at a fold O2 = (O2 + O) * factor and PV(i) restarts
+        // O; else O *= factor and O2 *= factor
+        const bool okw = __all_sync(0xffffffffu, mbar_wait(&S.ofull, (i - 1) & 1, &S.abort));
+        if (!okw) bad = true;
         tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < kDPad / 16; ++c) {
+        for (int c = 0; c < 2 && okw; ++c) {
           float o[16], o2[16];
-          tmem_ld16(tO + lane_base + 16 * c, o);
-          tmem_ld16(tO + kDPad + lane_base + 16 * c, o2);
+          tmem_ld16(tO + lane_base + col0 + 16 * c, o);
+          tmem_ld16(tO + kDPad + lane_base + col0 + 16 * c, o2);
           tmem_wait_ld();
 #pragma unroll
           for (int u = 0; u < 16; ++u) {
             o2[u] = (fold ? o2[u] + o[u] : o2[u]) * factor;
             o[u] *= factor;
           }
-          if (!fold) tmem_st16(tO + lane_base + 16 * c, o);
-          tmem_st16(tO + kDPad + lane_base + 16 * c, o2);
+          if (!fold) tmem_st16(tO + lane_base + col0 + 16 * c, o);
+          tmem_st16(tO + kDPad + lane_base + col0 + 16 * c, o2);
         }
         tmem_wait_st();
         tc_fence_before();
       }
-      // the P buffer is free once PV(i - 1) is done
-      if (i >= 1) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&S.pempty, (i - 1) & 1, &S.abort));
-        if (!ok) { failed = true; break; }
+#pragma unroll
+      for (int c = 0; c < 32; ++c) x[c] = ex2_approx(x[c] - ref);
+      float ls4[4] = {0.f, 0.f, 0.f, 0.f};
+      float em4[4] = {emax, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        ls4[c & 3] += x[c];
+        em4[c & 3] = fmaxf(em4[c & 3], x[c]);
       }
-      if ((i + 1) * kTile > nb) {
+      l += (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
+      emax = fmaxf(fmaxf(em4[0], em4[1]), fmaxf(em4[2], em4[3]));
+      // the P buffer is free once the previous phase's P V is done
+      const int ph = i * pps;
+      if (!bad && ph >= 1 && !__all_sync(0xffffffffu, mbar_wait(&S.pempty, (ph - 1) & 1, &S.abort))) bad = true;
+      if (!bad && (i + 1) * kTile > nb) {
         // slots past the sequence may hold anything (NaN): zero their V rows
-        // so that 0 * NaN never reaches the PV accumulator
-        ok = __all_sync(0xffffffffu, mbar_wait(&S.vfull[vs], (i >> 1) & 1, &S.abort));
-        if (!ok) { failed = true; break; }
-        if (i * kTile + tid >= nb) {
-          uint8_t* vrow = sm + kPfOffV + vs * kTileBytes + tid * 128;
+        // so that 0 * NaN never reaches the PV accumulator (each of the row's
+        // four threads zeroes 64 of its 256 bytes)
+        if (!__all_sync(0xffffffffu, mbar_wait(&S.vfull[vs], (i >> 1) & 1, &S.abort))) bad = true;
+        if (!bad && i * kTile + row >= nb) {
+          uint8_t* vrow = sm + kPfOffV + vs * kTileBytes + row * 128 + (cg >> 1) * kHalfTile + (cg & 1) * 64;
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            *reinterpret_cast<uint4*>(vrow + c * 16) = make_uint4(0, 0, 0, 0);
-            *reinterpret_cast<uint4*>(vrow + kHalfTile + c * 16) = make_uint4(0, 0, 0, 0);
-          }
+          for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4*>(vrow + c * 16) = make_uint4(0, 0, 0, 0);
         }
       }
-      float lsum = 0.f;
+      uint32_t lo[16];
 #pragma unroll
-      for (int c8 = 0; c8 < kTile / 8; ++c8) {
-        uint32_t hp[4], lp[4];
+      for (int c8 = 0; c8 < 4; ++c8) {
+        uint32_t hp[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float e0 = ex2_approx(x[8 * c8 + 2 * q] - ref);
-          const float e1 = ex2_approx(x[8 * c8 + 2 * q + 1] - ref);
-          lsum += e0 + e1;
-          emax = fmaxf(emax, fmaxf(e0, e1));
-          split_hi_lo(e0, e1, hp[q], lp[q]);
-        }
-        const uint32_t off = sw128_offset((uint32_t)tid, (uint32_t)(8 * c8), kTile);
-        *reinterpret_cast<uint4*>(phi_s + off) = make_uint4(hp[0], hp[1], hp[2], hp[3]);
-        if (precise) *reinterpret_cast<uint4*>(plo_s + off) = make_uint4(lp[0], lp[1], lp[2], lp[3]);
+        for (int q = 0; q < 4; ++q) split_hi_lo(x[8 * c8 + 2 * q], x[8 * c8 + 2 * q + 1], hp[q], lo[4 * c8 + q]);
+        const uint32_t off = sw128_offset((uint32_t)row, (uint32_t)(col0 + 8 * c8), kTile);
+        if (!bad) *reinterpret_cast<uint4*>(ps + off) = make_uint4(hp[0], hp[1], hp[2], hp[3]);
       }
-      l += lsum;
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.pfull);
+      if (precise) {
+        // the remainder, once P_hi V is done
+        if (!bad && !__all_sync(0xffffffffu, mbar_wait(&S.pempty, ph & 1, &S.abort))) bad = true;
+#pragma unroll
+        for (int c8 = 0; c8 < 4 && !bad; ++c8) {
+          const uint32_t off = sw128_offset((uint32_t)row, (uint32_t)(col0 + 8 * c8), kTile);
+          *reinterpret_cast<uint4*>(ps + off) = make_uint4(lo[4 * c8], lo[4 * c8 + 1], lo[4 * c8 + 2], lo[4 * c8 + 3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.pfull);
+      }
     }
     // ---------------------------------------------------- epilogue
     // The MMA warp commits `drain` once, after its last MMA.
     bool okw = false;
-    if (!failed) okw = mbar_wait(&S.drain, 0, &S.abort);
+    if (!failed && !bad) okw = mbar_wait(&S.drain, 0, &S.abort);
     okw = __all_sync(0xffffffffu, okw);
+    // the row's four partial sums and largest e (every softmax warp arrives)
+    S.red2[0][cg][row] = l;
+    S.red2[1][cg][row] = emax;
+    if (named_bar_or(kPfBar, kPfWorkers, !okw)) okw = false;
     if (okw) {
+      const float lt = (S.red2[0][0][row] + S.red2[0][1][row]) + (S.red2[0][2][row] + S.red2[0][3][row]);
+      const float et = fmaxf(fmaxf(S.red2[1][0][row], S.red2[1][1][row]), fmaxf(S.red2[1][2][row], S.red2[1][3][row]));
       tc_fence_after();
       const bool row_ok = pos < nb;
       const bool win = row_ok && pos >= nb - p.w;
       const int tw = pos - (nb - p.w);
       const int r = (hq - h * p.g) * p.w + tw;
       const size_t part = (size_t)unit * p.splits;          // the single partial of the row
-      const float inv_l = 1.0f / l;
+      const float inv_l = 1.0f / lt;
       __nv_bfloat16* orow = p.out + (((size_t)b * p.Hq + hq) * p.n_max + pos) * p.d;
 #pragma unroll
-      for (int c = 0; c < kDPad / 16; ++c) {
+      for (int c = 0; c < 2; ++c) {
         float o[16], o2[16];
-        tmem_ld16(tO + lane_base + 16 * c, o);
-        tmem_ld16(tO + kDPad + lane_base + 16 * c, o2);
+        tmem_ld16(tO + lane_base + col0 + 16 * c, o);
+        tmem_ld16(tO + kDPad + lane_base + col0 + 16 * c, o2);
         tmem_wait_ld();
 #pragma unroll
         for (int u = 0; u < 16; ++u) o[u] += o2[u];
-        if (row_ok && 16 * c < p.d) {
+        const int c0 = col0 + 16 * c;
+        if (row_ok && c0 < p.d) {
           uint32_t w8[8];
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
             const __nv_bfloat162 h2 = __floats2bfloat162_rn(o[2 * u] * inv_l, o[2 * u + 1] * inv_l);
             w8[u] = *reinterpret_cast<const uint32_t*>(&h2);
           }
-          *reinterpret_cast<uint4*>(orow + 16 * c) = make_uint4(w8[0], w8[1], w8[2], w8[3]);
-          if (16 * c + 8 < p.d) *reinterpret_cast<uint4*>(orow + 16 * c + 8) = make_uint4(w8[4], w8[5], w8[6], w8[7]);
+          *reinterpret_cast<uint4*>(orow + c0) = make_uint4(w8[0], w8[1], w8[2], w8[3]);
+          if (c0 + 8 < p.d) *reinterpret_cast<uint4*>(orow + c0 + 8) = make_uint4(w8[4], w8[5], w8[6], w8[7]);
           if (win) {
-            float* po = p.part_o + (part * p.R + r) * p.d + 16 * c;
+            float* po = p.part_o + (part * p.R + r) * p.d + c0;
 #pragma unroll
             for (int u = 0; u < 16; u += 4)
-              if (16 * c + u < p.d) *reinterpret_cast<float4*>(po + u) = make_float4(o[u], o[u + 1], o[u + 2], o[u + 3]);
+              if (c0 + u < p.d) *reinterpret_cast<float4*>(po + u) = make_float4(o[u], o[u + 1], o[u + 2], o[u + 3]);
           }
         }
       }
       tc_fence_before();
-      if (win) {
-        reinterpret_cast<float4*>(p.part_ml)[part * p.R + r] = make_float4(ref, l, emax, 0.f);
+      if (win && cg == 0) {
+        reinterpret_cast<float4*>(p.part_ml)[part * p.R + r] = make_float4(ref, lt, et, 0.f);
         const uint4* qs = reinterpret_cast<const uint4*>(p.q + (((size_t)b * p.Hq + hq) * p.n_max + pos) * p.d);
         uint4* qd = reinterpret_cast<uint4*>(p.q_win + (((size_t)b * p.Hq + hq) * p.w + tw) * p.d);
         for (int c = 0; c < p.d / 8; ++c) qd[c] = qs[c];

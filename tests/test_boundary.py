@@ -19,7 +19,7 @@ def test_library_exports_every_declared_symbol():
     declared = B.declared_functions()
     assert set(declared) == {"dropkv_workspace_size", "dropkv_score", "dropkv_score_timed", "dropkv_score_noalloc",
                              "dropkv_select", "dropkv_compact", "dropkv_evict", "dropkv_score_ex",
-                             "dropkv_evict_ex", "dropkv_evict_prefill", "dropkv_select_layer", "dropkv_compact_heads", "dropkv_read_status",
+                             "dropkv_evict_ex", "dropkv_evict_prefill", "dropkv_prefill_attention", "dropkv_select_layer", "dropkv_compact_heads", "dropkv_read_status",
                              "dropkv_version"}
     for name in declared:
         assert hasattr(lib, name), name

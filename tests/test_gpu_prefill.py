@@ -149,3 +149,16 @@ def test_prefill_matches_the_window_path():
     scale = np.abs(a).max(axis=-1, keepdims=True)
     assert np.all(np.abs(a - b) <= 2e-3 * np.abs(a) + 1e-6 * scale)
     assert np.array_equal(op.kept_len.cpu().numpy(), op_pf.kept_len.cpu().numpy())
+
+
+def test_attention_alone_equals_the_fused_output():
+    """dropkv_prefill_attention runs the fused call's kernel without the
+    eviction: the same bytes."""
+    wl = synth.make_workload("llama8b_gqa_d128_n32k", n_max=1500)
+    s = wl.spec
+    q_full = _prefill_inputs(wl, seed=16)
+    op, k, v, out = _run_prefill(wl, q_full, poison=False)
+    out2 = torch.full_like(out, -3.5)
+    op.prefill_attention(q_full.to(DEV), k, v, wl.lengths.to(DEV), out2)
+    op.check()
+    assert torch.equal(out, out2)
