@@ -1890,13 +1890,20 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.sempty[sb]);
       // keys past the row (or the sequence) only in the diagonal tile
-      const bool diag = i == qt;
       float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      if (i == qt) {   // the diagonal tile (uniform over the CTA)
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const int j = i * kTile + col0 + c;
-        x[c] = (!diag || (j <= pos && j < nb)) ? x[c] * scale : -INFINITY;
-        m4[c & 3] = fmaxf(m4[c & 3], x[c]);
+        for (int c = 0; c < 32; ++c) {
+          const int j = i * kTile + col0 + c;
+          x[c] = (j <= pos && j < nb) ? x[c] * scale : -INFINITY;
+          m4[c & 3] = fmaxf(m4[c & 3], x[c]);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          x[c] *= scale;
+          m4[c & 3] = fmaxf(m4[c & 3], x[c]);
+        }
       }
       S.red[par][cg][row] = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
       // one barrier per tile: the row's four partial maxima, and "some wait failed"
@@ -1949,14 +1956,15 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 #pragma unroll
       for (int c = 0; c < 32; ++c) x[c] = ex2_approx(x[c] - ref);
       float ls4[4] = {0.f, 0.f, 0.f, 0.f};
-      float em4[4] = {emax, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        ls4[c & 3] += x[c];
-        em4[c & 3] = fmaxf(em4[c & 3], x[c]);
-      }
+      for (int c = 0; c < 32; ++c) ls4[c & 3] += x[c];
       l += (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
-      emax = fmaxf(fmaxf(em4[0], em4[1]), fmaxf(em4[2], em4[3]));
+      if (precise) {   // the largest e is only wanted for window rows (uniform over the CTA)
+        float em4[4] = {emax, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int c = 0; c < 32; ++c) em4[c & 3] = fmaxf(em4[c & 3], x[c]);
+        emax = fmaxf(fmaxf(em4[0], em4[1]), fmaxf(em4[2], em4[3]));
+      }
       // the P buffer is free once the previous phase's P V is done
       const int ph = i * pps;
       if (!bad && ph >= 1 && !__all_sync(0xffffffffu, mbar_wait(&S.pempty, (ph - 1) & 1, &S.abort))) bad = true;

@@ -162,3 +162,59 @@ def test_attention_alone_equals_the_fused_output():
     op.prefill_attention(q_full.to(DEV), k, v, wl.lengths.to(DEV), out2)
     op.check()
     assert torch.equal(out, out2)
+
+
+def test_prefill_snapkv_kind_vs_oracle():
+    """The SnapKV score kind through the fused call (K only in pass 2; the
+    window states still come from the prefill attention)."""
+    wl = synth.make_workload("llama8b_gqa_d128_n32k", n_max=2500)
+    s = wl.spec
+    q_full = _prefill_inputs(wl, seed=17)
+    op = DropKV(s.B, s.Hq, s.Hkv, s.d, s.n_max, s.w, s.pool_kernel, s.protect, device=DEV, kind="snapkv")
+    k, v = wl.k.to(DEV), wl.v.to(DEV)
+    out = torch.empty((s.B, s.Hq, s.n_max, s.d), dtype=torch.bfloat16, device=DEV)
+    op.scores.fill_(SENTINEL)
+    op.raw_scores.fill_(SENTINEL)
+    op.kept_idx.fill_(-5)
+    op.run_prefill(q_full.to(DEV), k, v, wl.lengths.to(DEV), wl.evict_k.to(DEV), out)
+    op.check()
+    qw = _window_q(q_full, wl.lengths, s.w)
+    win = synth.Workload(spec=s, q=qw, k=wl.k, v=wl.v, lengths=wl.lengths, evict_k=wl.evict_k)
+    ref = oracle.run_path(qw, wl.k, wl.v, wl.lengths, wl.evict_k, s.pool_kernel, s.protect, kind="snapkv")
+    _compare(win, op, k, v, ref, "prefill snapkv", kind="snapkv")
+
+
+def test_prefill_entry_points_reject_bad_arguments():
+    """Host checks of dropkv_evict_prefill and dropkv_prefill_attention: an
+    output overlapping q, k or v, a misaligned pointer or a short workspace is
+    rejected with nothing launched."""
+    import ctypes
+    from kv_cache_eviction_dropkv_gb300 import _binding as B
+    wl = synth.make_workload("llama8b_gqa_d128_n32k", n_max=700)
+    s = wl.spec
+    op = DropKV(s.B, s.Hq, s.Hkv, s.d, s.n_max, s.w, s.pool_kernel, s.protect, device=DEV)
+    q = _prefill_inputs(wl, seed=18).to(DEV)
+    k, v = wl.k.to(DEV), wl.v.to(DEV)
+    out = torch.full_like(q, -3.5)
+    L = B.lib()
+
+    def attn(o=None, qq=None, ws=None):
+        return L.dropkv_prefill_attention(ctypes.byref(op.shape), qq or B._ptr(q), B._ptr(k), B._ptr(v), None,
+                                          o or B._ptr(out), B._ptr(op.workspace),
+                                          op.workspace.numel() if ws is None else ws, B._ptr(op.status),
+                                          B._stream(None))
+    assert attn(o=B._ptr(q)) == 1                                          # output on top of q
+    assert attn(o=ctypes.c_void_p(k.data_ptr())) == 1                      # ... or of k
+    assert attn(qq=ctypes.c_void_p(q.data_ptr() + 2)) == 1                 # misaligned
+    assert attn(ws=1024) == 2                                              # workspace too small
+    fused = L.dropkv_evict_prefill(ctypes.byref(op.shape), 0, B._ptr(q), B._ptr(k), B._ptr(v), None,
+                                   B._ptr(wl.evict_k.to(DEV)), 5, 8, B._ptr(q), B._ptr(op.scores), None,
+                                   B._ptr(op.kept_idx), B._ptr(op.kept_len), op.out_rows, B._ptr(op.k_out),
+                                   B._ptr(op.v_out), B._ptr(op.workspace), op.workspace.numel(), B._ptr(op.status),
+                                   B._stream(None))
+    assert fused == 1
+    torch.cuda.synchronize()
+    assert torch.all(out == -3.5) and int(op.status.item()) == 0           # nothing was launched
+    assert attn() == 0
+    op.check()
+    assert not torch.all(out == -3.5)
