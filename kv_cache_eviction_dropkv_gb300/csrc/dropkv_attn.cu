@@ -1890,22 +1890,21 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&S.sempty[sb]);
       // keys past the row (or the sequence) only in the diagonal tile
+      // the maximum of the raw logits (the scale is positive): x is scaled
+      // inside the exponent's FMA below
       float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
       if (i == qt) {   // the diagonal tile (uniform over the CTA)
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
           const int j = i * kTile + col0 + c;
-          x[c] = (j <= pos && j < nb) ? x[c] * scale : -INFINITY;
+          if (!(j <= pos && j < nb)) x[c] = -INFINITY;
           m4[c & 3] = fmaxf(m4[c & 3], x[c]);
         }
       } else {
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          x[c] *= scale;
-          m4[c & 3] = fmaxf(m4[c & 3], x[c]);
-        }
+        for (int c = 0; c < 32; ++c) m4[c & 3] = fmaxf(m4[c & 3], x[c]);
       }
-      S.red[par][cg][row] = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+      S.red[par][cg][row] = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * scale;
       // one barrier per tile: the row's four partial maxima, and "some wait failed"
       if (named_bar_or(kPfBar, kPfWorkers, bad || !ok)) { failed = true; break; }
       const float mt = fmaxf(fmaxf(S.red[par][0][row], S.red[par][1][row]),
@@ -1954,7 +1953,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         tc_fence_before();
       }
 #pragma unroll
-      for (int c = 0; c < 32; ++c) x[c] = ex2_approx(x[c] - ref);
+      for (int c = 0; c < 32; ++c) x[c] = ex2_approx(fmaf(x[c], scale, -ref));
       float ls4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c = 0; c < 32; ++c) ls4[c & 3] += x[c];
@@ -1984,7 +1983,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       for (int c8 = 0; c8 < 4; ++c8) {
         uint32_t hp[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) split_hi_lo(x[8 * c8 + 2 * q], x[8 * c8 + 2 * q + 1], hp[q], lo[4 * c8 + q]);
+        for (int q = 0; q < 4; ++q) {
+          if (precise) {
+            split_hi_lo(x[8 * c8 + 2 * q], x[8 * c8 + 2 * q + 1], hp[q], lo[4 * c8 + q]);
+          } else {
+            const __nv_bfloat162 h2 = __floats2bfloat162_rn(x[8 * c8 + 2 * q], x[8 * c8 + 2 * q + 1]);
+            hp[q] = *reinterpret_cast<const uint32_t*>(&h2);
+          }
+        }
         const uint32_t off = sw128_offset((uint32_t)row, (uint32_t)(col0 + 8 * c8), kTile);
         if (!bad) *reinterpret_cast<uint4*>(ps + off) = make_uint4(hp[0], hp[1], hp[2], hp[3]);
       }
