@@ -1399,13 +1399,48 @@ __device__ __forceinline__ bool p2_work(uint8_t* sV, uint8_t* sP, Pass2Small& S,
   }
   if constexpr (DOM) {
     // The dominant keys' terms.  The MMA warp commits `drain` after its last
-    // MMA (the final PV): a single-phase wait.
+    // MMA (the final PV): a single-phase wait.  This code runs once per call
+    // on one CTA per head, after the kernel's hot code: it is fetched cold, so
+    // it is kept short (loops not unrolled where the body is large) and every
+    // global load goes out in one round trip.
     bool okw = true;
     if (!failed) okw = __all_sync(0xffffffffu, mbar_wait(&S.drain, 0, &S.abort));
     if (named_bar_or(kBarWork, kWorkers, failed || !okw)) return true;
     tc_fence_after();
     float o[HR];   // O_rest^T: lane = head dimension tok, columns = rows
     tmem_ld_cols<HR>(tmem + 4 * NR + lane_base + r0, o);
+    // Copied to shared memory in one round trip (cp.async, no registers): the
+    // merge's O and L of the other splits for every dominated row and its
+    // dominant key's V row (warp w: rows w, w + 8, ...; lane: 4 columns), into
+    // the V ring, idle now that the last MMA is done: [kMaxR][kDPad] f32 O,
+    // [kMaxR][kDPad] bf16 V, [kMaxR] f32 L, then [kMaxR][kDPad] f32 for this
+    // thread's O_rest and, in place, its squared differences.  Warp 0 also
+    // loads the dominant keys' raw scores.
+    float* so = reinterpret_cast<float*>(sV);
+    __nv_bfloat16* svs = reinterpret_cast<__nv_bfloat16*>(sV + kMaxR * kDPad * 4);
+    float* sdl = reinterpret_cast<float*>(sV + kMaxR * kDPad * 6);
+    float* ssq = reinterpret_cast<float*>(sV + kMaxR * kDPad * 6 + kMaxR * 4);
+    const size_t rowbase = (size_t)unit * R;
+    const int d4 = p.d >> 2;
+#pragma unroll 1
+    for (int rr = warp; rr < R; rr += kWorkerWarps) {
+      const int jst = S.domj[rr];
+      if (((S.domf >> rr) & 1ull) && jst >= 0 && lane < d4) {
+        cp_async<16>(so + rr * kDPad + 4 * lane, p.dom_o + (rowbase + rr) * p.d + 4 * lane);
+        cp_async<8>(svs + rr * kDPad + 4 * lane, p.v + ((size_t)unit * p.n_max + jst) * p.d + 4 * lane);
+        if (lane == 0) cp_async<4>(sdl + rr, p.dom_l + rowbase + rr);
+      }
+    }
+    int key[2] = {-1, -1};
+    float cur[2] = {0.f, 0.f};
+    if (tid < 32) {
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        const int rr = lane + 32 * h2;
+        key[h2] = (rr < R && ((S.domf >> rr) & 1ull)) ? S.domj[rr] : -1;
+        if (key[h2] >= 0) cur[h2] = raw[key[h2]];
+      }
+    }
     tmem_wait_ld();
     tc_fence_before();
 #pragma unroll
@@ -1413,39 +1448,21 @@ __device__ __forceinline__ bool p2_work(uint8_t* sV, uint8_t* sP, Pass2Small& S,
       const float v = warp_sum(lrest[r]);
       if (lane == 0) S.fx.red[wq][r0 + r] = v;
     }
-    // Stage, with independent loads (one round trip), the merge's O and L of
-    // the other splits for every dominated row and its dominant key's V row,
-    // in the V ring, idle now that the last MMA is done: [kMaxR][kDPad] f32
-    // O, [kMaxR][kDPad] bf16 V, [kMaxR] f32 L.
-    float* so = reinterpret_cast<float*>(sV);
-    __nv_bfloat16* svs = reinterpret_cast<__nv_bfloat16*>(sV + kMaxR * kDPad * 4);
-    float* sdl = reinterpret_cast<float*>(sV + kMaxR * kDPad * 6);
-    const size_t rowbase = (size_t)unit * R;
-    const int d4 = p.d >> 2;
-    for (int idx = tid; idx < R * d4; idx += kWorkers) {
-      const int rr = idx / d4, c4 = idx - rr * d4;
-      const int jst = S.domj[rr];
-      if (((S.domf >> rr) & 1ull) && jst >= 0) {
-        reinterpret_cast<float4*>(so + rr * kDPad)[c4] =
-            reinterpret_cast<const float4*>(p.dom_o + (rowbase + rr) * p.d)[c4];
-        reinterpret_cast<uint2*>(svs + rr * kDPad)[c4] =
-            reinterpret_cast<const uint2*>(p.v + ((size_t)unit * p.n_max + jst) * p.d)[c4];
-        if (c4 == 0) sdl[rr] = p.dom_l[rowbase + rr];
-      }
-    }
+#pragma unroll
+    for (int r = 0; r < HR; ++r) ssq[(r0 + r) * kDPad + tok] = o[r];
+    cp_async_wait_all();
     named_bar(kBarAux, kWorkers);
     // (a) every thread: the squared differences of its token for the
-    // dominated rows of its half, into [kMaxR][kDPad] f32 (also in the ring)
-    float* ssq = reinterpret_cast<float*>(sV + kMaxR * kDPad * 6 + kMaxR * 4);
-#pragma unroll
+    // dominated rows of its half (rows it does not answer for are skipped the
+    // same way by the whole warp)
+#pragma unroll 1
     for (int r = 0; r < HR; ++r) {
-      if (!((dommask >> r) & 1u)) continue;       // the same in the whole warp
       const int rr = r0 + r;
-      if (S.domj[rr] < 0) continue;               // the same in the whole warp
+      if (!((dommask >> r) & 1u) || S.domj[rr] < 0) continue;
       const float lt = sdl[rr] + ((S.fx.red[0][rr] + S.fx.red[1][rr]) + (S.fx.red[2][rr] + S.fx.red[3][rr]));
       float sq = 0.f;
       if (tok < p.d) {
-        const float ar = (so[rr * kDPad + tok] + o[r]) / lt;
+        const float ar = (so[rr * kDPad + tok] + ssq[rr * kDPad + tok]) / lt;
         const float df = ar - __bfloat162float(svs[rr * kDPad + tok]);
         sq = df * df;
       }
@@ -1455,8 +1472,9 @@ __device__ __forceinline__ bool p2_work(uint8_t* sV, uint8_t* sP, Pass2Small& S,
     named_bar(kBarAux, kWorkers);
     // (b) |a_rest - v*|^2 of each dominated row: 8 threads per row, 16
     // tokens each in order, then a fixed butterfly over the 8
-    {
-      const int rr = tid >> 3, part = tid & 7;
+#pragma unroll 1
+    for (int rr = tid >> 3; rr < kMaxR; rr += kWorkers / 8) {
+      const int part = tid & 7;
       const bool act = rr < R && ((S.domf >> rr) & 1ull) && S.domj[rr] >= 0;
       float sum = 0.f;
       if (act)
@@ -1465,31 +1483,18 @@ __device__ __forceinline__ bool p2_work(uint8_t* sV, uint8_t* sP, Pass2Small& S,
       sum += __shfl_xor_sync(0xffffffffu, sum, 2);
       sum += __shfl_xor_sync(0xffffffffu, sum, 4);
       if (act && part == 0) S.fx.red2[0][rr] = sum;
-      if (R > 32) {   // rows 32 .. 63: a second pass
-        const int r2 = rr + 32;
-        const bool act2 = r2 < R && ((S.domf >> r2) & 1ull) && S.domj[r2] >= 0;
-        float sum2 = 0.f;
-        if (act2)
-          for (int c = part * 16; c < part * 16 + 16 && c < p.d; ++c) sum2 += ssq[r2 * kDPad + c];
-        sum2 += __shfl_xor_sync(0xffffffffu, sum2, 1);
-        sum2 += __shfl_xor_sync(0xffffffffu, sum2, 2);
-        sum2 += __shfl_xor_sync(0xffffffffu, sum2, 4);
-        if (act2 && part == 0) S.fx.red2[0][r2] = sum2;
-      }
     }
     named_bar(kBarAux, kWorkers);
     if (tid < 32) {
       // (c) one lane per row (two passes for rows 32 .. 63): the row's term;
       // the terms of the rows that share a dominant key are summed in row
       // order by the first of them, which adds them to the key's score with
-      // one read-modify-write (several rows may share a key)
+      // one write (several rows may share a key)
       float term[2];
-      int key[2];
       bool sing[2];
 #pragma unroll
       for (int h2 = 0; h2 < 2; ++h2) {
         const int rr = lane + 32 * h2;
-        key[h2] = (rr < R && ((S.domf >> rr) & 1ull)) ? S.domj[rr] : -1;
         term[h2] = 0.f;
         sing[h2] = false;
         if (key[h2] >= 0) {
@@ -1502,14 +1507,14 @@ __device__ __forceinline__ bool p2_work(uint8_t* sV, uint8_t* sP, Pass2Small& S,
           }
         }
       }
-#pragma unroll
-      for (int h2 = 0; h2 < 2; ++h2) {
-        if (32 * h2 >= R) break;
-        const int kk = key[h2];
+#pragma unroll 1
+      for (int h2 = 0; h2 < 2 && 32 * h2 < R; ++h2) {
+        const int kk = h2 ? key[1] : key[0];
         const int rr = lane + 32 * h2;
         float add = 0.f;
         bool sg = false, first = kk >= 0;
         // rows in order: q < rr with the same key makes this row not the first
+#pragma unroll 1
         for (int q = 0; q < R; ++q) {
           const int qh = q >> 5, ql = q & 31;
           const int kq = __shfl_sync(0xffffffffu, qh ? key[1] : key[0], ql);
@@ -1522,13 +1527,13 @@ __device__ __forceinline__ bool p2_work(uint8_t* sV, uint8_t* sP, Pass2Small& S,
           }
         }
         if (first) {
-          const float cur = raw[kk];
+          const float c0 = h2 ? cur[1] : cur[0];
           if (sg) {
             raw[kk] = INFINITY;
             flags |= DROPKV_FLAG_SINGULAR;
           } else {
-            const float nv = cur + add * inv_g;
-            if (!isfinite(nv) && !isinf(cur)) flags |= DROPKV_FLAG_NONFINITE | DROPKV_FLAG_NONFINITE_SCORE;
+            const float nv = c0 + add * inv_g;
+            if (!isfinite(nv) && !isinf(c0)) flags |= DROPKV_FLAG_NONFINITE | DROPKV_FLAG_NONFINITE_SCORE;
             raw[kk] = nv;
           }
         }
