@@ -1727,6 +1727,11 @@ cudaError_t launch_pass2_t(const AttnParams& p, const CUtensorMap& tk, const CUt
 //   written as a K-major SW128 bf16 operand (hi, and lo in the tiles that
 //   hold window rows, so their output keeps pass 1's precision);
 //   O += P V (N = the 128 head dimensions, V read MN-major) in TMEM.
+// A tile without window rows writes its P (bf16) to tensor memory instead, in
+// two buffers that alternate by key tile, and P V reads it from there: no
+// shared-memory round trip, and the softmax of tile i waits only for P V of
+// tile i - 2.  Its output is stored in bf16, so it needs neither the lo part
+// nor the periodic fold of the accumulator.
 // Window rows also write their state in pass 1's partial layout (one partial
 // per row) and their query row, for the merge and pass 2.
 // Softmax warps: warp w reads TMEM lane quarter w & 3 (rows 32 (w & 3) ..
@@ -1738,6 +1743,7 @@ constexpr uint32_t kPfBar = 1;                     // named barrier of the softm
 constexpr int kPfOffQ = 0, kPfOffK = kTileBytes, kPfOffV = 3 * kTileBytes, kPfOffP = 5 * kTileBytes;
 constexpr int kPfOffSmall = 6 * kTileBytes;       // after Q, two K and two V stages and P
 constexpr uint32_t kPfTmemCols = 512;             // S at [0, 256), O at [256, 384), O2 at [384, 512)
+constexpr uint32_t kPfColP = 384;                 // tiles without window rows: P buffers [384, 448), [448, 512)
 // Every kPfFold key tiles the accumulator O is folded into O2 with fp32
 // register adds and restarted, so no tensor-core accumulation chain runs over
 // more than kPfFold tiles (at n = 32K one chain of 256 tiles left the window
@@ -1746,6 +1752,11 @@ constexpr int kPfFold = 16;
 
 struct PrefillSmem {
   uint64_t qbar, kfull[2], kempty[2], vfull[2], vempty[2], sfull[2], sempty[2], pfull, pempty, ofull, drain;
+  // tiles without window rows: P buffer b in tensor memory written (all softmax
+  // warps) and read by its P V.  A full/free pair per buffer: one barrier for
+  // both buffers could run two phases ahead of the MMA warp's wait while a V
+  // tile is late, and a parity wait cannot tell those phases apart.
+  uint64_t ptfull[2], ptfree[2];
   uint32_t tmem_base;
   int abort;
   float red[2][4][kTile];       // per tile parity: each column group's largest x of row r
@@ -1786,6 +1797,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     }
     mbar_init(&S.pfull, kPfWarps);
     mbar_init(&S.pempty, 1);
+    mbar_init(&S.ptfull[0], kPfWarps);
+    mbar_init(&S.ptfull[1], kPfWarps);
+    mbar_init(&S.ptfree[0], 1);
+    mbar_init(&S.ptfree[1], 1);
     mbar_init(&S.ofull, 1);
     mbar_init(&S.drain, 1);
     S.abort = 0;
@@ -1843,7 +1858,16 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         const int vs = i & 1;
         if (!mbar_wait(&S.vfull[vs], (i >> 1) & 1, &S.abort)) { ok = false; break; }
         const uint32_t vb = smem_addr(sm + kPfOffV + vs * kTileBytes);
-        for (int part = 0; part < pps; ++part) {
+        if (!precise) {
+          if (!mbar_wait(&S.ptfull[i & 1], (i >> 1) & 1, &S.abort)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t pa = tmem + kPfColP + 64 * (i & 1);
+#pragma unroll
+          for (int s = 0; s < 8; ++s)
+            umma_bf16_tmem_a(tO, pa + 8 * s, desc_mnmajor_sw128(vb, kTile, s), idO, (i > 0 || s > 0));
+          umma_commit(&S.ptfree[i & 1]);
+        }
+        for (int part = 0; precise && part < pps; ++part) {
           const int ph = i * pps + part;
           if (!mbar_wait(&S.pfull, ph & 1, &S.abort)) { ok = false; break; }
           tc_fence_after();
@@ -1922,7 +1946,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         l *= factor;
         emax *= factor;
       }
-      if (i == 0) {
+      if (precise && i == 0) {
         // O2 starts at zero (TMEM holds anything after allocation)
         float z[16];
 #pragma unroll
@@ -1931,7 +1955,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         tmem_st16(tO + kDPad + lane_base + col0 + 16, z);
         tmem_wait_st();
       }
-      const bool fold = i > 0 && i % kPfFold == 0;   // the same in every thread
+      const bool fold = precise && i > 0 && i % kPfFold == 0;   // the same in every thread
+      // P buffer i & 1 in tensor memory is free once P V(i - 2) is done;
+      // waited for here, it also leaves ofull at most one phase behind
+      if (!precise && i >= 2 && !bad &&
+          !__all_sync(0xffffffffu, mbar_wait(&S.ptfree[i & 1], ((i >> 1) + 1) & 1, &S.abort)))
+        bad = true;
       if (fold || __any_sync(0xffffffffu, need && i > 0)) {
         // once PV(i - 1) is done (PV(i - 2) is: pempty was waited for at tile
         // i - 1, so ofull is at most one phase behind), on this thread's 32
@@ -1944,7 +1973,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         for (int c = 0; c < 2 && okw; ++c) {
           float o[16], o2[16];
           tmem_ld16(tO + lane_base + col0 + 16 * c, o);
-          tmem_ld16(tO + kDPad + lane_base + col0 + 16 * c, o2);
+          if (precise) tmem_ld16(tO + kDPad + lane_base + col0 + 16 * c, o2);
           tmem_wait_ld();
 #pragma unroll
           for (int u = 0; u < 16; ++u) {
@@ -1952,7 +1981,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             o[u] *= factor;
           }
           if (!fold) tmem_st16(tO + lane_base + col0 + 16 * c, o);
-          tmem_st16(tO + kDPad + lane_base + col0 + 16 * c, o2);
+          if (precise) tmem_st16(tO + kDPad + lane_base + col0 + 16 * c, o2);
         }
         tmem_wait_st();
         tc_fence_before();
@@ -1969,9 +1998,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         for (int c = 0; c < 32; ++c) em4[c & 3] = fmaxf(em4[c & 3], x[c]);
         emax = fmaxf(fmaxf(em4[0], em4[1]), fmaxf(em4[2], em4[3]));
       }
-      // the P buffer is free once the previous phase's P V is done
+      // the P buffer in shared memory is free once the previous phase's P V is done
       const int ph = i * pps;
-      if (!bad && ph >= 1 && !__all_sync(0xffffffffu, mbar_wait(&S.pempty, (ph - 1) & 1, &S.abort))) bad = true;
+      if (precise && !bad && ph >= 1 && !__all_sync(0xffffffffu, mbar_wait(&S.pempty, (ph - 1) & 1, &S.abort)))
+        bad = true;
       if (!bad && (i + 1) * kTile > nb) {
         // slots past the sequence may hold anything (NaN): zero their V rows
         // so that 0 * NaN never reaches the PV accumulator (each of the row's
@@ -1982,6 +2012,24 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 #pragma unroll
           for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4*>(vrow + c * 16) = make_uint4(0, 0, 0, 0);
         }
+      }
+      if (!precise) {
+        // P (bf16) of this thread's 32 keys into tensor memory, buffer i & 1
+        float pw[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          const __nv_bfloat162 h2 = __floats2bfloat162_rn(x[2 * q], x[2 * q + 1]);
+          pw[q] = __uint_as_float(*reinterpret_cast<const uint32_t*>(&h2));
+        }
+        if (!bad) {
+          tmem_st16(tmem + lane_base + kPfColP + 64 * (i & 1) + 16 * cg, pw);
+          tmem_wait_st();
+        }
+        if ((i + 1) * kTile > nb) fence_proxy_async_smem();   // V rows zeroed above
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.ptfull[i & 1]);
+        continue;
       }
       uint32_t lo[16];
 #pragma unroll
@@ -2039,10 +2087,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       for (int c = 0; c < 2; ++c) {
         float o[16], o2[16];
         tmem_ld16(tO + lane_base + col0 + 16 * c, o);
-        tmem_ld16(tO + kDPad + lane_base + col0 + 16 * c, o2);
+        if (precise) tmem_ld16(tO + kDPad + lane_base + col0 + 16 * c, o2);
         tmem_wait_ld();
+        if (precise) {
 #pragma unroll
-        for (int u = 0; u < 16; ++u) o[u] += o2[u];
+          for (int u = 0; u < 16; ++u) o[u] += o2[u];
+        }
         const int c0 = col0 + 16 * c;
         if (row_ok && c0 < p.d) {
           uint32_t w8[8];
