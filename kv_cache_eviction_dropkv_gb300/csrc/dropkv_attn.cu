@@ -1718,382 +1718,202 @@ cudaError_t launch_pass2_t(const AttnParams& p, const CUtensorMap& tk, const CUt
 // Causal attention of every query row of a prompt ("DropKV: Decoupling ...",
 // section 2.1): the kernel a scorer fused into prefill lives in.  Its last w
 // rows are step S1's window rows, so pass 1 and its read of K and V drop out
-// of the eviction.  One CTA per (128-row query tile, query head, sequence),
-// the latest (heaviest) tiles first.  Thread t of the four worker warps owns
-// TMEM lane t = query row qt * 128 + t, so a row's softmax needs no
-// cross-thread reduction:
-//   S = Q K^T on tcgen05 (M = 128 rows, N = 128 keys) into one of two TMEM
-//   buffers;  P = 2^(x - ref) with a lazily moved reference as in pass 1,
-//   written as a K-major SW128 bf16 operand (hi, and lo in the tiles that
-//   hold window rows, so their output keeps pass 1's precision);
-//   O += P V (N = the 128 head dimensions, V read MN-major) in TMEM.
-// A tile without window rows writes its P (bf16) to tensor memory instead, in
-// two buffers that alternate by key tile, and P V reads it from there: no
-// shared-memory round trip, and the softmax of tile i waits only for P V of
-// tile i - 2.  Its output is stored in bf16, so it needs neither the lo part
-// nor the periodic fold of the accumulator.
-// Window rows also write their state in pass 1's partial layout (one partial
+// of the eviction.
+//
+// A CTA holds two 128-row query tiles of one head, one per softmax group of
+// four warps; thread t of a group owns TMEM lane t, the whole of its row, so
+// the row maximum needs no exchange between threads.  Per key tile:
+//   S = Q K^T on tcgen05 (M = 128 rows, N = 128 keys) into the group's 128
+//   TMEM columns;  P = 2^(x - ref) with a lazily moved reference as in pass 1,
+//   written back over S as bf16 pairs;  O += P V with P read from tensor
+//   memory (V from shared memory, MN-major).
+// The group's next S is issued after its P V (the tensor core runs one
+// thread's MMAs in issue order, so S does not overwrite P before P V has
+// read it), and the MMA warp alternates the groups: one group's P V and next
+// S run while the other group's softmax works.  The tiles without window
+// rows go in pairs (t - 1, t), so the two key ranges differ by one tile.
+// The one or two tiles that hold window rows run alone in group 1 of their
+// own CTAs (started first: they are the longest): P in bf16 hi and lo parts
+// (two P V per key tile) and the accumulator folded every kPfFold key tiles
+// into the idle group's O columns, so their output keeps pass 1's precision;
+// their rows also write their state in pass 1's partial layout (one partial
 // per row) and their query row, for the merge and pass 2.
-// Softmax warps: warp w reads TMEM lane quarter w & 3 (rows 32 (w & 3) ..
-// + 31) and takes key columns 32 (w >> 2) .. + 31 of each tile, so four warps
-// share a row and one scheduler runs four softmax warps.
-constexpr int kPfWarps = 16, kPfWorkers = 32 * kPfWarps;
-constexpr int kPfProducerWarp = 16, kPfMmaWarp = 17, kPfThreads = 32 * 18;
-constexpr uint32_t kPfBar = 1;                     // named barrier of the softmax warps
-constexpr int kPfOffQ = 0, kPfOffK = kTileBytes, kPfOffV = 3 * kTileBytes, kPfOffP = 5 * kTileBytes;
-constexpr int kPfOffSmall = 6 * kTileBytes;       // after Q, two K and two V stages and P
-constexpr uint32_t kPfTmemCols = 512;             // S at [0, 256), O at [256, 384), O2 at [384, 512)
-constexpr uint32_t kPfColP = 384;                 // tiles without window rows: P buffers [384, 448), [448, 512)
-// Every kPfFold key tiles the accumulator O is folded into O2 with fp32
-// register adds and restarted, so no tensor-core accumulation chain runs over
-// more than kPfFold tiles (at n = 32K one chain of 256 tiles left the window
-// output 1.7e-4 off in relative terms; pass 1's splits chain about 54).
+constexpr int kPfProducerWarp = 8, kPfMmaWarp = 9, kPfThreads = 32 * 12;   // warps 10, 11 idle
+constexpr int kPfOffQ = 0, kPfOffK = 2 * kTileBytes, kPfOffV = 4 * kTileBytes, kPfOffSmall = 6 * kTileBytes;
+constexpr uint32_t kPfTmemCols = 512;   // group g: S at [128 g, 128 g + 128), O at [256 + 128 g, ...)
+// Every kPfFold key tiles the accumulator O of a window tile is folded into
+// O2 with fp32 register adds and restarted, so no tensor-core accumulation
+// chain runs over more than kPfFold tiles (at n = 32K one chain of 256 tiles
+// left the window output 1.7e-4 off in relative terms; pass 1's splits chain
+// about 54).
 constexpr int kPfFold = 16;
 
 struct PrefillSmem {
-  uint64_t qbar, kfull[2], kempty[2], vfull[2], vempty[2], sfull[2], sempty[2], pfull, pempty, ofull, drain;
-  // tiles without window rows: P buffer b in tensor memory written (all softmax
-  // warps) and read by its P V.  A full/free pair per buffer: one barrier for
-  // both buffers could run two phases ahead of the MMA warp's wait while a V
-  // tile is late, and a parity wait cannot tell those phases apart.
-  uint64_t ptfull[2], ptfree[2];
+  uint64_t qbar, kfull[2], kempty[2], vfull[2], vempty[2];
+  uint64_t sfull[2];   // group g: S(i) and every MMA issued before it complete
+  uint64_t pfull[2];   // group g: P(i) written by the group's four warps
+  uint64_t odone[2];   // group g: its last P V complete
+  uint64_t drain;
   uint32_t tmem_base;
   int abort;
-  float red[2][4][kTile];       // per tile parity: each column group's largest x of row r
-  float red2[2][4][kTile];      // at the end: each column group's sum and largest e of row r
 };
 constexpr int kPfSmem = kPfOffSmall + (int)sizeof(PrefillSmem) + 1024;
 static_assert(kPfSmem <= 232448, "prefill shared memory exceeds the per-CTA limit");
 
-__global__ void __launch_bounds__(kPfThreads, 1)
-    prefill_attention_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                             const __grid_constant__ CUtensorMap tmv, const PrefillParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = align1024(smem_raw);
-  PrefillSmem& S = *reinterpret_cast<PrefillSmem*>(sm + kPfOffSmall);
-  grid_dep_wait();                          // the inputs may come from the kernel before
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int b = blockIdx.z, hq = blockIdx.y;
-  const int nb = p.lengths ? p.lengths[b] : p.n_max;
-  const int qt = (int)gridDim.x - 1 - (int)blockIdx.x;
-  if (nb < p.w || nb > p.n_max) {
-    if (tid == 0 && blockIdx.x == 0 && hq == 0) atomicOr(p.status, DROPKV_FLAG_BAD_LENGTH);
-    return;
-  }
-  if (qt * kTile >= nb) return;             // past the sequence
-  const int h = hq / p.g, unit = b * p.Hkv + h;
-  const int nk = qt + 1;                    // key tiles 0 .. qt (causal)
-  // the tile holding window rows runs P V twice per key tile: P in bf16 hi,
-  // then its rounding remainder (lo) in the same buffer
-  const bool precise = qt * kTile + kTile > nb - p.w;
-  const int pps = precise ? 2 : 1;          // pfull / pempty phases per key tile
-
-  if (tid == 0) {
-    mbar_init(&S.qbar, 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&S.kfull[i], 1); mbar_init(&S.kempty[i], 1);
-      mbar_init(&S.vfull[i], 1); mbar_init(&S.vempty[i], 1);
-      mbar_init(&S.sfull[i], 1); mbar_init(&S.sempty[i], kPfWarps);
-    }
-    mbar_init(&S.pfull, kPfWarps);
-    mbar_init(&S.pempty, 1);
-    mbar_init(&S.ptfull[0], kPfWarps);
-    mbar_init(&S.ptfull[1], kPfWarps);
-    mbar_init(&S.ptfree[0], 1);
-    mbar_init(&S.ptfree[1], 1);
-    mbar_init(&S.ofull, 1);
-    mbar_init(&S.drain, 1);
-    S.abort = 0;
-    fence_mbar_init();
-  }
-  if (warp == kPfMmaWarp) tmem_alloc(&S.tmem_base, kPfTmemCols);
-  if (warp == kPfProducerWarp && lane == 0) {
-    tma_prefetch_desc(&tmq);
-    tma_prefetch_desc(&tmk);
-    tma_prefetch_desc(&tmv);
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = S.tmem_base;
-  const uint32_t tO = tmem + 256;
-  bool failed = false;
-  grid_dep_launch();
-
-  if (warp == kPfProducerWarp) {
-    if (lane == 0) {
-      mbar_arrive_expect_tx(&S.qbar, kTileBytes);
-      tma_load_3d(sm + kPfOffQ, &tmq, &S.qbar, 0, qt * kTile, b * p.Hq + hq);
-      tma_load_3d(sm + kPfOffQ + kHalfTile, &tmq, &S.qbar, 64, qt * kTile, b * p.Hq + hq);
-      stream_ring<2>(sm + kPfOffK, S.kfull, S.kempty, &tmk, 0, nk, unit, 0, &S.abort, p.status);
-      mbar_drain(&S.qbar, 0);               // the Q copy has landed before the CTA can leave
-    } else if (lane == 1) {
-      stream_ring<2>(sm + kPfOffV, S.vfull, S.vempty, &tmv, 0, nk, unit, 0, &S.abort, p.status);
-    }
-    __syncwarp();
-  } else if (warp == kPfMmaWarp) {
-    if (lane == 0) {
-      const uint32_t idS = umma_idesc_bf16(128, 128, 0, 0);
-      const uint32_t idO = umma_idesc_bf16(128, 128, 0, 1);
-      const uint32_t qaddr = smem_addr(sm + kPfOffQ);
-      const uint32_t paddr = smem_addr(sm + kPfOffP);
-      auto issue_S = [&](int i) -> bool {
-        const int slot = i & 1;
-        if (!mbar_wait(&S.kfull[slot], (i >> 1) & 1, &S.abort)) return false;
-        if (i >= 2 && !mbar_wait(&S.sempty[slot], ((i >> 1) + 1) & 1, &S.abort)) return false;
-        tc_fence_after();
-        const uint32_t kb = smem_addr(sm + kPfOffK + slot * kTileBytes);
+// The softmax group of a prefill CTA (warps 4g .. 4g + 3, one row per
+// thread); PRECISE: the window tiles' variant (hi and lo parts of P, the
+// accumulator fold, the rows' partial states).  One instance per CTA kind
+// keeps each loop's code short.
+template <bool PRECISE>
+__device__ __forceinline__ void prefill_softmax(const PrefillParams& p, PrefillSmem& S, uint8_t* sm, uint32_t tmem,
+                                                int warp, int lane, int b, int hq, int unit, int nb, int t0, int t1) {
+  const int h = hq / p.g;
+  const int g = warp >> 2, quarter = warp & 3;
+  const int tg = g ? t1 : t0;
+  const int row = quarter * 32 + lane, pos = tg * kTile + row;
+  const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+  const uint32_t tS = tmem + lane_base + 128 * g, tOg = tmem + lane_base + 256 + 128 * g;
+  const uint32_t tO2 = tmem + lane_base + 256;   // window tiles: the idle group 0's O columns
+  const float scale = p.scale_log2;
+  float ref = -INFINITY, l = 0.f, emax = 0.f;
+  // A wait this warp gave up on sets `bad`: it stops (no further arrivals),
+  // the MMA warp's next wait gives up and raises the abort flag, which ends
+  // every other wait of the CTA.
+  bool bad = tg < 0;
+  for (int i = 0; !bad && i <= tg; ++i) {
+    if (!__all_sync(0xffffffffu, mbar_wait(&S.sfull[g], i & 1, &S.abort))) { bad = true; break; }
+    tc_fence_after();
+    float x[128];
 #pragma unroll
-        for (int s = 0; s < 8; ++s)
-          umma_bf16(tmem + slot * 128, desc_kmajor_sw128(qaddr, kTile, s), desc_kmajor_sw128(kb, kTile, s), idS,
-                    s > 0);
-        umma_commit(&S.sfull[slot]);
-        umma_commit(&S.kempty[slot]);
-        return true;
-      };
-      bool ok = mbar_wait(&S.qbar, 0, &S.abort);
-      if (ok) ok = issue_S(0);
-      for (int i = 0; ok && i < nk; ++i) {
-        if (i + 1 < nk && !(ok = issue_S(i + 1))) break;
-        const int vs = i & 1;
-        if (!mbar_wait(&S.vfull[vs], (i >> 1) & 1, &S.abort)) { ok = false; break; }
-        const uint32_t vb = smem_addr(sm + kPfOffV + vs * kTileBytes);
-        if (!precise) {
-          if (!mbar_wait(&S.ptfull[i & 1], (i >> 1) & 1, &S.abort)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t pa = tmem + kPfColP + 64 * (i & 1);
+    for (int c = 0; c < 8; ++c) tmem_ld16(tS + 16 * c, x + 16 * c);
+    tmem_wait_ld();
+    if (i == tg) {   // the diagonal tile: keys past the row or the sequence
 #pragma unroll
-          for (int s = 0; s < 8; ++s)
-            umma_bf16_tmem_a(tO, pa + 8 * s, desc_mnmajor_sw128(vb, kTile, s), idO, (i > 0 || s > 0));
-          umma_commit(&S.ptfree[i & 1]);
-        }
-        for (int part = 0; precise && part < pps; ++part) {
-          const int ph = i * pps + part;
-          if (!mbar_wait(&S.pfull, ph & 1, &S.abort)) { ok = false; break; }
-          tc_fence_after();
-#pragma unroll
-          for (int s = 0; s < 8; ++s)
-            umma_bf16(tO, desc_kmajor_sw128(paddr, kTile, s), desc_mnmajor_sw128(vb, kTile, s), idO,
-                      (part > 0 || i % kPfFold != 0 || s > 0));
-          umma_commit(&S.pempty);
-        }
-        if (!ok) break;
-        umma_commit(&S.vempty[vs]);
-        umma_commit(&S.ofull);
+      for (int u = 0; u < 128; ++u) {
+        const int j = i * kTile + u;
+        if (!(j <= pos && j < nb)) x[u] = -INFINITY;
       }
-      if (!ok) {
-        failed = true;
-        S.abort = 1;
-        atomicOr(p.status, DROPKV_FLAG_TIMEOUT);
-      }
-      // make sure no MMA is still writing TMEM before it is released
-      umma_commit(&S.drain);
-      mbar_drain(&S.drain, 0);
     }
-    __syncwarp();
-  } else {
-    // ---------------------------------------------------- softmax
-    const int quarter = warp & 3, cg = warp >> 2;
-    const int row = quarter * 32 + lane, col0 = cg * 32;
-    const int pos = qt * kTile + row;
-    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
-    const float scale = p.scale_log2;
-    uint8_t* ps = sm + kPfOffP;
-    float ref = -INFINITY, l = 0.f, emax = 0.f;
-    // A wait this warp gave up on sets `bad`: the warp skips the work that
-    // depended on it, and the OR barrier of the next tile (or of the
-    // epilogue) makes every softmax warp leave together, so none is left at
-    // a named barrier the others never reach.
-    bool bad = false;
-    for (int i = 0; i < nk; ++i) {
-      const int sb = i & 1, vs = i & 1, par = i & 1;
-      bool ok = __all_sync(0xffffffffu, mbar_wait(&S.sfull[sb], (i >> 1) & 1, &S.abort));
-      float x[32];
-      if (ok) {
-        tc_fence_after();
-        tmem_ld16(tmem + lane_base + sb * 128 + col0, x);
-        tmem_ld16(tmem + lane_base + sb * 128 + col0 + 16, x + 16);
+    // the row's largest raw logit (the scale is positive: applied in the FMA below)
+    float m8[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) m8[u] = x[u];
+#pragma unroll
+    for (int u = 8; u < 128; ++u) m8[u & 7] = fmaxf(m8[u & 7], x[u]);
+    const float mt = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                           fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) * scale;
+    const bool need = mt > ref + kRescaleLog2;
+    float factor = 1.f;
+    if (need) {
+      factor = (ref == -INFINITY) ? 0.f : ex2_approx(ref - mt);
+      ref = mt;
+      l *= factor;
+      emax *= factor;
+    }
+#pragma unroll
+    for (int u = 0; u < 128; ++u) x[u] = ex2_approx(fmaf(x[u], scale, -ref));
+    float ls8[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) ls8[u] = x[u];
+#pragma unroll
+    for (int u = 8; u < 128; ++u) ls8[u & 7] += x[u];
+    l += ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
+    if (PRECISE) {   // the largest e is only wanted for window rows
+#pragma unroll
+      for (int u = 0; u < 128; ++u) emax = fmaxf(emax, x[u]);
+    }
+    // P over S's columns (all read by now): bf16 pairs at [0, 64), and in
+    // window tiles the rounding remainders at [64, 128)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      float hw[16], lw[16];
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        uint32_t hi, lo;
+        if (PRECISE) {
+          split_hi_lo(x[32 * c + 2 * q], x[32 * c + 2 * q + 1], hi, lo);
+        } else {
+          const __nv_bfloat162 h2 = __floats2bfloat162_rn(x[32 * c + 2 * q], x[32 * c + 2 * q + 1]);
+          hi = *reinterpret_cast<const uint32_t*>(&h2);
+          lo = 0u;
+        }
+        hw[q] = __uint_as_float(hi);
+        lw[q] = __uint_as_float(lo);
+      }
+      tmem_st16(tS + 16 * c, hw);
+      if (PRECISE) tmem_st16(tS + 64 + 16 * c, lw);
+    }
+    if (PRECISE && i == 0) {
+      // O2 starts at zero (TMEM holds anything after allocation)
+      float z[16];
+#pragma unroll
+      for (int u = 0; u < 16; ++u) z[u] = 0.f;
+#pragma unroll 1
+      for (int c = 0; c < 8; ++c) tmem_st16(tO2 + 16 * c, z);
+    }
+    // (after the P stores, so that x is dead) P V(i - 1) is complete (the
+    // commit S(i) signalled came after it): at a fold O2 = (O2 + O) * factor and P V(i) restarts O; else O *= factor
+    // (and O2 *= factor in window tiles)
+    const bool fold = PRECISE && i > 0 && i % kPfFold == 0;   // the same in every thread
+    if (fold || (i > 0 && __any_sync(0xffffffffu, need))) {
+#pragma unroll 1
+      for (int c = 0; c < 8; ++c) {
+        float o[16], o2[16];
+        tmem_ld16(tOg + 16 * c, o);
+        if (PRECISE) tmem_ld16(tO2 + 16 * c, o2);
         tmem_wait_ld();
-        tc_fence_before();
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&S.sempty[sb]);
-      // keys past the row (or the sequence) only in the diagonal tile
-      // the maximum of the raw logits (the scale is positive): x is scaled
-      // inside the exponent's FMA below
-      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-      if (i == qt) {   // the diagonal tile (uniform over the CTA)
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const int j = i * kTile + col0 + c;
-          if (!(j <= pos && j < nb)) x[c] = -INFINITY;
-          m4[c & 3] = fmaxf(m4[c & 3], x[c]);
+        for (int u = 0; u < 16; ++u) {
+          o2[u] = (fold ? o2[u] + o[u] : o2[u]) * factor;
+          o[u] *= factor;
         }
-      } else {
-#pragma unroll
-        for (int c = 0; c < 32; ++c) m4[c & 3] = fmaxf(m4[c & 3], x[c]);
+        if (!fold) tmem_st16(tOg + 16 * c, o);
+        if (PRECISE) tmem_st16(tO2 + 16 * c, o2);
       }
-      S.red[par][cg][row] = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * scale;
-      // one barrier per tile: the row's four partial maxima, and "some wait failed"
-      if (named_bar_or(kPfBar, kPfWorkers, bad || !ok)) { failed = true; break; }
-      const float mt = fmaxf(fmaxf(S.red[par][0][row], S.red[par][1][row]),
-                             fmaxf(S.red[par][2][row], S.red[par][3][row]));
-      const bool need = mt > ref + kRescaleLog2;   // the same in the row's four threads
-      float factor = 1.f;
-      if (need) {
-        factor = (ref == -INFINITY) ? 0.f : ex2_approx(ref - mt);
-        ref = mt;
-        l *= factor;
-        emax *= factor;
-      }
-      if (precise && i == 0) {
-        // O2 starts at zero (TMEM holds anything after allocation)
-        float z[16];
+    }
+    if (PRECISE && (i + 1) * kTile > nb) {
+      // the last key tile of a sequence whose length is not a multiple of
+      // the tile: slots past it may hold anything (NaN); zero their V rows
+      // so that 0 * NaN never reaches the accumulator (uniform over the CTA)
+      if (!__all_sync(0xffffffffu, mbar_wait(&S.vfull[i & 1], (i >> 1) & 1, &S.abort))) { bad = true; break; }
+      if (i * kTile + row >= nb) {
+        uint8_t* vrow = sm + kPfOffV + (i & 1) * kTileBytes + row * 128;
 #pragma unroll
-        for (int u = 0; u < 16; ++u) z[u] = 0.f;
-        tmem_st16(tO + kDPad + lane_base + col0, z);
-        tmem_st16(tO + kDPad + lane_base + col0 + 16, z);
-        tmem_wait_st();
-      }
-      const bool fold = precise && i > 0 && i % kPfFold == 0;   // the same in every thread
-      // P buffer i & 1 in tensor memory is free once P V(i - 2) is done;
-      // waited for here, it also leaves ofull at most one phase behind
-      if (!precise && i >= 2 && !bad &&
-          !__all_sync(0xffffffffu, mbar_wait(&S.ptfree[i & 1], ((i >> 1) + 1) & 1, &S.abort)))
-        bad = true;
-      if (fold || __any_sync(0xffffffffu, need && i > 0)) {
-        // once PV(i - 1) is done (PV(i - 2) is: pempty was waited for at tile
-        // i - 1, so ofull is at most one phase behind), on this thread's 32
-        // columns of O: at a fold O2 = (O2 + O) * factor and PV(i) restarts
-        // O; else O *= factor and O2 *= factor
-        const bool okw = __all_sync(0xffffffffu, mbar_wait(&S.ofull, (i - 1) & 1, &S.abort));
-        if (!okw) bad = true;
-        tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < 2 && okw; ++c) {
-          float o[16], o2[16];
-          tmem_ld16(tO + lane_base + col0 + 16 * c, o);
-          if (precise) tmem_ld16(tO + kDPad + lane_base + col0 + 16 * c, o2);
-          tmem_wait_ld();
-#pragma unroll
-          for (int u = 0; u < 16; ++u) {
-            o2[u] = (fold ? o2[u] + o[u] : o2[u]) * factor;
-            o[u] *= factor;
-          }
-          if (!fold) tmem_st16(tO + lane_base + col0 + 16 * c, o);
-          if (precise) tmem_st16(tO + kDPad + lane_base + col0 + 16 * c, o2);
+        for (int c = 0; c < 8; ++c) {
+          *reinterpret_cast<uint4*>(vrow + c * 16) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(vrow + kHalfTile + c * 16) = make_uint4(0, 0, 0, 0);
         }
-        tmem_wait_st();
-        tc_fence_before();
-      }
-#pragma unroll
-      for (int c = 0; c < 32; ++c) x[c] = ex2_approx(fmaf(x[c], scale, -ref));
-      float ls4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int c = 0; c < 32; ++c) ls4[c & 3] += x[c];
-      l += (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
-      if (precise) {   // the largest e is only wanted for window rows (uniform over the CTA)
-        float em4[4] = {emax, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int c = 0; c < 32; ++c) em4[c & 3] = fmaxf(em4[c & 3], x[c]);
-        emax = fmaxf(fmaxf(em4[0], em4[1]), fmaxf(em4[2], em4[3]));
-      }
-      // the P buffer in shared memory is free once the previous phase's P V is done
-      const int ph = i * pps;
-      if (precise && !bad && ph >= 1 && !__all_sync(0xffffffffu, mbar_wait(&S.pempty, (ph - 1) & 1, &S.abort)))
-        bad = true;
-      if (!bad && (i + 1) * kTile > nb) {
-        // slots past the sequence may hold anything (NaN): zero their V rows
-        // so that 0 * NaN never reaches the PV accumulator (each of the row's
-        // four threads zeroes 64 of its 256 bytes)
-        if (!__all_sync(0xffffffffu, mbar_wait(&S.vfull[vs], (i >> 1) & 1, &S.abort))) bad = true;
-        if (!bad && i * kTile + row >= nb) {
-          uint8_t* vrow = sm + kPfOffV + vs * kTileBytes + row * 128 + (cg >> 1) * kHalfTile + (cg & 1) * 64;
-#pragma unroll
-          for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4*>(vrow + c * 16) = make_uint4(0, 0, 0, 0);
-        }
-      }
-      if (!precise) {
-        // P (bf16) of this thread's 32 keys into tensor memory, buffer i & 1
-        float pw[16];
-#pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          const __nv_bfloat162 h2 = __floats2bfloat162_rn(x[2 * q], x[2 * q + 1]);
-          pw[q] = __uint_as_float(*reinterpret_cast<const uint32_t*>(&h2));
-        }
-        if (!bad) {
-          tmem_st16(tmem + lane_base + kPfColP + 64 * (i & 1) + 16 * cg, pw);
-          tmem_wait_st();
-        }
-        if ((i + 1) * kTile > nb) fence_proxy_async_smem();   // V rows zeroed above
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&S.ptfull[i & 1]);
-        continue;
-      }
-      uint32_t lo[16];
-#pragma unroll
-      for (int c8 = 0; c8 < 4; ++c8) {
-        uint32_t hp[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          if (precise) {
-            split_hi_lo(x[8 * c8 + 2 * q], x[8 * c8 + 2 * q + 1], hp[q], lo[4 * c8 + q]);
-          } else {
-            const __nv_bfloat162 h2 = __floats2bfloat162_rn(x[8 * c8 + 2 * q], x[8 * c8 + 2 * q + 1]);
-            hp[q] = *reinterpret_cast<const uint32_t*>(&h2);
-          }
-        }
-        const uint32_t off = sw128_offset((uint32_t)row, (uint32_t)(col0 + 8 * c8), kTile);
-        if (!bad) *reinterpret_cast<uint4*>(ps + off) = make_uint4(hp[0], hp[1], hp[2], hp[3]);
       }
       fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&S.pfull);
-      if (precise) {
-        // the remainder, once P_hi V is done
-        if (!bad && !__all_sync(0xffffffffu, mbar_wait(&S.pempty, ph & 1, &S.abort))) bad = true;
-#pragma unroll
-        for (int c8 = 0; c8 < 4 && !bad; ++c8) {
-          const uint32_t off = sw128_offset((uint32_t)row, (uint32_t)(col0 + 8 * c8), kTile);
-          *reinterpret_cast<uint4*>(ps + off) = make_uint4(lo[4 * c8], lo[4 * c8 + 1], lo[4 * c8 + 2], lo[4 * c8 + 3]);
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&S.pfull);
-      }
     }
-    // ---------------------------------------------------- epilogue
-    // The MMA warp commits `drain` once, after its last MMA.
-    bool okw = false;
-    if (!failed && !bad) okw = mbar_wait(&S.drain, 0, &S.abort);
-    okw = __all_sync(0xffffffffu, okw);
-    // the row's four partial sums and largest e (every softmax warp arrives)
-    S.red2[0][cg][row] = l;
-    S.red2[1][cg][row] = emax;
-    if (named_bar_or(kPfBar, kPfWorkers, !okw)) okw = false;
+    tmem_wait_st();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.pfull[g]);
+  }
+  // ---------------------------------------------------- epilogue
+  if (tg >= 0) {
+    const bool okw = !bad && __all_sync(0xffffffffu, mbar_wait(&S.odone[g], 0, &S.abort));
     if (okw) {
-      const float lt = (S.red2[0][0][row] + S.red2[0][1][row]) + (S.red2[0][2][row] + S.red2[0][3][row]);
-      const float et = fmaxf(fmaxf(S.red2[1][0][row], S.red2[1][1][row]), fmaxf(S.red2[1][2][row], S.red2[1][3][row]));
       tc_fence_after();
       const bool row_ok = pos < nb;
-      const bool win = row_ok && pos >= nb - p.w;
+      const bool win = PRECISE && row_ok && pos >= nb - p.w;
       const int tw = pos - (nb - p.w);
       const int r = (hq - h * p.g) * p.w + tw;
       const size_t part = (size_t)unit * p.splits;          // the single partial of the row
-      const float inv_l = 1.0f / lt;
+      const float inv_l = 1.0f / l;
       __nv_bfloat16* orow = p.out + (((size_t)b * p.Hq + hq) * p.n_max + pos) * p.d;
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
+#pragma unroll 1
+      for (int c = 0; c < 8; ++c) {
         float o[16], o2[16];
-        tmem_ld16(tO + lane_base + col0 + 16 * c, o);
-        if (precise) tmem_ld16(tO + kDPad + lane_base + col0 + 16 * c, o2);
+        tmem_ld16(tOg + 16 * c, o);
+        if (PRECISE) tmem_ld16(tO2 + 16 * c, o2);
         tmem_wait_ld();
-        if (precise) {
+        if (PRECISE) {
 #pragma unroll
           for (int u = 0; u < 16; ++u) o[u] += o2[u];
         }
-        const int c0 = col0 + 16 * c;
+        const int c0 = 16 * c;
         if (row_ok && c0 < p.d) {
           uint32_t w8[8];
 #pragma unroll
@@ -2111,14 +1931,138 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           }
         }
       }
-      tc_fence_before();
-      if (win && cg == 0) {
-        reinterpret_cast<float4*>(p.part_ml)[part * p.R + r] = make_float4(ref, lt, et, 0.f);
+      if (win) {
+        reinterpret_cast<float4*>(p.part_ml)[part * p.R + r] = make_float4(ref, l, emax, 0.f);
         const uint4* qs = reinterpret_cast<const uint4*>(p.q + (((size_t)b * p.Hq + hq) * p.n_max + pos) * p.d);
         uint4* qd = reinterpret_cast<uint4*>(p.q_win + (((size_t)b * p.Hq + hq) * p.w + tw) * p.d);
         for (int c = 0; c < p.d / 8; ++c) qd[c] = qs[c];
       }
     }
+  }
+}
+
+__global__ void __launch_bounds__(kPfThreads, 1)
+    prefill_attention_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                             const __grid_constant__ CUtensorMap tmv, const PrefillParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = align1024(smem_raw);
+  PrefillSmem& S = *reinterpret_cast<PrefillSmem*>(sm + kPfOffSmall);
+  grid_dep_wait();                          // the inputs may come from the kernel before
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int b = blockIdx.z, hq = blockIdx.y;
+  const int nb = p.lengths ? p.lengths[b] : p.n_max;
+  if (nb < p.w || nb > p.n_max) {
+    if (tid == 0 && blockIdx.x == 0 && hq == 0) atomicOr(p.status, DROPKV_FLAG_BAD_LENGTH);
+    return;
+  }
+  // Query tiles 0 .. F - 1 hold no window row.  Blocks 0 and 1 take tiles F
+  // and F + 1 (those before the sequence's end), blocks 2, 3, ... the pairs
+  // (F - 2, F - 1), (F - 4, F - 3), ... down to tile 0.  Group 1 takes t1,
+  // group 0 t0 (-1: none).
+  const int F = (nb - p.w) / kTile;
+  const bool precise = blockIdx.x < 2;
+  const int t1 = precise ? F + (int)blockIdx.x : F - 1 - 2 * ((int)blockIdx.x - 2);
+  const int t0 = precise ? -1 : t1 - 1;
+  if (t1 < 0 || t1 * kTile >= nb) return;
+  const int h = hq / p.g, unit = b * p.Hkv + h;
+  const int nk = t1 + 1;                    // key tiles 0 .. t1 (causal)
+
+  if (tid == 0) {
+    mbar_init(&S.qbar, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&S.kfull[i], 1); mbar_init(&S.kempty[i], 1);
+      mbar_init(&S.vfull[i], 1); mbar_init(&S.vempty[i], 1);
+      mbar_init(&S.sfull[i], 1); mbar_init(&S.pfull[i], 4);
+      mbar_init(&S.odone[i], 1);
+    }
+    mbar_init(&S.drain, 1);
+    S.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == kPfMmaWarp) tmem_alloc(&S.tmem_base, kPfTmemCols);
+  if (warp == kPfProducerWarp && lane == 0) {
+    tma_prefetch_desc(&tmq);
+    tma_prefetch_desc(&tmk);
+    tma_prefetch_desc(&tmv);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = S.tmem_base;
+  grid_dep_launch();
+
+  if (warp == kPfProducerWarp) {
+    if (lane == 0) {
+      const int zq = b * p.Hq + hq;
+      mbar_arrive_expect_tx(&S.qbar, (t0 >= 0 ? 2 : 1) * kTileBytes);
+      if (t0 >= 0) {
+        tma_load_3d(sm + kPfOffQ, &tmq, &S.qbar, 0, t0 * kTile, zq);
+        tma_load_3d(sm + kPfOffQ + kHalfTile, &tmq, &S.qbar, 64, t0 * kTile, zq);
+      }
+      tma_load_3d(sm + kPfOffQ + kTileBytes, &tmq, &S.qbar, 0, t1 * kTile, zq);
+      tma_load_3d(sm + kPfOffQ + kTileBytes + kHalfTile, &tmq, &S.qbar, 64, t1 * kTile, zq);
+      stream_ring<2>(sm + kPfOffK, S.kfull, S.kempty, &tmk, 0, nk, unit, 0, &S.abort, p.status);
+      mbar_drain(&S.qbar, 0);               // the Q copies have landed before the CTA can leave
+    } else if (lane == 1) {
+      stream_ring<2>(sm + kPfOffV, S.vfull, S.vempty, &tmv, 0, nk, unit, 0, &S.abort, p.status);
+    }
+    __syncwarp();
+  } else if (warp == kPfMmaWarp) {
+    if (lane == 0) {
+      const uint32_t idS = umma_idesc_bf16(128, 128, 0, 0);
+      const uint32_t idO = umma_idesc_bf16(128, 128, 0, 1);
+      const int pps = precise ? 2 : 1;      // P V per key tile: the hi and lo parts in window tiles
+      auto issue_S = [&](int g, int i) {    // K tile i has landed
+        const uint32_t qa = smem_addr(sm + kPfOffQ + g * kTileBytes);
+        const uint32_t kb = smem_addr(sm + kPfOffK + (i & 1) * kTileBytes);
+#pragma unroll
+        for (int s = 0; s < 8; ++s)
+          umma_bf16(tmem + 128 * g, desc_kmajor_sw128(qa, kTile, s), desc_kmajor_sw128(kb, kTile, s), idS, s > 0);
+        umma_commit(&S.sfull[g]);
+      };
+      bool ok = mbar_wait(&S.qbar, 0, &S.abort) && mbar_wait(&S.kfull[0], 0, &S.abort);
+      if (ok) {
+        tc_fence_after();
+        if (t0 >= 0) issue_S(0, 0);
+        issue_S(1, 0);
+        umma_commit(&S.kempty[0]);
+      }
+      for (int i = 0; ok && i < nk; ++i) {
+        const bool more = i + 1 < nk;
+        if (!(ok = mbar_wait(&S.vfull[i & 1], (i >> 1) & 1, &S.abort))) break;
+        if (more && !(ok = mbar_wait(&S.kfull[(i + 1) & 1], ((i + 1) >> 1) & 1, &S.abort))) break;
+        const uint32_t vb = smem_addr(sm + kPfOffV + (i & 1) * kTileBytes);
+        for (int g = 0; g < 2; ++g) {
+          const int tg = g ? t1 : t0;
+          if (i > tg) continue;             // group 0's tile ends one key tile earlier (or is absent)
+          if (!(ok = mbar_wait(&S.pfull[g], i & 1, &S.abort))) break;
+          tc_fence_after();
+          for (int part = 0; part < pps; ++part) {
+#pragma unroll
+            for (int s = 0; s < 8; ++s)
+              umma_bf16_tmem_a(tmem + 256 + 128 * g, tmem + 128 * g + 64 * part + 8 * s,
+                               desc_mnmajor_sw128(vb, kTile, s), idO,
+                               precise ? (part > 0 || i % kPfFold != 0 || s > 0) : (i > 0 || s > 0));
+          }
+          if (i < tg) issue_S(g, i + 1);    // overwrites P(i) after P V(i) has read it
+          else umma_commit(&S.odone[g]);
+        }
+        if (!ok) break;
+        if (more) umma_commit(&S.kempty[(i + 1) & 1]);
+        umma_commit(&S.vempty[i & 1]);
+      }
+      if (!ok) {
+        S.abort = 1;
+        atomicOr(p.status, DROPKV_FLAG_TIMEOUT);
+      }
+      // no MMA may still be writing TMEM when it is released
+      umma_commit(&S.drain);
+      mbar_drain(&S.drain, 0);
+    }
+    __syncwarp();
+  } else if (warp < 8) {
+    if (precise) prefill_softmax<true>(p, S, sm, tmem, warp, lane, b, hq, unit, nb, t0, t1);
+    else prefill_softmax<false>(p, S, sm, tmem, warp, lane, b, hq, unit, nb, t0, t1);
   }
   tc_fence_before();
   __syncthreads();
@@ -2149,7 +2093,8 @@ cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tq, const 
                            const CUtensorMap& tv, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(prefill_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPfSmem);
   if (e != cudaSuccess) return e;
-  const dim3 grid((p.n_max + kTile - 1) / kTile, p.Hq, p.B);
+  // two blocks for the tiles holding window rows, then one per pair of the others
+  const dim3 grid(2 + (p.n_max / kTile + 1) / 2, p.Hq, p.B);
   return launch_pdl(prefill_attention_kernel, grid, dim3(kPfThreads), kPfSmem, st, tq, tk, tv, p);
 }
 
