@@ -1810,14 +1810,20 @@ __device__ __forceinline__ void prefill_softmax(const PrefillParams& p, PrefillS
       l *= factor;
       emax *= factor;
     }
+    // e = 2^(x scale - ref), the exponent two columns per packed FMA, and
+    // the row sum over four packed accumulators
+    const uint64_t sc2 = f2_pack(scale, scale), nr2 = f2_pack(-ref, -ref);
 #pragma unroll
-    for (int u = 0; u < 128; ++u) x[u] = ex2_approx(fmaf(x[u], scale, -ref));
-    float ls8[8];
+    for (int u = 0; u < 128; u += 2) {
+      const uint64_t y = f2_fma(f2_pack(x[u], x[u + 1]), sc2, nr2);
+      x[u] = ex2_approx(f2_lo(y));
+      x[u + 1] = ex2_approx(f2_hi(y));
+    }
+    uint64_t ls2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-    for (int u = 0; u < 8; ++u) ls8[u] = x[u];
-#pragma unroll
-    for (int u = 8; u < 128; ++u) ls8[u & 7] += x[u];
-    l += ((ls8[0] + ls8[1]) + (ls8[2] + ls8[3])) + ((ls8[4] + ls8[5]) + (ls8[6] + ls8[7]));
+    for (int u = 0; u < 128; u += 2) ls2[(u >> 1) & 3] = f2_add(ls2[(u >> 1) & 3], f2_pack(x[u], x[u + 1]));
+    const uint64_t lsum = f2_add(f2_add(ls2[0], ls2[1]), f2_add(ls2[2], ls2[3]));
+    l += f2_lo(lsum) + f2_hi(lsum);
     if (PRECISE) {   // the largest e is only wanted for window rows
 #pragma unroll
       for (int u = 0; u < 128; ++u) emax = fmaxf(emax, x[u]);
