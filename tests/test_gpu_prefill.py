@@ -99,6 +99,21 @@ def test_prefill_output_and_eviction_vs_oracle(case):
     _check_output(out, ref_out, wl.v, wl.lengths.numpy(), s.g, label=case)
 
 
+@pytest.mark.parametrize("n", [1000, 1030, 1153])
+def test_prefill_tile_pairing_edges(n):
+    """The CTA tiling's edge cases on a GQA layer: n = 1000 leaves an odd
+    number of tiles before the window (the last pair CTA has one tile), n =
+    1030 puts the window across two query tiles (two window tiles, the first
+    full), n = 1153 leaves one row in the last tile.  Every row's output and
+    the eviction against the oracle."""
+    wl = synth.make_workload("llama8b_gqa_d128_n32k", n_max=n)
+    s = wl.spec
+    q_full = _prefill_inputs(wl, seed=19)
+    op, out = _check_path(wl, q_full, "prefill pairing n=%d" % n)
+    ref_out = oracle.prefill_attention(q_full, wl.k, wl.v, wl.lengths.numpy())
+    _check_output(out, ref_out, wl.v, wl.lengths.numpy(), s.g, label="pairing n=%d" % n)
+
+
 def test_prefill_full_size_c1_layer():
     """The Phi-3-like MHA layer at its full size (n = 4096, 32 heads): every
     row's output and the whole eviction against the oracle."""
