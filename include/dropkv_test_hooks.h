@@ -25,6 +25,12 @@ extern "C" {
  * device symbol); returns DROPKV_ERR_CUDA if that copy fails. */
 DROPKV_API dropkv_status dropkv_test_skip_pass2_k(int32_t unit, int32_t tile);
 
+/* The same for the prefill attention (dropkv_evict_prefill,
+ * dropkv_prefill_attention): every CTA of (unit, key tile) leaves that K tile
+ * copy out, its MMA issuer's wait runs out, and the CTA takes the same exit.
+ * (-1, -1) switches the hook off. */
+DROPKV_API dropkv_status dropkv_test_skip_prefill_k(int32_t unit, int32_t tile);
+
 #ifdef __cplusplus
 }
 #endif

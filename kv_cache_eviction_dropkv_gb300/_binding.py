@@ -79,9 +79,10 @@ def _load(path):
     L.dropkv_read_status.restype = ctypes.c_int
     L.dropkv_version.argtypes = []
     L.dropkv_version.restype = ctypes.c_char_p
-    if hasattr(L, "dropkv_test_skip_pass2_k"):
-        L.dropkv_test_skip_pass2_k.argtypes = [I32, I32]
-        L.dropkv_test_skip_pass2_k.restype = ctypes.c_int
+    for hook in ("dropkv_test_skip_pass2_k", "dropkv_test_skip_prefill_k"):
+        if hasattr(L, hook):
+            getattr(L, hook).argtypes = [I32, I32]
+            getattr(L, hook).restype = ctypes.c_int
     return L
 
 

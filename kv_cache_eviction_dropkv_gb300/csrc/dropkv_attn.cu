@@ -215,11 +215,19 @@ __device__ __forceinline__ float sumsq_bf16x8(const uint4 v, float acc) {
   return acc;
 }
 
+#ifdef DROPKV_TEST_HOOKS
+// Test build only: the (unit, tile) whose K copy the prefill attention leaves
+// out, so that the MMA issuer's bounded wait for it runs out and the kernel
+// takes its timeout exit.  {-1, -1}: none.
+__device__ int g_test_skip_pf_k[2] = {-1, -1};
+#endif
+
 // TMA producer of one ring: streams the tiles [t0, t0 + T) of one tensor into
 // a ring of DEPTH 32 KB stages.  K and V rings are driven by different lanes
 // of the producer warp, so each can run ahead of the consumers by its own depth.
 // The first `start` tiles were issued already (during the CTA's set-up).
-template <int DEPTH>
+// HOOK: the prefill's K stream (the test build may leave one copy out).
+template <int DEPTH, bool HOOK = false>
 __device__ __forceinline__ void stream_ring(uint8_t* ring, uint64_t* full, uint64_t* empty, const CUtensorMap* map,
                                             int t0, int T, int unit, int start, volatile int* abort,
                                             uint32_t* status) {
@@ -228,9 +236,14 @@ __device__ __forceinline__ void stream_ring(uint8_t* ring, uint64_t* full, uint6
   for (int i = start; i < T; ++i) {
     const int s = i % DEPTH;
     if (i >= DEPTH && !mbar_wait(&empty[s], ((i / DEPTH) + 1) & 1, abort)) { ok = false; break; }
-    mbar_arrive_expect_tx(&full[s], kTileBytes);
-    tma_load_3d(ring + s * kTileBytes, map, &full[s], 0, (t0 + i) * kTile, unit);
-    tma_load_3d(ring + s * kTileBytes + kHalfTile, map, &full[s], 64, (t0 + i) * kTile, unit);
+#ifdef DROPKV_TEST_HOOKS
+    if (!HOOK || unit != g_test_skip_pf_k[0] || t0 + i != g_test_skip_pf_k[1])
+#endif
+    {
+      mbar_arrive_expect_tx(&full[s], kTileBytes);
+      tma_load_3d(ring + s * kTileBytes, map, &full[s], 0, (t0 + i) * kTile, unit);
+      tma_load_3d(ring + s * kTileBytes + kHalfTile, map, &full[s], 64, (t0 + i) * kTile, unit);
+    }
     ++issued;
   }
   if (!ok) {
@@ -1776,12 +1789,19 @@ __device__ __forceinline__ void prefill_softmax(const PrefillParams& p, PrefillS
   const uint32_t tO2 = tmem + lane_base + 256;   // window tiles: the idle group 0's O columns
   const float scale = p.scale_log2;
   float ref = -INFINITY, l = 0.f, emax = 0.f;
-  // A wait this warp gave up on sets `bad`: it stops (no further arrivals),
-  // the MMA warp's next wait gives up and raises the abort flag, which ends
-  // every other wait of the CTA.
+  // A wait this warp gave up on sets `bad` and raises the timeout flag and
+  // the CTA's abort flag, which ends every other wait of the CTA; the warp
+  // stops (no further arrivals).
   bool bad = tg < 0;
+  auto give_up = [&]() {
+    bad = true;
+    if (lane == 0) {
+      S.abort = 1;
+      atomicOr(p.status, DROPKV_FLAG_TIMEOUT);
+    }
+  };
   for (int i = 0; !bad && i <= tg; ++i) {
-    if (!__all_sync(0xffffffffu, mbar_wait(&S.sfull[g], i & 1, &S.abort))) { bad = true; break; }
+    if (!__all_sync(0xffffffffu, mbar_wait(&S.sfull[g], i & 1, &S.abort))) { give_up(); break; }
     tc_fence_after();
     float x[128];
 #pragma unroll
@@ -1881,7 +1901,7 @@ __device__ __forceinline__ void prefill_softmax(const PrefillParams& p, PrefillS
       // the last key tile of a sequence whose length is not a multiple of
       // the tile: slots past it may hold anything (NaN); zero their V rows
       // so that 0 * NaN never reaches the accumulator (uniform over the CTA)
-      if (!__all_sync(0xffffffffu, mbar_wait(&S.vfull[i & 1], (i >> 1) & 1, &S.abort))) { bad = true; break; }
+      if (!__all_sync(0xffffffffu, mbar_wait(&S.vfull[i & 1], (i >> 1) & 1, &S.abort))) { give_up(); break; }
       if (i * kTile + row >= nb) {
         uint8_t* vrow = sm + kPfOffV + (i & 1) * kTileBytes + row * 128;
 #pragma unroll
@@ -1900,6 +1920,7 @@ __device__ __forceinline__ void prefill_softmax(const PrefillParams& p, PrefillS
   // ---------------------------------------------------- epilogue
   if (tg >= 0) {
     const bool okw = !bad && __all_sync(0xffffffffu, mbar_wait(&S.odone[g], 0, &S.abort));
+    if (!bad && !okw) give_up();
     if (okw) {
       tc_fence_after();
       const bool row_ok = pos < nb;
@@ -2007,7 +2028,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       }
       tma_load_3d(sm + kPfOffQ + kTileBytes, &tmq, &S.qbar, 0, t1 * kTile, zq);
       tma_load_3d(sm + kPfOffQ + kTileBytes + kHalfTile, &tmq, &S.qbar, 64, t1 * kTile, zq);
-      stream_ring<2>(sm + kPfOffK, S.kfull, S.kempty, &tmk, 0, nk, unit, 0, &S.abort, p.status);
+      stream_ring<2, true>(sm + kPfOffK, S.kfull, S.kempty, &tmk, 0, nk, unit, 0, &S.abort, p.status);
       mbar_drain(&S.qbar, 0);               // the Q copies have landed before the CTA can leave
     } else if (lane == 1) {
       stream_ring<2>(sm + kPfOffV, S.vfull, S.vempty, &tmv, 0, nk, unit, 0, &S.abort, p.status);
@@ -2122,5 +2143,9 @@ cudaError_t launch_score(const AttnParams& p, int NR, const CUtensorMap& tk, con
 extern "C" dropkv_status dropkv_test_skip_pass2_k(int32_t unit, int32_t tile) {
   const int v[2] = {unit, tile};
   return cudaMemcpyToSymbol(dropkv::g_test_skip_k, v, sizeof v) == cudaSuccess ? DROPKV_OK : DROPKV_ERR_CUDA;
+}
+extern "C" dropkv_status dropkv_test_skip_prefill_k(int32_t unit, int32_t tile) {
+  const int v[2] = {unit, tile};
+  return cudaMemcpyToSymbol(dropkv::g_test_skip_pf_k, v, sizeof v) == cudaSuccess ? DROPKV_OK : DROPKV_ERR_CUDA;
 }
 #endif

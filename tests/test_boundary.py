@@ -34,7 +34,7 @@ def test_product_library_exports_no_test_hook():
     """include/dropkv_test_hooks.h is served only by the test build."""
     path = _build.build_library()
     hooks = B.declared_functions(os.path.join(_build.INCLUDE, "dropkv_test_hooks.h"))
-    assert hooks == ["dropkv_test_skip_pass2_k"]
+    assert hooks == ["dropkv_test_skip_pass2_k", "dropkv_test_skip_prefill_k"]
     out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True, check=True).stdout
     assert not any(h in out for h in hooks)
     assert "DROPKV_TEST_HOOKS" not in " ".join(_build.NVCC_FLAGS)

@@ -114,6 +114,30 @@ def test_prefill_tile_pairing_edges(n):
     _check_output(out, ref_out, wl.v, wl.lengths.numpy(), s.g, label="pairing n=%d" % n)
 
 
+def test_prefill_leaves_rows_past_each_sequence_untouched():
+    """A ragged batch at a longer n_max, called twice (the second time with
+    shorter lengths): no call writes an output row at or past its sequence's
+    length."""
+    wl = synth.make_workload("qwen_gqa7_b4_ragged_n64k", n_max=5000)
+    s = wl.spec
+    q_full = _prefill_inputs(wl, seed=20)
+    op = DropKV(s.B, s.Hq, s.Hkv, s.d, s.n_max, s.w, s.pool_kernel, s.protect, device=DEV)
+    q, k, v = q_full.to(DEV), wl.k.to(DEV), wl.v.to(DEV)
+    out = torch.full((s.B, s.Hq, s.n_max, s.d), -3.5, dtype=torch.bfloat16, device=DEV)
+    for lengths in (wl.lengths, torch.clamp(wl.lengths - 150, min=s.w + s.protect + int(wl.evict_k.max()) + 1)):
+        out.fill_(-3.5)
+        op.run_prefill(q, k, v, lengths.to(torch.int32).to(DEV), wl.evict_k.to(DEV), out)
+        op.check()
+        got = out.float().cpu().numpy()
+        for b in range(s.B):
+            nb = int(lengths[b])
+            assert np.all(got[b, :, nb:] == -3.5), "b=%d: rows past n_b = %d written (first at %s)" % (
+                b, nb, np.argwhere(got[b, :, nb:] != -3.5)[:1].tolist())
+            miss = np.argwhere(np.all(got[b, :, :nb] == -3.5, axis=-1))
+            assert len(miss) == 0, "b=%d (n_b = %d): %d rows not written, e.g. (head, row) %s; query tiles %s" % (
+                b, nb, len(miss), miss[:6].tolist(), sorted(set((miss[:, 1] // 128).tolist()))[:20])
+
+
 def test_prefill_full_size_c1_layer():
     """The Phi-3-like MHA layer at its full size (n = 4096, 32 heads): every
     row's output and the whole eviction against the oracle."""
