@@ -138,6 +138,46 @@ def test_prefill_leaves_rows_past_each_sequence_untouched():
                 b, nb, len(miss), miss[:6].tolist(), sorted(set((miss[:, 1] // 128).tolist()))[:20])
 
 
+def _prefill_sweep_cases(count, seed):
+    """Random shapes for the prefill path: d, g, w up to g w = 64, ragged
+    lengths, every pooling size and protection width."""
+    rng = np.random.default_rng(seed)
+    cases = []
+    while len(cases) < count:
+        Hkv = int(rng.integers(1, 3))
+        g = int(rng.integers(1, 9))
+        w = int(rng.integers(1, 9))
+        if g * w > 64:
+            continue
+        d = int(rng.choice([8, 16, 24, 64, 96, 120, 128]))
+        B = int(rng.integers(1, 4))
+        n = int(rng.integers(w + 1, 1400))
+        lens = rng.integers(max(w, 1), n + 1, size=B)
+        protect = int(rng.integers(0, w + 1))
+        pool = int(rng.choice([1, 3, 5, 9]))
+        evict = [int(rng.integers(0, max(1, int(L) - protect) + 1)) for L in lens]
+        cases.append((B, g * Hkv, Hkv, d, n, w, pool, protect, lens.tolist(), evict))
+    return cases
+
+
+@pytest.mark.parametrize("case", _prefill_sweep_cases(8, 2027))
+def test_prefill_random_shape_sweep(case):
+    """The fused prefill on random shapes: every row's output and the whole
+    eviction against the oracle, as the fixed cases above."""
+    B, Hq, Hkv, d, n, w, pool, protect, lens, evict = case
+    rng = np.random.default_rng(sum(lens) + d + 7)
+    q_full = synth.bf16_round(rng.standard_normal((B, Hq, n, d)).astype(np.float32))
+    k = synth.bf16_round(rng.standard_normal((B, Hkv, n, d)).astype(np.float32))
+    v = synth.bf16_round(rng.standard_normal((B, Hkv, n, d)).astype(np.float32))
+    lengths = torch.tensor(lens, dtype=torch.int32)
+    spec = synth.WorkloadSpec("custom", B, Hq, Hkv, d, n, w, pool, protect, 0, "custom")
+    wl = synth.Workload(spec=spec, q=_window_q(q_full, lengths, w), k=k, v=v, lengths=lengths,
+                        evict_k=torch.tensor(evict, dtype=torch.int32))
+    op, out = _check_path(wl, q_full, "prefill sweep %s" % (case,))
+    ref_out = oracle.prefill_attention(q_full, k, v, lengths.numpy())
+    _check_output(out, ref_out, v, lengths.numpy(), Hq // Hkv, label="sweep %s" % (case,))
+
+
 def test_prefill_full_size_c1_layer():
     """The Phi-3-like MHA layer at its full size (n = 4096, 32 heads): every
     row's output and the whole eviction against the oracle."""
