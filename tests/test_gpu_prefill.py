@@ -212,6 +212,19 @@ def test_prefill_with_dominated_rows():
     _check_path(wl, q_full, "prefill sink")
 
 
+def test_prefill_with_value_offset_and_sink():
+    """Values sharing an 8-sigma offset (the expanded distance's hard case)
+    and a sink of about 0.9999 of each window row's mass, through the fused
+    call: the window states of one partial per row take the shifted basis and
+    the dominant mode; exact against the oracle, and every row's output."""
+    wl = synth.make_workload("llama8b_gqa_d128_n32k", n_max=3000, sink_margin=float(np.log(9999.0)), v_offset=8.0)
+    s = wl.spec
+    q_full = _prefill_inputs(wl, seed=21)
+    op, out = _check_path(wl, q_full, "prefill offset + sink")
+    ref_out = oracle.prefill_attention(q_full, wl.k, wl.v, wl.lengths.numpy())
+    _check_output(out, ref_out, wl.v, wl.lengths.numpy(), s.g, label="offset + sink")
+
+
 def test_prefill_matches_the_window_path():
     """The same layer through dropkv_evict (pass 1 over the window rows) and
     through the prefilled call: scores within the tolerance of each other and
