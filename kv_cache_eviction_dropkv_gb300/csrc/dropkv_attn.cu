@@ -28,6 +28,7 @@
 // states merged, then a second pass accumulating scores over key tiles without
 // materialising the attention matrix).
 #include <cuda_bf16.h>
+#include <algorithm>
 #include <cuda_runtime.h>
 
 #include "dropkv_internal.cuh"
@@ -327,6 +328,10 @@ constexpr int kMergeSplitRegs = kMaxSplits / 32;
 static_assert(kMergeSplitRegs * 32 == kMaxSplits, "split states are held 32 per register slot");
 
 __global__ void __launch_bounds__(kMergeThreads) merge_splits_kernel(const AttnParams p) {
+  // the O column of up to 32 splits per row (warp), [warp][split][lane],
+  // staged with cp.async: in flight with the statistics' loads, and the
+  // reduction below runs as a short loop (this kernel's code is fetched cold)
+  extern __shared__ float4 mo_s[];
   __shared__ float wts_s[kMergeRows][32];
   __shared__ float wex_s[kMergeRows][32];       // the same weights without split s* (dominated rows)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -377,11 +382,16 @@ __global__ void __launch_bounds__(kMergeThreads) merge_splits_kernel(const AttnP
       const int s = q * 32 + lane;
       v[q] = (s < S) ? __ldcg(ml + (size_t)s * R + r) : make_float4(-INFINITY, 0.f, 0.f, 0.f);
     }
-    float4 o[32];
-#pragma unroll
-    for (int u = 0; u < 32; ++u)
-      o[u] = (!stats_only && lane < D4 && u < S) ? __ldcg(po4 + (size_t)u * split_stride + (size_t)r * D4 + lane)
-                                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+    const int CH = min(32, p.splits);            // splits staged per round (the launch sized mo_s for it)
+    float4* mo = mo_s + (size_t)warp * CH * 32;
+    auto stage = [&](int q) {
+      if (stats_only || lane >= D4) return;
+      const int n = min(CH, S - q * CH);
+#pragma unroll 1
+      for (int u = 0; u < n; ++u)
+        cp_async_cg16(mo + u * 32 + lane, po4 + (size_t)(q * CH + u) * split_stride + (size_t)r * D4 + lane);
+    };
+    stage(0);
 #pragma unroll
     for (int q = 0; q < kMergeSplitRegs; ++q)
       if (v[q].y > 0.f) M = fmaxf(M, v[q].x);
@@ -432,42 +442,48 @@ __global__ void __launch_bounds__(kMergeThreads) merge_splits_kernel(const AttnP
     }
     if (!stats_only) {
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f), acx = make_float4(0.f, 0.f, 0.f, 0.f);
+      // splits in order, CH at a time (their weights through wts_s / wex_s,
+      // 32 per register slot); a split without visible keys has weight 0 and
+      // is dropped by a select, not a multiply, so whatever its O holds
+      // cannot leak in
+      for (int q = 0; q * CH < S; ++q) {
+        if (q > 0) stage(q);
+        cp_async_wait_all();
+        const int n = min(CH, S - q * CH);
+#pragma unroll 1
+        for (int u = 0; u < n; ++u) {
+          const int s = q * CH + u;                 // split index
+          if ((s & 31) == 0) {                      // the next 32 splits' weights
+            const int qi = s >> 5;
+            float w0 = wgt[0], x0 = dom ? wex[0] : 0.f;
 #pragma unroll
-      for (int q = 0; q < kMergeSplitRegs; ++q) {
-        if (q * 32 >= S) break;
-        __syncwarp();
-        wts_s[warp][lane] = wgt[q];
-        if (dom) wex_s[warp][lane] = wex[q];
-        __syncwarp();
-        if (q > 0) {
-#pragma unroll
-          for (int u = 0; u < 32; ++u)
-            o[u] = (lane < D4 && q * 32 + u < S)
-                       ? __ldcg(po4 + (size_t)(q * 32 + u) * split_stride + (size_t)r * D4 + lane)
-                       : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-#pragma unroll
-        for (int u = 0; u < 32; ++u) {
-          const float wu = wts_s[warp][u];
+            for (int k = 1; k < kMergeSplitRegs; ++k)
+              if (k == qi) {
+                w0 = wgt[k];
+                if (dom) x0 = wex[k];
+              }
+            __syncwarp();
+            wts_s[warp][lane] = w0;
+            wex_s[warp][lane] = x0;
+            __syncwarp();
+          }
+          const float wu = wts_s[warp][s & 31];
+          const float wx = wex_s[warp][s & 31];
+          const float4 ov = mo[u * 32 + lane];
           if (wu != 0.f) {
-            acc.x = fmaf(o[u].x, wu, acc.x);
-            acc.y = fmaf(o[u].y, wu, acc.y);
-            acc.z = fmaf(o[u].z, wu, acc.z);
-            acc.w = fmaf(o[u].w, wu, acc.w);
+            acc.x = fmaf(ov.x, wu, acc.x);
+            acc.y = fmaf(ov.y, wu, acc.y);
+            acc.z = fmaf(ov.z, wu, acc.z);
+            acc.w = fmaf(ov.w, wu, acc.w);
+          }
+          if (dom && wx != 0.f) {
+            acx.x = fmaf(ov.x, wx, acx.x);
+            acx.y = fmaf(ov.y, wx, acx.y);
+            acx.z = fmaf(ov.z, wx, acx.z);
+            acx.w = fmaf(ov.w, wx, acx.w);
           }
         }
-        if (dom) {
-#pragma unroll
-          for (int u = 0; u < 32; ++u) {
-            const float wx = wex_s[warp][u];
-            if (wx != 0.f) {
-              acx.x = fmaf(o[u].x, wx, acx.x);
-              acx.y = fmaf(o[u].y, wx, acx.y);
-              acx.z = fmaf(o[u].z, wx, acx.z);
-              acx.w = fmaf(o[u].w, wx, acx.w);
-            }
-          }
-        }
+        __syncwarp();                                // the next round overwrites mo
       }
       const float inv = 1.0f / L;
       a = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
@@ -2112,8 +2128,14 @@ cudaError_t launch_window_attention(const AttnParams& p, int NR, const CUtensorM
 }
 
 cudaError_t launch_merge(const AttnParams& p, cudaStream_t st) {
-  // row groups covering the NR rows of the A.V^T operand (rows past R get zeros)
-  return launch_pdl(merge_splits_kernel, dim3(p.NR / kMergeRows, p.U), dim3(kMergeThreads), 0, st, p);
+  // row groups covering the NR rows of the A.V^T operand (rows past R get
+  // zeros); shared memory for the O columns of up to 32 splits per row
+  const size_t smem = (p.kind == kKindSnapKV) ? 0 : (size_t)kMergeRows * std::min(32, p.splits) * 32 * sizeof(float4);
+  if (smem > 48 * 1024) {
+    const cudaError_t e = cudaFuncSetAttribute(merge_splits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  return launch_pdl(merge_splits_kernel, dim3(p.NR / kMergeRows, p.U), dim3(kMergeThreads), smem, st, p);
 }
 
 cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
